@@ -1,0 +1,404 @@
+"""Benchmark of the MXFP4 MoE layer on one GB300 (or N replicas under torchrun).
+
+Metric: effective HBM bandwidth of one layer call, TB/s = algorithmic bytes /
+time, where the bytes are the packed weights + E8M0 scales of the distinct
+experts the call touches plus the bf16 activations read and written
+(3*I*H*(1/2 + 1/32) per expert + 4*T*H).  Router weights are not counted
+(reported beside).  us_per_call is reported as well.
+
+A step is one moe_layer_forward call (router -> top-k + grouping -> gate/up ->
+down + combine) on the workload's inputs, already resident in HBM.  Steps
+rotate over L distinct device copies of the weights (a multi-layer decode), so
+that no step finds its weights in L2 (L * touched bytes > 2.5 x L2).  Steps
+are replayed from a CUDA graph; W warm-up steps precede the K timed ones.
+
+Extra JSON keys:
+  roofline      the dominant kernel (gate/up + SiLU*up) timed by CUDA events
+                inside a graph replay of the same steps, against the measured
+                HBM copy bandwidth; traffic from the committed ncu capture.
+  cpu_baseline  the FP64 oracle on this host, a bounded sample.
+  e2e           the same metric through moe_layer_forward_hostio, with the
+                pinned host->device copy of x and the device->host copy of y
+                inside every step.
+  clocks        nvidia-smi samples taken during the timed region.
+
+--impl reference times the oracle (the only other implementation of this
+layer) on the same workload and prints the same line with "impl":
+"reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from block_scaled_fp4_moe_gb300 import inputs  # noqa: E402
+
+METRIC = "MoE layer µs/call and effective HBM TB/s (% of 8 TB/s) at T=1/4/16 tokens"
+PAGES_ROOFLINE_TBS = 8.0
+DEFAULT_CONFIG = "glm_t1"
+# dram__bytes_read.sum + dram__bytes_write.sum per gate/up launch, glm_t1,
+# from profiles/ffn_gateup_glm_t1.md (None until captured for this kernel).
+GATEUP_TRAFFIC_BYTES = {}
+
+
+def touched_bytes(cfg: inputs.MoEConfig, n_experts: int) -> dict:
+    per_expert = 3 * cfg.I * cfg.H * (0.5 + 1.0 / 32)
+    act = 2 * cfg.T * cfg.H * 2
+    return {"per_expert": per_expert, "weights": n_experts * per_expert, "activations": act,
+            "total": n_experts * per_expert + act,
+            "gateup": n_experts * 2 * cfg.I * cfg.H * (0.5 + 1.0 / 32) + cfg.T * cfg.H * 2,
+            "router": cfg.H * cfg.E * 4}
+
+
+def read_peaks() -> dict:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return {}
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ---------------------------------------------------------------- reference
+
+def oracle_call_factory(cfg: inputs.MoEConfig):
+    import oracle
+    x = inputs.make_x(cfg)
+    wr, bias = inputs.make_router(cfg)
+    route = oracle.route(x, wr, bias, cfg.top_k)
+    experts = {}
+    for e in sorted(set(int(v) for v in route["ids"].ravel())):
+        experts[e] = inputs.make_expert(cfg, e)
+
+    def call(tokens):
+        r = oracle.route(x, wr, bias, cfg.top_k)
+        return oracle.moe_tokens(x, r["ids"], r["w"], lambda e: experts[e], tokens)
+    return call, route
+
+
+def time_oracle(cfg, budget_s: float, max_calls: int | None = None):
+    """Wall time of whole oracle layer calls on a bounded sample of tokens."""
+    import oracle
+    call, route = oracle_call_factory(cfg)
+    n_exp = len(set(int(v) for v in route["ids"].ravel()))
+    # tokens per call: all of them when the whole call fits the budget, else a prefix
+    t0 = time.perf_counter()
+    call(np.arange(1, dtype=np.int32))
+    per_token = time.perf_counter() - t0
+    n_tok = max(1, min(cfg.T, int(budget_s / max(per_token, 1e-6))))
+    tokens = np.arange(n_tok, dtype=np.int32)
+    times = []
+    t_start = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        call(tokens)
+        times.append(time.perf_counter() - t0)
+        if (max_calls and len(times) >= max_calls) or time.perf_counter() - t_start > budget_s:
+            break
+    per_call = statistics.median(times) * cfg.T / n_tok          # scaled to the whole batch
+    b = touched_bytes(cfg, n_exp)
+    cores = oracle.num_threads()
+    return {"per_call_s": per_call, "tbs": b["total"] / per_call / 1e12, "cores": cores,
+            "sample": f"{len(times)} oracle call(s) on {n_tok} of {cfg.T} token(s), scaled to T={cfg.T}",
+            "n_experts": n_exp}
+
+
+def run_reference(args, cfg):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        time_oracle(cfg, budget_s=0.0, max_calls=1)
+    res = [time_oracle(cfg, budget_s=budget, max_calls=1) for _ in range(args.steps)]
+    per_call = statistics.median(r["per_call_s"] for r in res)
+    b = touched_bytes(cfg, res[0]["n_experts"])
+    val = b["total"] / per_call / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_call * 1e3,
+            "us_per_call": per_call * 1e6, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": describe(cfg), "name": cfg.name},
+            "cpu_baseline": {"value": val, "unit": "TB/s", "cores": res[0]["cores"], "kind": "oracle",
+                             "sample": res[0]["sample"]},
+            "e2e": {"value": val, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def describe(cfg):
+    return (f"{cfg.name}: T={cfg.T}, H={cfg.H}, {cfg.E} routed + {cfg.has_shared} shared experts, "
+            f"top-{cfg.top_k}, I={cfg.I}, MXFP4 (E2M1 + E8M0/32) weights, bf16 activations")
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_mine(args, cfg):
+    import torch
+    import torch.distributed as dist
+
+    from block_scaled_fp4_moe_gb300 import _build, moe
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build()
+    moe.lib()
+
+    # inputs (seeded, resident in HBM before timing)
+    x = inputs.make_x(cfg)
+    wr, bias = inputs.make_router(cfg)
+    bank_np = inputs.make_bank(cfg)
+    base = moe.MXFP4Bank.from_host(bank_np, cfg.E, cfg.has_shared, device=dev)
+    del bank_np
+    xd = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    wrd = torch.from_numpy(wr).to(dev)
+    bd = None if bias is None else torch.from_numpy(bias).to(dev)
+    ws = moe.alloc_workspace(cfg.T, base, cfg.top_k, device=dev)
+    y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+    ids = torch.empty((cfg.T, cfg.slots), dtype=torch.int32, device=dev)
+    tw = torch.empty((cfg.T, cfg.slots), dtype=torch.float32, device=dev)
+    moe.moe_layer_forward(xd, wrd, bd, cfg.top_k, base, 1.0, y, ids, tw, ws)
+    st = moe.moe_check_device_status(ws)
+    if st != 0:
+        raise RuntimeError(moe.moe_status_string(st))
+    n_exp = len(set(ids.cpu().numpy().ravel().tolist()))
+    b = touched_bytes(cfg, n_exp)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_layers = max(2, math.ceil(2.5 * l2 / b["total"]))
+    banks = [base] + [moe.MXFP4Bank(base.w13.clone(), base.s13.clone(), base.w2.clone(), base.s2.clone(),
+                                    cfg.E, cfg.has_shared) for _ in range(n_layers - 1)]
+    routers = [wrd] + [wrd.clone() for _ in range(n_layers - 1)]
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i, s):
+        moe.moe_layer_forward(xd, routers[i % n_layers], bd, cfg.top_k, banks[i % n_layers], 1.0, y, ws=ws,
+                              stream=s)
+
+    # graph of one rotation over all layers
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, n_layers)):
+            step(i, stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(n_layers):
+            step(i, torch.cuda.current_stream())
+    steps = max(1, args.steps)
+    reps, rest = divmod(steps, n_layers)
+    tail = None
+    if rest:
+        tail = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(tail, stream=stream):
+            for i in range(rest):
+                step(i, torch.cuda.current_stream())
+    for _ in range(max(1, math.ceil(args.warmup / n_layers))):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region: exactly `steps` layer calls
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            if tail is not None:
+                tail.replay()
+            ev1.record(stream)
+        stream.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    t_max = elapsed
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+    per_call = t_max / steps
+    st = moe.moe_check_device_status(ws)
+    if st != 0:
+        raise RuntimeError(moe.moe_status_string(st))
+
+    # ---- per-kernel times from event nodes inside a graph of the same steps
+    kern = {"router": [], "topk_group": [], "gateup": [], "down_combine": []}
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_layers)]
+    for row in evs:              # torch creates the CUDA event on first record
+        for e in row:
+            e.record(stream)
+    stream.synchronize()
+    pgraph = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(pgraph, stream=stream):
+            for i in range(n_layers):
+                moe.moe_layer_forward_profiled(xd, routers[i], bd, cfg.top_k, banks[i], 1.0, y, ws, evs[i],
+                                               stream=torch.cuda.current_stream())
+        for rep in range(max(1, min(max(reps, 1), 2000 // n_layers))):
+            pgraph.replay()
+            stream.synchronize()
+            for i in range(n_layers):
+                e = evs[i]
+                for j, name in enumerate(kern):
+                    kern[name].append(e[j].elapsed_time(e[j + 1]) * 1e3)
+        kernel_source = "cuda events recorded inside graph replay"
+    except Exception as exc:      # event nodes unavailable: eager profiled calls
+        kernel_source = f"eager cuda events ({type(exc).__name__})"
+        for rep in range(200):
+            i = rep % n_layers
+            moe.moe_layer_forward_profiled(xd, routers[i], bd, cfg.top_k, banks[i], 1.0, y, ws, evs[i],
+                                           stream=stream)
+            stream.synchronize()
+            for j, name in enumerate(kern):
+                kern[name].append(evs[i][j].elapsed_time(evs[i][j + 1]) * 1e3)
+    kern_us = {k: statistics.median(v) for k, v in kern.items()}
+
+    # ---- end to end through host buffers
+    xh = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    yh = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
+    for i in range(3):
+        moe.moe_layer_forward_hostio(xh, routers[i % n_layers], bd, cfg.top_k, banks[i % n_layers], 1.0, yh, ws,
+                                     stream=stream)
+    n_e2e = min(steps, 2000)
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        moe.moe_layer_forward_hostio(xh, routers[i % n_layers], bd, cfg.top_k, banks[i % n_layers], 1.0, yh, ws,
+                                     stream=stream)
+    e2e_per_call = (time.perf_counter() - t0) / n_e2e
+    if not torch.equal(yh.to(dev), y):
+        raise RuntimeError("host-buffer entry point disagrees with the device entry point")
+
+    peaks = read_peaks()
+    peak = peaks.get("hbm_gbs")
+    gate_gbs = b["gateup"] / (kern_us["gateup"] * 1e-6) / 1e9
+    line = None
+    if rank == 0:
+        cpu = time_oracle(cfg, budget_s=args.cpu_budget)
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC, "value": world * b["total"] / per_call / 1e12, "unit": "TB/s", "n_gpus": world,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": per_call * 1e3, "us_per_call": per_call * 1e6,
+            "pct_of_8TBs": 100 * b["total"] / per_call / 1e12 / PAGES_ROOFLINE_TBS,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "mxfp4 weights x f16 activations -> f32 accumulate, bf16 out", "data": "synthetic",
+            "config": {"workload": describe(cfg), "name": cfg.name, "T": cfg.T, "experts_touched": n_exp,
+                       "bytes_per_call": b["total"], "router_bytes_not_counted": b["router"],
+                       "l2": f"inputs larger than L2: steps rotate over {n_layers} weight copies "
+                             f"({n_layers} x {b['total'] / 1e6:.1f} MB vs L2 {l2 / 1e6:.0f} MB)",
+                       "launch": "cuda graph replay, 4 kernels per call", "parallelism": f"replicas x{world}"},
+            "kernel_us": kern_us, "kernel_timing": kernel_source,
+            "roofline": {"bound": "hbm", "kernel": "ffn_kernel<gate/up>", "achieved": gate_gbs,
+                         "peak": peak if peak else 6800.0, "unit": "GB/s",
+                         "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak else "fallback",
+                         "frac": gate_gbs / (peak if peak else 6800.0),
+                         "traffic": GATEUP_TRAFFIC_BYTES.get(cfg.name),
+                         "algorithmic_bytes": b["gateup"]},
+            "cpu_baseline": {"value": cpu["tbs"], "unit": "TB/s", "cores": cpu["cores"], "kind": "oracle",
+                             "sample": cpu["sample"]},
+            "e2e": {"value": world * b["total"] / e2e_per_call / 1e12, "unit": "TB/s",
+                    "us_per_call": e2e_per_call * 1e6,
+                    "h2d_bytes_per_step": cfg.T * cfg.H * 2, "d2h_bytes_per_step": cfg.T * cfg.H * 2},
+            "gpu_launches": 4 * steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(inputs.CONFIGS))
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)     # never fewer than 3 untimed warm-up steps
+    cfg = inputs.CONFIGS[args.config]
+    if args.impl == "reference":
+        return run_reference(args, cfg)
+    return run_mine(args, cfg)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,332 @@
+// capi.cu -- the extern "C" boundary of the MoE library: argument checks,
+// workspace layout and the launch sequence on the caller's stream.
+#include <atomic>
+#include <cstdint>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace moe;
+
+namespace {
+
+std::atomic<int> g_sms[64];
+
+__global__ void set_word_kernel(uint32_t *p, uint32_t v) { *p = v; }
+
+// Streaming-multiprocessor count of the current device; rejects devices the
+// library was not built for.
+moe_status_t current_device_sms(int *sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    const int cached = g_sms[dev & 63].load(std::memory_order_relaxed);
+    if (cached > 0) {
+        *sms = cached;
+        return MOE_OK;
+    }
+    int major = 0, minor = 0, n = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (major != 10 || minor != 3)
+        return MOE_ERR_UNSUPPORTED_DEVICE;
+    g_sms[dev & 63].store(n, std::memory_order_relaxed);
+    *sms = n;
+    return MOE_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+moe_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status_t check_routing_shape(int T, int H, int E, int k, int S) {
+    if (T < 0 || H <= 0 || E <= 0 || k <= 0 || (S != 0 && S != 1))
+        return MOE_ERR_INVALID_ARG;
+    if (T > kMaxTokens || k > E || E + S > kMaxExperts || k + S > kMaxSlots)
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    return MOE_OK;
+}
+
+moe_status_t check_bank(const moe_mxfp4_bank_t *b) {
+    if (!b || !b->w13 || !b->s13 || !b->w2 || !b->s2)
+        return MOE_ERR_INVALID_ARG;
+    if (b->hidden <= 0 || b->inter <= 0 || b->num_experts <= 0 || (b->has_shared != 0 && b->has_shared != 1))
+        return MOE_ERR_INVALID_ARG;
+    if (!ffn_shape_supported(b->hidden, b->inter) || b->hidden > 65536 || b->inter > 65536)
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(b->w13, 16) || !aligned(b->s13, 16) || !aligned(b->w2, 16) || !aligned(b->s2, 16))
+        return MOE_ERR_MISALIGNED;
+    return MOE_OK;
+}
+
+GroupOut group_out_for(void *ws, const WsLayout &L, int H) {
+    GroupOut go{};
+    go.offsets = ws_at<int32_t>(ws, L.offsets);
+    go.sorted_tok = ws_at<int32_t>(ws, L.sorted_tok);
+    go.sorted_slot = ws_at<int32_t>(ws, L.sorted_slot);
+    go.inv_pos = ws_at<int32_t>(ws, L.inv_pos);
+    go.active = ws_at<int32_t>(ws, L.active);
+    go.num_active = nullptr;
+    go.passes = ws_at<Pass>(ws, L.passes);
+    go.counters = ws_at<uint32_t>(ws, L.counters);
+    go.n_counters = H / 16;
+    return go;
+}
+
+// Shared body of the full-layer entry points.
+moe_status_t layer_forward(const uint16_t *x, const float *router_w, const float *logit_bias, int T, int top_k,
+                           const moe_mxfp4_bank_t *bank, float shared_weight, uint16_t *y, int32_t *ids_out,
+                           float *w_out, void *ws, size_t ws_bytes, cudaEvent_t *ev, cudaStream_t stream) {
+    moe_status_t st = check_bank(bank);
+    if (st != MOE_OK)
+        return st;
+    const int H = bank->hidden, I = bank->inter, E = bank->num_experts, S = bank->has_shared;
+    if ((st = check_routing_shape(T, H, E, top_k, S)) != MOE_OK)
+        return st;
+    if (T == 0)
+        return MOE_OK;
+    if (!x || !router_w || !y || !ws)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(y, 16) || !aligned(ws, 256) || !aligned(router_w, 4) ||
+        !aligned(logit_bias, 4) || !aligned(ids_out, 4) || !aligned(w_out, 4))
+        return MOE_ERR_MISALIGNED;
+    const WsLayout L = WsLayout::make(T, H, I, E, top_k, S);
+    if (ws_bytes < L.total)
+        return MOE_ERR_WORKSPACE_TOO_SMALL;
+    int sms = 0;
+    if ((st = current_device_sms(&sms)) != MOE_OK)
+        return st;
+    (void)cudaGetLastError();
+    if (T == 0)
+        return MOE_OK;
+    int32_t *ids = ids_out ? ids_out : ws_at<int32_t>(ws, L.topk_ids);
+    float *w = w_out ? w_out : ws_at<float>(ws, L.topk_w);
+    const GroupOut go = group_out_for(ws, L, H);
+    if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    cudaError_t err = launch_route(x, router_w, logit_bias, T, H, E, top_k, S, shared_weight, ids, w, ws, L,
+                                   true, go, stream, ev ? ev[1] : nullptr);
+    if (err != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (ev && cudaEventRecord(ev[2], stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    FfnProblem pr{x, bank, w, y, T, top_k + S};
+    err = launch_ffn(pr, ws, L, sms, stream, ev ? ev[3] : nullptr);
+    if (err != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (ev && cudaEventRecord(ev[4], stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_size(int T, int H, int I, int E, int top_k, int has_shared) {
+    if (T < 0 || H <= 0 || I <= 0 || E <= 0 || top_k <= 0 || (has_shared != 0 && has_shared != 1))
+        return 0;
+    return WsLayout::make(T, H, I, E, top_k, has_shared).total;
+}
+
+moe_status_t moe_route_topk(const uint16_t *x, const float *router_w, const float *logit_bias, int T, int H, int E,
+                            int top_k, int has_shared, float shared_weight, int32_t *topk_ids, float *topk_w,
+                            void *ws, size_t ws_bytes, cudaStream_t stream) {
+    moe_status_t st = check_routing_shape(T, H, E, top_k, has_shared);
+    if (st != MOE_OK)
+        return st;
+    if (T == 0)
+        return MOE_OK;
+    if (!x || !router_w || !topk_ids || !topk_w || !ws)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 2) || !aligned(router_w, 4) || !aligned(logit_bias, 4) || !aligned(topk_ids, 4) ||
+        !aligned(topk_w, 4) || !aligned(ws, 256))
+        return MOE_ERR_MISALIGNED;
+    const WsLayout L = WsLayout::make(T, H, 64, E, top_k, has_shared);
+    if (ws_bytes < L.topk_ids)
+        return MOE_ERR_WORKSPACE_TOO_SMALL;
+    int sms = 0;
+    if ((st = current_device_sms(&sms)) != MOE_OK)
+        return st;
+    (void)cudaGetLastError();
+    if (T == 0)
+        return MOE_OK;
+    const GroupOut none{};
+    return from_cuda(launch_route(x, router_w, logit_bias, T, H, E, top_k, has_shared, shared_weight, topk_ids,
+                                  topk_w, ws, L, false, none, stream));
+}
+
+moe_status_t moe_group_tokens(const int32_t *topk_ids, int T, int k_plus_s, int n_experts_total,
+                              int32_t *expert_offsets, int32_t *sorted_tok, int32_t *sorted_slot,
+                              int32_t *active_experts, int32_t *num_active, void *ws, size_t ws_bytes,
+                              cudaStream_t stream) {
+    if (T < 0 || k_plus_s <= 0 || n_experts_total <= 0)
+        return MOE_ERR_INVALID_ARG;
+    if (T > kMaxTokens || k_plus_s > kMaxSlots || n_experts_total > kMaxExperts)
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!topk_ids || !expert_offsets || !sorted_tok || !sorted_slot || !active_experts || !num_active || !ws)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(topk_ids, 4) || !aligned(expert_offsets, 4) || !aligned(sorted_tok, 4) ||
+        !aligned(sorted_slot, 4) || !aligned(active_experts, 4) || !aligned(num_active, 4) || !aligned(ws, 256))
+        return MOE_ERR_MISALIGNED;
+    if (ws_bytes < kHdrWords * sizeof(uint32_t))
+        return MOE_ERR_WORKSPACE_TOO_SMALL;
+    int sms = 0;
+    moe_status_t st = current_device_sms(&sms);
+    if (st != MOE_OK)
+        return st;
+    (void)cudaGetLastError();
+    GroupOut go{};
+    go.offsets = expert_offsets;
+    go.sorted_tok = sorted_tok;
+    go.sorted_slot = sorted_slot;
+    go.inv_pos = nullptr;
+    go.active = active_experts;
+    go.num_active = num_active;
+    go.passes = nullptr;
+    go.counters = nullptr;
+    go.n_counters = 0;
+    return from_cuda(launch_group(topk_ids, T, k_plus_s, n_experts_total, go, ws_at<uint32_t>(ws, 0), stream));
+}
+
+moe_status_t moe_expert_ffn_mxfp4(const uint16_t *x, const int32_t *topk_ids, const float *topk_w, int T, int top_k,
+                                  const moe_mxfp4_bank_t *bank, uint16_t *y, void *ws, size_t ws_bytes,
+                                  cudaStream_t stream) {
+    moe_status_t st = check_bank(bank);
+    if (st != MOE_OK)
+        return st;
+    const int H = bank->hidden, I = bank->inter, E = bank->num_experts, S = bank->has_shared;
+    if ((st = check_routing_shape(T, H, E, top_k, S)) != MOE_OK)
+        return st;
+    if (T == 0)
+        return MOE_OK;
+    if (!x || !topk_ids || !topk_w || !y || !ws)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(y, 16) || !aligned(ws, 256) || !aligned(topk_ids, 4) || !aligned(topk_w, 4))
+        return MOE_ERR_MISALIGNED;
+    const WsLayout L = WsLayout::make(T, H, I, E, top_k, S);
+    if (ws_bytes < L.total)
+        return MOE_ERR_WORKSPACE_TOO_SMALL;
+    int sms = 0;
+    if ((st = current_device_sms(&sms)) != MOE_OK)
+        return st;
+    (void)cudaGetLastError();
+    if (T == 0)
+        return MOE_OK;
+    const GroupOut go = group_out_for(ws, L, H);
+    cudaError_t err = launch_group(topk_ids, T, top_k + S, E + S, go, ws_at<uint32_t>(ws, 0), stream);
+    if (err != cudaSuccess)
+        return MOE_ERR_CUDA;
+    FfnProblem pr{x, bank, topk_w, y, T, top_k + S};
+    return from_cuda(launch_ffn(pr, ws, L, sms, stream, nullptr));
+}
+
+moe_status_t moe_layer_forward(const uint16_t *x, const float *router_w, const float *logit_bias, int T, int top_k,
+                               const moe_mxfp4_bank_t *bank, float shared_weight, uint16_t *y,
+                               int32_t *topk_ids_out, float *topk_w_out, void *ws, size_t ws_bytes,
+                               cudaStream_t stream) {
+    return layer_forward(x, router_w, logit_bias, T, top_k, bank, shared_weight, y, topk_ids_out, topk_w_out, ws,
+                         ws_bytes, nullptr, stream);
+}
+
+moe_status_t moe_layer_forward_profiled(const uint16_t *x, const float *router_w, const float *logit_bias, int T,
+                                        int top_k, const moe_mxfp4_bank_t *bank, float shared_weight, uint16_t *y,
+                                        void *ws, size_t ws_bytes, cudaEvent_t *events, int n_events,
+                                        cudaStream_t stream) {
+    if (!events || n_events != 5)
+        return MOE_ERR_INVALID_ARG;
+    for (int i = 0; i < 5; ++i)
+        if (!events[i])
+            return MOE_ERR_INVALID_ARG;
+    return layer_forward(x, router_w, logit_bias, T, top_k, bank, shared_weight, y, nullptr, nullptr, ws, ws_bytes,
+                         events, stream);
+}
+
+moe_status_t moe_layer_forward_hostio(const uint16_t *x_host, const float *router_w, const float *logit_bias, int T,
+                                      int top_k, const moe_mxfp4_bank_t *bank, float shared_weight,
+                                      uint16_t *y_host, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    moe_status_t st = check_bank(bank);
+    if (st != MOE_OK)
+        return st;
+    if (!x_host || !y_host || !ws || T < 0)
+        return MOE_ERR_INVALID_ARG;
+    const int H = bank->hidden;
+    if ((st = check_routing_shape(T, H, bank->num_experts, top_k, bank->has_shared)) != MOE_OK)
+        return st;
+    if (!aligned(ws, 256))
+        return MOE_ERR_MISALIGNED;
+    const WsLayout L = WsLayout::make(T, H, bank->inter, bank->num_experts, top_k, bank->has_shared);
+    if (ws_bytes < L.total)
+        return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if (T == 0)
+        return MOE_OK;
+    uint16_t *xd = ws_at<uint16_t>(ws, L.xstage);
+    uint16_t *yd = ws_at<uint16_t>(ws, L.ystage);
+    const size_t bytes = (size_t)T * H * sizeof(uint16_t);
+    (void)cudaGetLastError();
+    if (cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    st = layer_forward(xd, router_w, logit_bias, T, top_k, bank, shared_weight, yd, nullptr, nullptr, ws, ws_bytes,
+                       nullptr, stream);
+    if (st != MOE_OK)
+        return st;
+    if (cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return from_cuda(cudaStreamSynchronize(stream));
+}
+
+moe_status_t moe_check_device_status(void *ws, cudaStream_t stream) {
+    if (!ws)
+        return MOE_ERR_INVALID_ARG;
+    uint32_t word = 0;
+    uint32_t *hdr = ws_at<uint32_t>(ws, 0);
+    if (cudaMemcpyAsync(&word, hdr + kHdrStatus, sizeof word, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (word != 0) {
+        set_word_kernel<<<1, 1, 0, stream>>>(hdr + kHdrStatus, 0u);
+        if (cudaGetLastError() != cudaSuccess || cudaStreamSynchronize(stream) != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
+    return static_cast<moe_status_t>(word);
+}
+
+moe_status_t moe_debug_set_flags(void *ws, uint32_t flags, cudaStream_t stream) {
+    if (!ws || !aligned(ws, 256))
+        return MOE_ERR_INVALID_ARG;
+    if (flags & ~kDebugForceTimeout)
+        return MOE_ERR_INVALID_ARG;
+    set_word_kernel<<<1, 1, 0, stream>>>(ws_at<uint32_t>(ws, 0) + kHdrDebugFlags, flags);
+    return from_cuda(cudaGetLastError());
+}
+
+moe_status_t moe_selftest_decode_e2m1(const uint8_t *codes, uint16_t *out, int n, cudaStream_t stream) {
+    if (!codes || !out || n < 0)
+        return MOE_ERR_INVALID_ARG;
+    int sms = 0;
+    moe_status_t st = current_device_sms(&sms);
+    if (st != MOE_OK)
+        return st;
+    if (n == 0)
+        return MOE_OK;
+    return from_cuda(launch_selftest_decode(codes, out, n, stream));
+}
+
+const char *moe_status_string(moe_status_t s) {
+    switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_MISALIGNED: return "misaligned pointer";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_DEVICE_ASSERT: return "device-side input check failed";
+    case MOE_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs sm_103)";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

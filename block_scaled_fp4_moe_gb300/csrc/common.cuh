@@ -1,0 +1,202 @@
+// common.cuh -- shared definitions of the sm_103a MoE kernels: workspace
+// layout, status word, and thin wrappers over the PTX the kernels use
+// (mbarrier, bulk async copies, mma.sync, E2M1 conversion).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "moe_fp4.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ sizes
+
+constexpr int kRouteRows = 128;       // router rows (of H) per CTA
+constexpr int kRouteCols = 32;        // router experts per CTA (one per lane)
+constexpr int kRouteThreads = 256;
+constexpr int kFinishWarps = 8;       // tokens per top-k CTA (one warp each)
+constexpr int kGroupThreads = 256;
+constexpr int kPassTokens = 8;        // MMA N: tokens (or entries) per pass
+constexpr int kConsumerWarps = 8;
+constexpr int kFfnThreads = 32 * (kConsumerWarps + 1);
+constexpr int kMaxExperts = 1025;     // E + S (E <= 1024)
+constexpr int kMaxSlots = 32;         // k + S
+constexpr int kMaxTokens = 4096;
+
+// header words of the workspace
+enum HeaderWord : int {
+    kHdrStatus = 0,
+    kHdrDebugFlags = 1,
+    kHdrRouteTicket = 2,
+    kHdrNumActive = 3,
+    kHdrNumPasses = 4,
+    kHdrWords = 64
+};
+constexpr uint32_t kDebugForceTimeout = 1u;
+
+// A pass: up to kPassTokens consecutive entries of one expert's group.
+struct Pass {
+    int32_t expert;
+    int32_t begin;   // first entry (sorted position)
+    int32_t count;   // 1..kPassTokens
+    int32_t pad;
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline int max_passes(int T, int kps, int n_tot) {
+    long entries = (long)T * kps;
+    long na = entries < n_tot ? entries : n_tot;
+    return (int)((entries + kPassTokens - 1) / kPassTokens + na + 1);
+}
+
+// Offsets (bytes) of the workspace regions for one problem size.
+struct WsLayout {
+    size_t route_part, topk_ids, topk_w, offsets, sorted_tok, sorted_slot, inv_pos, active,
+        passes, h, ypart, counters, xstage, ystage, total;
+
+    static WsLayout make(int T, int H, int I, int E, int k, int S) {
+        WsLayout L{};
+        const int kps = k + S, n_tot = E + S;
+        const size_t entries = (size_t)T * kps;
+        const int nh = (H + kRouteRows - 1) / kRouteRows;
+        size_t o = kHdrWords * sizeof(uint32_t);
+        auto take = [&](size_t bytes) { o = align_up(o, 256); size_t r = o; o += bytes; return r; };
+        L.route_part = take((size_t)nh * T * E * 2 * sizeof(float));
+        L.topk_ids = take(entries * sizeof(int32_t));
+        L.topk_w = take(entries * sizeof(float));
+        L.offsets = take((size_t)(n_tot + 1) * sizeof(int32_t));
+        L.sorted_tok = take(entries * sizeof(int32_t));
+        L.sorted_slot = take(entries * sizeof(int32_t));
+        L.inv_pos = take(entries * sizeof(int32_t));
+        L.active = take((size_t)n_tot * sizeof(int32_t));
+        L.passes = take((size_t)max_passes(T, kps, n_tot) * sizeof(Pass));
+        L.h = take(entries * (size_t)I * sizeof(float));
+        L.ypart = take(entries * (size_t)H * sizeof(float));
+        L.counters = take((size_t)(H / 16) * sizeof(uint32_t));
+        L.xstage = take((size_t)T * H * sizeof(uint16_t));
+        L.ystage = take((size_t)T * H * sizeof(uint16_t));
+        L.total = align_up(o, 256);
+        return L;
+    }
+};
+
+template <typename P>
+inline P *ws_at(void *ws, size_t off) { return reinterpret_cast<P *>(static_cast<char *>(ws) + off); }
+
+// --------------------------------------------------------- device helpers
+
+__device__ __forceinline__ void record_status(uint32_t *hdr, uint32_t code) {
+    atomicCAS(hdr + kHdrStatus, 0u, code);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Make initialised barriers visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bulk async copy global -> shared (this CTA), completion counted in bytes on
+// `bar`.  dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// L2 policy for data read exactly once (streamed expert weights).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// D = A(16x16 f16, row) * B(16x8 f16, col) + C, fp32 accumulate.
+__device__ __forceinline__ void mma_m16n8k16_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                 uint32_t a3, uint32_t b0, uint32_t b1,
+                                                 const float (&c)[4]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
+          "f"(c[3]));
+}
+
+// Four bytes of packed E2M1 pairs -> four f16x2 (element of the low nibble in
+// the low half), using the sm_100-family conversion instruction.
+__device__ __forceinline__ void decode_e2m1x8(uint32_t w, uint32_t (&out)[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(out[0]), "=r"(out[1]), "=r"(out[2]), "=r"(out[3])
+        : "r"(w));
+}
+
+// E8M0 exponent byte -> 2^(s-127) as fp32 (s = 0 gives the subnormal 2^-127,
+// s = 255 gives NaN).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
+    uint32_t bits = s == 0 ? 0x00400000u : (s == 255 ? 0x7FFFFFFFu : (s << 23));
+    return __uint_as_float(bits);
+}
+
+// 2^e as fp32 for |e| <= 126.
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+// Exponent shift that maps a maximum magnitude m into [2^14, 2^15), clamped
+// so that 2^shift stays a normal fp32.
+__device__ __forceinline__ int f16_shift_for_max(float m) {
+    if (!(m > 0.0f) || !isfinite(m))
+        return 0;
+    int e;
+    frexpf(m, &e);          // m = f * 2^e, 0.5 <= f < 1
+    int s = 15 - e;
+    return s < -126 ? -126 : (s > 126 ? 126 : s);
+}
+
+}  // namespace moe

@@ -1,0 +1,50 @@
+// kernels.h -- launch functions of the MoE kernels (internal to the library).
+#pragma once
+
+#include "common.cuh"
+
+namespace moe {
+
+// Where grouping writes its results (device pointers; nullable where noted).
+struct GroupOut {
+    int32_t *offsets;      // [n_tot + 1]
+    int32_t *sorted_tok;   // [T*kps]
+    int32_t *sorted_slot;  // [T*kps]
+    int32_t *inv_pos;      // [T*kps] nullable: sorted position of entry t*kps+s
+    int32_t *active;       // [n_tot]
+    int32_t *num_active;   // [1] nullable (the header always gets it)
+    Pass *passes;          // nullable
+    uint32_t *counters;    // down-kernel row-block counters to zero
+    int n_counters;
+};
+
+// static shared memory of the grouping code (two int arrays of kMaxExperts)
+constexpr size_t kGroupStaticSmem = 2 * kMaxExperts * sizeof(int) + 64;
+
+cudaError_t launch_route(const uint16_t *x, const float *wr, const float *bias, int T, int H, int E, int k,
+                         int has_shared, float shared_weight, int32_t *ids, float *w, void *ws,
+                         const WsLayout &L, bool do_group, const GroupOut &go, cudaStream_t stream,
+                         cudaEvent_t ev_after_partial = nullptr);
+
+cudaError_t launch_group(const int32_t *ids, int T, int kps, int n_tot, const GroupOut &go, uint32_t *hdr,
+                         cudaStream_t stream);
+
+// Expert FFN: gate/up + SiLU*up (writes h), then down + weighted combine
+// (writes y).  Grouping results must already be in the workspace.
+struct FfnProblem {
+    const uint16_t *x;       // [T, H] bf16
+    const moe_mxfp4_bank_t *bank;
+    const float *topk_w;     // [T, kps]
+    uint16_t *y;             // [T, H] bf16
+    int T, kps;
+};
+
+cudaError_t launch_ffn(const FfnProblem &p, void *ws, const WsLayout &L, int num_sms, cudaStream_t stream,
+                       cudaEvent_t ev_after_gateup);
+
+cudaError_t launch_selftest_decode(const uint8_t *codes, uint16_t *out, int n, cudaStream_t stream);
+
+// Shape rules shared by validation and the kernels' staging choices.
+bool ffn_shape_supported(int H, int I);
+
+}  // namespace moe

@@ -1,0 +1,362 @@
+// route.cu -- router logits, top-k selection with the fused shared slot, and
+// token-to-expert grouping (sm_103a).
+//
+// Router logits l[t,e] = sum_h x[t,h] Wr[h,e] + b[e] decide which experts a
+// token visits, so the kernels evaluate them with error-free transformations:
+// each product is split exactly into p + e with one FMA, and the running sum
+// is kept as an unevaluated pair (Dot2 of Ogita, Rump and Oishi, "Accurate sum
+// and dot product", SIAM J. Sci. Comput. 26(6), 2005).  The result carries
+// about twice fp32 precision, so the chosen experts and their order match the
+// exact logits except for near-ties far below anything the workloads produce.
+//
+// Top-k semantics: the k largest logits (equal logits: the lower expert index
+// first), ordered by descending logit; softmax over the k kept logits; the
+// shared expert, always selected, appended as slot k ("Optimizing GLM4-MoE for
+// production", section 1 "Shared experts fusion": top-9 of 161, the shared
+// expert always in the 9th position).
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+// --------------------------------------------------- error-free arithmetic
+
+__device__ __forceinline__ void two_prod(float a, float b, float &p, float &e) {
+    p = __fmul_rn(a, b);
+    e = __fmaf_rn(a, b, -p);
+}
+
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = __fadd_rn(a, b);
+    float z = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, z)), __fsub_rn(b, z));
+}
+
+// (p, s) += (p2, s2) for unevaluated sums p + s.
+__device__ __forceinline__ void pair_add(float &p, float &s, float p2, float s2) {
+    float q;
+    two_sum(p, p2, p, q);
+    s = __fadd_rn(s, __fadd_rn(s2, q));
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// ------------------------------------------------------------ router GEMV
+
+// Grid (ceil(E/32), ceil(H/128)); CTA (bx, by) owns experts [32bx, 32bx+32)
+// (one per lane) and router rows [128by, 128by+128) (16 per warp) for all T
+// tokens, and writes the partial Dot2 pairs part[by][t][e].
+__global__ void __launch_bounds__(kRouteThreads)
+route_partial_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wr, int T, int H, int E,
+                     float2 *__restrict__ part, uint32_t *__restrict__ hdr) {
+    constexpr int kWarps = kRouteThreads / 32;
+    constexpr int kRowsPerWarp = kRouteRows / kWarps;
+    constexpr int kTok = 8;
+    __shared__ float xs[kTok][kRouteRows];
+    __shared__ float2 red[kWarps][kTok][32];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * kRouteCols + lane;
+    const int h0 = blockIdx.y * kRouteRows;
+    const int hw = h0 + warp * kRowsPerWarp;
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+        hdr[kHdrRouteTicket] = 0;
+
+    float w[kRowsPerWarp];
+#pragma unroll
+    for (int i = 0; i < kRowsPerWarp; ++i) {
+        const int h = hw + i;
+        w[i] = (e < E && h < H) ? __ldg(wr + (size_t)h * E + e) : 0.0f;
+    }
+
+    for (int t0 = 0; t0 < T; t0 += kTok) {
+        const int tn = min(kTok, T - t0);
+        __syncthreads();
+        for (int i = threadIdx.x; i < kTok * kRouteRows; i += kRouteThreads) {
+            const int tt = i / kRouteRows, hh = i % kRouteRows;
+            float v = 0.0f;
+            if (tt < tn && h0 + hh < H)
+                v = bf16_bits_to_float(__ldg(x + (size_t)(t0 + tt) * H + h0 + hh));
+            xs[tt][hh] = v;
+        }
+        __syncthreads();
+#pragma unroll 1
+        for (int tt = 0; tt < kTok; ++tt) {
+            const float *xr = &xs[tt][warp * kRowsPerWarp];
+            float p, s;
+            two_prod(xr[0], w[0], p, s);
+#pragma unroll
+            for (int i = 1; i < kRowsPerWarp; ++i) {
+                float hp, r, q;
+                two_prod(xr[i], w[i], hp, r);
+                two_sum(p, hp, p, q);
+                s = __fadd_rn(s, __fadd_rn(q, r));
+            }
+            red[warp][tt][lane] = make_float2(p, s);
+        }
+        __syncthreads();
+        const int tt = warp;   // one warp per token of the chunk
+        if (tt < tn && e < E) {
+            float p = red[0][tt][lane].x, s = red[0][tt][lane].y;
+#pragma unroll
+            for (int w2 = 1; w2 < kWarps; ++w2)
+                pair_add(p, s, red[w2][tt][lane].x, red[w2][tt][lane].y);
+            part[((size_t)blockIdx.y * T + t0 + tt) * E + e] = make_float2(p, s);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ grouping
+
+// Grouping of ids [T*kps] (entry i = t*kps + s) by one CTA of kGroupThreads:
+// per-expert counts, exclusive offsets, the stable scatter of entries sorted
+// by (expert, entry), the ascending list of active experts, the passes (runs
+// of up to kPassTokens entries of one expert) and the reset of the down-kernel
+// row-block counters.
+__device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const GroupOut &o, uint32_t *hdr) {
+    __shared__ int cnt[kMaxExperts];
+    __shared__ int cursor[kMaxExperts];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n = T * kps;
+
+    for (int e = tid; e < n_tot; e += blockDim.x)
+        cnt[e] = 0;
+    for (int i = tid; i < o.n_counters; i += blockDim.x)
+        o.counters[i] = 0;
+    __syncthreads();
+    int bad = 0;
+    for (int i = tid; i < n; i += blockDim.x) {
+        const int e = __ldcg(ids + i);
+        if (e < 0 || e >= n_tot)
+            bad = 1;
+        else
+            atomicAdd(&cnt[e], 1);
+    }
+    bad = __syncthreads_or(bad);
+    if (bad) {
+        if (tid == 0) {
+            record_status(hdr, MOE_ERR_DEVICE_ASSERT);
+            hdr[kHdrNumActive] = 0;
+            hdr[kHdrNumPasses] = 0;
+            if (o.num_active)
+                *o.num_active = 0;
+        }
+        return;
+    }
+
+    if (warp == 0) {
+        int run = 0, na = 0, np = 0;
+        for (int base = 0; base < n_tot; base += 32) {
+            const int e = base + lane;
+            const int v = e < n_tot ? cnt[e] : 0;
+            int incl = v;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d)
+                    incl += y;
+            }
+            const int excl = run + incl - v;
+            const unsigned act = __ballot_sync(0xffffffffu, v > 0);
+            const int rank = __popc(act & ((1u << lane) - 1u));
+            const int npass = (v + kPassTokens - 1) / kPassTokens;
+            int pincl = npass;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, pincl, d);
+                if (lane >= d)
+                    pincl += y;
+            }
+            const int pexcl = np + pincl - npass;
+            if (e < n_tot) {
+                cursor[e] = excl;
+                o.offsets[e] = excl;
+                if (v > 0)
+                    o.active[na + rank] = e;
+                if (o.passes)
+                    for (int p = 0; p < npass; ++p) {
+                        Pass ps;
+                        ps.expert = e;
+                        ps.begin = excl + p * kPassTokens;
+                        ps.count = min(kPassTokens, v - p * kPassTokens);
+                        ps.pad = 0;
+                        o.passes[pexcl + p] = ps;
+                    }
+            }
+            run += __shfl_sync(0xffffffffu, incl, 31);
+            np += __shfl_sync(0xffffffffu, pincl, 31);
+            na += __popc(act);
+        }
+        if (lane == 0) {
+            o.offsets[n_tot] = run;
+            hdr[kHdrNumActive] = na;
+            hdr[kHdrNumPasses] = np;
+            if (o.num_active)
+                *o.num_active = na;
+        }
+        __syncwarp();
+        // stable scatter in entry order, 32 entries at a time
+        for (int base = 0; base < n; base += 32) {
+            const int i = base + lane;
+            const int e = i < n ? __ldcg(ids + i) : -1;
+            const unsigned same = __match_any_sync(0xffffffffu, e);
+            if (i < n) {
+                const int pos = cursor[e] + __popc(same & ((1u << lane) - 1u));
+                o.sorted_tok[pos] = i / kps;
+                o.sorted_slot[pos] = i % kps;
+                if (o.inv_pos)
+                    o.inv_pos[i] = pos;
+            }
+            __syncwarp();
+            if (i < n && lane == 31 - __clz(same))
+                cursor[e] += __popc(same);
+            __syncwarp();
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kGroupThreads)
+group_kernel(const int32_t *ids, int T, int kps, int n_tot, GroupOut o, uint32_t *hdr) {
+    group_block(ids, T, kps, n_tot, o, hdr);
+}
+
+// ------------------------------------------------------- top-k + shared slot
+
+// One warp per token.  Sums the partial pairs of every expert in a fixed
+// order, adds the bias, selects the top k, writes ids and softmax weights and
+// the shared slot.  With do_group, the last CTA to finish (atomic ticket)
+// groups all tokens.
+__global__ void __launch_bounds__(kFinishWarps * 32)
+route_finish_kernel(const float2 *__restrict__ part, int nh, const float *__restrict__ bias, int T, int E,
+                    int k, int has_shared, float shared_weight, int32_t *__restrict__ ids_out,
+                    float *__restrict__ w_out, uint32_t *__restrict__ hdr, int do_group, GroupOut go) {
+    extern __shared__ float2 lsm[];   // [kFinishWarps][E] normalised (hi, lo) logits
+    __shared__ int last_cta;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int t = blockIdx.x * kFinishWarps + warp;
+    const int kps = k + has_shared;
+    float2 *L = lsm + (size_t)warp * E;
+
+    if (t < T) {
+        for (int e = lane; e < E; e += 32) {
+            float p = 0.0f, s = 0.0f;
+            for (int c = 0; c < nh; ++c) {
+                const float2 v = part[((size_t)c * T + t) * E + e];
+                pair_add(p, s, v.x, v.y);
+            }
+            if (bias)
+                pair_add(p, s, bias[e], 0.0f);
+            float hi, lo;
+            two_sum(p, s, hi, lo);
+            L[e] = make_float2(hi, lo);
+        }
+        __syncwarp();
+        // k rounds of a warp-wide argmax over (hi, lo, -index)
+        const int per_lane = (E + 31) / 32;   // <= 32 (E <= 1024)
+        unsigned taken = 0;
+        float sel_num = 0.0f, top_hi = 0.0f, top_lo = 0.0f, denom = 0.0f;
+        int sel_id = 0;
+        for (int r = 0; r < k; ++r) {
+            float bh = -INFINITY, bl = -INFINITY;
+            int bi = 0x7fffffff;
+            for (int j = 0; j < per_lane; ++j) {
+                const int e = lane + 32 * j;
+                if (e >= E || ((taken >> j) & 1u))
+                    continue;
+                const float2 v = L[e];
+                if (v.x > bh || (v.x == bh && (v.y > bl || (v.y == bl && e < bi)))) {
+                    bh = v.x;
+                    bl = v.y;
+                    bi = e;
+                }
+            }
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) {
+                const float oh = __shfl_xor_sync(0xffffffffu, bh, d);
+                const float ol = __shfl_xor_sync(0xffffffffu, bl, d);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
+                if (oh > bh || (oh == bh && (ol > bl || (ol == bl && oi < bi)))) {
+                    bh = oh;
+                    bl = ol;
+                    bi = oi;
+                }
+            }
+            if (bi < E && (bi & 31) == lane)
+                taken |= 1u << (bi >> 5);
+            if (r == 0) {
+                top_hi = bh;
+                top_lo = bl;
+            }
+            // softmax numerator relative to the largest logit
+            const float d = __fadd_rn(__fsub_rn(bh, top_hi), __fsub_rn(bl, top_lo));
+            const float ex = expf(d);
+            denom += ex;
+            if (lane == r) {
+                sel_num = ex;
+                sel_id = bi;
+            }
+        }
+        if (lane < k) {
+            ids_out[(size_t)t * kps + lane] = sel_id;
+            w_out[(size_t)t * kps + lane] = sel_num / denom;
+        }
+        if (has_shared && lane == k) {
+            ids_out[(size_t)t * kps + k] = E;
+            w_out[(size_t)t * kps + k] = shared_weight;
+        }
+    }
+    if (!do_group)
+        return;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned ticket = atomicAdd(hdr + kHdrRouteTicket, 1u);
+        last_cta = ticket == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!last_cta)
+        return;
+    __threadfence();
+    group_block(ids_out, T, kps, E + has_shared, go, hdr);
+    if (threadIdx.x == 0)
+        hdr[kHdrRouteTicket] = 0;
+}
+
+// ------------------------------------------------------------------ launchers
+
+cudaError_t launch_route(const uint16_t *x, const float *wr, const float *bias, int T, int H, int E, int k,
+                         int has_shared, float shared_weight, int32_t *ids, float *w, void *ws,
+                         const WsLayout &L, bool do_group, const GroupOut &go, cudaStream_t stream,
+                         cudaEvent_t ev_after_partial) {
+    uint32_t *hdr = ws_at<uint32_t>(ws, 0);
+    float2 *part = ws_at<float2>(ws, L.route_part);
+    const int nh = (H + kRouteRows - 1) / kRouteRows;
+    dim3 g1((E + kRouteCols - 1) / kRouteCols, nh);
+    route_partial_kernel<<<g1, kRouteThreads, 0, stream>>>(x, wr, T, H, E, part, hdr);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess)
+        return err;
+    if (ev_after_partial && (err = cudaEventRecord(ev_after_partial, stream)) != cudaSuccess)
+        return err;
+    const size_t smem = (size_t)kFinishWarps * E * sizeof(float2);
+    if (smem + kGroupStaticSmem > 48 * 1024) {
+        err = cudaFuncSetAttribute(route_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess)
+            return err;
+    }
+    const int blocks = (T + kFinishWarps - 1) / kFinishWarps;
+    route_finish_kernel<<<blocks, kFinishWarps * 32, smem, stream>>>(part, nh, bias, T, E, k, has_shared,
+                                                                      shared_weight, ids, w, hdr,
+                                                                      do_group ? 1 : 0, go);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_group(const int32_t *ids, int T, int kps, int n_tot, const GroupOut &go, uint32_t *hdr,
+                         cudaStream_t stream) {
+    group_kernel<<<1, kGroupThreads, 0, stream>>>(ids, T, kps, n_tot, go, hdr);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

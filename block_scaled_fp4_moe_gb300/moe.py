@@ -1,0 +1,233 @@
+"""Python binding of libmoe_fp4.so: the C-ABI calls under the same names.
+
+Argument marshalling only: tensors are passed as device pointers, the stream
+is torch's current stream unless one is given, and a nonzero status raises
+MoEError.  Every computation runs in the library's CUDA kernels; if the
+library is not built or cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import dataclasses
+import os
+import threading
+
+import torch
+
+from . import _build
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED_SHAPE = 2
+MOE_ERR_MISALIGNED = 3
+MOE_ERR_WORKSPACE_TOO_SMALL = 4
+MOE_ERR_CUDA = 5
+MOE_ERR_DEVICE_TIMEOUT = 6
+MOE_ERR_DEVICE_ASSERT = 7
+MOE_ERR_UNSUPPORTED_DEVICE = 8
+DEBUG_FORCE_TIMEOUT = 1
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {moe_status_string(status)} (status {status})")
+
+
+class _Bank(C.Structure):
+    _fields_ = [("w13", C.c_void_p), ("s13", C.c_void_p), ("w2", C.c_void_p), ("s2", C.c_void_p),
+                ("num_experts", C.c_int32), ("has_shared", C.c_int32), ("hidden", C.c_int32), ("inter", C.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> C.CDLL:
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(_build.LIB_PATH):
+                    raise RuntimeError(f"CUDA library {_build.LIB_PATH} is missing: run __graft_entry__.build() "
+                                       "(or python -m block_scaled_fp4_moe_gb300._build)")
+                L = C.CDLL(_build.LIB_PATH)
+                p, i, f, s = C.c_void_p, C.c_int, C.c_float, C.c_size_t
+                sig = {
+                    "moe_workspace_size": (s, [i, i, i, i, i, i]),
+                    "moe_route_topk": (i, [p, p, p, i, i, i, i, i, f, p, p, p, s, p]),
+                    "moe_group_tokens": (i, [p, i, i, i, p, p, p, p, p, p, s, p]),
+                    "moe_expert_ffn_mxfp4": (i, [p, p, p, i, i, C.POINTER(_Bank), p, p, s, p]),
+                    "moe_layer_forward": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, p, p, s, p]),
+                    "moe_layer_forward_hostio": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, s, p]),
+                    "moe_layer_forward_profiled": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, s, p, i, p]),
+                    "moe_check_device_status": (i, [p, p]),
+                    "moe_debug_set_flags": (i, [p, C.c_uint32, p]),
+                    "moe_selftest_decode_e2m1": (i, [p, p, i, p]),
+                    "moe_status_string": (C.c_char_p, [i]),
+                }
+                for name, (res, args) in sig.items():
+                    fn = getattr(L, name)
+                    fn.restype = res
+                    fn.argtypes = args
+                _lib = L
+    return _lib
+
+
+def exported_symbols() -> list[str]:
+    return ["moe_workspace_size", "moe_route_topk", "moe_group_tokens", "moe_expert_ffn_mxfp4",
+            "moe_layer_forward", "moe_layer_forward_hostio", "moe_layer_forward_profiled",
+            "moe_check_device_status", "moe_debug_set_flags", "moe_selftest_decode_e2m1", "moe_status_string"]
+
+
+def moe_status_string(status: int) -> str:
+    return lib().moe_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != MOE_OK:
+        raise MoEError(status, where)
+
+
+def _stream(stream) -> C.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t: torch.Tensor | None, dtype=None, name: str = "") -> C.c_void_p | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name}: expected {dtype}, got {t.dtype}")
+    return C.c_void_p(t.data_ptr())
+
+
+@dataclasses.dataclass
+class MXFP4Bank:
+    """Device-resident packed expert bank (expert E is the shared expert)."""
+    w13: torch.Tensor    # uint8 [E+S, 2I, H/2]
+    s13: torch.Tensor    # uint8 [E+S, 2I, H/32]
+    w2: torch.Tensor     # uint8 [E+S, H, I/2]
+    s2: torch.Tensor     # uint8 [E+S, H, I/32]
+    num_experts: int
+    has_shared: int
+
+    @property
+    def hidden(self) -> int:
+        return self.w2.shape[1]
+
+    @property
+    def inter(self) -> int:
+        return self.w13.shape[1] // 2
+
+    def c_struct(self) -> _Bank:
+        for name in ("w13", "s13", "w2", "s2"):
+            _ptr(getattr(self, name), torch.uint8, name)
+        return _Bank(self.w13.data_ptr(), self.s13.data_ptr(), self.w2.data_ptr(), self.s2.data_ptr(),
+                     self.num_experts, self.has_shared, self.hidden, self.inter)
+
+    @staticmethod
+    def from_host(arrays: dict, num_experts: int, has_shared: int, device="cuda") -> "MXFP4Bank":
+        t = {k: torch.from_numpy(arrays[k]).to(device) for k in ("w13", "s13", "w2", "s2")}
+        return MXFP4Bank(num_experts=num_experts, has_shared=has_shared, **t)
+
+
+def moe_workspace_size(T: int, H: int, I: int, E: int, top_k: int, has_shared: int) -> int:
+    return int(lib().moe_workspace_size(T, H, I, E, top_k, has_shared))
+
+
+def alloc_workspace(T: int, bank: MXFP4Bank, top_k: int, device="cuda") -> torch.Tensor:
+    n = moe_workspace_size(T, bank.hidden, bank.inter, bank.num_experts, top_k, bank.has_shared)
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def moe_route_topk(x, router_w, logit_bias, top_k, has_shared, shared_weight, topk_ids, topk_w, ws, stream=None):
+    T, H = x.shape
+    E = router_w.shape[1]
+    _check(lib().moe_route_topk(_ptr(x, torch.bfloat16, "x"), _ptr(router_w, torch.float32, "router_w"),
+                                _ptr(logit_bias, torch.float32, "logit_bias"), T, H, E, top_k, has_shared,
+                                float(shared_weight), _ptr(topk_ids, torch.int32, "topk_ids"),
+                                _ptr(topk_w, torch.float32, "topk_w"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+                                _stream(stream)), "moe_route_topk")
+
+
+def moe_group_tokens(topk_ids, n_experts_total, expert_offsets, sorted_tok, sorted_slot, active_experts,
+                     num_active, ws, stream=None):
+    T, kps = topk_ids.shape
+    i32 = torch.int32
+    _check(lib().moe_group_tokens(_ptr(topk_ids, i32, "topk_ids"), T, kps, n_experts_total,
+                                  _ptr(expert_offsets, i32, "expert_offsets"), _ptr(sorted_tok, i32, "sorted_tok"),
+                                  _ptr(sorted_slot, i32, "sorted_slot"), _ptr(active_experts, i32, "active"),
+                                  _ptr(num_active, i32, "num_active"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+                                  _stream(stream)), "moe_group_tokens")
+
+
+def moe_expert_ffn_mxfp4(x, topk_ids, topk_w, top_k, bank: MXFP4Bank, y, ws, stream=None):
+    T = x.shape[0]
+    b = bank.c_struct()
+    _check(lib().moe_expert_ffn_mxfp4(_ptr(x, torch.bfloat16, "x"), _ptr(topk_ids, torch.int32, "topk_ids"),
+                                      _ptr(topk_w, torch.float32, "topk_w"), T, top_k, C.byref(b),
+                                      _ptr(y, torch.bfloat16, "y"), _ptr(ws, torch.uint8, "ws"), ws.numel(),
+                                      _stream(stream)), "moe_expert_ffn_mxfp4")
+
+
+def moe_layer_forward(x, router_w, logit_bias, top_k, bank: MXFP4Bank, shared_weight, y, topk_ids_out=None,
+                      topk_w_out=None, ws=None, stream=None):
+    T = x.shape[0]
+    b = bank.c_struct()
+    _check(lib().moe_layer_forward(_ptr(x, torch.bfloat16, "x"), _ptr(router_w, torch.float32, "router_w"),
+                                   _ptr(logit_bias, torch.float32, "logit_bias"), T, top_k, C.byref(b),
+                                   float(shared_weight), _ptr(y, torch.bfloat16, "y"),
+                                   _ptr(topk_ids_out, torch.int32, "topk_ids_out"),
+                                   _ptr(topk_w_out, torch.float32, "topk_w_out"), _ptr(ws, torch.uint8, "ws"),
+                                   ws.numel(), _stream(stream)), "moe_layer_forward")
+
+
+def moe_layer_forward_profiled(x, router_w, logit_bias, top_k, bank: MXFP4Bank, shared_weight, y, ws, events,
+                               stream=None):
+    T = x.shape[0]
+    b = bank.c_struct()
+    ev = (C.c_void_p * 5)(*[e.cuda_event for e in events])
+    _check(lib().moe_layer_forward_profiled(_ptr(x, torch.bfloat16, "x"), _ptr(router_w, torch.float32, "router_w"),
+                                            _ptr(logit_bias, torch.float32, "logit_bias"), T, top_k, C.byref(b),
+                                            float(shared_weight), _ptr(y, torch.bfloat16, "y"),
+                                            _ptr(ws, torch.uint8, "ws"), ws.numel(), ev, 5, _stream(stream)),
+           "moe_layer_forward_profiled")
+
+
+def moe_layer_forward_hostio(x_host, router_w, logit_bias, top_k, bank: MXFP4Bank, shared_weight, y_host, ws,
+                             stream=None):
+    """x_host / y_host: CPU bf16 tensors (pinned for asynchronous copies)."""
+    for name, t in (("x_host", x_host), ("y_host", y_host)):
+        if t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16:
+            raise ValueError(f"{name}: expected a contiguous CPU bf16 tensor")
+    T = x_host.shape[0]
+    b = bank.c_struct()
+    _check(lib().moe_layer_forward_hostio(C.c_void_p(x_host.data_ptr()), _ptr(router_w, torch.float32, "router_w"),
+                                          _ptr(logit_bias, torch.float32, "logit_bias"), T, top_k, C.byref(b),
+                                          float(shared_weight), C.c_void_p(y_host.data_ptr()),
+                                          _ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)),
+           "moe_layer_forward_hostio")
+
+
+def moe_check_device_status(ws, stream=None) -> int:
+    return int(lib().moe_check_device_status(_ptr(ws, torch.uint8, "ws"), _stream(stream)))
+
+
+def moe_debug_set_flags(ws, flags: int, stream=None) -> None:
+    _check(lib().moe_debug_set_flags(_ptr(ws, torch.uint8, "ws"), int(flags), _stream(stream)), "moe_debug_set_flags")
+
+
+def moe_selftest_decode_e2m1(codes, out, stream=None) -> None:
+    _check(lib().moe_selftest_decode_e2m1(_ptr(codes, torch.uint8, "codes"), _ptr(out, torch.int16, "out"),
+                                          codes.numel(), _stream(stream)), "moe_selftest_decode_e2m1")

@@ -1,0 +1,196 @@
+/*
+ * moe_fp4.h -- C ABI of the GB300 (sm_103a) small-T Mixture-of-Experts FFN
+ * layer with MXFP4 expert weights.
+ *
+ * The layer (for each of T tokens with hidden state x[t], a bf16 row of H):
+ *   a1  router logits      l[t,e] = sum_h x[t,h] * Wr[h,e] + b[e]      (e < E)
+ *   a2  top-k + shared     the k largest logits (ties to the lower expert
+ *                          index), ordered by descending logit; softmax over
+ *                          the k kept logits; the shared expert (index E) is
+ *                          appended as slot k with weight shared_weight.
+ *   a3  grouping           (token, slot) pairs sorted by (expert, token).
+ *   a4  gate/up + SiLU*up  h = silu(Wg x) * (Wu x),  silu(z) = z/(1+e^-z)
+ *   a5  down               Y = Wd h
+ *   a6  combine            y[t] = bf16_rn( sum_{s=0..k} w[t,s] * Y_s ),
+ *                          summed in slot order in fp32.
+ *
+ * Where the definition comes from:
+ *   - the shared expert merged into the routed MoE as one more expert that is
+ *     always chosen (top-9 of 161 for GLM, shared expert in the 9th slot),
+ *     with all expert outputs weighted and aggregated: "Optimizing GLM4-MoE
+ *     for production" (blogs.novita.ai), section 1 "Shared experts fusion";
+ *   - experts stored as MXFP4, 32-element blocks sharing one exponent:
+ *     "How Xiaomi reached 1,000 tokens/s on a 1T-parameter model"
+ *     (molayo1419.me), section 2 "MXFP4 with QAT" (element format E2M1 and
+ *     scale format E8M0 of the OCP MX v1.0 specification);
+ *   - top-8 routed experts per token, batch-1 decode being bound by streaming
+ *     each active expert's weights from HBM once: GLM-5.2 on B300
+ *     (d9249.github.io), sections "What it solves" and "1. ... Split-K".
+ *
+ * Data formats (all tensors row-major, all pointers DEVICE pointers owned by
+ * the caller unless stated otherwise):
+ *   x, y            bf16 bit patterns (uint16_t) [T, H]
+ *   router_w        float [H, E]; logit_bias float [E] or NULL
+ *   topk_ids        int32 [T, k+S]  (S = has_shared), routed ids in 0..E-1,
+ *                   slot k = E when S = 1
+ *   topk_w          float [T, k+S]
+ *   bank.w13        uint8 [E+S, 2I, H/2]: rows 0..I-1 gate, I..2I-1 up; two
+ *                   E2M1 codes per byte, element 2j in the low nibble
+ *   bank.s13        uint8 [E+S, 2I, H/32]: E8M0 exponent of each 32-element
+ *                   block along a row, value 2^(s-127) (s = 255 is NaN)
+ *   bank.w2         uint8 [E+S, H, I/2];  bank.s2 uint8 [E+S, H, I/32]
+ *
+ * Shapes supported: H and I multiples of 64, each either a multiple of 512
+ * or at most 2048; 1 <= k <= E <= 4096; k + S <= 32; 0 <= T <= 4096.
+ * Pointers: x, y, bank arrays and the workspace 16-byte aligned; router_w,
+ * logit_bias, topk_ids, topk_w 4-byte aligned.
+ *
+ * Execution: every call enqueues kernels on `stream` and returns without
+ * synchronising (moe_check_device_status and the *_hostio call excepted).
+ * Calls that share one workspace must not overlap on the GPU.
+ *
+ * Errors: calls return a moe_status_t.  Argument errors are found on the host
+ * before anything is enqueued.  MOE_ERR_CUDA reports a failed launch (the
+ * sticky-free CUDA error is cleared).  Errors found on the device (an expert
+ * id out of range in caller-supplied topk_ids, a pipeline wait that did not
+ * complete within its time limit) are recorded in a status word inside the
+ * workspace; the affected outputs are then unspecified, and
+ * moe_check_device_status reports and clears the word.
+ */
+#ifndef MOE_FP4_H
+#define MOE_FP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,        /* NULL pointer, negative size, bad flag */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2,  /* H, I, E, k outside the supported set */
+    MOE_ERR_MISALIGNED = 3,         /* a pointer breaks its alignment rule */
+    MOE_ERR_WORKSPACE_TOO_SMALL = 4,/* ws_bytes < moe_workspace_size(...) */
+    MOE_ERR_CUDA = 5,               /* a CUDA runtime call or launch failed */
+    MOE_ERR_DEVICE_TIMEOUT = 6,     /* a device-side wait ran past its limit */
+    MOE_ERR_DEVICE_ASSERT = 7,      /* device-side input check failed */
+    MOE_ERR_UNSUPPORTED_DEVICE = 8  /* current device is not sm_103 */
+} moe_status_t;
+
+/* Packed MXFP4 expert bank.  Expert index E is the shared expert when
+ * has_shared = 1; it has the same shapes as the routed experts. */
+typedef struct {
+    const uint8_t *w13;   /* [E+S, 2I, H/2]  */
+    const uint8_t *s13;   /* [E+S, 2I, H/32] */
+    const uint8_t *w2;    /* [E+S, H, I/2]   */
+    const uint8_t *s2;    /* [E+S, H, I/32]  */
+    int32_t num_experts;  /* E, routed experts */
+    int32_t has_shared;   /* S, 0 or 1 */
+    int32_t hidden;       /* H */
+    int32_t inter;        /* I */
+} moe_mxfp4_bank_t;
+
+/* Bytes of device workspace the calls below need for these sizes (a caller
+ * may pass a larger one).  The workspace needs no initialisation and carries
+ * no state between calls except the device status word. */
+size_t moe_workspace_size(int T, int H, int I, int E, int top_k, int has_shared);
+
+/*
+ * a1 + a2: router logits, top-k selection, softmax weights and the shared
+ * slot.  Logits are evaluated with error-free products and compensated
+ * summation (Dot2 of Ogita, Rump and Oishi, "Accurate sum and dot product",
+ * 2005), so the selection equals that of the exact logits unless two of them
+ * lie within a few units in the 2^-40 range of each other.
+ * x [T,H] bf16; router_w [H,E]; logit_bias [E] or NULL; outputs topk_ids and
+ * topk_w [T, k+S] (device).  ws: device workspace of
+ * moe_workspace_size(T, H, 64, E, top_k, has_shared) bytes or more.
+ */
+moe_status_t moe_route_topk(const uint16_t *x, const float *router_w, const float *logit_bias,
+                            int T, int H, int E, int top_k, int has_shared, float shared_weight,
+                            int32_t *topk_ids, float *topk_w, void *ws, size_t ws_bytes,
+                            cudaStream_t stream);
+
+/*
+ * a3: token-to-expert grouping of caller-supplied topk_ids [T, k_plus_s].
+ * Outputs (device): expert_offsets [n_experts_total+1] (exclusive prefix of
+ * per-expert counts), sorted_tok and sorted_slot [T*k_plus_s] (pairs sorted
+ * by expert, then token, then slot), active_experts [n_experts_total]
+ * (experts with a nonzero count, ascending; entries past *num_active are
+ * unspecified), num_active [1].  An id outside 0..n_experts_total-1 sets
+ * MOE_ERR_DEVICE_ASSERT in the status word.
+ */
+moe_status_t moe_group_tokens(const int32_t *topk_ids, int T, int k_plus_s, int n_experts_total,
+                              int32_t *expert_offsets, int32_t *sorted_tok, int32_t *sorted_slot,
+                              int32_t *active_experts, int32_t *num_active, void *ws,
+                              size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * a3..a6 for a given routing: grouping, gate/up + SiLU*up, down and the
+ * weighted combine.  topk_ids / topk_w [T, top_k + bank->has_shared] (device;
+ * the shared slot, if any, must name expert E).  bank: host pointer to the
+ * descriptor (its arrays are device memory).  y [T,H] bf16 (device).
+ */
+moe_status_t moe_expert_ffn_mxfp4(const uint16_t *x, const int32_t *topk_ids, const float *topk_w,
+                                  int T, int top_k, const moe_mxfp4_bank_t *bank, uint16_t *y,
+                                  void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * The whole layer a1..a6.  topk_ids_out / topk_w_out [T, top_k+S] are
+ * optional (NULL: kept in the workspace).
+ */
+moe_status_t moe_layer_forward(const uint16_t *x, const float *router_w, const float *logit_bias,
+                               int T, int top_k, const moe_mxfp4_bank_t *bank, float shared_weight,
+                               uint16_t *y, int32_t *topk_ids_out, float *topk_w_out, void *ws,
+                               size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * The whole layer with the activations in HOST memory: copies x_host [T,H]
+ * to the workspace, runs moe_layer_forward, copies y back to y_host [T,H]
+ * and waits for the stream.  x_host / y_host should be pinned
+ * (cudaHostAlloc) for asynchronous copies.  The weights, router and
+ * workspace are device memory as above.
+ */
+moe_status_t moe_layer_forward_hostio(const uint16_t *x_host, const float *router_w,
+                                      const float *logit_bias, int T, int top_k,
+                                      const moe_mxfp4_bank_t *bank, float shared_weight,
+                                      uint16_t *y_host, void *ws, size_t ws_bytes,
+                                      cudaStream_t stream);
+
+/*
+ * Diagnostic form of moe_layer_forward: records events[0] before the first
+ * kernel and events[i] after kernel i (router, top-k/grouping, gate/up,
+ * down/combine), so n_events must be 5.  Events are created by the caller.
+ */
+moe_status_t moe_layer_forward_profiled(const uint16_t *x, const float *router_w,
+                                        const float *logit_bias, int T, int top_k,
+                                        const moe_mxfp4_bank_t *bank, float shared_weight,
+                                        uint16_t *y, void *ws, size_t ws_bytes,
+                                        cudaEvent_t *events, int n_events, cudaStream_t stream);
+
+/* Waits for `stream`, then returns and clears the device status word of the
+ * workspace (MOE_OK when no device-side error was recorded). */
+moe_status_t moe_check_device_status(void *ws, cudaStream_t stream);
+
+/* Test hook: sets debug flags in the workspace header (enqueued on stream).
+ * Bit 0: the next expert-FFN kernels treat their first pipeline wait as timed
+ * out, record MOE_ERR_DEVICE_TIMEOUT and finish without touching y.  Flags
+ * stay set until cleared with flags = 0. */
+moe_status_t moe_debug_set_flags(void *ws, uint32_t flags, cudaStream_t stream);
+
+/* Self-test of the in-register E2M1 decode: out[2i], out[2i+1] (fp16 bit
+ * patterns) are the elements held in the low and high nibble of codes[i].
+ * n bytes; device pointers. */
+moe_status_t moe_selftest_decode_e2m1(const uint8_t *codes, uint16_t *out, int n,
+                                      cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char *moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FP4_H */

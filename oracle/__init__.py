@@ -23,22 +23,18 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lib = None
-_omp = False
 
 
 def build(force: bool = False) -> str:
     """Compile moe_oracle.c into liboracle.so (OpenMP when the compiler has it)."""
-    global _omp
     if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
         return _LIB_PATH
     cc = os.environ.get("CC") or shutil.which("gcc") or shutil.which("cc") or sysconfig.get_config_var("CC")
     base = [cc, "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", _SRC, "-o", _LIB_PATH + ".tmp", "-lm"]
     try:
         subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
-        _omp = True
     except subprocess.CalledProcessError:
         subprocess.run(base, check=True, capture_output=True)
-        _omp = False
     os.replace(_LIB_PATH + ".tmp", _LIB_PATH)
     return _LIB_PATH
 
@@ -67,15 +63,17 @@ def lib():
         L.oracle_expert_token.argtypes = [p, p, p, p, i, i, p, p, p]
         L.oracle_moe_tokens.restype = None
         L.oracle_moe_tokens.argtypes = [p, i, i, i, p, p, p, p, p, p, p, i, p, p, p]
+        L.oracle_num_threads.restype = i
+        L.oracle_num_threads.argtypes = []
         L.oracle_bf16_round_array.restype = None
         L.oracle_bf16_round_array.argtypes = [p, C.c_size_t, p]
         _lib = L
     return _lib
 
 
-def uses_openmp() -> bool:
-    lib()
-    return _omp
+def num_threads() -> int:
+    """Threads the oracle's parallel loops use on this host."""
+    return int(lib().oracle_num_threads())
 
 
 def _ptr(a: np.ndarray | None):

@@ -1,0 +1,105 @@
+"""The C-ABI library loads, exports every symbol include/moe_fp4.h declares,
+and rejects bad arguments on the host before touching a GPU.
+
+These tests run without a GPU: every call below fails its argument checks,
+which come before any CUDA runtime call, so no pointer is dereferenced (the
+"device pointers" here are plain integers that are never used).
+"""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from block_scaled_fp4_moe_gb300 import _build, moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return moe.lib()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "moe_fp4.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_function_is_exported(L):
+    declared = header_functions()
+    assert "moe_layer_forward" in declared and "moe_route_topk" in declared
+    for name in declared:
+        assert hasattr(L, name), name
+    assert sorted(moe.exported_symbols()) == declared
+
+
+def test_status_strings(L):
+    for code in range(9):
+        s = moe.moe_status_string(code)
+        assert s and s != "unknown status"
+    assert moe.moe_status_string(99) == "unknown status"
+
+
+def test_workspace_size(L):
+    a = moe.moe_workspace_size(1, 5120, 1536, 160, 8, 1)
+    b = moe.moe_workspace_size(4, 5120, 1536, 160, 8, 1)
+    assert 0 < a < b
+    assert a % 256 == 0
+    assert moe.moe_workspace_size(1, 5120, 1536, 160, 0, 1) == 0
+    assert moe.moe_workspace_size(-1, 5120, 1536, 160, 8, 1) == 0
+
+
+FAKE = 1 << 40          # 16-byte aligned integer that is never dereferenced
+
+
+def bank(w13=FAKE, s13=FAKE, w2=FAKE, s2=FAKE, E=160, S=1, H=5120, I=1536):
+    return moe._Bank(w13, s13, w2, s2, E, S, H, I)
+
+
+def forward(L, b, T=1, k=8, x=FAKE, wr=FAKE, y=FAKE, ws=FAKE, ws_bytes=1 << 40):
+    return L.moe_layer_forward(C.c_void_p(x), C.c_void_p(wr), None, T, k, C.byref(b), 1.0, C.c_void_p(y), None,
+                               None, C.c_void_p(ws), ws_bytes, None)
+
+
+def test_layer_forward_argument_checks(L):
+    assert forward(L, bank(w13=0)) == moe.MOE_ERR_INVALID_ARG
+    assert forward(L, bank(), x=0) == moe.MOE_ERR_INVALID_ARG
+    assert forward(L, bank(), T=-1) == moe.MOE_ERR_INVALID_ARG
+    assert forward(L, bank(S=2)) == moe.MOE_ERR_INVALID_ARG
+    assert forward(L, bank(), k=0) == moe.MOE_ERR_INVALID_ARG
+    assert forward(L, bank(), k=161) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    assert forward(L, bank(H=5000)) == moe.MOE_ERR_UNSUPPORTED_SHAPE       # not a multiple of 64
+    assert forward(L, bank(H=2112)) == moe.MOE_ERR_UNSUPPORTED_SHAPE       # > 2048 and not a multiple of 512
+    assert forward(L, bank(E=2000)) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    assert forward(L, bank(), T=5000) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    assert forward(L, bank(w2=FAKE + 8)) == moe.MOE_ERR_MISALIGNED
+    assert forward(L, bank(), x=FAKE + 2) == moe.MOE_ERR_MISALIGNED
+    assert forward(L, bank(), ws=FAKE + 16) == moe.MOE_ERR_MISALIGNED
+    need = moe.moe_workspace_size(1, 5120, 1536, 160, 8, 1)
+    assert forward(L, bank(), ws_bytes=need - 1) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_other_entry_points_argument_checks(L):
+    p = C.c_void_p(FAKE)
+    assert L.moe_route_topk(p, p, None, 1, 5120, 160, 9, 1, 1.0, None, p, p, 1 << 30, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_route_topk(p, p, None, 1, 5120, 8, 9, 1, 1.0, p, p, p, 1 << 30, None) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    assert L.moe_route_topk(p, p, None, 1, 5120, 160, 8, 1, 1.0, p, p, p, 16, None) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert L.moe_group_tokens(p, 1, 9, 161, p, p, p, p, None, p, 1 << 20, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_group_tokens(p, 1, 40, 161, p, p, p, p, p, p, 1 << 20, None) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    b = bank()
+    assert L.moe_expert_ffn_mxfp4(p, p, None, 1, 8, C.byref(b), p, p, 1 << 40, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_check_device_status(None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_debug_set_flags(p, 2, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_layer_forward_profiled(p, p, None, 1, 8, C.byref(b), 1.0, p, p, 1 << 40, None, 5, None) == \
+        moe.MOE_ERR_INVALID_ARG
+    assert L.moe_selftest_decode_e2m1(None, p, 4, None) == moe.MOE_ERR_INVALID_ARG
+
+
+def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(moe, "_lib", None)
+    monkeypatch.setattr(_build, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        moe.lib()
