@@ -131,6 +131,16 @@ size_t moe_workspace_size(int T, int H, int I, int E, int top_k, int has_shared)
     return WsLayout::make(T, H, I, E, top_k, has_shared).total;
 }
 
+moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!ws)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(ws, 256))
+        return MOE_ERR_MISALIGNED;
+    if (ws_bytes < kHdrWords * sizeof(uint32_t))
+        return MOE_ERR_WORKSPACE_TOO_SMALL;
+    return from_cuda(cudaMemsetAsync(ws, 0, kHdrWords * sizeof(uint32_t), stream));
+}
+
 moe_status_t moe_route_topk(const uint16_t *x, const float *router_w, const float *logit_bias, int T, int H, int E,
                             int top_k, int has_shared, float shared_weight, int32_t *topk_ids, float *topk_w,
                             void *ws, size_t ws_bytes, cudaStream_t stream) {

@@ -60,6 +60,7 @@ def lib() -> C.CDLL:
                 p, i, f, s = C.c_void_p, C.c_int, C.c_float, C.c_size_t
                 sig = {
                     "moe_workspace_size": (s, [i, i, i, i, i, i]),
+                    "moe_workspace_init": (i, [p, s, p]),
                     "moe_route_topk": (i, [p, p, p, i, i, i, i, i, f, p, p, p, s, p]),
                     "moe_group_tokens": (i, [p, i, i, i, p, p, p, p, p, p, s, p]),
                     "moe_expert_ffn_mxfp4": (i, [p, p, p, i, i, C.POINTER(_Bank), p, p, s, p]),
@@ -80,7 +81,7 @@ def lib() -> C.CDLL:
 
 
 def exported_symbols() -> list[str]:
-    return ["moe_workspace_size", "moe_route_topk", "moe_group_tokens", "moe_expert_ffn_mxfp4",
+    return ["moe_workspace_size", "moe_workspace_init", "moe_route_topk", "moe_group_tokens", "moe_expert_ffn_mxfp4",
             "moe_layer_forward", "moe_layer_forward_hostio", "moe_layer_forward_profiled",
             "moe_check_device_status", "moe_debug_set_flags", "moe_selftest_decode_e2m1", "moe_status_string"]
 
@@ -146,9 +147,17 @@ def moe_workspace_size(T: int, H: int, I: int, E: int, top_k: int, has_shared: i
     return int(lib().moe_workspace_size(T, H, I, E, top_k, has_shared))
 
 
+def moe_workspace_init(ws, stream=None) -> None:
+    _check(lib().moe_workspace_init(_ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)), "moe_workspace_init")
+
+
 def alloc_workspace(T: int, bank: MXFP4Bank, top_k: int, device="cuda") -> torch.Tensor:
+    """Device workspace for T tokens, header initialised."""
     n = moe_workspace_size(T, bank.hidden, bank.inter, bank.num_experts, top_k, bank.has_shared)
-    return torch.empty(n, dtype=torch.uint8, device=device)
+    ws = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+    with torch.cuda.device(ws.device):
+        moe_workspace_init(ws)
+    return ws
 
 
 def moe_route_topk(x, router_w, logit_bias, top_k, has_shared, shared_weight, topk_ids, topk_w, ws, stream=None):

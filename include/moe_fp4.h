@@ -41,7 +41,7 @@
  *   bank.w2         uint8 [E+S, H, I/2];  bank.s2 uint8 [E+S, H, I/32]
  *
  * Shapes supported: H and I multiples of 64, each either a multiple of 512
- * or at most 2048; 1 <= k <= E <= 4096; k + S <= 32; 0 <= T <= 4096.
+ * or at most 2048; 1 <= k <= E <= 1024; k + S <= 32; 0 <= T <= 4096.
  * Pointers: x, y, bank arrays and the workspace 16-byte aligned; router_w,
  * logit_bias, topk_ids, topk_w 4-byte aligned.
  *
@@ -94,16 +94,22 @@ typedef struct {
 } moe_mxfp4_bank_t;
 
 /* Bytes of device workspace the calls below need for these sizes (a caller
- * may pass a larger one).  The workspace needs no initialisation and carries
- * no state between calls except the device status word. */
+ * may pass a larger one).  The workspace carries no state between calls
+ * except its header (the device status word and the debug flags). */
 size_t moe_workspace_size(int T, int H, int I, int E, int top_k, int has_shared);
+
+/* Clears the workspace header (status word and debug flags) on `stream`.
+ * Call it once on a newly allocated workspace before its first use (a
+ * zero-filled workspace needs no call).  ws: device pointer, 256-byte
+ * aligned; ws_bytes at least 256. */
+moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * a1 + a2: router logits, top-k selection, softmax weights and the shared
  * slot.  Logits are evaluated with error-free products and compensated
  * summation (Dot2 of Ogita, Rump and Oishi, "Accurate sum and dot product",
  * 2005), so the selection equals that of the exact logits unless two of them
- * lie within a few units in the 2^-40 range of each other.
+ * differ by less than about 2^-40 times the sum of the |x*w| terms.
  * x [T,H] bf16; router_w [H,E]; logit_bias [E] or NULL; outputs topk_ids and
  * topk_w [T, k+S] (device).  ws: device workspace of
  * moe_workspace_size(T, H, 64, E, top_k, has_shared) bytes or more.

@@ -92,6 +92,9 @@ def test_other_entry_points_argument_checks(L):
     b = bank()
     assert L.moe_expert_ffn_mxfp4(p, p, None, 1, 8, C.byref(b), p, p, 1 << 40, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_check_device_status(None, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_workspace_init(None, 1024, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_workspace_init(C.c_void_p(FAKE + 16), 1024, None) == moe.MOE_ERR_MISALIGNED
+    assert L.moe_workspace_init(p, 64, None) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
     assert L.moe_debug_set_flags(p, 2, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_layer_forward_profiled(p, p, None, 1, 8, C.byref(b), 1.0, p, p, 1 << 40, None, 5, None) == \
         moe.MOE_ERR_INVALID_ARG

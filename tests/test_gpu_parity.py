@@ -96,9 +96,10 @@ def test_route_topk_matches_oracle(name):
     wr, bias = inputs.make_router(cfg)
     ids = torch.empty((cfg.T, cfg.slots), dtype=torch.int32, device="cuda")
     w = torch.empty((cfg.T, cfg.slots), dtype=torch.float32, device="cuda")
-    ws = torch.empty(moe.moe_workspace_size(cfg.T, cfg.H, 64, cfg.E, cfg.top_k, 1), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(moe.moe_workspace_size(cfg.T, cfg.H, 64, cfg.E, cfg.top_k, 1), dtype=torch.uint8, device="cuda")
     moe.moe_route_topk(dev_bf16(x), torch.from_numpy(wr).cuda(), None if bias is None else torch.from_numpy(bias).cuda(),
                        cfg.top_k, 1, 1.0, ids, w, ws)
+    assert moe.moe_check_device_status(ws) == 0
     r = oracle.route(x, wr, bias, cfg.top_k)
     np.testing.assert_array_equal(ids.cpu().numpy(), r["ids"])
     np.testing.assert_allclose(w.cpu().numpy(), r["w"], rtol=2e-6, atol=1e-7)
@@ -155,7 +156,7 @@ def test_zero_tokens_is_a_noop():
     p = random_problem(T=1, H=1024, E=16, k=4, I=512)
     y = torch.empty((0, p.H), dtype=torch.bfloat16, device="cuda")
     x = torch.empty((0, p.H), dtype=torch.bfloat16, device="cuda")
-    ws = torch.empty(moe.moe_workspace_size(0, p.H, 512, 16, 4, 1) + 256, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(moe.moe_workspace_size(0, p.H, 512, 16, 4, 1) + 256, dtype=torch.uint8, device="cuda")
     moe.moe_layer_forward(x, p.wrd, p.bd, 4, p.bank, 1.0, y, ws=ws)
     torch.cuda.synchronize()
 
