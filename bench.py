@@ -384,6 +384,29 @@ def run_mine(args, cfg):
     return 0
 
 
+def run_profile_case(args, cfg):
+    """A short, plain sequence of layer calls for ncu: one weight copy, no
+    graphs, no oracle; the command a committed profile summary names."""
+    import torch
+
+    from block_scaled_fp4_moe_gb300 import _build, moe
+    _build.build()
+    dev = torch.device("cuda", 0)
+    x = inputs.make_x(cfg)
+    wr, bias = inputs.make_router(cfg)
+    bank = moe.MXFP4Bank.from_host(inputs.make_bank(cfg), cfg.E, cfg.has_shared, device=dev)
+    xd = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    wrd = torch.from_numpy(wr).to(dev)
+    bd = None if bias is None else torch.from_numpy(bias).to(dev)
+    ws = moe.alloc_workspace(cfg.T, bank, cfg.top_k, device=dev)
+    y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+    for _ in range(args.profile_calls):
+        moe.moe_layer_forward(xd, wrd, bd, cfg.top_k, bank, 1.0, y, ws=ws)
+    st = moe.moe_check_device_status(ws)
+    print(json.dumps({"profile_case": cfg.name, "calls": args.profile_calls, "status": st}))
+    return 0 if st == 0 else 1
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -392,9 +415,13 @@ def main():
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(inputs.CONFIGS))
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--profile-calls", type=int, default=0,
+                    help="profiling mode: run this many plain layer calls on one weight copy and exit")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)     # never fewer than 3 untimed warm-up steps
     cfg = inputs.CONFIGS[args.config]
+    if args.profile_calls:
+        return run_profile_case(args, cfg)
     if args.impl == "reference":
         return run_reference(args, cfg)
     return run_mine(args, cfg)

@@ -104,19 +104,19 @@ moe_status_t layer_forward(const uint16_t *x, const float *router_w, const float
     int32_t *ids = ids_out ? ids_out : ws_at<int32_t>(ws, L.topk_ids);
     float *w = w_out ? w_out : ws_at<float>(ws, L.topk_w);
     const GroupOut go = group_out_for(ws, L, H);
-    if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess)
+    if (ev && cudaEventRecordWithFlags(ev[0], stream, cudaEventRecordExternal) != cudaSuccess)
         return MOE_ERR_CUDA;
     cudaError_t err = launch_route(x, router_w, logit_bias, T, H, E, top_k, S, shared_weight, ids, w, ws, L,
                                    true, go, stream, ev ? ev[1] : nullptr);
     if (err != cudaSuccess)
         return MOE_ERR_CUDA;
-    if (ev && cudaEventRecord(ev[2], stream) != cudaSuccess)
+    if (ev && cudaEventRecordWithFlags(ev[2], stream, cudaEventRecordExternal) != cudaSuccess)
         return MOE_ERR_CUDA;
     FfnProblem pr{x, bank, w, y, T, top_k + S};
     err = launch_ffn(pr, ws, L, sms, stream, ev ? ev[3] : nullptr);
     if (err != cudaSuccess)
         return MOE_ERR_CUDA;
-    if (ev && cudaEventRecord(ev[4], stream) != cudaSuccess)
+    if (ev && cudaEventRecordWithFlags(ev[4], stream, cudaEventRecordExternal) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
 }

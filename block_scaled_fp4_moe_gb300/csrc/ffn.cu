@@ -596,7 +596,8 @@ cudaError_t launch_ffn(const FfnProblem &pr, void *ws, const WsLayout &L, int nu
     ffn_kernel<kGateUp><<<num_sms, kFfnThreads, g.smem_bytes, stream>>>(g);
     if ((err = cudaGetLastError()) != cudaSuccess)
         return err;
-    if (ev_after_gateup && (err = cudaEventRecord(ev_after_gateup, stream)) != cudaSuccess)
+    if (ev_after_gateup &&
+        (err = cudaEventRecordWithFlags(ev_after_gateup, stream, cudaEventRecordExternal)) != cudaSuccess)
         return err;
     ffn_kernel<kDown><<<num_sms, kFfnThreads, d.smem_bytes, stream>>>(d);
     return cudaGetLastError();

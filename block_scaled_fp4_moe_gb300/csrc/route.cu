@@ -338,7 +338,8 @@ cudaError_t launch_route(const uint16_t *x, const float *wr, const float *bias, 
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess)
         return err;
-    if (ev_after_partial && (err = cudaEventRecord(ev_after_partial, stream)) != cudaSuccess)
+    if (ev_after_partial &&
+        (err = cudaEventRecordWithFlags(ev_after_partial, stream, cudaEventRecordExternal)) != cudaSuccess)
         return err;
     const size_t smem = (size_t)kFinishWarps * E * sizeof(float2);
     if (smem + kGroupStaticSmem > 48 * 1024) {
