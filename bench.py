@@ -238,8 +238,7 @@ def run_mine(args, cfg):
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     n_layers = max(2, math.ceil(2.5 * l2 / b["total"]))
-    banks = [base] + [moe.MXFP4Bank(base.w13.clone(), base.s13.clone(), base.w2.clone(), base.s2.clone(),
-                                    cfg.E, cfg.has_shared) for _ in range(n_layers - 1)]
+    banks = [base] + [base.clone_packed() for _ in range(n_layers - 1)]
     routers = [wrd] + [wrd.clone() for _ in range(n_layers - 1)]
     stream = torch.cuda.Stream(device=dev)
 

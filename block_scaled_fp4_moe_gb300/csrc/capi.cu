@@ -46,17 +46,36 @@ moe_status_t check_routing_shape(int T, int H, int E, int k, int S) {
         return MOE_ERR_INVALID_ARG;
     if (T > kMaxTokens || k > E || E + S > kMaxExperts || k + S > kMaxSlots)
         return MOE_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)T * H >= (1LL << 31))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
     return MOE_OK;
 }
 
-moe_status_t check_bank(const moe_mxfp4_bank_t *b) {
-    if (!b || !b->w13 || !b->s13 || !b->w2 || !b->s2)
+// The kernels address activation rows with 32-bit element offsets.
+moe_status_t check_ffn_extent(int T, int kps, int H, int I) {
+    if ((long long)T * kps * 2 * I >= (1LL << 31) || (long long)T * kps * H >= (1LL << 31))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    return MOE_OK;
+}
+
+moe_status_t check_bank_dims(const moe_mxfp4_bank_t *b) {
+    if (!b)
         return MOE_ERR_INVALID_ARG;
     if (b->hidden <= 0 || b->inter <= 0 || b->num_experts <= 0 || (b->has_shared != 0 && b->has_shared != 1))
         return MOE_ERR_INVALID_ARG;
-    if (!ffn_shape_supported(b->hidden, b->inter) || b->hidden > 65536 || b->inter > 65536)
+    if (!ffn_shape_supported(b->hidden, b->inter) || b->hidden > 65536 || b->num_experts + b->has_shared > kMaxExperts)
         return MOE_ERR_UNSUPPORTED_SHAPE;
-    if (!aligned(b->w13, 16) || !aligned(b->s13, 16) || !aligned(b->w2, 16) || !aligned(b->s2, 16))
+    return MOE_OK;
+}
+
+// The expert-FFN calls read only the repacked bank.
+moe_status_t check_bank(const moe_mxfp4_bank_t *b) {
+    moe_status_t st = check_bank_dims(b);
+    if (st != MOE_OK)
+        return st;
+    if (!b->packed)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(b->packed, 16))
         return MOE_ERR_MISALIGNED;
     return MOE_OK;
 }
@@ -71,7 +90,7 @@ GroupOut group_out_for(void *ws, const WsLayout &L, int H) {
     go.num_active = nullptr;
     go.passes = ws_at<Pass>(ws, L.passes);
     go.counters = ws_at<uint32_t>(ws, L.counters);
-    go.n_counters = H / 16;
+    go.n_counters = 0;
     return go;
 }
 
@@ -83,7 +102,8 @@ moe_status_t layer_forward(const uint16_t *x, const float *router_w, const float
     if (st != MOE_OK)
         return st;
     const int H = bank->hidden, I = bank->inter, E = bank->num_experts, S = bank->has_shared;
-    if ((st = check_routing_shape(T, H, E, top_k, S)) != MOE_OK)
+    if ((st = check_routing_shape(T, H, E, top_k, S)) != MOE_OK ||
+        (st = check_ffn_extent(T, top_k + S, H, I)) != MOE_OK)
         return st;
     if (T == 0)
         return MOE_OK;
@@ -129,6 +149,30 @@ size_t moe_workspace_size(int T, int H, int I, int E, int top_k, int has_shared)
     if (T < 0 || H <= 0 || I <= 0 || E <= 0 || top_k <= 0 || (has_shared != 0 && has_shared != 1))
         return 0;
     return WsLayout::make(T, H, I, E, top_k, has_shared).total;
+}
+
+size_t moe_packed_bank_size(int H, int I, int E, int has_shared) {
+    if (H <= 0 || I <= 0 || E <= 0 || (has_shared != 0 && has_shared != 1) || H % 64 || I % 64)
+        return 0;
+    return packed_layout(H, I, E + has_shared).total;
+}
+
+moe_status_t moe_pack_bank(const moe_mxfp4_bank_t *bank, void *packed, size_t packed_bytes, cudaStream_t stream) {
+    moe_status_t st = check_bank_dims(bank);
+    if (st != MOE_OK)
+        return st;
+    if (!bank->w13 || !bank->s13 || !bank->w2 || !bank->s2 || !packed)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(bank->w13, 16) || !aligned(bank->s13, 16) || !aligned(bank->w2, 16) || !aligned(bank->s2, 16) ||
+        !aligned(packed, 256))
+        return MOE_ERR_MISALIGNED;
+    if (packed_bytes < packed_layout(bank->hidden, bank->inter, bank->num_experts + bank->has_shared).total)
+        return MOE_ERR_WORKSPACE_TOO_SMALL;
+    int sms = 0;
+    if ((st = current_device_sms(&sms)) != MOE_OK)
+        return st;
+    (void)cudaGetLastError();
+    return from_cuda(launch_pack(*bank, static_cast<uint8_t *>(packed), stream));
 }
 
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) {
@@ -208,7 +252,8 @@ moe_status_t moe_expert_ffn_mxfp4(const uint16_t *x, const int32_t *topk_ids, co
     if (st != MOE_OK)
         return st;
     const int H = bank->hidden, I = bank->inter, E = bank->num_experts, S = bank->has_shared;
-    if ((st = check_routing_shape(T, H, E, top_k, S)) != MOE_OK)
+    if ((st = check_routing_shape(T, H, E, top_k, S)) != MOE_OK ||
+        (st = check_ffn_extent(T, top_k + S, H, I)) != MOE_OK)
         return st;
     if (T == 0)
         return MOE_OK;
@@ -227,6 +272,8 @@ moe_status_t moe_expert_ffn_mxfp4(const uint16_t *x, const int32_t *topk_ids, co
         return MOE_OK;
     const GroupOut go = group_out_for(ws, L, H);
     cudaError_t err = launch_group(topk_ids, T, top_k + S, E + S, go, ws_at<uint32_t>(ws, 0), stream);
+    if (err == cudaSuccess)
+        err = launch_x16(x, T, H, ws, L, stream);
     if (err != cudaSuccess)
         return MOE_ERR_CUDA;
     FfnProblem pr{x, bank, topk_w, y, T, top_k + S};
@@ -301,15 +348,6 @@ moe_status_t moe_check_device_status(void *ws, cudaStream_t stream) {
             return MOE_ERR_CUDA;
     }
     return static_cast<moe_status_t>(word);
-}
-
-moe_status_t moe_debug_set_flags(void *ws, uint32_t flags, cudaStream_t stream) {
-    if (!ws || !aligned(ws, 256))
-        return MOE_ERR_INVALID_ARG;
-    if (flags & ~kDebugForceTimeout)
-        return MOE_ERR_INVALID_ARG;
-    set_word_kernel<<<1, 1, 0, stream>>>(ws_at<uint32_t>(ws, 0) + kHdrDebugFlags, flags);
-    return from_cuda(cudaGetLastError());
 }
 
 moe_status_t moe_selftest_decode_e2m1(const uint8_t *codes, uint16_t *out, int n, cudaStream_t stream) {

@@ -5,6 +5,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "moe_fp4.h"
@@ -13,14 +14,15 @@ namespace moe {
 
 // ------------------------------------------------------------------ sizes
 
-constexpr int kRouteRows = 128;       // router rows (of H) per CTA
+constexpr int kRouteRows = 512;       // router rows (of H) per CTA
 constexpr int kRouteCols = 32;        // router experts per CTA (one per lane)
 constexpr int kRouteThreads = 256;
-constexpr int kFinishWarps = 8;       // tokens per top-k CTA (one warp each)
 constexpr int kGroupThreads = 256;
 constexpr int kPassTokens = 8;        // MMA N: tokens (or entries) per pass
-constexpr int kConsumerWarps = 8;
-constexpr int kFfnThreads = 32 * (kConsumerWarps + 1);
+constexpr int kFfnWarps = 8;          // warps per expert-FFN CTA (one CTA per SM)
+constexpr int kFfnDepth = 16;         // 16-byte loads each lane keeps in flight
+constexpr int kTargetWarps = 152 * kFfnWarps;
+enum FfnMode { kFfnGateUp = 0, kFfnDown = 1 };
 constexpr int kMaxExperts = 1025;     // E + S (E <= 1024)
 constexpr int kMaxSlots = 32;         // k + S
 constexpr int kMaxTokens = 4096;
@@ -28,13 +30,12 @@ constexpr int kMaxTokens = 4096;
 // header words of the workspace
 enum HeaderWord : int {
     kHdrStatus = 0,
-    kHdrDebugFlags = 1,
+    kHdrReserved = 1,
     kHdrRouteTicket = 2,
     kHdrNumActive = 3,
     kHdrNumPasses = 4,
     kHdrWords = 64
 };
-constexpr uint32_t kDebugForceTimeout = 1u;
 
 // A pass: up to kPassTokens consecutive entries of one expert's group.
 struct Pass {
@@ -52,16 +53,32 @@ inline int max_passes(int T, int kps, int n_tot) {
     return (int)((entries + kPassTokens - 1) / kPassTokens + na + 1);
 }
 
+// Split of a row block's K/64 steps into K-chunks: the smallest divisor of
+// `steps` that gives a full grid (kTargetWarps warps) about eight units per
+// warp.  A function of the shapes only, so every call agrees on it.
+inline int pick_kchunks(int steps, long long units_no_split) {
+    const long long target = 8LL * kTargetWarps;
+    for (int d = 1; d <= steps; ++d)
+        if (steps % d == 0 && units_no_split * d >= target)
+            return d;
+    return steps;
+}
+
 // Offsets (bytes) of the workspace regions for one problem size.
 struct WsLayout {
-    size_t route_part, topk_ids, topk_w, offsets, sorted_tok, sorted_slot, inv_pos, active,
-        passes, h, ypart, counters, xstage, ystage, total;
+    size_t route_part, topk_ids, topk_w, offsets, sorted_tok, sorted_slot, inv_pos, active, passes, x16, xundo,
+        gpart, h16, hundo, ypart, counters, xstage, ystage, total;
+    int n_kc_gu, n_kc_dn;
 
     static WsLayout make(int T, int H, int I, int E, int k, int S) {
         WsLayout L{};
         const int kps = k + S, n_tot = E + S;
         const size_t entries = (size_t)T * kps;
         const int nh = (H + kRouteRows - 1) / kRouteRows;
+        // largest possible number of (expert, <= 8 tokens) passes, without splits
+        const long long active = entries < (size_t)n_tot ? (long long)entries : n_tot;
+        L.n_kc_gu = pick_kchunks(H / 64, active * (I / 8));
+        L.n_kc_dn = pick_kchunks(I / 64, active * (H / 16));
         size_t o = kHdrWords * sizeof(uint32_t);
         auto take = [&](size_t bytes) { o = align_up(o, 256); size_t r = o; o += bytes; return r; };
         L.route_part = take((size_t)nh * T * E * 2 * sizeof(float));
@@ -73,9 +90,13 @@ struct WsLayout {
         L.inv_pos = take(entries * sizeof(int32_t));
         L.active = take((size_t)n_tot * sizeof(int32_t));
         L.passes = take((size_t)max_passes(T, kps, n_tot) * sizeof(Pass));
-        L.h = take(entries * (size_t)I * sizeof(float));
-        L.ypart = take(entries * (size_t)H * sizeof(float));
-        L.counters = take((size_t)(H / 16) * sizeof(uint32_t));
+        L.x16 = take((size_t)T * H * 2);
+        L.xundo = take((size_t)T * sizeof(float));
+        L.gpart = take((size_t)L.n_kc_gu * entries * 2 * I * sizeof(float));
+        L.h16 = take(entries * 2 * (size_t)I * 2);
+        L.hundo = take(entries * sizeof(float));
+        L.ypart = take((size_t)L.n_kc_dn * entries * H * sizeof(float));
+        L.counters = take(256);
         L.xstage = take((size_t)T * H * sizeof(uint16_t));
         L.ystage = take((size_t)T * H * sizeof(uint16_t));
         L.total = align_up(o, 256);
@@ -197,6 +218,51 @@ __device__ __forceinline__ int f16_shift_for_max(float m) {
     frexpf(m, &e);          // m = f * 2^e, 0.5 <= f < 1
     int s = 15 - e;
     return s < -126 ? -126 : (s > 126 ? 126 : s);
+}
+
+}  // namespace moe
+
+namespace moe {
+
+// One CTA: x[t] (bf16, length H, H % 8 == 0) -> x16[t] = f16(x * 2^s), where
+// s maps the row's largest magnitude into [2^14, 2^15), and xundo[t] = 2^-s.
+__device__ inline void convert_x_row(const uint16_t *__restrict__ x, int t, int H, __half *x16, float *xundo) {
+    __shared__ float red[32];
+    const uint16_t *xr = x + (size_t)t * H;
+    float m = 0.0f;
+    for (int i = threadIdx.x * 8; i < H; i += blockDim.x * 8) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + i));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+    if ((threadIdx.x & 31) == 0)
+        red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    m = red[0];
+    for (int w = 1; w < (int)((blockDim.x + 31) >> 5); ++w)
+        m = fmaxf(m, red[w]);
+    const int sh = f16_shift_for_max(m);
+    const float sc = exp2i(sh);
+    for (int i = threadIdx.x * 8; i < H; i += blockDim.x * 8) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + i));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            __half2 h2 = __floats2half2_rn(__uint_as_float(w[j] << 16) * sc,
+                                           __uint_as_float(w[j] & 0xFFFF0000u) * sc);
+            o[j] = *reinterpret_cast<uint32_t *>(&h2);
+        }
+        *reinterpret_cast<uint4 *>(x16 + (size_t)t * H + i) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (threadIdx.x == 0)
+        xundo[t] = exp2i(-sh);
+    __syncthreads();
 }
 
 }  // namespace moe

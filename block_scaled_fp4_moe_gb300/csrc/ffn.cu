@@ -2,35 +2,28 @@
 //
 // Decode of a few tokens is bound by streaming each active expert's packed
 // weights from HBM once (GLM-5.2 on B300, d9249.github.io, "What it solves":
-// batch-1 decode time is set by how fast the active expert weights stream, and
-// the first GEMMs reached 26% of peak because too few CTAs issued requests).
-// The design here follows from that:
+// the first batch-1 GEMMs reached 26% of peak because too few CTAs issued too
+// few requests).  The kernels here are built around that stream:
 //
-//  * Work is split into units of 16 weight rows of one expert (gate/up: 8 gate
-//    rows + the 8 matching up rows; down: 16 output rows) for one "pass" (up
-//    to 8 tokens routed to that expert).  Units of all active experts are
-//    spread evenly over one persistent CTA per SM, so every SM streams at
-//    T = 1 as well; no split of K across CTAs is needed for parallelism.
-//  * Inside a CTA one producer warp streams each unit's rows with bulk async
-//    copies (cp.async.bulk, completion on mbarriers) into a ring of shared
-//    memory stages; 8 consumer warps split each stage along K.
-//  * Consumers decode E2M1 codes in registers (cvt.rn.f16x2.e2m1x2) into the
-//    A operand of mma.sync m16n8k16 (f16 in, fp32 accumulate); the tokens are
-//    the N = 8 columns.  Each 32-element block is accumulated separately and
-//    then scaled by its E8M0 exponent in fp32, so block scales never enter the
-//    f16 operands and are exact.
-//  * Activations enter as f16: x (bf16) is scaled per token by a power of two
-//    that maps its largest magnitude into [2^14, 2^15), which represents
-//    every bf16 value within 2^28 of that maximum exactly; h (fp32) is split
-//    into two f16 terms, hi + lo, after the same kind of scaling, and both are
-//    multiplied in (the spare MMA work is free at these sizes).  The scale is
-//    undone in fp32 after accumulation.
-//  * The down kernel writes per-entry partial outputs; the CTA that finishes
-//    the last pass of a 16-row block (atomic counter, no spin-waits) sums the
-//    entries of every token in slot order and rounds to bf16.
-//  * Every mbarrier wait is bounded (2 s by %globaltimer); on timeout the
-//    kernel records MOE_ERR_DEVICE_TIMEOUT, stops issuing copies, waits for
-//    its copies in flight and returns.
+//  * The bank is repacked once (pack.cu) so that a warp-wide 16-byte load per
+//    lane returns exactly the mma.sync A-fragments of a 16-row x 64-element
+//    tile; no shared memory staging and no inter-warp synchronisation is
+//    needed.  Each warp keeps D such loads in flight (L1 no-allocate, L2
+//    evict-first), enough for the SM to pull its share of HBM bandwidth.
+//  * Work is cut into units of 16 rows x one K-chunk of one pass (<= 8
+//    tokens of one expert) and spread as contiguous ranges over all warps of
+//    the grid; K-chunks keep every warp busy even at T = 1.  Each unit writes
+//    fp32 partial sums; small kernels sum the partials in a fixed order
+//    (deterministic, no atomics).
+//  * E2M1 codes are decoded in registers (cvt.rn.f16x2.e2m1x2) into f16 A
+//    operands; tokens are the N = 8 columns of mma.sync m16n8k16 with fp32
+//    accumulation.  Each 32-element block is accumulated on its own and then
+//    scaled by its E8M0 exponent in fp32, so block scales are exact and never
+//    enter the f16 operands.
+//  * Activations enter as f16: x is scaled per token by a power of two that
+//    maps its largest magnitude into [2^14, 2^15) (exact for every bf16 value
+//    within 2^28 of the maximum), h is split into hi + lo f16 terms after the
+//    same kind of scaling; scales are undone in fp32.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -41,423 +34,339 @@
 
 namespace moe {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr int kMaxStages = 16;
-constexpr int kSmemLimit = 227 * 1024;
+constexpr int kStepBytes = 544;          // one 16 x 64 tile: 512 B codes + 32 B exponents
+constexpr int kCacheInts = 20;           // per cached pass: expert, begin, count, pad, boff[8], boff_lo[8]
 
-enum FfnMode { kGateUp = 0, kDown = 1 };
-
-struct FfnParams {
-    const uint8_t *codes;     // w13 or w2 of the whole bank
-    const uint8_t *scales;    // s13 or s2
-    int K;                    // reduction length (H for gate/up, I for down)
-    int KC;                   // K per pipeline stage
-    int n_kc;                 // K / KC
-    int scale_block_mode;     // 1: KC == K and scales arrive as two 8-row blocks
-    int rows_per_expert;      // 2I or H
-    int n_rowblocks;          // I/8 or H/16
-    int row_step;             // first row of row block rb is rb * row_step
-    int row_gap;              // rows 8..15 of a unit start at base + 8 + row_gap
-    int n_stages;
-    // shared memory plan (bytes)
-    int codes_stride, scales_off, stage_bytes, win_off, win_stride, red_off, bar_off, meta_off, smem_bytes;
-    // activations
-    int T, window_all;        // gate/up: whole batch held in the window (T <= 8)
-    const uint16_t *x;        // [T, H] bf16
-    const float *hin;         // [entries, I]
-    // routing
-    const int32_t *sorted_tok;
+struct FfnArgs {
+    const uint8_t *packed;       // section of the repacked bank
+    size_t unit_bytes;           // steps * 544
+    int units_per_expert;        // row blocks per expert
+    int steps;                   // K / 64
+    int n_kc;                    // K-chunks per row block (divides steps)
+    const __half *b16;           // gate/up: x16 [T][H]; down: h16 [entries][2][I]
+    int b_row;                   // B row length (H or I)
     const Pass *passes;
-    uint32_t *hdr;
-    // outputs
-    float *hout;              // [entries, I]
-    int I;
-    float *ypart;             // [entries, H]
-    uint32_t *counters;       // [H / 16]
-    const int32_t *inv_pos;   // [T * kps]
-    const float *topk_w;      // [T * kps]
-    int kps;
-    uint16_t *y;              // [T, H]
-    int H;
+    const int32_t *sorted_tok;
+    const uint32_t *hdr;
+    float *part;                 // gate/up: [n_kc][entries][2][I]; down: [n_kc][entries][H]
+    int n_entries;
+    int out_len;                 // I (gate/up) or H (down)
+    const float *bundo;          // down: per-entry factor that undoes the h scaling
 };
 
-// ------------------------------------------------------------ waiting
+__device__ __forceinline__ uint4 ld_stream16(const void *p, uint64_t policy) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(policy));
+    return v;
+}
 
-// Warp-uniform bounded wait for phase `parity` of `bar`.  Returns false when
-// the CTA is aborting (another warp timed out) or this wait timed out.
-__device__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag, uint32_t *hdr,
-                          bool force_timeout) {
-    const int lane = threadIdx.x & 31;
-    if (force_timeout) {
-        if (lane == 0) {
-            record_status(hdr, MOE_ERR_DEVICE_TIMEOUT);
-            *abort_flag = 1;
-        }
-        __syncwarp();
-        return false;
+__device__ __forceinline__ uint32_t ld_stream4(const void *p, uint64_t policy) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(policy));
+    return v;
+}
+
+// Byte k of a word of E8M0 exponents -> 2^(s-127) in fp32 (s = 0: 2^-127).
+__device__ __forceinline__ float e8m0_byte(uint32_t w, int k) {
+    const uint32_t top = __byte_perm(w, 0u, 0x0444u | ((uint32_t)k << 12));   // s << 24
+    return __uint_as_float(max(top >> 1, 0x00400000u));
+}
+
+// Position of one warp in its list of units, one 64-element step at a time.
+struct Cursor {
+    int it;                      // step within the unit's K-chunk
+    int P, rb, kc;
+    const int *pc;               // cached pass record
+    const uint8_t *ptr;          // address of the current step
+};
+
+struct Walker {
+    const FfnArgs &a;
+    const int *cache;
+    int P0, m, upp;
+
+    __device__ Walker(const FfnArgs &args, const int *c, int p0, int m_, int upp_)
+        : a(args), cache(c), P0(p0), m(m_), upp(upp_) {}
+
+    __device__ void seek(Cursor &cu, long long u) const {
+        cu.it = 0;
+        cu.P = (int)(u / upp);
+        const int r = (int)(u % upp);
+        cu.rb = r / a.n_kc;
+        cu.kc = r % a.n_kc;
+        locate(cu);
     }
-    bool ok = mbar_try_wait(bar, parity);
-    if (__all_sync(0xffffffffu, ok))
-        return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 0;; ++it) {
-        if (!ok)
-            ok = mbar_try_wait(bar, parity);
-        if (__all_sync(0xffffffffu, ok))
-            return true;
-        int stop = 0;
-        if (lane == 0) {
-            if (*abort_flag) {
-                stop = 1;
-            } else if ((it & 63u) == 63u && globaltimer_ns() - t0 > kWaitLimitNs) {
-                record_status(hdr, MOE_ERR_DEVICE_TIMEOUT);
-                *abort_flag = 1;
-                stop = 1;
+    __device__ void locate(Cursor &cu) const {
+        cu.pc = cache + (cu.P - P0) * kCacheInts;
+        const int expert = cu.pc[0];
+        cu.ptr = a.packed + ((size_t)expert * a.units_per_expert + cu.rb) * a.unit_bytes +
+                 (size_t)(cu.kc * m) * kStepBytes;
+    }
+    // One step forward; true when a unit was completed (the cursor then
+    // points at the next unit, which may lie past the warp's range).
+    __device__ bool advance(Cursor &cu) const {
+        cu.ptr += kStepBytes;
+        if (++cu.it < m)
+            return false;
+        cu.it = 0;
+        if (++cu.kc == a.n_kc) {
+            cu.kc = 0;
+            if (++cu.rb == a.units_per_expert) {
+                cu.rb = 0;
+                ++cu.P;
             }
         }
-        if (__shfl_sync(0xffffffffu, stop, 0))
-            return false;
+        return true;
     }
-}
+};
 
-// Bounded wait of one thread, used only to drain copies already issued.
-__device__ void drain_wait(uint64_t *bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (globaltimer_ns() - t0 > kWaitLimitNs)
-            return;
-}
-
-// --------------------------------------------------------- activations
-
-__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
-
-__device__ __forceinline__ float warp_max(float m) {
-#pragma unroll
-    for (int d = 16; d > 0; d >>= 1)
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
-    return m;
-}
-
-__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
-    __half2 h = __floats2half2_rn(a, b);
-    return *reinterpret_cast<uint32_t *>(&h);
-}
-
-// One warp: x row (bf16, H) -> f16 window row scaled by 2^shift; stores the
-// factor that undoes the scaling.
-__device__ void load_x_row(const uint16_t *__restrict__ xrow, int H, uint8_t *dst, float *undo) {
-    const int lane = threadIdx.x & 31;
-    float m = 0.0f;
-    for (int i = lane * 8; i < H; i += 256) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xrow + i));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            m = fmaxf(m, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
-    }
-    m = warp_max(m);
-    const int sh = f16_shift_for_max(m);
-    const float sc = exp2i(sh);
-    for (int i = lane * 8; i < H; i += 256) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xrow + i));
-        uint4 o;
-        o.x = pack_half2(bf16_lo(v.x) * sc, bf16_hi(v.x) * sc);
-        o.y = pack_half2(bf16_lo(v.y) * sc, bf16_hi(v.y) * sc);
-        o.z = pack_half2(bf16_lo(v.z) * sc, bf16_hi(v.z) * sc);
-        o.w = pack_half2(bf16_lo(v.w) * sc, bf16_hi(v.w) * sc);
-        *reinterpret_cast<uint4 *>(dst + (size_t)i * 2) = o;
-    }
-    if (lane == 0)
-        *undo = exp2i(-sh);
-}
-
-// One warp: h row (fp32, I) -> f16 hi and lo window rows, h * 2^shift = hi + lo.
-__device__ void load_h_row(const float *__restrict__ hrow, int I, uint8_t *dst_hi, uint8_t *dst_lo,
-                           float *undo) {
-    const int lane = threadIdx.x & 31;
-    float m = 0.0f;
-    for (int i = lane * 8; i < I; i += 256) {
-        const float4 a = __ldg(reinterpret_cast<const float4 *>(hrow + i));
-        const float4 b = __ldg(reinterpret_cast<const float4 *>(hrow + i + 4));
-        m = fmaxf(m, fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(a.z), fabsf(a.w))));
-        m = fmaxf(m, fmaxf(fmaxf(fabsf(b.x), fabsf(b.y)), fmaxf(fabsf(b.z), fabsf(b.w))));
-    }
-    m = warp_max(m);
-    const int sh = f16_shift_for_max(m);
-    const float sc = exp2i(sh);
-    for (int i = lane * 8; i < I; i += 256) {
-        const float4 a = __ldg(reinterpret_cast<const float4 *>(hrow + i));
-        const float4 b = __ldg(reinterpret_cast<const float4 *>(hrow + i + 4));
-        const float v[8] = {a.x * sc, a.y * sc, a.z * sc, a.w * sc, b.x * sc, b.y * sc, b.z * sc, b.w * sc};
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const __half h0 = __float2half_rn(v[2 * j]), h1 = __float2half_rn(v[2 * j + 1]);
-            const float r0 = v[2 * j] - __half2float(h0), r1 = v[2 * j + 1] - __half2float(h1);
-            __half2 hh = __halves2half2(h0, h1);
-            hi[j] = *reinterpret_cast<uint32_t *>(&hh);
-            lo[j] = pack_half2(r0, r1);
-        }
-        *reinterpret_cast<uint4 *>(dst_hi + (size_t)i * 2) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4 *>(dst_lo + (size_t)i * 2) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    }
-    if (lane == 0)
-        *undo = exp2i(-sh);
-}
-
-// ---------------------------------------------------------------- kernel
-
-template <int MODE>
-__global__ void __launch_bounds__(kFfnThreads, 1) ffn_kernel(const __grid_constant__ FfnParams p) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + p.bar_off);
-    uint64_t *empty = full + p.n_stages;
-    int *meta = reinterpret_cast<int *>(smem + p.meta_off);
-    volatile int *abort_flag = meta;
-    volatile int *last_flag = meta + 1;
-    float *win_undo = reinterpret_cast<float *>(meta + 8);   // [8]
-    float *red = reinterpret_cast<float *>(smem + p.red_off);
-    uint8_t *win = smem + p.win_off;
-
+template <int MODE, int NW, int D>
+__global__ void __launch_bounds__(NW * 32, 1) ffn_kernel(const __grid_constant__ FfnArgs a) {
+    extern __shared__ int cache[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint32_t *hdr = p.hdr;
-    const bool force_timeout = (*reinterpret_cast<volatile uint32_t *>(hdr + kHdrDebugFlags)) & kDebugForceTimeout;
-    const int n_passes = *reinterpret_cast<volatile int *>(hdr + kHdrNumPasses);
+    const int g = lane >> 2, c = lane & 3;
+    const int n_passes = *reinterpret_cast<const volatile int *>(a.hdr + kHdrNumPasses);
+    const int m = a.steps / a.n_kc;
+    const int upp = a.units_per_expert * a.n_kc;
+    const long long n_units = (long long)n_passes * upp;
+    const long long W = (long long)gridDim.x * NW;
+    const long long gw0 = (long long)blockIdx.x * NW;
+    const long long U0 = gw0 * n_units / W, U1 = (gw0 + NW) * n_units / W;
+    if (U1 <= U0)
+        return;
+    const int P0 = (int)(U0 / upp), P1 = (int)((U1 - 1) / upp);
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < p.n_stages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+    // Cache the passes this CTA touches: expert, begin, count and the B-row
+    // element offsets of the 8 MMA columns.  A cursor is only located on a
+    // unit inside its warp's range, so it never reads past these records.
+    const int n_cached = P1 - P0 + 1;
+    for (int i = threadIdx.x; i < n_cached * 8; i += blockDim.x) {
+        const int pi = i >> 3, n = i & 7;
+        const Pass ps = a.passes[P0 + pi];
+        int *rec = cache + pi * kCacheInts;
+        if (n == 0) {
+            rec[0] = ps.expert;
+            rec[1] = ps.begin;
+            rec[2] = ps.count;
+            rec[3] = 0;
         }
-        meta[0] = 0;
-        meta[1] = 0;
-        fence_barrier_init();
+        if (MODE == kFfnGateUp) {
+            const int col = n < ps.count ? n : 0;
+            rec[4 + n] = a.sorted_tok[ps.begin + col] * a.b_row;
+            rec[12 + n] = 0;
+        } else if (ps.count <= 4) {      // columns 0..3: hi of entries, 4..7: lo of the same entries
+            const int e = ps.begin + ((n & 3) < ps.count ? (n & 3) : 0);
+            rec[4 + n] = (e * 2 + (n >> 2)) * a.b_row;
+            rec[12 + n] = 0;
+        } else {                         // two MMA sets: hi, then lo
+            const int e = ps.begin + (n < ps.count ? n : 0);
+            rec[4 + n] = (e * 2) * a.b_row;
+            rec[12 + n] = (e * 2 + 1) * a.b_row;
+        }
     }
     __syncthreads();
 
-    const long long n_units = (long long)n_passes * p.n_rowblocks;
-    const long long u0 = n_units * blockIdx.x / gridDim.x;
-    const long long u1 = n_units * (blockIdx.x + 1) / gridDim.x;
-    const int nrb = p.n_rowblocks;
-
-    if (warp == 0) {
-        // ------------------------------------------------------ producer
-        const uint64_t policy = l2_evict_first_policy();
-        const uint32_t stage_tx = 16u * (uint32_t)(p.KC / 2) + 16u * (uint32_t)(p.KC / 32);
-        int stage = 0;
-        uint32_t ph = 0, filled = 0, fill_parity = 0;
-        bool aborted = false;
-        for (long long u = u0; u < u1 && !aborted; ++u) {
-            const int P = (int)(u / nrb), rb = (int)(u % nrb);
-            const Pass ps = p.passes[P];
-            const size_t ebase = (size_t)ps.expert * p.rows_per_expert;
-            const int rbase = rb * p.row_step;
-            for (int kc = 0; kc < p.n_kc; ++kc) {
-                if (!warp_wait(&empty[stage], ph ^ 1u, abort_flag, hdr, false)) {
-                    aborted = true;
-                    break;
-                }
-                if (lane == 0)
-                    mbar_arrive_expect_tx(&full[stage], stage_tx);
-                __syncwarp();
-                uint8_t *sb = smem + (size_t)stage * p.stage_bytes;
-                if (lane < 16) {
-                    const int row = rbase + lane + (lane >= 8 ? p.row_gap : 0);
-                    const uint8_t *src = p.codes + (ebase + row) * (size_t)(p.K / 2) + (size_t)kc * (p.KC / 2);
-                    bulk_g2s(sb + lane * p.codes_stride, src, p.KC / 2, &full[stage], policy);
-                } else if (!p.scale_block_mode) {
-                    const int i = lane - 16;
-                    const int row = rbase + i + (i >= 8 ? p.row_gap : 0);
-                    const uint8_t *src =
-                        p.scales + (ebase + row) * (size_t)(p.K / 32) + (size_t)kc * (p.KC / 32);
-                    bulk_g2s(sb + p.scales_off + i * (p.KC / 32), src, p.KC / 32, &full[stage], policy);
-                } else if (lane < 18) {
-                    const int half = lane - 16;
-                    const int row = rbase + half * (8 + p.row_gap);
-                    const uint8_t *src = p.scales + (ebase + row) * (size_t)(p.K / 32);
-                    bulk_g2s(sb + p.scales_off + half * 8 * (p.K / 32), src, 8 * (p.K / 32), &full[stage],
-                             policy);
-                }
-                filled |= 1u << stage;
-                fill_parity = (fill_parity & ~(1u << stage)) | (ph << stage);
-                if (++stage == p.n_stages) {
-                    stage = 0;
-                    ph ^= 1u;
-                }
-            }
-        }
-        // Never leave the CTA with bulk copies still writing its shared memory:
-        // wait (bounded) for the latest fill of every stage.  On the normal path
-        // these phases have already completed.
-        if (lane == 0)
-            for (int s = 0; s < p.n_stages; ++s)
-                if ((filled >> s) & 1u)
-                    drain_wait(&full[s], (fill_parity >> s) & 1u);
-        __syncwarp();
+    const long long gw = gw0 + warp;
+    const long long ub = gw * n_units / W, ue = (gw + 1) * n_units / W;
+    const long long F = (ue - ub) * m;
+    if (F == 0)
         return;
-    }
 
-    // ---------------------------------------------------------- consumers
-    const int cw = warp - 1, ctid = threadIdx.x - 32;
-    const int g = lane >> 2, c = lane & 3;
-    const int nblk = p.KC / 32;
-    const int sstride = p.KC / 32;
-    constexpr int kBar = 1, kBarThreads = 32 * kConsumerWarps;
+    Walker wk(a, cache, P0, m, upp);
+    const uint64_t policy = l2_evict_first_policy();
+    Cursor pf, cc;
+    wk.seek(pf, ub);
+    wk.seek(cc, ub);
 
-    // clear the activation window once (unused MMA columns read zeros)
-    {
-        const int win_rows = MODE == kGateUp ? 8 : 16;
-        uint4 *wz = reinterpret_cast<uint4 *>(win);
-        const int n16 = win_rows * p.win_stride / 16;
-        for (int i = ctid; i < n16; i += kBarThreads)
-            wz[i] = make_uint4(0, 0, 0, 0);
-    }
-    named_barrier_sync(kBar, kBarThreads);
-    const bool whole_batch = MODE == kGateUp && p.window_all;
-    if (whole_batch) {
-        if (cw < p.T)
-            load_x_row(p.x + (size_t)cw * p.H, p.H, win + cw * p.win_stride, &win_undo[cw]);
-        named_barrier_sync(kBar, kBarThreads);
-    }
-
-    int stage = 0;
-    uint32_t ph = 0;
-    int loaded = -1, buf = 0;
-    bool aborted = false;
-    for (long long u = u0; u < u1; ++u) {
-        const int P = (int)(u / nrb), rb = (int)(u % nrb);
-        const Pass ps = p.passes[P];
-        if (!whole_batch && P != loaded) {
-            named_barrier_sync(kBar, kBarThreads);
-            if (cw < ps.count) {
-                if (MODE == kGateUp) {
-                    const int t = p.sorted_tok[ps.begin + cw];
-                    load_x_row(p.x + (size_t)t * p.H, p.H, win + cw * p.win_stride, &win_undo[cw]);
-                } else {
-                    load_h_row(p.hin + (size_t)(ps.begin + cw) * p.I, p.I, win + cw * p.win_stride,
-                               win + (8 + cw) * p.win_stride, &win_undo[cw]);
-                }
-            }
-            named_barrier_sync(kBar, kBarThreads);
-            loaded = P;
-        }
-        int brow = g;
-        if (whole_batch)
-            brow = g < ps.count ? p.sorted_tok[ps.begin + g] : 0;
-        const uint8_t *bptr = win + brow * p.win_stride + 16 * c;
-
-        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int kc = 0; kc < p.n_kc; ++kc) {
-            if (!aborted)
-                aborted = !warp_wait(&full[stage], ph, abort_flag, hdr, force_timeout);
-            if (!aborted) {
-                const uint8_t *sb = smem + (size_t)stage * p.stage_bytes;
-                const uint8_t *arow = sb + g * p.codes_stride + 4 * c;
-                const uint8_t *srow = sb + p.scales_off + g * sstride;
-                const uint8_t *bk = bptr + (size_t)kc * p.KC * 2;
-#pragma unroll 2
-                for (int kb = cw; kb < nblk; kb += kConsumerWarps) {
-                    const uint32_t alo = *reinterpret_cast<const uint32_t *>(arow + kb * 16);
-                    const uint32_t ahi = *reinterpret_cast<const uint32_t *>(arow + 8 * p.codes_stride + kb * 16);
-                    const float slo = e8m0_to_f32(srow[kb]);
-                    const float shi = e8m0_to_f32(srow[8 * sstride + kb]);
-                    const uint4 b = *reinterpret_cast<const uint4 *>(bk + kb * 64);
-                    uint32_t pa[4], qa[4];
-                    decode_e2m1x8(alo, pa);
-                    decode_e2m1x8(ahi, qa);
-                    const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                    float d[4];
-                    mma_m16n8k16_f16(d, pa[0], qa[0], pa[1], qa[1], b.x, b.y, zero);
-                    mma_m16n8k16_f16(d, pa[2], qa[2], pa[3], qa[3], b.z, b.w, d);
-                    if (MODE == kDown) {
-                        const uint4 bl = *reinterpret_cast<const uint4 *>(bk + 8 * p.win_stride + kb * 64);
-                        mma_m16n8k16_f16(d, pa[0], qa[0], pa[1], qa[1], bl.x, bl.y, d);
-                        mma_m16n8k16_f16(d, pa[2], qa[2], pa[3], qa[3], bl.z, bl.w, d);
-                    }
-                    acc[0] = fmaf(d[0], slo, acc[0]);
-                    acc[1] = fmaf(d[1], slo, acc[1]);
-                    acc[2] = fmaf(d[2], shi, acc[2]);
-                    acc[3] = fmaf(d[3], shi, acc[3]);
-                }
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(&empty[stage]);
-            }
-            if (++stage == p.n_stages) {
-                stage = 0;
-                ph ^= 1u;
-            }
-        }
-
-        // ------------------------------------------------ unit epilogue
-        float *mine = red + buf * (kConsumerWarps * 128) + cw * 128;
-        mine[g * 8 + 2 * c] = acc[0];
-        mine[g * 8 + 2 * c + 1] = acc[1];
-        mine[(g + 8) * 8 + 2 * c] = acc[2];
-        mine[(g + 8) * 8 + 2 * c + 1] = acc[3];
-        named_barrier_sync(kBar, kBarThreads);
-        const float *rr = red + buf * (kConsumerWarps * 128);
-        const bool ok = !*abort_flag;
-        if (MODE == kGateUp) {
-            if (ctid < 64 && ok) {
-                const int jj = ctid >> 3, n = ctid & 7;
-                if (n < ps.count) {
-                    float G = 0.0f, U = 0.0f;
+    uint4 rq[D];
+    uint32_t rs[D];
 #pragma unroll
-                    for (int w = 0; w < kConsumerWarps; ++w) {
-                        G += rr[w * 128 + jj * 8 + n];
-                        U += rr[w * 128 + (jj + 8) * 8 + n];
-                    }
-                    const float undo = whole_batch ? win_undo[p.sorted_tok[ps.begin + n]] : win_undo[n];
-                    G *= undo;
-                    U *= undo;
-                    const float hv = G / (1.0f + expf(-G)) * U;
-                    p.hout[(size_t)(ps.begin + n) * p.I + rb * 8 + jj] = hv;
-                }
-            }
-        } else {
-            if (ctid < 128 && ok) {
-                const int i = ctid >> 3, n = ctid & 7;
-                if (n < ps.count) {
-                    float Y = 0.0f;
+    for (int j = 0; j < D; ++j) {
+        if (j < F) {
+            rq[j] = ld_stream16(pf.ptr + lane * 16, policy);
+            rs[j] = ld_stream4(pf.ptr + 512 + g * 4, policy);
+            if (wk.advance(pf) && j + 1 < F)
+                wk.locate(pf);
+        }
+    }
+
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (long long f0 = 0; f0 < F; f0 += D) {
 #pragma unroll
-                    for (int w = 0; w < kConsumerWarps; ++w)
-                        Y += rr[w * 128 + i * 8 + n];
-                    p.ypart[(size_t)(ps.begin + n) * p.H + rb * 16 + i] = Y * win_undo[n];
+        for (int j = 0; j < D; ++j) {
+            if (f0 + j < F) {
+                const uint4 q = rq[j];
+                const uint32_t s = rs[j];
+                if (f0 + j + D < F) {
+                    rq[j] = ld_stream16(pf.ptr + lane * 16, policy);
+                    rs[j] = ld_stream4(pf.ptr + 512 + g * 4, policy);
+                    if (wk.advance(pf) && f0 + j + D + 1 < F)
+                        wk.locate(pf);
                 }
-            }
-            __threadfence();
-            named_barrier_sync(kBar, kBarThreads);
-            if (ctid == 0) {
-                int last = 0;
-                if (!*abort_flag) {
-                    const unsigned old = atomicAdd(&p.counters[rb], 1u);
-                    last = old == (unsigned)(n_passes - 1);
+                const int *pc = cc.pc;
+                const int k0 = (cc.kc * m + cc.it) * 64 + 8 * c;    // element offset in the B row
+                const bool two_sets = MODE == kFfnDown && pc[2] > 4;
+                const __half *brow = a.b16 + pc[4 + g] + k0;
+                const uint4 b0 = __ldg(reinterpret_cast<const uint4 *>(brow));
+                const uint4 b1 = __ldg(reinterpret_cast<const uint4 *>(brow + 32));
+                uint32_t pa[4], qa[4];
+                const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                float d[4];
+                // block 2q: words q.x (row g), q.y (row g+8)
+                decode_e2m1x8(q.x, pa);
+                decode_e2m1x8(q.y, qa);
+                mma_m16n8k16_f16(d, pa[0], qa[0], pa[1], qa[1], b0.x, b0.y, zero);
+                mma_m16n8k16_f16(d, pa[2], qa[2], pa[3], qa[3], b0.z, b0.w, d);
+                if (two_sets) {
+                    const uint4 l0 = __ldg(reinterpret_cast<const uint4 *>(a.b16 + pc[12 + g] + k0));
+                    mma_m16n8k16_f16(d, pa[0], qa[0], pa[1], qa[1], l0.x, l0.y, d);
+                    mma_m16n8k16_f16(d, pa[2], qa[2], pa[3], qa[3], l0.z, l0.w, d);
                 }
-                *last_flag = last;
-            }
-            named_barrier_sync(kBar, kBarThreads);
-            if (*last_flag) {
-                __threadfence();
-                for (int idx = ctid; idx < p.T * 16; idx += kBarThreads) {
-                    const int t = idx >> 4, i = idx & 15;
-                    float s = 0.0f;
-                    for (int sl = 0; sl < p.kps; ++sl) {
-                        const int pos = __ldcg(p.inv_pos + t * p.kps + sl);
-                        s = fmaf(__ldcg(p.topk_w + t * p.kps + sl),
-                                 __ldcg(p.ypart + (size_t)pos * p.H + rb * 16 + i), s);
+                const float sg0 = e8m0_byte(s, 0), sh0 = e8m0_byte(s, 2);
+                acc[0] = fmaf(d[0], sg0, acc[0]);
+                acc[1] = fmaf(d[1], sg0, acc[1]);
+                acc[2] = fmaf(d[2], sh0, acc[2]);
+                acc[3] = fmaf(d[3], sh0, acc[3]);
+                // block 2q+1: words q.z (row g), q.w (row g+8)
+                decode_e2m1x8(q.z, pa);
+                decode_e2m1x8(q.w, qa);
+                mma_m16n8k16_f16(d, pa[0], qa[0], pa[1], qa[1], b1.x, b1.y, zero);
+                mma_m16n8k16_f16(d, pa[2], qa[2], pa[3], qa[3], b1.z, b1.w, d);
+                if (two_sets) {
+                    const uint4 l1 = __ldg(reinterpret_cast<const uint4 *>(a.b16 + pc[12 + g] + k0 + 32));
+                    mma_m16n8k16_f16(d, pa[0], qa[0], pa[1], qa[1], l1.x, l1.y, d);
+                    mma_m16n8k16_f16(d, pa[2], qa[2], pa[3], qa[3], l1.z, l1.w, d);
+                }
+                const float sg1 = e8m0_byte(s, 1), sh1 = e8m0_byte(s, 3);
+                acc[0] = fmaf(d[0], sg1, acc[0]);
+                acc[1] = fmaf(d[1], sg1, acc[1]);
+                acc[2] = fmaf(d[2], sh1, acc[2]);
+                acc[3] = fmaf(d[3], sh1, acc[3]);
+
+                const int rb = cc.rb, kc = cc.kc;
+                if (wk.advance(cc)) {
+                    // unit finished: write the partial sums of its real columns
+                    const int count = pc[2], begin = pc[1];
+                    if (MODE == kFfnGateUp) {
+                        const int j0 = rb * 8 + g;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int n = 2 * c + h;
+                            if (n < count) {
+                                float *dst =
+                                    a.part + ((size_t)kc * a.n_entries + begin + n) * 2 * a.out_len + j0;
+                                dst[0] = acc[h];                 // gate row j0
+                                dst[a.out_len] = acc[2 + h];     // up row j0
+                            }
+                        }
+                    } else {
+                        float y[4] = {acc[0], acc[1], acc[2], acc[3]};
+                        if (count <= 4) {                        // add lo column n+4 to hi column n
+#pragma unroll
+                            for (int i = 0; i < 4; ++i)
+                                y[i] += __shfl_xor_sync(0xffffffffu, acc[i], 2);
+                        }
+                        const int lim = count <= 4 ? 2 : 4;      // threads c < lim own real columns
+                        if (c < lim) {
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int n = 2 * c + h;
+                                if (n < count) {
+                                    const int e = begin + n;
+                                    const float u = a.bundo[e];
+                                    float *dst = a.part + ((size_t)kc * a.n_entries + e) * a.out_len + rb * 16;
+                                    dst[g] = y[h] * u;
+                                    dst[g + 8] = y[2 + h] * u;
+                                }
+                            }
+                        }
                     }
-                    const __nv_bfloat16 b = __float2bfloat16_rn(s);
-                    p.y[(size_t)t * p.H + rb * 16 + i] = *reinterpret_cast<const uint16_t *>(&b);
+                    acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
+                    if (f0 + j + 1 < F)
+                        wk.locate(cc);
                 }
-                if (ctid == 0)
-                    p.counters[rb] = 0;
             }
         }
-        buf ^= 1;
     }
+}
+
+// --------------------------------------------------------- finalize + combine
+
+// h = silu(G) * U from the K-chunk partials of gate/up (fp32, fixed order),
+// then h * 2^shift = hi + lo in f16 with the shift chosen per entry.
+__global__ void __launch_bounds__(256)
+hfin_kernel(const float *__restrict__ part, int n_kc, int n_entries, int I, const int32_t *__restrict__ sorted_tok,
+            const float *__restrict__ xundo, __half *__restrict__ h16, float *__restrict__ hundo,
+            const uint32_t *__restrict__ hdr) {
+    extern __shared__ float hbuf[];   // [I]
+    __shared__ float wmax[8];
+    const int r = blockIdx.x;
+    if (*reinterpret_cast<const volatile int *>(hdr + kHdrNumPasses) == 0)
+        return;                       // grouping rejected the routing
+    const float xu = xundo[sorted_tok[r]];
+    float mx = 0.0f;
+    for (int j = threadIdx.x; j < I; j += blockDim.x) {
+        float G = 0.0f, U = 0.0f;
+        for (int kc = 0; kc < n_kc; ++kc) {
+            const float *p = part + ((size_t)kc * n_entries + r) * 2 * I + j;
+            G += p[0];
+            U += p[I];
+        }
+        G *= xu;
+        U *= xu;
+        const float h = G / (1.0f + expf(-G)) * U;
+        hbuf[j] = h;
+        mx = fmaxf(mx, fabsf(h));
+    }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+    if ((threadIdx.x & 31) == 0)
+        wmax[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = wmax[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w)
+        mx = fmaxf(mx, wmax[w]);
+    const int sh = f16_shift_for_max(mx);
+    const float sc = exp2i(sh);
+    __half *hi = h16 + (size_t)r * 2 * I, *lo = hi + I;
+    for (int j = threadIdx.x; j < I; j += blockDim.x) {
+        const float v = hbuf[j] * sc;
+        const __half a = __float2half_rn(v);
+        hi[j] = a;
+        lo[j] = __float2half_rn(v - __half2float(a));
+    }
+    if (threadIdx.x == 0)
+        hundo[r] = exp2i(-sh);
+}
+
+// y[t] = bf16_rn( sum over slots s in order of w[t,s] * sum over K-chunks of Y )
+__global__ void __launch_bounds__(256)
+combine_kernel(const float *__restrict__ part, int n_kc, int n_entries, const int32_t *__restrict__ inv_pos,
+               const float *__restrict__ topk_w, int T, int kps, int H, uint16_t *__restrict__ y,
+               const uint32_t *__restrict__ hdr) {
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (long long)T * H || *reinterpret_cast<const volatile int *>(hdr + kHdrNumPasses) == 0)
+        return;                       // out of range, or grouping rejected the routing
+    const int t = (int)(idx / H), n = (int)(idx % H);
+    float s = 0.0f;
+    for (int sl = 0; sl < kps; ++sl) {
+        const int pos = inv_pos[t * kps + sl];
+        if (pos < 0 || pos >= n_entries)
+            return;
+        float v = 0.0f;
+        for (int kc = 0; kc < n_kc; ++kc)
+            v += part[((size_t)kc * n_entries + pos) * H + n];
+        s = fmaf(topk_w[t * kps + sl], v, s);
+    }
+    const __nv_bfloat16 b = __float2bfloat16_rn(s);
+    y[idx] = *reinterpret_cast<const uint16_t *>(&b);
+}
+
+__global__ void __launch_bounds__(256) x16_kernel(const uint16_t *__restrict__ x, int H, __half *x16, float *xundo) {
+    convert_x_row(x, blockIdx.x, H, x16, xundo);
 }
 
 __global__ void selftest_decode_kernel(const uint8_t *codes, uint16_t *out, int n) {
@@ -477,129 +386,97 @@ __global__ void selftest_decode_kernel(const uint8_t *codes, uint16_t *out, int 
 
 // ---------------------------------------------------------------- host side
 
-static bool ok_K(int K) { return K > 0 && K % 64 == 0 && (K % 512 == 0 || K <= 2048); }
-
-bool ffn_shape_supported(int H, int I) { return ok_K(H) && ok_K(I); }
-
-static int pick_kc(int K) {
-    if (K % 512 == 0) {
-        const int cands[] = {2048, 1536, 1024, 512};
-        for (int kc : cands)
-            if (K % kc == 0)
-                return kc;
-    }
-    return K;
-}
-
-// Fills the K / staging / shared-memory fields of p; returns false if no plan fits.
-static bool plan_ffn(FfnParams &p, int K, int win_rows) {
-    p.K = K;
-    p.KC = pick_kc(K);
-    p.n_kc = K / p.KC;
-    p.scale_block_mode = K % 512 != 0;
-    p.codes_stride = p.KC / 2 + 16;
-    p.scales_off = 16 * p.codes_stride;
-    p.stage_bytes = (int)align_up((size_t)p.scales_off + 16 * (p.KC / 32), 128);
-    p.win_stride = 2 * K + 64;
-    const int win_bytes = win_rows * p.win_stride;
-    const int red_bytes = 2 * kConsumerWarps * 128 * (int)sizeof(float);
-    const int fixed = win_bytes + red_bytes + 2 * kMaxStages * 8 + 256 + 128;
-    int n = (72 * 1024 + p.stage_bytes - 1) / p.stage_bytes;
-    n = n < 4 ? 4 : (n > kMaxStages ? kMaxStages : n);
-    while (n > 2 && n * p.stage_bytes + fixed > kSmemLimit)
-        --n;
-    if (n * p.stage_bytes + fixed > kSmemLimit)
-        return false;
-    p.n_stages = n;
-    p.win_off = n * p.stage_bytes;
-    p.red_off = (int)align_up((size_t)p.win_off + win_bytes, 128);
-    p.bar_off = (int)align_up((size_t)p.red_off + red_bytes, 16);
-    p.meta_off = p.bar_off + 2 * n * 8;
-    p.smem_bytes = (int)align_up((size_t)p.meta_off + 256, 128);
-    return true;
-}
-
-static std::atomic<int> g_smem_set[2][64];
+bool ffn_shape_supported(int H, int I) { return H > 0 && I > 0 && H % 64 == 0 && I % 64 == 0 && I <= 16384; }
 
 template <int MODE>
-static cudaError_t ensure_smem(int bytes) {
+static cudaError_t launch_one(const FfnArgs &a, int grid, int cache_passes, cudaStream_t stream) {
+    constexpr int NW = kFfnWarps, D = kFfnDepth;
+    const size_t smem = (size_t)cache_passes * kCacheInts * sizeof(int);
+    static std::atomic<int> set_bytes[64];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
         return err;
-    std::atomic<int> &cur = g_smem_set[MODE][dev & 63];
-    if (cur.load(std::memory_order_relaxed) >= bytes)
-        return cudaSuccess;
-    err = cudaFuncSetAttribute(ffn_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (err == cudaSuccess) {
-        int prev = cur.load();
-        while (prev < bytes && !cur.compare_exchange_weak(prev, bytes)) {
-        }
+    if (smem > 48 * 1024 && set_bytes[dev & 63].load() < (int)smem) {
+        err = cudaFuncSetAttribute(ffn_kernel<MODE, NW, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess)
+            return err;
+        set_bytes[dev & 63].store((int)smem);
     }
-    return err;
+    ffn_kernel<MODE, NW, D><<<grid, NW * 32, smem, stream>>>(a);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_ffn(const FfnProblem &pr, void *ws, const WsLayout &L, int num_sms, cudaStream_t stream,
                        cudaEvent_t ev_after_gateup) {
     const moe_mxfp4_bank_t &b = *pr.bank;
-    const int H = b.hidden, I = b.inter, T = pr.T;
+    const int H = b.hidden, I = b.inter, T = pr.T, kps = pr.kps;
+    const int n_tot = b.num_experts + b.has_shared;
+    const int entries = T * kps;
+    const PackedLayout PL = packed_layout(H, I, n_tot);
     uint32_t *hdr = ws_at<uint32_t>(ws, 0);
+    // passes a CTA can touch: its share of all passes plus both boundary passes
+    const int cache_passes = max_passes(T, kps, n_tot) / num_sms + 3;
+    cudaError_t err;
 
-    FfnParams g{};
-    g.codes = b.w13;
-    g.scales = b.s13;
-    g.rows_per_expert = 2 * I;
-    g.n_rowblocks = I / 8;
-    g.row_step = 8;
-    g.row_gap = I - 8;
-    g.T = T;
-    g.window_all = T <= kPassTokens;
-    g.x = pr.x;
-    g.sorted_tok = ws_at<int32_t>(ws, L.sorted_tok);
+    FfnArgs g{};
+    g.packed = b.packed + PL.gu_offset;
+    g.unit_bytes = PL.gu_unit_bytes;
+    g.units_per_expert = PL.gu_units_per_expert;
+    g.steps = H / 64;
+    g.n_kc = L.n_kc_gu;
+    g.b16 = ws_at<__half>(ws, L.x16);
+    g.b_row = H;
     g.passes = ws_at<Pass>(ws, L.passes);
+    g.sorted_tok = ws_at<int32_t>(ws, L.sorted_tok);
     g.hdr = hdr;
-    g.hout = ws_at<float>(ws, L.h);
-    g.I = I;
-    g.H = H;
-    if (!plan_ffn(g, H, 8))
-        return cudaErrorInvalidConfiguration;
-
-    FfnParams d{};
-    d.codes = b.w2;
-    d.scales = b.s2;
-    d.rows_per_expert = H;
-    d.n_rowblocks = H / 16;
-    d.row_step = 16;
-    d.row_gap = 0;
-    d.T = T;
-    d.window_all = 0;
-    d.hin = ws_at<float>(ws, L.h);
-    d.sorted_tok = g.sorted_tok;
-    d.passes = g.passes;
-    d.hdr = hdr;
-    d.I = I;
-    d.H = H;
-    d.ypart = ws_at<float>(ws, L.ypart);
-    d.counters = ws_at<uint32_t>(ws, L.counters);
-    d.inv_pos = ws_at<int32_t>(ws, L.inv_pos);
-    d.topk_w = pr.topk_w;
-    d.kps = pr.kps;
-    d.y = pr.y;
-    if (!plan_ffn(d, I, 16))
-        return cudaErrorInvalidConfiguration;
-
-    cudaError_t err = ensure_smem<kGateUp>(g.smem_bytes);
-    if (err == cudaSuccess)
-        err = ensure_smem<kDown>(d.smem_bytes);
-    if (err != cudaSuccess)
+    g.part = ws_at<float>(ws, L.gpart);
+    g.n_entries = entries;
+    g.out_len = I;
+    if ((err = launch_one<kFfnGateUp>(g, num_sms, cache_passes, stream)) != cudaSuccess)
         return err;
-    ffn_kernel<kGateUp><<<num_sms, kFfnThreads, g.smem_bytes, stream>>>(g);
+
+    const size_t hsmem = (size_t)I * sizeof(float);
+    if (hsmem > 48 * 1024 &&
+        (err = cudaFuncSetAttribute(hfin_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsmem)) !=
+            cudaSuccess)
+        return err;
+    hfin_kernel<<<entries, 256, hsmem, stream>>>(ws_at<float>(ws, L.gpart), L.n_kc_gu, entries, I,
+                                                 ws_at<int32_t>(ws, L.sorted_tok), ws_at<float>(ws, L.xundo),
+                                                 ws_at<__half>(ws, L.h16), ws_at<float>(ws, L.hundo), hdr);
     if ((err = cudaGetLastError()) != cudaSuccess)
         return err;
     if (ev_after_gateup &&
         (err = cudaEventRecordWithFlags(ev_after_gateup, stream, cudaEventRecordExternal)) != cudaSuccess)
         return err;
-    ffn_kernel<kDown><<<num_sms, kFfnThreads, d.smem_bytes, stream>>>(d);
+
+    FfnArgs d{};
+    d.packed = b.packed + PL.dn_offset;
+    d.unit_bytes = PL.dn_unit_bytes;
+    d.units_per_expert = PL.dn_units_per_expert;
+    d.steps = I / 64;
+    d.n_kc = L.n_kc_dn;
+    d.b16 = ws_at<__half>(ws, L.h16);
+    d.b_row = I;
+    d.passes = g.passes;
+    d.sorted_tok = g.sorted_tok;
+    d.hdr = hdr;
+    d.part = ws_at<float>(ws, L.ypart);
+    d.n_entries = entries;
+    d.out_len = H;
+    d.bundo = ws_at<float>(ws, L.hundo);
+    if ((err = launch_one<kFfnDown>(d, num_sms, cache_passes, stream)) != cudaSuccess)
+        return err;
+
+    const long long outs = (long long)T * H;
+    combine_kernel<<<(unsigned)((outs + 255) / 256), 256, 0, stream>>>(
+        ws_at<float>(ws, L.ypart), L.n_kc_dn, entries, ws_at<int32_t>(ws, L.inv_pos), pr.topk_w, T, kps, H, pr.y,
+        hdr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_x16(const uint16_t *x, int T, int H, void *ws, const WsLayout &L, cudaStream_t stream) {
+    x16_kernel<<<T, 256, 0, stream>>>(x, H, ws_at<__half>(ws, L.x16), ws_at<float>(ws, L.xundo));
     return cudaGetLastError();
 }
 

@@ -21,6 +21,7 @@ struct GroupOut {
 // static shared memory of the grouping code (two int arrays of kMaxExperts)
 constexpr size_t kGroupStaticSmem = 2 * kMaxExperts * sizeof(int) + 64;
 
+// Router logits + top-k (+ grouping and the f16 copy of x when do_group).
 cudaError_t launch_route(const uint16_t *x, const float *wr, const float *bias, int T, int H, int E, int k,
                          int has_shared, float shared_weight, int32_t *ids, float *w, void *ws,
                          const WsLayout &L, bool do_group, const GroupOut &go, cudaStream_t stream,
@@ -41,6 +42,17 @@ struct FfnProblem {
 
 cudaError_t launch_ffn(const FfnProblem &p, void *ws, const WsLayout &L, int num_sms, cudaStream_t stream,
                        cudaEvent_t ev_after_gateup);
+
+// f16 copy of x with per-token power-of-two scaling (x16, xundo regions).
+cudaError_t launch_x16(const uint16_t *x, int T, int H, void *ws, const WsLayout &L, cudaStream_t stream);
+
+// Byte offsets inside a repacked bank (pack.cu).
+struct PackedLayout {
+    size_t gu_unit_bytes, dn_unit_bytes, gu_offset, dn_offset, total;
+    int gu_units_per_expert, dn_units_per_expert;
+};
+PackedLayout packed_layout(int H, int I, int n_experts_total);
+cudaError_t launch_pack(const moe_mxfp4_bank_t &b, uint8_t *out, cudaStream_t stream);
 
 cudaError_t launch_selftest_decode(const uint8_t *codes, uint16_t *out, int n, cudaStream_t stream);
 

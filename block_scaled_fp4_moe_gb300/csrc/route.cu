@@ -224,36 +224,41 @@ group_kernel(const int32_t *ids, int T, int kps, int n_tot, GroupOut o, uint32_t
 
 // ------------------------------------------------------- top-k + shared slot
 
-// One warp per token.  Sums the partial pairs of every expert in a fixed
-// order, adds the bias, selects the top k, writes ids and softmax weights and
-// the shared slot.  With do_group, the last CTA to finish (atomic ticket)
+// One CTA per token.  All threads sum the partial pairs of the experts in a
+// fixed order (loads of one expert issued together) and add the bias; warp 0
+// selects the top k (warp-wide argmax over (hi, lo, -index)), writes ids and
+// softmax weights and the shared slot.  With do_group, the CTA also writes
+// the f16 copy of its token's x, and the last CTA to finish (atomic ticket)
 // groups all tokens.
-__global__ void __launch_bounds__(kFinishWarps * 32)
-route_finish_kernel(const float2 *__restrict__ part, int nh, const float *__restrict__ bias, int T, int E,
-                    int k, int has_shared, float shared_weight, int32_t *__restrict__ ids_out,
-                    float *__restrict__ w_out, uint32_t *__restrict__ hdr, int do_group, GroupOut go) {
-    extern __shared__ float2 lsm[];   // [kFinishWarps][E] normalised (hi, lo) logits
+__global__ void __launch_bounds__(256)
+route_finish_kernel(const float2 *__restrict__ part, int nh, const float *__restrict__ bias, int T, int E, int k,
+                    int has_shared, float shared_weight, int32_t *__restrict__ ids_out, float *__restrict__ w_out,
+                    uint32_t *__restrict__ hdr, int do_group, GroupOut go, const uint16_t *__restrict__ x, int H,
+                    __half *x16, float *xundo) {
+    extern __shared__ float2 L[];   // [E] normalised (hi, lo) logits
     __shared__ int last_cta;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int t = blockIdx.x * kFinishWarps + warp;
+    const int t = blockIdx.x;
     const int kps = k + has_shared;
-    float2 *L = lsm + (size_t)warp * E;
 
-    if (t < T) {
-        for (int e = lane; e < E; e += 32) {
-            float p = 0.0f, s = 0.0f;
-            for (int c = 0; c < nh; ++c) {
-                const float2 v = part[((size_t)c * T + t) * E + e];
-                pair_add(p, s, v.x, v.y);
-            }
-            if (bias)
-                pair_add(p, s, bias[e], 0.0f);
-            float hi, lo;
-            two_sum(p, s, hi, lo);
-            L[e] = make_float2(hi, lo);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        float p = 0.0f, s = 0.0f;
+#pragma unroll 8
+        for (int c = 0; c < nh; ++c) {
+            const float2 v = part[((size_t)c * T + t) * E + e];
+            pair_add(p, s, v.x, v.y);
         }
-        __syncwarp();
-        // k rounds of a warp-wide argmax over (hi, lo, -index)
+        if (bias)
+            pair_add(p, s, bias[e], 0.0f);
+        float hi, lo;
+        two_sum(p, s, hi, lo);
+        L[e] = make_float2(hi, lo);
+    }
+    if (do_group && x16)
+        convert_x_row(x, t, H, x16, xundo);
+    __syncthreads();
+
+    if (warp == 0) {
         const int per_lane = (E + 31) / 32;   // <= 32 (E <= 1024)
         unsigned taken = 0;
         float sel_num = 0.0f, top_hi = 0.0f, top_lo = 0.0f, denom = 0.0f;
@@ -290,8 +295,8 @@ route_finish_kernel(const float2 *__restrict__ part, int nh, const float *__rest
                 top_lo = bl;
             }
             // softmax numerator relative to the largest logit
-            const float d = __fadd_rn(__fsub_rn(bh, top_hi), __fsub_rn(bl, top_lo));
-            const float ex = expf(d);
+            const float dlt = __fadd_rn(__fsub_rn(bh, top_hi), __fsub_rn(bl, top_lo));
+            const float ex = expf(dlt);
             denom += ex;
             if (lane == r) {
                 sel_num = ex;
@@ -312,7 +317,7 @@ route_finish_kernel(const float2 *__restrict__ part, int nh, const float *__rest
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
-        const unsigned ticket = atomicAdd(hdr + kHdrRouteTicket, 1u);
+        const unsigned ticket = gridDim.x == 1 ? 0u : atomicAdd(hdr + kHdrRouteTicket, 1u);
         last_cta = ticket == gridDim.x - 1;
     }
     __syncthreads();
@@ -341,16 +346,11 @@ cudaError_t launch_route(const uint16_t *x, const float *wr, const float *bias, 
     if (ev_after_partial &&
         (err = cudaEventRecordWithFlags(ev_after_partial, stream, cudaEventRecordExternal)) != cudaSuccess)
         return err;
-    const size_t smem = (size_t)kFinishWarps * E * sizeof(float2);
-    if (smem + kGroupStaticSmem > 48 * 1024) {
-        err = cudaFuncSetAttribute(route_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (err != cudaSuccess)
-            return err;
-    }
-    const int blocks = (T + kFinishWarps - 1) / kFinishWarps;
-    route_finish_kernel<<<blocks, kFinishWarps * 32, smem, stream>>>(part, nh, bias, T, E, k, has_shared,
-                                                                      shared_weight, ids, w, hdr,
-                                                                      do_group ? 1 : 0, go);
+    const size_t smem = (size_t)E * sizeof(float2);
+    __half *x16 = do_group ? ws_at<__half>(ws, L.x16) : nullptr;
+    float *xundo = do_group ? ws_at<float>(ws, L.xundo) : nullptr;
+    route_finish_kernel<<<T, 256, smem, stream>>>(part, nh, bias, T, E, k, has_shared, shared_weight, ids, w, hdr,
+                                                  do_group ? 1 : 0, go, x, H, x16, xundo);
     return cudaGetLastError();
 }
 

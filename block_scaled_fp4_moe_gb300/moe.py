@@ -25,7 +25,6 @@ MOE_ERR_CUDA = 5
 MOE_ERR_DEVICE_TIMEOUT = 6
 MOE_ERR_DEVICE_ASSERT = 7
 MOE_ERR_UNSUPPORTED_DEVICE = 8
-DEBUG_FORCE_TIMEOUT = 1
 
 
 class MoEError(RuntimeError):
@@ -36,7 +35,8 @@ class MoEError(RuntimeError):
 
 class _Bank(C.Structure):
     _fields_ = [("w13", C.c_void_p), ("s13", C.c_void_p), ("w2", C.c_void_p), ("s2", C.c_void_p),
-                ("num_experts", C.c_int32), ("has_shared", C.c_int32), ("hidden", C.c_int32), ("inter", C.c_int32)]
+                ("packed", C.c_void_p), ("num_experts", C.c_int32), ("has_shared", C.c_int32),
+                ("hidden", C.c_int32), ("inter", C.c_int32)]
 
 
 _lib = None
@@ -61,6 +61,8 @@ def lib() -> C.CDLL:
                 sig = {
                     "moe_workspace_size": (s, [i, i, i, i, i, i]),
                     "moe_workspace_init": (i, [p, s, p]),
+                    "moe_packed_bank_size": (s, [i, i, i, i]),
+                    "moe_pack_bank": (i, [C.POINTER(_Bank), p, s, p]),
                     "moe_route_topk": (i, [p, p, p, i, i, i, i, i, f, p, p, p, s, p]),
                     "moe_group_tokens": (i, [p, i, i, i, p, p, p, p, p, p, s, p]),
                     "moe_expert_ffn_mxfp4": (i, [p, p, p, i, i, C.POINTER(_Bank), p, p, s, p]),
@@ -68,7 +70,6 @@ def lib() -> C.CDLL:
                     "moe_layer_forward_hostio": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, s, p]),
                     "moe_layer_forward_profiled": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, s, p, i, p]),
                     "moe_check_device_status": (i, [p, p]),
-                    "moe_debug_set_flags": (i, [p, C.c_uint32, p]),
                     "moe_selftest_decode_e2m1": (i, [p, p, i, p]),
                     "moe_status_string": (C.c_char_p, [i]),
                 }
@@ -81,9 +82,9 @@ def lib() -> C.CDLL:
 
 
 def exported_symbols() -> list[str]:
-    return ["moe_workspace_size", "moe_workspace_init", "moe_route_topk", "moe_group_tokens", "moe_expert_ffn_mxfp4",
+    return ["moe_workspace_size", "moe_workspace_init", "moe_packed_bank_size", "moe_pack_bank", "moe_route_topk", "moe_group_tokens", "moe_expert_ffn_mxfp4",
             "moe_layer_forward", "moe_layer_forward_hostio", "moe_layer_forward_profiled",
-            "moe_check_device_status", "moe_debug_set_flags", "moe_selftest_decode_e2m1", "moe_status_string"]
+            "moe_check_device_status", "moe_selftest_decode_e2m1", "moe_status_string"]
 
 
 def moe_status_string(status: int) -> str:
@@ -115,32 +116,63 @@ def _ptr(t: torch.Tensor | None, dtype=None, name: str = "") -> C.c_void_p | Non
 
 @dataclasses.dataclass
 class MXFP4Bank:
-    """Device-resident packed expert bank (expert E is the shared expert)."""
-    w13: torch.Tensor    # uint8 [E+S, 2I, H/2]
-    s13: torch.Tensor    # uint8 [E+S, 2I, H/32]
-    w2: torch.Tensor     # uint8 [E+S, H, I/2]
-    s2: torch.Tensor     # uint8 [E+S, H, I/32]
+    """Device-resident MXFP4 expert bank (expert E is the shared expert).
+
+    ``packed`` is the repacked copy the expert-FFN kernels read; the canonical
+    arrays (w13 [E+S, 2I, H/2], s13 [E+S, 2I, H/32], w2 [E+S, H, I/2],
+    s2 [E+S, H, I/32]) are only needed to build it and may be dropped.
+    """
     num_experts: int
     has_shared: int
-
-    @property
-    def hidden(self) -> int:
-        return self.w2.shape[1]
-
-    @property
-    def inter(self) -> int:
-        return self.w13.shape[1] // 2
+    hidden: int
+    inter: int
+    packed: torch.Tensor | None = None
+    w13: torch.Tensor | None = None
+    s13: torch.Tensor | None = None
+    w2: torch.Tensor | None = None
+    s2: torch.Tensor | None = None
 
     def c_struct(self) -> _Bank:
-        for name in ("w13", "s13", "w2", "s2"):
-            _ptr(getattr(self, name), torch.uint8, name)
-        return _Bank(self.w13.data_ptr(), self.s13.data_ptr(), self.w2.data_ptr(), self.s2.data_ptr(),
-                     self.num_experts, self.has_shared, self.hidden, self.inter)
+        ptrs = []
+        for name in ("w13", "s13", "w2", "s2", "packed"):
+            t = getattr(self, name)
+            ptrs.append(None if t is None else _ptr(t, torch.uint8, name).value)
+        return _Bank(*ptrs, self.num_experts, self.has_shared, self.hidden, self.inter)
+
+    def pack(self, stream=None) -> "MXFP4Bank":
+        """Fill ``packed`` from the canonical arrays (moe_pack_bank)."""
+        n = moe_packed_bank_size(self.hidden, self.inter, self.num_experts, self.has_shared)
+        if self.packed is None or self.packed.numel() < n:
+            self.packed = torch.empty(n, dtype=torch.uint8, device=self.w13.device)
+        b = self.c_struct()
+        _check(lib().moe_pack_bank(C.byref(b), _ptr(self.packed, torch.uint8, "packed"), self.packed.numel(),
+                                   _stream(stream)), "moe_pack_bank")
+        return self
+
+    def drop_canonical(self) -> "MXFP4Bank":
+        self.w13 = self.s13 = self.w2 = self.s2 = None
+        return self
+
+    def clone_packed(self) -> "MXFP4Bank":
+        return MXFP4Bank(self.num_experts, self.has_shared, self.hidden, self.inter, packed=self.packed.clone())
 
     @staticmethod
-    def from_host(arrays: dict, num_experts: int, has_shared: int, device="cuda") -> "MXFP4Bank":
+    def from_host(arrays: dict, num_experts: int, has_shared: int, device="cuda",
+                  keep_canonical: bool = False) -> "MXFP4Bank":
         t = {k: torch.from_numpy(arrays[k]).to(device) for k in ("w13", "s13", "w2", "s2")}
-        return MXFP4Bank(num_experts=num_experts, has_shared=has_shared, **t)
+        hidden = t["w2"].shape[1]
+        inter = t["w13"].shape[1] // 2
+        bank = MXFP4Bank(num_experts, has_shared, hidden, inter, **t)
+        with torch.cuda.device(t["w13"].device):
+            bank.pack()
+        if not keep_canonical:
+            torch.cuda.current_stream(t["w13"].device).synchronize()
+            bank.drop_canonical()
+        return bank
+
+
+def moe_packed_bank_size(H: int, I: int, E: int, has_shared: int) -> int:
+    return int(lib().moe_packed_bank_size(H, I, E, has_shared))
 
 
 def moe_workspace_size(T: int, H: int, I: int, E: int, top_k: int, has_shared: int) -> int:
@@ -231,10 +263,6 @@ def moe_layer_forward_hostio(x_host, router_w, logit_bias, top_k, bank: MXFP4Ban
 
 def moe_check_device_status(ws, stream=None) -> int:
     return int(lib().moe_check_device_status(_ptr(ws, torch.uint8, "ws"), _stream(stream)))
-
-
-def moe_debug_set_flags(ws, flags: int, stream=None) -> None:
-    _check(lib().moe_debug_set_flags(_ptr(ws, torch.uint8, "ws"), int(flags), _stream(stream)), "moe_debug_set_flags")
 
 
 def moe_selftest_decode_e2m1(codes, out, stream=None) -> None:

@@ -37,11 +37,12 @@
  *   bank.w13        uint8 [E+S, 2I, H/2]: rows 0..I-1 gate, I..2I-1 up; two
  *                   E2M1 codes per byte, element 2j in the low nibble
  *   bank.s13        uint8 [E+S, 2I, H/32]: E8M0 exponent of each 32-element
- *                   block along a row, value 2^(s-127) (s = 255 is NaN)
+ *                   block along a row, value 2^(s-127)
  *   bank.w2         uint8 [E+S, H, I/2];  bank.s2 uint8 [E+S, H, I/32]
  *
- * Shapes supported: H and I multiples of 64, each either a multiple of 512
- * or at most 2048; 1 <= k <= E <= 1024; k + S <= 32; 0 <= T <= 4096.
+ * Shapes supported: H and I multiples of 64, I <= 16384, H <= 65536;
+ * 1 <= k <= E <= 1024; k + S <= 32; 0 <= T <= 4096.  E8M0 exponent 255 (NaN
+ * in the MX specification) is not supported.
  * Pointers: x, y, bank arrays and the workspace 16-byte aligned; router_w,
  * logit_bias, topk_ids, topk_w 4-byte aligned.
  *
@@ -51,11 +52,12 @@
  *
  * Errors: calls return a moe_status_t.  Argument errors are found on the host
  * before anything is enqueued.  MOE_ERR_CUDA reports a failed launch (the
- * sticky-free CUDA error is cleared).  Errors found on the device (an expert
- * id out of range in caller-supplied topk_ids, a pipeline wait that did not
- * complete within its time limit) are recorded in a status word inside the
- * workspace; the affected outputs are then unspecified, and
- * moe_check_device_status reports and clears the word.
+ * sticky-free CUDA error is cleared).  An expert id outside 0..E+S-1 in
+ * caller-supplied topk_ids (or produced from non-finite router logits) is
+ * found on the device: it is recorded in a status word inside the workspace,
+ * the remaining kernels of the call do no work and leave y untouched, and
+ * moe_check_device_status reports and clears the word.  No kernel waits on
+ * another CTA or on a flag, so no call can hang the device.
  */
 #ifndef MOE_FP4_H
 #define MOE_FP4_H
@@ -75,30 +77,54 @@ typedef enum {
     MOE_ERR_MISALIGNED = 3,         /* a pointer breaks its alignment rule */
     MOE_ERR_WORKSPACE_TOO_SMALL = 4,/* ws_bytes < moe_workspace_size(...) */
     MOE_ERR_CUDA = 5,               /* a CUDA runtime call or launch failed */
-    MOE_ERR_DEVICE_TIMEOUT = 6,     /* a device-side wait ran past its limit */
+    MOE_ERR_DEVICE_TIMEOUT = 6,     /* reserved: the kernels contain no device-side waits */
     MOE_ERR_DEVICE_ASSERT = 7,      /* device-side input check failed */
     MOE_ERR_UNSUPPORTED_DEVICE = 8  /* current device is not sm_103 */
 } moe_status_t;
 
-/* Packed MXFP4 expert bank.  Expert index E is the shared expert when
- * has_shared = 1; it has the same shapes as the routed experts. */
+/* MXFP4 expert bank.  Expert index E is the shared expert when has_shared =
+ * 1; it has the same shapes as the routed experts.  w13/s13/w2/s2 are the
+ * canonical arrays described above, the input of moe_pack_bank; `packed` is
+ * the repacked copy moe_pack_bank writes, which the expert-FFN calls read (the
+ * canonical pointers may be NULL there). */
 typedef struct {
-    const uint8_t *w13;   /* [E+S, 2I, H/2]  */
-    const uint8_t *s13;   /* [E+S, 2I, H/32] */
-    const uint8_t *w2;    /* [E+S, H, I/2]   */
-    const uint8_t *s2;    /* [E+S, H, I/32]  */
-    int32_t num_experts;  /* E, routed experts */
-    int32_t has_shared;   /* S, 0 or 1 */
-    int32_t hidden;       /* H */
-    int32_t inter;        /* I */
+    const uint8_t *w13;    /* [E+S, 2I, H/2]  */
+    const uint8_t *s13;    /* [E+S, 2I, H/32] */
+    const uint8_t *w2;     /* [E+S, H, I/2]   */
+    const uint8_t *s2;     /* [E+S, H, I/32]  */
+    const uint8_t *packed; /* moe_packed_bank_size(...) bytes, 256-byte aligned */
+    int32_t num_experts;   /* E, routed experts */
+    int32_t has_shared;    /* S, 0 or 1 */
+    int32_t hidden;        /* H */
+    int32_t inter;         /* I */
 } moe_mxfp4_bank_t;
+
+/* Bytes of a repacked bank (same bytes as the canonical arrays, permuted),
+ * 0 for unsupported sizes. */
+size_t moe_packed_bank_size(int H, int I, int E, int has_shared);
+
+/*
+ * Repacks the canonical arrays of `bank` into `packed` (device, 256-byte
+ * aligned, moe_packed_bank_size bytes): a pure permutation of the E2M1 code
+ * bytes and E8M0 exponent bytes into the order in which the expert-FFN
+ * kernels stream them.  For each expert and each block of 16 weight rows
+ * (gate/up: 8 gate rows with their 8 up rows; down: 16 consecutive rows) and
+ * each 64-element step along K, 544 bytes: lane l = 4g + c of a warp finds at
+ * bytes [16l, 16l+16) the 4-byte words c of blocks 2q, 2q of row g+8, 2q+1
+ * of row g and 2q+1 of row g+8; bytes [512 + 4g, 516 + 4g) hold the
+ * exponents of blocks 2q, 2q+1 of row g and of row g+8.  Gate/up section
+ * first, then the down section at a 256-byte aligned offset.  Done once when
+ * the weights are loaded; enqueued on `stream`.
+ */
+moe_status_t moe_pack_bank(const moe_mxfp4_bank_t *bank, void *packed, size_t packed_bytes,
+                           cudaStream_t stream);
 
 /* Bytes of device workspace the calls below need for these sizes (a caller
  * may pass a larger one).  The workspace carries no state between calls
- * except its header (the device status word and the debug flags). */
+ * except its header (the device status word). */
 size_t moe_workspace_size(int T, int H, int I, int E, int top_k, int has_shared);
 
-/* Clears the workspace header (status word and debug flags) on `stream`.
+/* Clears the workspace header (status word) on `stream`.
  * Call it once on a newly allocated workspace before its first use (a
  * zero-filled workspace needs no call).  ws: device pointer, 256-byte
  * aligned; ws_bytes at least 256. */
@@ -179,12 +205,6 @@ moe_status_t moe_layer_forward_profiled(const uint16_t *x, const float *router_w
 /* Waits for `stream`, then returns and clears the device status word of the
  * workspace (MOE_OK when no device-side error was recorded). */
 moe_status_t moe_check_device_status(void *ws, cudaStream_t stream);
-
-/* Test hook: sets debug flags in the workspace header (enqueued on stream).
- * Bit 0: the next expert-FFN kernels treat their first pipeline wait as timed
- * out, record MOE_ERR_DEVICE_TIMEOUT and finish without touching y.  Flags
- * stay set until cleared with flags = 0. */
-moe_status_t moe_debug_set_flags(void *ws, uint32_t flags, cudaStream_t stream);
 
 /* Self-test of the in-register E2M1 decode: out[2i], out[2i+1] (fp16 bit
  * patterns) are the elements held in the low and high nibble of codes[i].

@@ -29,7 +29,7 @@ class Problem:
         self.E, self.top_k, self.has_shared, self.shared_weight = E, top_k, has_shared, shared_weight
         self.T, self.H = x.shape
         self.kps = top_k + has_shared
-        self.bank = moe.MXFP4Bank.from_host(bank_np, E, has_shared)
+        self.bank = moe.MXFP4Bank.from_host(bank_np, E, has_shared)      # uploads and repacks
         self.xd = dev_bf16(x)
         self.wrd = torch.from_numpy(wr).cuda()
         self.bd = None if bias is None else torch.from_numpy(bias).cuda()

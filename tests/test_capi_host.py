@@ -55,8 +55,8 @@ def test_workspace_size(L):
 FAKE = 1 << 40          # 16-byte aligned integer that is never dereferenced
 
 
-def bank(w13=FAKE, s13=FAKE, w2=FAKE, s2=FAKE, E=160, S=1, H=5120, I=1536):
-    return moe._Bank(w13, s13, w2, s2, E, S, H, I)
+def bank(w13=FAKE, s13=FAKE, w2=FAKE, s2=FAKE, packed=FAKE, E=160, S=1, H=5120, I=1536):
+    return moe._Bank(w13, s13, w2, s2, packed, E, S, H, I)
 
 
 def forward(L, b, T=1, k=8, x=FAKE, wr=FAKE, y=FAKE, ws=FAKE, ws_bytes=1 << 40):
@@ -65,21 +65,36 @@ def forward(L, b, T=1, k=8, x=FAKE, wr=FAKE, y=FAKE, ws=FAKE, ws_bytes=1 << 40):
 
 
 def test_layer_forward_argument_checks(L):
-    assert forward(L, bank(w13=0)) == moe.MOE_ERR_INVALID_ARG
+    assert forward(L, bank(packed=0)) == moe.MOE_ERR_INVALID_ARG
     assert forward(L, bank(), x=0) == moe.MOE_ERR_INVALID_ARG
     assert forward(L, bank(), T=-1) == moe.MOE_ERR_INVALID_ARG
     assert forward(L, bank(S=2)) == moe.MOE_ERR_INVALID_ARG
     assert forward(L, bank(), k=0) == moe.MOE_ERR_INVALID_ARG
     assert forward(L, bank(), k=161) == moe.MOE_ERR_UNSUPPORTED_SHAPE
     assert forward(L, bank(H=5000)) == moe.MOE_ERR_UNSUPPORTED_SHAPE       # not a multiple of 64
-    assert forward(L, bank(H=2112)) == moe.MOE_ERR_UNSUPPORTED_SHAPE       # > 2048 and not a multiple of 512
+    assert forward(L, bank(I=16448)) == moe.MOE_ERR_UNSUPPORTED_SHAPE      # I > 16384
     assert forward(L, bank(E=2000)) == moe.MOE_ERR_UNSUPPORTED_SHAPE
     assert forward(L, bank(), T=5000) == moe.MOE_ERR_UNSUPPORTED_SHAPE
-    assert forward(L, bank(w2=FAKE + 8)) == moe.MOE_ERR_MISALIGNED
+    assert forward(L, bank(packed=FAKE + 8)) == moe.MOE_ERR_MISALIGNED
     assert forward(L, bank(), x=FAKE + 2) == moe.MOE_ERR_MISALIGNED
     assert forward(L, bank(), ws=FAKE + 16) == moe.MOE_ERR_MISALIGNED
     need = moe.moe_workspace_size(1, 5120, 1536, 160, 8, 1)
     assert forward(L, bank(), ws_bytes=need - 1) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_pack_argument_checks(L):
+    p = C.c_void_p(FAKE)
+    assert moe.moe_packed_bank_size(5120, 1536, 160, 1) == moe.moe_packed_bank_size(5120, 1536, 160, 1)
+    n = moe.moe_packed_bank_size(5120, 1536, 160, 1)
+    # same bytes as the canonical arrays (a permutation), up to section alignment
+    canon = 161 * (2 * 1536 * 5120 // 2 + 2 * 1536 * 5120 // 32 + 5120 * 1536 // 2 + 5120 * 1536 // 32)
+    assert canon <= n < canon + 512
+    assert moe.moe_packed_bank_size(5000, 1536, 160, 1) == 0
+    assert L.moe_pack_bank(C.byref(bank(w13=0)), p, n, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_pack_bank(C.byref(bank()), None, n, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_pack_bank(C.byref(bank(s2=FAKE + 4)), p, n, None) == moe.MOE_ERR_MISALIGNED
+    assert L.moe_pack_bank(C.byref(bank()), C.c_void_p(FAKE + 16), n, None) == moe.MOE_ERR_MISALIGNED
+    assert L.moe_pack_bank(C.byref(bank()), p, n - 1, None) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
 
 
 def test_other_entry_points_argument_checks(L):
@@ -95,7 +110,6 @@ def test_other_entry_points_argument_checks(L):
     assert L.moe_workspace_init(None, 1024, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_workspace_init(C.c_void_p(FAKE + 16), 1024, None) == moe.MOE_ERR_MISALIGNED
     assert L.moe_workspace_init(p, 64, None) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
-    assert L.moe_debug_set_flags(p, 2, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_layer_forward_profiled(p, p, None, 1, 8, C.byref(b), 1.0, p, p, 1 << 40, None, 5, None) == \
         moe.MOE_ERR_INVALID_ARG
     assert L.moe_selftest_decode_e2m1(None, p, 4, None) == moe.MOE_ERR_INVALID_ARG

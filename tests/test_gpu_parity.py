@@ -62,6 +62,61 @@ def test_e2m1_decode_lane_layout():
     np.testing.assert_array_equal(got, want)
 
 
+def numpy_pack_section(codes, scales, row_of):
+    """The documented repacked order of one section, written with numpy:
+    codes [n, R, K/2], scales [n, R, K/32]; row_of(rb, m) -> canonical row."""
+    n, R, Kh = codes.shape
+    K = 2 * Kh
+    out = []
+    for e in range(n):
+        for rb in range(row_of.n_rb):
+            rows = [row_of(rb, m) for m in range(16)]
+            for q in range(K // 64):
+                step = np.zeros(544, dtype=np.uint8)
+                for lane in range(32):
+                    g, c = lane // 4, lane % 4
+                    words = []
+                    for blk, m in ((2 * q, g), (2 * q, g + 8), (2 * q + 1, g), (2 * q + 1, g + 8)):
+                        words.append(codes[e, rows[m], 16 * blk + 4 * c: 16 * blk + 4 * c + 4])
+                    step[16 * lane: 16 * lane + 16] = np.concatenate(words)
+                for g in range(8):
+                    step[512 + 4 * g: 516 + 4 * g] = [scales[e, rows[g], 2 * q], scales[e, rows[g], 2 * q + 1],
+                                                      scales[e, rows[g + 8], 2 * q], scales[e, rows[g + 8], 2 * q + 1]]
+                out.append(step)
+    return np.concatenate(out)
+
+
+class _Rows:
+    def __init__(self, n_rb, fn):
+        self.n_rb, self.fn = n_rb, fn
+
+    def __call__(self, rb, m):
+        return self.fn(rb, m)
+
+
+def test_pack_bank_matches_documented_layout():
+    rng = np.random.default_rng(4)
+    E, S, H, I = 3, 1, 128, 192
+    n = E + S
+    arrs = {"w13": rng.integers(0, 256, (n, 2 * I, H // 2), dtype=np.uint8),
+            "s13": rng.integers(0, 256, (n, 2 * I, H // 32), dtype=np.uint8),
+            "w2": rng.integers(0, 256, (n, H, I // 2), dtype=np.uint8),
+            "s2": rng.integers(0, 256, (n, H, I // 32), dtype=np.uint8)}
+    bank = moe.MXFP4Bank.from_host(arrs, E, S, keep_canonical=True)
+    torch.cuda.synchronize()
+    got = bank.packed.cpu().numpy()
+    gu = numpy_pack_section(arrs["w13"], arrs["s13"], _Rows(I // 8, lambda rb, m: 8 * rb + m if m < 8 else I + 8 * rb + m - 8))
+    dn = numpy_pack_section(arrs["w2"], arrs["s2"], _Rows(H // 16, lambda rb, m: 16 * rb + m))
+    dn_off = (len(gu) + 255) // 256 * 256
+    assert got.size == moe.moe_packed_bank_size(H, I, E, S)
+    np.testing.assert_array_equal(got[:len(gu)], gu)
+    np.testing.assert_array_equal(got[dn_off:dn_off + len(dn)], dn)
+    # a permutation: the multiset of bytes is the canonical one
+    canon = np.concatenate([a.ravel() for a in arrs.values()])
+    np.testing.assert_array_equal(np.bincount(canon, minlength=256),
+                                  np.bincount(np.concatenate([gu, dn]), minlength=256))
+
+
 def test_group_tokens_matches_oracle():
     rng = np.random.default_rng(2)
     for T, k, E in [(1, 8, 160), (37, 4, 20), (256, 8, 160), (3, 2, 1024)]:
@@ -161,18 +216,20 @@ def test_zero_tokens_is_a_noop():
     torch.cuda.synchronize()
 
 
-def test_forced_timeout_is_reported_and_recoverable():
+def test_bad_routing_is_reported_and_leaves_outputs_untouched():
+    """A caller-supplied expert id out of range is caught on the device: the
+    status word reports it, y keeps its contents, and the next call works."""
     p = random_problem(T=3, H=1024, E=16, k=4, I=512, seed=9)
     ws = p.workspace()
-    moe.moe_debug_set_flags(ws, moe.DEBUG_FORCE_TIMEOUT)
+    ids = torch.tensor([[0, 1, 2, 3, 16], [4, 5, 6, 99, 16], [1, 2, 3, 4, 16]], dtype=torch.int32, device="cuda")
+    w = torch.full((3, 5), 0.25, dtype=torch.float32, device="cuda")
     y = torch.full((p.T, p.H), 7.0, dtype=torch.bfloat16, device="cuda")
-    moe.moe_layer_forward(p.xd, p.wrd, p.bd, p.top_k, p.bank, 1.0, y, ws=ws)
-    assert moe.moe_check_device_status(ws) == moe.MOE_ERR_DEVICE_TIMEOUT
-    assert torch.all(y == 7.0)                            # outputs untouched
-    moe.moe_debug_set_flags(ws, 0)
+    moe.moe_expert_ffn_mxfp4(p.xd, ids, w, p.top_k, p.bank, y, ws)
+    assert moe.moe_check_device_status(ws) == moe.MOE_ERR_DEVICE_ASSERT
+    assert torch.all(y == 7.0)
     out = p.forward(ws)                                    # the context is still usable
     r = p.oracle_route()
-    check_output(out["y"], p.oracle_tokens(r, np.arange(p.T))["y"], "after timeout")
+    check_output(out["y"], p.oracle_tokens(r, np.arange(p.T))["y"], "after a rejected call")
 
 
 # ------------------------------------------------------ full-size workloads
