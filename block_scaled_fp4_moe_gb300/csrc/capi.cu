@@ -89,6 +89,7 @@ GroupOut group_out_for(void *ws, const WsLayout &L, int H) {
     go.active = ws_at<int32_t>(ws, L.active);
     go.num_active = nullptr;
     go.passes = ws_at<Pass>(ws, L.passes);
+    go.passes4 = ws_at<Pass>(ws, L.passes4);
     go.counters = ws_at<uint32_t>(ws, L.counters);
     go.n_counters = 0;
     return go;
@@ -124,19 +125,19 @@ moe_status_t layer_forward(const uint16_t *x, const float *router_w, const float
     int32_t *ids = ids_out ? ids_out : ws_at<int32_t>(ws, L.topk_ids);
     float *w = w_out ? w_out : ws_at<float>(ws, L.topk_w);
     const GroupOut go = group_out_for(ws, L, H);
-    if (ev && cudaEventRecordWithFlags(ev[0], stream, cudaEventRecordExternal) != cudaSuccess)
+    if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess)
         return MOE_ERR_CUDA;
     cudaError_t err = launch_route(x, router_w, logit_bias, T, H, E, top_k, S, shared_weight, ids, w, ws, L,
                                    true, go, stream, ev ? ev[1] : nullptr);
     if (err != cudaSuccess)
         return MOE_ERR_CUDA;
-    if (ev && cudaEventRecordWithFlags(ev[2], stream, cudaEventRecordExternal) != cudaSuccess)
+    if (ev && cudaEventRecord(ev[2], stream) != cudaSuccess)
         return MOE_ERR_CUDA;
     FfnProblem pr{x, bank, w, y, T, top_k + S};
     err = launch_ffn(pr, ws, L, sms, stream, ev ? ev[3] : nullptr);
     if (err != cudaSuccess)
         return MOE_ERR_CUDA;
-    if (ev && cudaEventRecordWithFlags(ev[4], stream, cudaEventRecordExternal) != cudaSuccess)
+    if (ev && cudaEventRecord(ev[4], stream) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;
 }
@@ -240,6 +241,7 @@ moe_status_t moe_group_tokens(const int32_t *topk_ids, int T, int k_plus_s, int 
     go.active = active_experts;
     go.num_active = num_active;
     go.passes = nullptr;
+    go.passes4 = nullptr;
     go.counters = nullptr;
     go.n_counters = 0;
     return from_cuda(launch_group(topk_ids, T, k_plus_s, n_experts_total, go, ws_at<uint32_t>(ws, 0), stream));

@@ -18,10 +18,13 @@ constexpr int kRouteRows = 512;       // router rows (of H) per CTA
 constexpr int kRouteCols = 32;        // router experts per CTA (one per lane)
 constexpr int kRouteThreads = 256;
 constexpr int kGroupThreads = 256;
-constexpr int kPassTokens = 8;        // MMA N: tokens (or entries) per pass
+constexpr int kPassTokens = 8;        // MMA N: tokens per gate/up pass
+constexpr int kPassEntries = 4;       // entries per down pass (hi and lo f16 terms fill N = 8)
 constexpr int kFfnWarps = 8;          // warps per expert-FFN CTA (one CTA per SM)
-constexpr int kFfnDepth = 16;         // 16-byte loads each lane keeps in flight
+constexpr int kFfnBatch = 8;          // steps per batch of loads (two batches in flight)
 constexpr int kTargetWarps = 152 * kFfnWarps;
+constexpr int kMaxKChunks = 8;        // K-chunks per row block (partial sums per output)
+constexpr int kWindowBudget = 200 * 1024;   // shared memory for an FFN CTA's activation window
 enum FfnMode { kFfnGateUp = 0, kFfnDown = 1 };
 constexpr int kMaxExperts = 1025;     // E + S (E <= 1024)
 constexpr int kMaxSlots = 32;         // k + S
@@ -34,6 +37,7 @@ enum HeaderWord : int {
     kHdrRouteTicket = 2,
     kHdrNumActive = 3,
     kHdrNumPasses = 4,
+    kHdrNumPasses4 = 5,
     kHdrWords = 64
 };
 
@@ -47,10 +51,11 @@ struct Pass {
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-inline int max_passes(int T, int kps, int n_tot) {
+// Upper bound on the passes of capacity `cap` over T*kps entries.
+inline int max_passes(int T, int kps, int n_tot, int cap = kPassTokens) {
     long entries = (long)T * kps;
     long na = entries < n_tot ? entries : n_tot;
-    return (int)((entries + kPassTokens - 1) / kPassTokens + na + 1);
+    return (int)((entries + cap - 1) / cap + na + 1);
 }
 
 // Split of a row block's K/64 steps into K-chunks: the smallest divisor of
@@ -58,15 +63,20 @@ inline int max_passes(int T, int kps, int n_tot) {
 // warp.  A function of the shapes only, so every call agrees on it.
 inline int pick_kchunks(int steps, long long units_no_split) {
     const long long target = 8LL * kTargetWarps;
-    for (int d = 1; d <= steps; ++d)
-        if (steps % d == 0 && units_no_split * d >= target)
-            return d;
-    return steps;
+    int best = 1;
+    for (int d = 1; d <= steps && d <= kMaxKChunks; ++d) {
+        if (steps % d)
+            continue;
+        best = d;
+        if (units_no_split * d >= target)
+            break;
+    }
+    return best;
 }
 
 // Offsets (bytes) of the workspace regions for one problem size.
 struct WsLayout {
-    size_t route_part, topk_ids, topk_w, offsets, sorted_tok, sorted_slot, inv_pos, active, passes, x16, xundo,
+    size_t route_part, topk_ids, topk_w, offsets, sorted_tok, sorted_slot, inv_pos, active, passes, passes4, x16, xundo,
         gpart, h16, hundo, ypart, counters, xstage, ystage, total;
     int n_kc_gu, n_kc_dn;
 
@@ -90,6 +100,7 @@ struct WsLayout {
         L.inv_pos = take(entries * sizeof(int32_t));
         L.active = take((size_t)n_tot * sizeof(int32_t));
         L.passes = take((size_t)max_passes(T, kps, n_tot) * sizeof(Pass));
+        L.passes4 = take((size_t)max_passes(T, kps, n_tot, kPassEntries) * sizeof(Pass));
         L.x16 = take((size_t)T * H * 2);
         L.xundo = take((size_t)T * sizeof(float));
         L.gpart = take((size_t)L.n_kc_gu * entries * 2 * I * sizeof(float));
@@ -229,10 +240,24 @@ namespace moe {
 __device__ inline void convert_x_row(const uint16_t *__restrict__ x, int t, int H, __half *x16, float *xundo) {
     __shared__ float red[32];
     const uint16_t *xr = x + (size_t)t * H;
+    const int nchunk = H / 8;
+    uint4 keep[4];                        // rows of up to 4 * 8 * blockDim elements stay in registers
     float m = 0.0f;
-    for (int i = threadIdx.x * 8; i < H; i += blockDim.x * 8) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + i));
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int i = threadIdx.x + q * blockDim.x;
+        keep[q] = i < nchunk ? __ldg(reinterpret_cast<const uint4 *>(xr) + i) : make_uint4(0, 0, 0, 0);
+    }
+    for (int i = threadIdx.x + 4 * blockDim.x; i < nchunk; i += blockDim.x) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr) + i);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t w[4] = {keep[q].x, keep[q].y, keep[q].z, keep[q].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
             m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w[j] << 16)), fabsf(__uint_as_float(w[j] & 0xFFFF0000u))));
@@ -248,18 +273,24 @@ __device__ inline void convert_x_row(const uint16_t *__restrict__ x, int t, int 
         m = fmaxf(m, red[w]);
     const int sh = f16_shift_for_max(m);
     const float sc = exp2i(sh);
-    for (int i = threadIdx.x * 8; i < H; i += blockDim.x * 8) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + i));
+    auto convert = [&](uint4 v, int i) {
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         uint32_t o[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            __half2 h2 = __floats2half2_rn(__uint_as_float(w[j] << 16) * sc,
-                                           __uint_as_float(w[j] & 0xFFFF0000u) * sc);
+            __half2 h2 = __floats2half2_rn(__uint_as_float(w[j] << 16) * sc, __uint_as_float(w[j] & 0xFFFF0000u) * sc);
             o[j] = *reinterpret_cast<uint32_t *>(&h2);
         }
-        *reinterpret_cast<uint4 *>(x16 + (size_t)t * H + i) = make_uint4(o[0], o[1], o[2], o[3]);
+        reinterpret_cast<uint4 *>(x16 + (size_t)t * H)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    };
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int i = threadIdx.x + q * blockDim.x;
+        if (i < nchunk)
+            convert(keep[q], i);
     }
+    for (int i = threadIdx.x + 4 * blockDim.x; i < nchunk; i += blockDim.x)
+        convert(__ldg(reinterpret_cast<const uint4 *>(xr) + i), i);
     if (threadIdx.x == 0)
         xundo[t] = exp2i(-sh);
     __syncthreads();

@@ -45,13 +45,17 @@ struct FfnArgs {
     int n_kc;                    // K-chunks per row block (divides steps)
     const __half *b16;           // gate/up: x16 [T][H]; down: h16 [entries][2][I]
     int b_row;                   // B row length (H or I)
-    const Pass *passes;
+    const Pass *passes;          // gate/up: passes of <= 8 tokens; down: of <= 4 entries
+    int passes_word;             // header word holding the number of passes
     const int32_t *sorted_tok;
     const uint32_t *hdr;
     float *part;                 // gate/up: [n_kc][entries][2][I]; down: [n_kc][entries][H]
     int n_entries;
     int out_len;                 // I (gate/up) or H (down)
     const float *bundo;          // down: per-entry factor that undoes the h scaling
+    int T;                       // tokens (gate/up window rows)
+    int win_offset;              // byte offset of the activation window in shared memory
+    int win_row;                 // window row stride in elements (B row length + 32)
 };
 
 __device__ __forceinline__ uint4 ld_stream16(const void *p, uint64_t policy) {
@@ -122,12 +126,55 @@ struct Walker {
     }
 };
 
-template <int MODE, int NW, int D>
+// A unit is finished: write the partial sums of its real columns.  Kept out
+// of line so that the unrolled streaming loop stays small in the I-cache.
+template <int MODE>
+__device__ __noinline__ void write_partials(const FfnArgs *a, float a0, float a1, float a2, float a3, int begin,
+                                            int count, int rb, int kc, int lane) {
+    const int g = lane >> 2, c = lane & 3;
+    const float acc[4] = {a0, a1, a2, a3};
+    if (MODE == kFfnGateUp) {
+        const int j0 = rb * 8 + g;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int n = 2 * c + h;
+            if (n < count) {
+                float *dst = a->part + ((size_t)kc * a->n_entries + begin + n) * 2 * a->out_len + j0;
+                dst[0] = acc[h];                 // gate row j0
+                dst[a->out_len] = acc[2 + h];    // up row j0
+            }
+        }
+    } else {
+        float y[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)              // add the lo column n+4 to the hi column n
+            y[i] = acc[i] + __shfl_xor_sync(0xffffffffu, acc[i], 2);
+        if (c < 2) {                             // threads c < 2 own columns 0..3
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int n = 2 * c + h;
+                if (n < count) {
+                    const int e = begin + n;
+                    const float u = a->bundo[e];
+                    float *dst = a->part + ((size_t)kc * a->n_entries + e) * a->out_len + rb * 16;
+                    dst[g] = y[h] * u;
+                    dst[g + 8] = y[2 + h] * u;
+                }
+            }
+        }
+    }
+}
+
+// WIN: the B operand (x16 rows for gate/up, h16 hi/lo rows for down) of the
+// CTA's passes is first copied to a shared-memory window; otherwise it is read
+// from global memory.
+template <int MODE, int NW, int S, bool WIN>
 __global__ void __launch_bounds__(NW * 32, 1) ffn_kernel(const __grid_constant__ FfnArgs a) {
-    extern __shared__ int cache[];
+    extern __shared__ __align__(16) int cache[];
+    __half *win = reinterpret_cast<__half *>(reinterpret_cast<uint8_t *>(cache) + a.win_offset);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
-    const int n_passes = *reinterpret_cast<const volatile int *>(a.hdr + kHdrNumPasses);
+    const int n_passes = *reinterpret_cast<const volatile int *>(a.hdr + a.passes_word);
     const int m = a.steps / a.n_kc;
     const int upp = a.units_per_expert * a.n_kc;
     const long long n_units = (long long)n_passes * upp;
@@ -142,6 +189,11 @@ __global__ void __launch_bounds__(NW * 32, 1) ffn_kernel(const __grid_constant__
     // element offsets of the 8 MMA columns.  A cursor is only located on a
     // unit inside its warp's range, so it never reads past these records.
     const int n_cached = P1 - P0 + 1;
+    // first entry of the CTA's passes: the window of the down kernel starts
+    // there (B offsets are window-relative with WIN, absolute without)
+    const int e_lo = MODE == kFfnDown ? a.passes[P0].begin : 0;
+    const int e_base = WIN ? e_lo : 0;
+    const int brow = WIN ? a.win_row : a.b_row;        // element stride of B rows
     for (int i = threadIdx.x; i < n_cached * 8; i += blockDim.x) {
         const int pi = i >> 3, n = i & 7;
         const Pass ps = a.passes[P0 + pi];
@@ -154,16 +206,12 @@ __global__ void __launch_bounds__(NW * 32, 1) ffn_kernel(const __grid_constant__
         }
         if (MODE == kFfnGateUp) {
             const int col = n < ps.count ? n : 0;
-            rec[4 + n] = a.sorted_tok[ps.begin + col] * a.b_row;
+            rec[4 + n] = a.sorted_tok[ps.begin + col] * brow;
             rec[12 + n] = 0;
-        } else if (ps.count <= 4) {      // columns 0..3: hi of entries, 4..7: lo of the same entries
-            const int e = ps.begin + ((n & 3) < ps.count ? (n & 3) : 0);
-            rec[4 + n] = (e * 2 + (n >> 2)) * a.b_row;
+        } else {                         // columns 0..3: hi of entries, 4..7: lo of the same entries
+            const int e = ps.begin + ((n & 3) < ps.count ? (n & 3) : 0) - e_base;
+            rec[4 + n] = (e * 2 + (n >> 2)) * brow;
             rec[12 + n] = 0;
-        } else {                         // two MMA sets: hi, then lo
-            const int e = ps.begin + (n < ps.count ? n : 0);
-            rec[4 + n] = (e * 2) * a.b_row;
-            rec[12 + n] = (e * 2 + 1) * a.b_row;
         }
     }
     __syncthreads();
@@ -171,154 +219,185 @@ __global__ void __launch_bounds__(NW * 32, 1) ffn_kernel(const __grid_constant__
     const long long gw = gw0 + warp;
     const long long ub = gw * n_units / W, ue = (gw + 1) * n_units / W;
     const long long F = (ue - ub) * m;
-    if (F == 0)
-        return;
 
     Walker wk(a, cache, P0, m, upp);
     const uint64_t policy = l2_evict_first_policy();
     Cursor pf, cc;
-    wk.seek(pf, ub);
-    wk.seek(cc, ub);
-
-    uint4 rq[D];
-    uint32_t rs[D];
+    // Two buffers of S steps.  The loads of one batch are issued together and
+    // consumed together after the next batch has been issued: the hardware
+    // tracks outstanding loads with a handful of scoreboards per warp, so a
+    // finer-grained ring (one step consumed per step issued) serialises.
+    uint4 bq[2][S];
+    uint32_t bs[2][S];
+    auto issue = [&](uint4 (&q)[S], uint32_t (&sc)[S], long long f_first) {
 #pragma unroll
-    for (int j = 0; j < D; ++j) {
-        if (j < F) {
-            rq[j] = ld_stream16(pf.ptr + lane * 16, policy);
-            rs[j] = ld_stream4(pf.ptr + 512 + g * 4, policy);
-            if (wk.advance(pf) && j + 1 < F)
-                wk.locate(pf);
+        for (int j = 0; j < S; ++j) {
+            if (f_first + j < F) {
+                q[j] = ld_stream16(pf.ptr + lane * 16, policy);
+                sc[j] = ld_stream4(pf.ptr + 512 + g * 4, policy);
+                if (wk.advance(pf) && f_first + j + 1 < F)
+                    wk.locate(pf);
+            }
         }
+    };
+    if (F > 0) {
+        wk.seek(pf, ub);
+        wk.seek(cc, ub);
+        issue(bq[0], bs[0], 0);          // start the weight stream before the window copy
     }
+    if (WIN) {
+        // copy the B rows of the CTA's passes into the window (16-byte chunks)
+        const int row_len = a.b_row;                      // elements per B row in global memory
+        const int chunks_per_row = row_len / 8;
+        int rows;
+        const __half *src;
+        if (MODE == kFfnGateUp) {
+            rows = a.T;
+            src = a.b16;
+        } else {
+            const int *last = cache + (n_cached - 1) * kCacheInts;
+            rows = 2 * (last[1] + last[2] - e_lo);
+            src = a.b16 + (size_t)e_lo * 2 * row_len;
+        }
+        const int total = rows * chunks_per_row;
+        for (int i0 = threadIdx.x; i0 < total; i0 += 4 * blockDim.x) {
+            uint4 v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int i = i0 + q * blockDim.x;
+                if (i < total) {
+                    const int r = i / chunks_per_row, k8 = i - r * chunks_per_row;
+                    v[q] = __ldg(reinterpret_cast<const uint4 *>(src + (size_t)r * row_len) + k8);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int i = i0 + q * blockDim.x;
+                if (i < total) {
+                    const int r = i / chunks_per_row, k8 = i - r * chunks_per_row;
+                    *reinterpret_cast<uint4 *>(win + (size_t)r * a.win_row + k8 * 8) = v[q];
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (F == 0)
+        return;
+    const __half *bbase = WIN ? win : a.b16;
+    auto load_b = [](const __half *p) -> uint4 {
+        if (WIN)
+            return *reinterpret_cast<const uint4 *>(p);
+        return __ldg(reinterpret_cast<const uint4 *>(p));
+    };
 
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (long long f0 = 0; f0 < F; f0 += D) {
+    // one 16 x 64 step: decode, two (or four) MMAs per 32-element block, block scales
+    auto step = [&](const uint4 q, const uint32_t s) {
+        const int *pc = cc.pc;
+        const int k0 = (cc.kc * m + cc.it) * 64 + 8 * c;    // element offset in the B row
+        const __half *bp = bbase + pc[4 + g] + k0;
+        const uint4 b0 = load_b(bp);
+        const uint4 b1 = load_b(bp + 32);
+        uint32_t pa[4], qa[4];
+        const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        float d[4];
+        // block 2q: words q.x (row g), q.y (row g+8)
+        decode_e2m1x8(q.x, pa);
+        decode_e2m1x8(q.y, qa);
+        mma_m16n8k16_f16(d, pa[0], qa[0], pa[1], qa[1], b0.x, b0.y, zero);
+        mma_m16n8k16_f16(d, pa[2], qa[2], pa[3], qa[3], b0.z, b0.w, d);
+        const float sg0 = e8m0_byte(s, 0), sh0 = e8m0_byte(s, 2);
+        acc[0] = fmaf(d[0], sg0, acc[0]);
+        acc[1] = fmaf(d[1], sg0, acc[1]);
+        acc[2] = fmaf(d[2], sh0, acc[2]);
+        acc[3] = fmaf(d[3], sh0, acc[3]);
+        // block 2q+1: words q.z (row g), q.w (row g+8)
+        decode_e2m1x8(q.z, pa);
+        decode_e2m1x8(q.w, qa);
+        mma_m16n8k16_f16(d, pa[0], qa[0], pa[1], qa[1], b1.x, b1.y, zero);
+        mma_m16n8k16_f16(d, pa[2], qa[2], pa[3], qa[3], b1.z, b1.w, d);
+        const float sg1 = e8m0_byte(s, 1), sh1 = e8m0_byte(s, 3);
+        acc[0] = fmaf(d[0], sg1, acc[0]);
+        acc[1] = fmaf(d[1], sg1, acc[1]);
+        acc[2] = fmaf(d[2], sh1, acc[2]);
+        acc[3] = fmaf(d[3], sh1, acc[3]);
+        return pc;
+    };
+    auto consume = [&](const uint4 (&q)[S], const uint32_t (&sc)[S], long long f_first) {
 #pragma unroll
-        for (int j = 0; j < D; ++j) {
-            if (f0 + j < F) {
-                const uint4 q = rq[j];
-                const uint32_t s = rs[j];
-                if (f0 + j + D < F) {
-                    rq[j] = ld_stream16(pf.ptr + lane * 16, policy);
-                    rs[j] = ld_stream4(pf.ptr + 512 + g * 4, policy);
-                    if (wk.advance(pf) && f0 + j + D + 1 < F)
-                        wk.locate(pf);
-                }
-                const int *pc = cc.pc;
-                const int k0 = (cc.kc * m + cc.it) * 64 + 8 * c;    // element offset in the B row
-                const bool two_sets = MODE == kFfnDown && pc[2] > 4;
-                const __half *brow = a.b16 + pc[4 + g] + k0;
-                const uint4 b0 = __ldg(reinterpret_cast<const uint4 *>(brow));
-                const uint4 b1 = __ldg(reinterpret_cast<const uint4 *>(brow + 32));
-                uint32_t pa[4], qa[4];
-                const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                float d[4];
-                // block 2q: words q.x (row g), q.y (row g+8)
-                decode_e2m1x8(q.x, pa);
-                decode_e2m1x8(q.y, qa);
-                mma_m16n8k16_f16(d, pa[0], qa[0], pa[1], qa[1], b0.x, b0.y, zero);
-                mma_m16n8k16_f16(d, pa[2], qa[2], pa[3], qa[3], b0.z, b0.w, d);
-                if (two_sets) {
-                    const uint4 l0 = __ldg(reinterpret_cast<const uint4 *>(a.b16 + pc[12 + g] + k0));
-                    mma_m16n8k16_f16(d, pa[0], qa[0], pa[1], qa[1], l0.x, l0.y, d);
-                    mma_m16n8k16_f16(d, pa[2], qa[2], pa[3], qa[3], l0.z, l0.w, d);
-                }
-                const float sg0 = e8m0_byte(s, 0), sh0 = e8m0_byte(s, 2);
-                acc[0] = fmaf(d[0], sg0, acc[0]);
-                acc[1] = fmaf(d[1], sg0, acc[1]);
-                acc[2] = fmaf(d[2], sh0, acc[2]);
-                acc[3] = fmaf(d[3], sh0, acc[3]);
-                // block 2q+1: words q.z (row g), q.w (row g+8)
-                decode_e2m1x8(q.z, pa);
-                decode_e2m1x8(q.w, qa);
-                mma_m16n8k16_f16(d, pa[0], qa[0], pa[1], qa[1], b1.x, b1.y, zero);
-                mma_m16n8k16_f16(d, pa[2], qa[2], pa[3], qa[3], b1.z, b1.w, d);
-                if (two_sets) {
-                    const uint4 l1 = __ldg(reinterpret_cast<const uint4 *>(a.b16 + pc[12 + g] + k0 + 32));
-                    mma_m16n8k16_f16(d, pa[0], qa[0], pa[1], qa[1], l1.x, l1.y, d);
-                    mma_m16n8k16_f16(d, pa[2], qa[2], pa[3], qa[3], l1.z, l1.w, d);
-                }
-                const float sg1 = e8m0_byte(s, 1), sh1 = e8m0_byte(s, 3);
-                acc[0] = fmaf(d[0], sg1, acc[0]);
-                acc[1] = fmaf(d[1], sg1, acc[1]);
-                acc[2] = fmaf(d[2], sh1, acc[2]);
-                acc[3] = fmaf(d[3], sh1, acc[3]);
-
+        for (int j = 0; j < S; ++j) {
+            if (f_first + j < F) {
                 const int rb = cc.rb, kc = cc.kc;
+                const int *pc = step(q[j], sc[j]);
                 if (wk.advance(cc)) {
-                    // unit finished: write the partial sums of its real columns
-                    const int count = pc[2], begin = pc[1];
-                    if (MODE == kFfnGateUp) {
-                        const int j0 = rb * 8 + g;
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int n = 2 * c + h;
-                            if (n < count) {
-                                float *dst =
-                                    a.part + ((size_t)kc * a.n_entries + begin + n) * 2 * a.out_len + j0;
-                                dst[0] = acc[h];                 // gate row j0
-                                dst[a.out_len] = acc[2 + h];     // up row j0
-                            }
-                        }
-                    } else {
-                        float y[4] = {acc[0], acc[1], acc[2], acc[3]};
-                        if (count <= 4) {                        // add lo column n+4 to hi column n
-#pragma unroll
-                            for (int i = 0; i < 4; ++i)
-                                y[i] += __shfl_xor_sync(0xffffffffu, acc[i], 2);
-                        }
-                        const int lim = count <= 4 ? 2 : 4;      // threads c < lim own real columns
-                        if (c < lim) {
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                const int n = 2 * c + h;
-                                if (n < count) {
-                                    const int e = begin + n;
-                                    const float u = a.bundo[e];
-                                    float *dst = a.part + ((size_t)kc * a.n_entries + e) * a.out_len + rb * 16;
-                                    dst[g] = y[h] * u;
-                                    dst[g + 8] = y[2 + h] * u;
-                                }
-                            }
-                        }
-                    }
+                    write_partials<MODE>(&a, acc[0], acc[1], acc[2], acc[3], pc[1], pc[2], rb, kc, lane);
                     acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
-                    if (f0 + j + 1 < F)
+                    if (f_first + j + 1 < F)
                         wk.locate(cc);
                 }
             }
         }
+    };
+
+    for (long long f0 = 0; f0 < F; f0 += 2 * S) {
+        issue(bq[1], bs[1], f0 + S);             // no-op past the end
+        consume(bq[0], bs[0], f0);
+        if (f0 + S >= F)
+            break;
+        issue(bq[0], bs[0], f0 + 2 * S);
+        consume(bq[1], bs[1], f0 + S);
     }
 }
 
 // --------------------------------------------------------- finalize + combine
 
-// h = silu(G) * U from the K-chunk partials of gate/up (fp32, fixed order),
-// then h * 2^shift = hi + lo in f16 with the shift chosen per entry.
-__global__ void __launch_bounds__(256)
+// h = silu(G) * U from the K-chunk partials of gate/up (fp32, summed in
+// K-chunk order), then h * 2^shift = hi + lo in f16 with the shift chosen per
+// entry.  Loads of four columns x all K-chunks are issued together.
+__global__ void __launch_bounds__(512)
 hfin_kernel(const float *__restrict__ part, int n_kc, int n_entries, int I, const int32_t *__restrict__ sorted_tok,
             const float *__restrict__ xundo, __half *__restrict__ h16, float *__restrict__ hundo,
             const uint32_t *__restrict__ hdr) {
     extern __shared__ float hbuf[];   // [I]
-    __shared__ float wmax[8];
+    __shared__ float wmax[16];
     const int r = blockIdx.x;
     if (*reinterpret_cast<const volatile int *>(hdr + kHdrNumPasses) == 0)
         return;                       // grouping rejected the routing
     const float xu = xundo[sorted_tok[r]];
+    const float *base = part + (size_t)r * 2 * I;
+    const size_t kstride = (size_t)n_entries * 2 * I;
     float mx = 0.0f;
-    for (int j = threadIdx.x; j < I; j += blockDim.x) {
-        float G = 0.0f, U = 0.0f;
-        for (int kc = 0; kc < n_kc; ++kc) {
-            const float *p = part + ((size_t)kc * n_entries + r) * 2 * I + j;
-            G += p[0];
-            U += p[I];
+    for (int j0 = threadIdx.x; j0 < I; j0 += 4 * blockDim.x) {
+        float gv[4][kMaxKChunks], uv[4][kMaxKChunks];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int j = j0 + q * blockDim.x;
+#pragma unroll
+            for (int kc = 0; kc < kMaxKChunks; ++kc) {
+                if (j < I && kc < n_kc) {
+                    gv[q][kc] = base[kc * kstride + j];
+                    uv[q][kc] = base[kc * kstride + I + j];
+                }
+            }
         }
-        G *= xu;
-        U *= xu;
-        const float h = G / (1.0f + expf(-G)) * U;
-        hbuf[j] = h;
-        mx = fmaxf(mx, fabsf(h));
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int j = j0 + q * blockDim.x;
+            if (j < I) {
+                float G = 0.0f, U = 0.0f;
+#pragma unroll
+                for (int kc = 0; kc < kMaxKChunks; ++kc)
+                    if (kc < n_kc) {
+                        G += gv[q][kc];
+                        U += uv[q][kc];
+                    }
+                G *= xu;
+                U *= xu;
+                const float h = G / (1.0f + expf(-G)) * U;
+                hbuf[j] = h;
+                mx = fmaxf(mx, fabsf(h));
+            }
+        }
     }
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1)
@@ -342,27 +421,48 @@ hfin_kernel(const float *__restrict__ part, int n_kc, int n_entries, int I, cons
         hundo[r] = exp2i(-sh);
 }
 
-// y[t] = bf16_rn( sum over slots s in order of w[t,s] * sum over K-chunks of Y )
+// y[t] = bf16_rn( sum over slots s in order of w[t,s] * sum over K-chunks of Y ).
+// A CTA covers 256 outputs of one token (H % 64 == 0 and H >= 256, or one CTA
+// per token otherwise); slot positions and weights are read once per CTA.
 __global__ void __launch_bounds__(256)
 combine_kernel(const float *__restrict__ part, int n_kc, int n_entries, const int32_t *__restrict__ inv_pos,
                const float *__restrict__ topk_w, int T, int kps, int H, uint16_t *__restrict__ y,
                const uint32_t *__restrict__ hdr) {
-    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= (long long)T * H || *reinterpret_cast<const volatile int *>(hdr + kHdrNumPasses) == 0)
-        return;                       // out of range, or grouping rejected the routing
-    const int t = (int)(idx / H), n = (int)(idx % H);
-    float s = 0.0f;
-    for (int sl = 0; sl < kps; ++sl) {
-        const int pos = inv_pos[t * kps + sl];
+    __shared__ int spos[kMaxSlots];
+    __shared__ float sw[kMaxSlots];
+    __shared__ int bad;
+    const int per_tok = (H + 255) / 256;
+    const int t = blockIdx.x / per_tok;
+    const int n = (blockIdx.x % per_tok) * 256 + threadIdx.x;
+    if (*reinterpret_cast<const volatile int *>(hdr + kHdrNumPasses) == 0)
+        return;                       // grouping rejected the routing
+    if (threadIdx.x == 0)
+        bad = 0;
+    __syncthreads();
+    if (threadIdx.x < kps) {
+        const int pos = inv_pos[t * kps + threadIdx.x];
+        spos[threadIdx.x] = pos;
+        sw[threadIdx.x] = topk_w[t * kps + threadIdx.x];
         if (pos < 0 || pos >= n_entries)
-            return;
+            bad = 1;
+    }
+    __syncthreads();
+    if (bad || n >= H)
+        return;
+    const size_t kstride = (size_t)n_entries * H;
+    float s = 0.0f;
+#pragma unroll 4
+    for (int sl = 0; sl < kps; ++sl) {
+        const float *p = part + (size_t)spos[sl] * H + n;
         float v = 0.0f;
-        for (int kc = 0; kc < n_kc; ++kc)
-            v += part[((size_t)kc * n_entries + pos) * H + n];
-        s = fmaf(topk_w[t * kps + sl], v, s);
+#pragma unroll
+        for (int kc = 0; kc < kMaxKChunks; ++kc)
+            if (kc < n_kc)
+                v += p[kc * kstride];
+        s = fmaf(sw[sl], v, s);
     }
     const __nv_bfloat16 b = __float2bfloat16_rn(s);
-    y[idx] = *reinterpret_cast<const uint16_t *>(&b);
+    y[(size_t)t * H + n] = *reinterpret_cast<const uint16_t *>(&b);
 }
 
 __global__ void __launch_bounds__(256) x16_kernel(const uint16_t *__restrict__ x, int H, __half *x16, float *xundo) {
@@ -388,23 +488,36 @@ __global__ void selftest_decode_kernel(const uint8_t *codes, uint16_t *out, int 
 
 bool ffn_shape_supported(int H, int I) { return H > 0 && I > 0 && H % 64 == 0 && I % 64 == 0 && I <= 16384; }
 
-template <int MODE>
-static cudaError_t launch_one(const FfnArgs &a, int grid, int cache_passes, cudaStream_t stream) {
-    constexpr int NW = kFfnWarps, D = kFfnDepth;
-    const size_t smem = (size_t)cache_passes * kCacheInts * sizeof(int);
+template <int MODE, bool WIN>
+static cudaError_t launch_one(const FfnArgs &a, int grid, size_t smem, cudaStream_t stream) {
+    constexpr int NW = kFfnWarps, D = kFfnBatch;
     static std::atomic<int> set_bytes[64];
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess)
         return err;
     if (smem > 48 * 1024 && set_bytes[dev & 63].load() < (int)smem) {
-        err = cudaFuncSetAttribute(ffn_kernel<MODE, NW, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        err = cudaFuncSetAttribute(ffn_kernel<MODE, NW, D, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)smem);
         if (err != cudaSuccess)
             return err;
         set_bytes[dev & 63].store((int)smem);
     }
-    ffn_kernel<MODE, NW, D><<<grid, NW * 32, smem, stream>>>(a);
+    ffn_kernel<MODE, NW, D, WIN><<<grid, NW * 32, smem, stream>>>(a);
     return cudaGetLastError();
+}
+
+// Chooses the shared-memory window when the B rows a CTA can need fit.
+template <int MODE>
+static cudaError_t launch_mode(FfnArgs &a, int grid, int cache_passes, int window_rows, cudaStream_t stream) {
+    const size_t cache_bytes = align_up((size_t)cache_passes * kCacheInts * sizeof(int), 16);
+    a.win_offset = (int)cache_bytes;
+    a.win_row = a.b_row + 32;
+    const size_t win_bytes = (size_t)window_rows * a.win_row * sizeof(__half);
+    if (cache_bytes + win_bytes <= (size_t)kWindowBudget)
+        return launch_one<MODE, true>(a, grid, cache_bytes + win_bytes, stream);
+    a.win_row = a.b_row;
+    return launch_one<MODE, false>(a, grid, cache_bytes, stream);
 }
 
 cudaError_t launch_ffn(const FfnProblem &pr, void *ws, const WsLayout &L, int num_sms, cudaStream_t stream,
@@ -417,6 +530,7 @@ cudaError_t launch_ffn(const FfnProblem &pr, void *ws, const WsLayout &L, int nu
     uint32_t *hdr = ws_at<uint32_t>(ws, 0);
     // passes a CTA can touch: its share of all passes plus both boundary passes
     const int cache_passes = max_passes(T, kps, n_tot) / num_sms + 3;
+    const int cache_passes4 = max_passes(T, kps, n_tot, kPassEntries) / num_sms + 3;
     cudaError_t err;
 
     FfnArgs g{};
@@ -428,12 +542,14 @@ cudaError_t launch_ffn(const FfnProblem &pr, void *ws, const WsLayout &L, int nu
     g.b16 = ws_at<__half>(ws, L.x16);
     g.b_row = H;
     g.passes = ws_at<Pass>(ws, L.passes);
+    g.passes_word = kHdrNumPasses;
     g.sorted_tok = ws_at<int32_t>(ws, L.sorted_tok);
     g.hdr = hdr;
     g.part = ws_at<float>(ws, L.gpart);
     g.n_entries = entries;
     g.out_len = I;
-    if ((err = launch_one<kFfnGateUp>(g, num_sms, cache_passes, stream)) != cudaSuccess)
+    g.T = T;
+    if ((err = launch_mode<kFfnGateUp>(g, num_sms, cache_passes, T, stream)) != cudaSuccess)
         return err;
 
     const size_t hsmem = (size_t)I * sizeof(float);
@@ -441,13 +557,13 @@ cudaError_t launch_ffn(const FfnProblem &pr, void *ws, const WsLayout &L, int nu
         (err = cudaFuncSetAttribute(hfin_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsmem)) !=
             cudaSuccess)
         return err;
-    hfin_kernel<<<entries, 256, hsmem, stream>>>(ws_at<float>(ws, L.gpart), L.n_kc_gu, entries, I,
+    hfin_kernel<<<entries, 512, hsmem, stream>>>(ws_at<float>(ws, L.gpart), L.n_kc_gu, entries, I,
                                                  ws_at<int32_t>(ws, L.sorted_tok), ws_at<float>(ws, L.xundo),
                                                  ws_at<__half>(ws, L.h16), ws_at<float>(ws, L.hundo), hdr);
     if ((err = cudaGetLastError()) != cudaSuccess)
         return err;
     if (ev_after_gateup &&
-        (err = cudaEventRecordWithFlags(ev_after_gateup, stream, cudaEventRecordExternal)) != cudaSuccess)
+        (err = cudaEventRecord(ev_after_gateup, stream)) != cudaSuccess)
         return err;
 
     FfnArgs d{};
@@ -458,18 +574,21 @@ cudaError_t launch_ffn(const FfnProblem &pr, void *ws, const WsLayout &L, int nu
     d.n_kc = L.n_kc_dn;
     d.b16 = ws_at<__half>(ws, L.h16);
     d.b_row = I;
-    d.passes = g.passes;
+    d.passes = ws_at<Pass>(ws, L.passes4);
+    d.passes_word = kHdrNumPasses4;
     d.sorted_tok = g.sorted_tok;
     d.hdr = hdr;
     d.part = ws_at<float>(ws, L.ypart);
     d.n_entries = entries;
     d.out_len = H;
     d.bundo = ws_at<float>(ws, L.hundo);
-    if ((err = launch_one<kFfnDown>(d, num_sms, cache_passes, stream)) != cudaSuccess)
+    d.T = T;
+    // entries a CTA's passes can hold: at most 4 per cached pass
+    const int down_rows = 2 * (entries < kPassEntries * cache_passes4 ? entries : kPassEntries * cache_passes4);
+    if ((err = launch_mode<kFfnDown>(d, num_sms, cache_passes4, down_rows, stream)) != cudaSuccess)
         return err;
 
-    const long long outs = (long long)T * H;
-    combine_kernel<<<(unsigned)((outs + 255) / 256), 256, 0, stream>>>(
+    combine_kernel<<<(unsigned)(T * ((H + 255) / 256)), 256, 0, stream>>>(
         ws_at<float>(ws, L.ypart), L.n_kc_dn, entries, ws_at<int32_t>(ws, L.inv_pos), pr.topk_w, T, kps, H, pr.y,
         hdr);
     return cudaGetLastError();

@@ -13,7 +13,8 @@ struct GroupOut {
     int32_t *inv_pos;      // [T*kps] nullable: sorted position of entry t*kps+s
     int32_t *active;       // [n_tot]
     int32_t *num_active;   // [1] nullable (the header always gets it)
-    Pass *passes;          // nullable
+    Pass *passes;          // nullable: passes of <= 8 entries (gate/up)
+    Pass *passes4;         // with passes: passes of <= 4 entries (down)
     uint32_t *counters;    // down-kernel row-block counters to zero
     int n_counters;
 };

@@ -74,12 +74,19 @@ route_partial_kernel(const uint16_t *__restrict__ x, const float *__restrict__ w
     for (int t0 = 0; t0 < T; t0 += kTok) {
         const int tn = min(kTok, T - t0);
         __syncthreads();
-        for (int i = threadIdx.x; i < kTok * kRouteRows; i += kRouteThreads) {
-            const int tt = i / kRouteRows, hh = i % kRouteRows;
-            float v = 0.0f;
-            if (tt < tn && h0 + hh < H)
-                v = bf16_bits_to_float(__ldg(x + (size_t)(t0 + tt) * H + h0 + hh));
-            xs[tt][hh] = v;
+        // 8 tokens x 512 rows of bf16 = 512 chunks of 8 elements, two per thread
+#pragma unroll
+        for (int i = threadIdx.x; i < kTok * kRouteRows / 8; i += kRouteThreads) {
+            const int tt = i / (kRouteRows / 8), h8 = (i % (kRouteRows / 8)) * 8;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (tt < tn && h0 + h8 < H)      // H % 8 == 0: a chunk is either inside or outside
+                v = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + tt) * H + h0 + h8));
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                xs[tt][h8 + 2 * j] = __uint_as_float(w4[j] << 16);
+                xs[tt][h8 + 2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
+            }
         }
         __syncthreads();
 #pragma unroll 1
@@ -140,6 +147,7 @@ __device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const
             record_status(hdr, MOE_ERR_DEVICE_ASSERT);
             hdr[kHdrNumActive] = 0;
             hdr[kHdrNumPasses] = 0;
+            hdr[kHdrNumPasses4] = 0;
             if (o.num_active)
                 *o.num_active = 0;
         }
@@ -147,7 +155,7 @@ __device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const
     }
 
     if (warp == 0) {
-        int run = 0, na = 0, np = 0;
+        int run = 0, na = 0, np = 0, np4 = 0;
         for (int base = 0; base < n_tot; base += 32) {
             const int e = base + lane;
             const int v = e < n_tot ? cnt[e] : 0;
@@ -161,38 +169,43 @@ __device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const
             const int excl = run + incl - v;
             const unsigned act = __ballot_sync(0xffffffffu, v > 0);
             const int rank = __popc(act & ((1u << lane) - 1u));
+            // passes of up to kPassTokens (gate/up) and kPassEntries (down) entries
             const int npass = (v + kPassTokens - 1) / kPassTokens;
-            int pincl = npass;
+            const int npass4 = (v + kPassEntries - 1) / kPassEntries;
+            int pincl = npass, pincl4 = npass4;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
                 const int y = __shfl_up_sync(0xffffffffu, pincl, d);
-                if (lane >= d)
+                const int y4 = __shfl_up_sync(0xffffffffu, pincl4, d);
+                if (lane >= d) {
                     pincl += y;
+                    pincl4 += y4;
+                }
             }
-            const int pexcl = np + pincl - npass;
+            const int pexcl = np + pincl - npass, pexcl4 = np4 + pincl4 - npass4;
             if (e < n_tot) {
                 cursor[e] = excl;
                 o.offsets[e] = excl;
                 if (v > 0)
                     o.active[na + rank] = e;
-                if (o.passes)
-                    for (int p = 0; p < npass; ++p) {
-                        Pass ps;
-                        ps.expert = e;
-                        ps.begin = excl + p * kPassTokens;
-                        ps.count = min(kPassTokens, v - p * kPassTokens);
-                        ps.pad = 0;
-                        o.passes[pexcl + p] = ps;
-                    }
+                if (o.passes) {
+                    for (int p = 0; p < npass; ++p)
+                        o.passes[pexcl + p] = Pass{e, excl + p * kPassTokens, min(kPassTokens, v - p * kPassTokens), 0};
+                    for (int p = 0; p < npass4; ++p)
+                        o.passes4[pexcl4 + p] =
+                            Pass{e, excl + p * kPassEntries, min(kPassEntries, v - p * kPassEntries), 0};
+                }
             }
             run += __shfl_sync(0xffffffffu, incl, 31);
             np += __shfl_sync(0xffffffffu, pincl, 31);
+            np4 += __shfl_sync(0xffffffffu, pincl4, 31);
             na += __popc(act);
         }
         if (lane == 0) {
             o.offsets[n_tot] = run;
             hdr[kHdrNumActive] = na;
             hdr[kHdrNumPasses] = np;
+            hdr[kHdrNumPasses4] = np4;
             if (o.num_active)
                 *o.num_active = na;
         }
@@ -243,10 +256,18 @@ route_finish_kernel(const float2 *__restrict__ part, int nh, const float *__rest
 
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         float p = 0.0f, s = 0.0f;
-#pragma unroll 8
-        for (int c = 0; c < nh; ++c) {
-            const float2 v = part[((size_t)c * T + t) * E + e];
-            pair_add(p, s, v.x, v.y);
+        float2 v[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c)             // issue the loads of all chunks first
+            if (c < nh)
+                v[c] = part[((size_t)c * T + t) * E + e];
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+            if (c < nh)
+                pair_add(p, s, v[c].x, v[c].y);
+        for (int c = 16; c < nh; ++c) {          // H > 8192
+            const float2 u = part[((size_t)c * T + t) * E + e];
+            pair_add(p, s, u.x, u.y);
         }
         if (bias)
             pair_add(p, s, bias[e], 0.0f);
@@ -344,7 +365,7 @@ cudaError_t launch_route(const uint16_t *x, const float *wr, const float *bias, 
     if (err != cudaSuccess)
         return err;
     if (ev_after_partial &&
-        (err = cudaEventRecordWithFlags(ev_after_partial, stream, cudaEventRecordExternal)) != cudaSuccess)
+        (err = cudaEventRecord(ev_after_partial, stream)) != cudaSuccess)
         return err;
     const size_t smem = (size_t)E * sizeof(float2);
     __half *x16 = do_group ? ws_at<__half>(ws, L.x16) : nullptr;

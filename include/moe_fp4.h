@@ -193,8 +193,9 @@ moe_status_t moe_layer_forward_hostio(const uint16_t *x_host, const float *route
 
 /*
  * Diagnostic form of moe_layer_forward: records events[0] before the first
- * kernel and events[i] after kernel i (router, top-k/grouping, gate/up,
- * down/combine), so n_events must be 5.  Events are created by the caller.
+ * kernel, events[1] after the router GEMV, events[2] after top-k/grouping,
+ * events[3] after gate/up + h finalize and events[4] after down + combine, so
+ * n_events must be 5.  Events are created by the caller.
  */
 moe_status_t moe_layer_forward_profiled(const uint16_t *x, const float *router_w,
                                         const float *logit_bias, int T, int top_k,
