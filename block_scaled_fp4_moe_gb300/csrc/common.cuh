@@ -20,7 +20,7 @@ constexpr int kRouteThreads = 256;
 constexpr int kGroupThreads = 256;
 constexpr int kPassTokens = 8;        // MMA N: tokens per gate/up pass
 constexpr int kPassEntries = 4;       // entries per down pass (hi and lo f16 terms fill N = 8)
-constexpr int kFfnWarps = 8;          // warps per expert-FFN CTA (one CTA per SM)
+constexpr int kFfnWarps = 12;         // warps per expert-FFN CTA (one CTA per SM)
 constexpr int kFfnBatch = 8;          // steps per batch of loads (two batches in flight)
 constexpr int kTargetWarps = 152 * kFfnWarps;
 constexpr int kMaxKChunks = 8;        // K-chunks per row block (partial sums per output)
@@ -181,6 +181,12 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     return p;
 }
 
+// Programmatic dependent launch: wait until the preceding grid on the stream
+// has completed and its writes are visible (a no-op without a prerequisite
+// grid), and allow the next grid to be scheduled.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -235,20 +241,24 @@ __device__ __forceinline__ int f16_shift_for_max(float m) {
 
 namespace moe {
 
-// One CTA: x[t] (bf16, length H, H % 8 == 0) -> x16[t] = f16(x * 2^s), where
-// s maps the row's largest magnitude into [2^14, 2^15), and xundo[t] = 2^-s.
-__device__ inline void convert_x_row(const uint16_t *__restrict__ x, int t, int H, __half *x16, float *xundo) {
+// x[t] (bf16, length H, H % 8 == 0) -> x16[t] = f16(x * 2^s), where s maps
+// the row's largest magnitude into [2^14, 2^15), and xundo[t] = 2^-s.  Run by
+// the warps first_warp .. first_warp+nwarps-1 of the CTA, which synchronise
+// on named barrier bar_id (nwarps == all warps may use barrier 0).
+__device__ inline void convert_x_row(const uint16_t *__restrict__ x, int t, int H, __half *x16, float *xundo,
+                                     int first_warp, int nwarps, int bar_id) {
     __shared__ float red[32];
+    const int lt = threadIdx.x - first_warp * 32, nt = nwarps * 32;
     const uint16_t *xr = x + (size_t)t * H;
     const int nchunk = H / 8;
-    uint4 keep[4];                        // rows of up to 4 * 8 * blockDim elements stay in registers
+    uint4 keep[4];                        // rows of up to 32 * nt elements stay in registers
     float m = 0.0f;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const int i = threadIdx.x + q * blockDim.x;
+        const int i = lt + q * nt;
         keep[q] = i < nchunk ? __ldg(reinterpret_cast<const uint4 *>(xr) + i) : make_uint4(0, 0, 0, 0);
     }
-    for (int i = threadIdx.x + 4 * blockDim.x; i < nchunk; i += blockDim.x) {
+    for (int i = lt + 4 * nt; i < nchunk; i += nt) {
         const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr) + i);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -265,11 +275,11 @@ __device__ inline void convert_x_row(const uint16_t *__restrict__ x, int t, int 
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1)
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
-    if ((threadIdx.x & 31) == 0)
-        red[threadIdx.x >> 5] = m;
-    __syncthreads();
+    if ((lt & 31) == 0)
+        red[lt >> 5] = m;
+    named_barrier_sync(bar_id, nt);
     m = red[0];
-    for (int w = 1; w < (int)((blockDim.x + 31) >> 5); ++w)
+    for (int w = 1; w < nwarps; ++w)
         m = fmaxf(m, red[w]);
     const int sh = f16_shift_for_max(m);
     const float sc = exp2i(sh);
@@ -285,15 +295,15 @@ __device__ inline void convert_x_row(const uint16_t *__restrict__ x, int t, int 
     };
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const int i = threadIdx.x + q * blockDim.x;
+        const int i = lt + q * nt;
         if (i < nchunk)
             convert(keep[q], i);
     }
-    for (int i = threadIdx.x + 4 * blockDim.x; i < nchunk; i += blockDim.x)
+    for (int i = lt + 4 * nt; i < nchunk; i += nt)
         convert(__ldg(reinterpret_cast<const uint4 *>(xr) + i), i);
-    if (threadIdx.x == 0)
+    if (lt == 0)
         xundo[t] = exp2i(-sh);
-    __syncthreads();
+    named_barrier_sync(bar_id, nt);
 }
 
 }  // namespace moe

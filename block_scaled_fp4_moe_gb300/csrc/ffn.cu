@@ -84,6 +84,7 @@ struct Cursor {
     int P, rb, kc;
     const int *pc;               // cached pass record
     const uint8_t *ptr;          // address of the current step
+    int bk;                      // element offset of this lane's B fragment for the step
 };
 
 struct Walker {
@@ -107,11 +108,14 @@ struct Walker {
         const int expert = cu.pc[0];
         cu.ptr = a.packed + ((size_t)expert * a.units_per_expert + cu.rb) * a.unit_bytes +
                  (size_t)(cu.kc * m) * kStepBytes;
+        const int lane = threadIdx.x & 31;
+        cu.bk = cu.pc[4 + (lane >> 2)] + cu.kc * m * 64 + 8 * (lane & 3);
     }
     // One step forward; true when a unit was completed (the cursor then
     // points at the next unit, which may lie past the warp's range).
     __device__ bool advance(Cursor &cu) const {
         cu.ptr += kStepBytes;
+        cu.bk += 64;
         if (++cu.it < m)
             return false;
         cu.it = 0;
@@ -174,6 +178,8 @@ __global__ void __launch_bounds__(NW * 32, 1) ffn_kernel(const __grid_constant__
     __half *win = reinterpret_cast<__half *>(reinterpret_cast<uint8_t *>(cache) + a.win_offset);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, c = lane & 3;
+    pdl_wait();
+    pdl_trigger();
     const int n_passes = *reinterpret_cast<const volatile int *>(a.hdr + a.passes_word);
     const int m = a.steps / a.n_kc;
     const int upp = a.units_per_expert * a.n_kc;
@@ -294,8 +300,7 @@ __global__ void __launch_bounds__(NW * 32, 1) ffn_kernel(const __grid_constant__
     // one 16 x 64 step: decode, two (or four) MMAs per 32-element block, block scales
     auto step = [&](const uint4 q, const uint32_t s) {
         const int *pc = cc.pc;
-        const int k0 = (cc.kc * m + cc.it) * 64 + 8 * c;    // element offset in the B row
-        const __half *bp = bbase + pc[4 + g] + k0;
+        const __half *bp = bbase + cc.bk;
         const uint4 b0 = load_b(bp);
         const uint4 b1 = load_b(bp + 32);
         uint32_t pa[4], qa[4];
@@ -361,6 +366,8 @@ hfin_kernel(const float *__restrict__ part, int n_kc, int n_entries, int I, cons
     extern __shared__ float hbuf[];   // [I]
     __shared__ float wmax[16];
     const int r = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
     if (*reinterpret_cast<const volatile int *>(hdr + kHdrNumPasses) == 0)
         return;                       // grouping rejected the routing
     const float xu = xundo[sorted_tok[r]];
@@ -422,51 +429,61 @@ hfin_kernel(const float *__restrict__ part, int n_kc, int n_entries, int I, cons
 }
 
 // y[t] = bf16_rn( sum over slots s in order of w[t,s] * sum over K-chunks of Y ).
-// A CTA covers 256 outputs of one token (H % 64 == 0 and H >= 256, or one CTA
-// per token otherwise); slot positions and weights are read once per CTA.
+// A CTA covers 256 outputs of one token; the positions and weights of the
+// token's slots are read once per CTA, then all partial loads of a thread are
+// issued before they are summed.
 __global__ void __launch_bounds__(256)
 combine_kernel(const float *__restrict__ part, int n_kc, int n_entries, const int32_t *__restrict__ inv_pos,
                const float *__restrict__ topk_w, int T, int kps, int H, uint16_t *__restrict__ y,
                const uint32_t *__restrict__ hdr) {
     __shared__ int spos[kMaxSlots];
     __shared__ float sw[kMaxSlots];
-    __shared__ int bad;
     const int per_tok = (H + 255) / 256;
     const int t = blockIdx.x / per_tok;
     const int n = (blockIdx.x % per_tok) * 256 + threadIdx.x;
-    if (*reinterpret_cast<const volatile int *>(hdr + kHdrNumPasses) == 0)
-        return;                       // grouping rejected the routing
-    if (threadIdx.x == 0)
-        bad = 0;
-    __syncthreads();
+    pdl_wait();
+    pdl_trigger();
+    int bad = 0;
+    if (threadIdx.x == 0)             // grouping rejected the routing
+        bad = *reinterpret_cast<const volatile int *>(hdr + kHdrNumPasses) == 0;
     if (threadIdx.x < kps) {
         const int pos = inv_pos[t * kps + threadIdx.x];
         spos[threadIdx.x] = pos;
         sw[threadIdx.x] = topk_w[t * kps + threadIdx.x];
-        if (pos < 0 || pos >= n_entries)
-            bad = 1;
+        bad |= pos < 0 || pos >= n_entries;
     }
-    __syncthreads();
-    if (bad || n >= H)
+    if (__syncthreads_or(bad) || n >= H)
         return;
     const size_t kstride = (size_t)n_entries * H;
     float s = 0.0f;
-#pragma unroll 4
-    for (int sl = 0; sl < kps; ++sl) {
-        const float *p = part + (size_t)spos[sl] * H + n;
-        float v = 0.0f;
+    for (int s0 = 0; s0 < kps; s0 += 12) {
+        float v[12][kMaxKChunks];
 #pragma unroll
-        for (int kc = 0; kc < kMaxKChunks; ++kc)
-            if (kc < n_kc)
-                v += p[kc * kstride];
-        s = fmaf(sw[sl], v, s);
+        for (int i = 0; i < 12; ++i)
+#pragma unroll
+            for (int kc = 0; kc < kMaxKChunks; ++kc)
+                if (s0 + i < kps && kc < n_kc)
+                    v[i][kc] = part[(size_t)spos[s0 + i] * H + n + kc * kstride];
+#pragma unroll
+        for (int i = 0; i < 12; ++i) {
+            if (s0 + i < kps) {
+                float a = 0.0f;
+#pragma unroll
+                for (int kc = 0; kc < kMaxKChunks; ++kc)
+                    if (kc < n_kc)
+                        a += v[i][kc];
+                s = fmaf(sw[s0 + i], a, s);
+            }
+        }
     }
     const __nv_bfloat16 b = __float2bfloat16_rn(s);
     y[(size_t)t * H + n] = *reinterpret_cast<const uint16_t *>(&b);
 }
 
 __global__ void __launch_bounds__(256) x16_kernel(const uint16_t *__restrict__ x, int H, __half *x16, float *xundo) {
-    convert_x_row(x, blockIdx.x, H, x16, xundo);
+    pdl_wait();
+    pdl_trigger();
+    convert_x_row(x, blockIdx.x, H, x16, xundo, 0, 8, 1);
 }
 
 __global__ void selftest_decode_kernel(const uint8_t *codes, uint16_t *out, int n) {
@@ -503,8 +520,7 @@ static cudaError_t launch_one(const FfnArgs &a, int grid, size_t smem, cudaStrea
             return err;
         set_bytes[dev & 63].store((int)smem);
     }
-    ffn_kernel<MODE, NW, D, WIN><<<grid, NW * 32, smem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(ffn_kernel<MODE, NW, D, WIN>, dim3(grid), dim3(NW * 32), smem, stream, a);
 }
 
 // Chooses the shared-memory window when the B rows a CTA can need fit.
@@ -557,10 +573,11 @@ cudaError_t launch_ffn(const FfnProblem &pr, void *ws, const WsLayout &L, int nu
         (err = cudaFuncSetAttribute(hfin_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsmem)) !=
             cudaSuccess)
         return err;
-    hfin_kernel<<<entries, 512, hsmem, stream>>>(ws_at<float>(ws, L.gpart), L.n_kc_gu, entries, I,
-                                                 ws_at<int32_t>(ws, L.sorted_tok), ws_at<float>(ws, L.xundo),
-                                                 ws_at<__half>(ws, L.h16), ws_at<float>(ws, L.hundo), hdr);
-    if ((err = cudaGetLastError()) != cudaSuccess)
+    err = launch_pdl(hfin_kernel, dim3(entries), dim3(512), hsmem, stream, (const float *)ws_at<float>(ws, L.gpart),
+                     L.n_kc_gu, entries, I, (const int32_t *)ws_at<int32_t>(ws, L.sorted_tok),
+                     (const float *)ws_at<float>(ws, L.xundo), ws_at<__half>(ws, L.h16), ws_at<float>(ws, L.hundo),
+                     (const uint32_t *)hdr);
+    if (err != cudaSuccess)
         return err;
     if (ev_after_gateup &&
         (err = cudaEventRecord(ev_after_gateup, stream)) != cudaSuccess)
@@ -588,15 +605,15 @@ cudaError_t launch_ffn(const FfnProblem &pr, void *ws, const WsLayout &L, int nu
     if ((err = launch_mode<kFfnDown>(d, num_sms, cache_passes4, down_rows, stream)) != cudaSuccess)
         return err;
 
-    combine_kernel<<<(unsigned)(T * ((H + 255) / 256)), 256, 0, stream>>>(
-        ws_at<float>(ws, L.ypart), L.n_kc_dn, entries, ws_at<int32_t>(ws, L.inv_pos), pr.topk_w, T, kps, H, pr.y,
-        hdr);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3(T * ((H + 255) / 256)), dim3(256), 0, stream,
+                      (const float *)ws_at<float>(ws, L.ypart), L.n_kc_dn, entries,
+                      (const int32_t *)ws_at<int32_t>(ws, L.inv_pos), pr.topk_w, T, kps, H, pr.y,
+                      (const uint32_t *)hdr);
 }
 
 cudaError_t launch_x16(const uint16_t *x, int T, int H, void *ws, const WsLayout &L, cudaStream_t stream) {
-    x16_kernel<<<T, 256, 0, stream>>>(x, H, ws_at<__half>(ws, L.x16), ws_at<float>(ws, L.xundo));
-    return cudaGetLastError();
+    return launch_pdl(x16_kernel, dim3(T), dim3(256), 0, stream, x, H, ws_at<__half>(ws, L.x16),
+                      ws_at<float>(ws, L.xundo));
 }
 
 cudaError_t launch_selftest_decode(const uint8_t *codes, uint16_t *out, int n, cudaStream_t stream) {

@@ -19,6 +19,25 @@ struct GroupOut {
     int n_counters;
 };
 
+// Launch with programmatic stream serialization, so the kernel can be
+// scheduled while its predecessor on the stream is still running; the kernel
+// itself waits (pdl_wait) before it reads anything the predecessor writes.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // static shared memory of the grouping code (two int arrays of kMaxExperts)
 constexpr size_t kGroupStaticSmem = 2 * kMaxExperts * sizeof(int) + 64;
 

@@ -45,9 +45,12 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_
 
 // ------------------------------------------------------------ router GEMV
 
-// Grid (ceil(E/32), ceil(H/128)); CTA (bx, by) owns experts [32bx, 32bx+32)
-// (one per lane) and router rows [128by, 128by+128) (16 per warp) for all T
-// tokens, and writes the partial Dot2 pairs part[by][t][e].
+// Grid (ceil(E/32), ceil(H/512)); CTA (bx, by) owns experts [32bx, 32bx+32)
+// (one per lane) and router rows [512by, 512by+512) (64 per warp, summed in
+// four interleaved Dot2 chains for instruction-level parallelism) for all T
+// tokens, and writes the partial pairs part[by][t][e].  The router weights do
+// not depend on earlier kernels, so they are loaded before the wait on the
+// preceding grid.
 __global__ void __launch_bounds__(kRouteThreads)
 route_partial_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wr, int T, int H, int E,
                      float2 *__restrict__ part, uint32_t *__restrict__ hdr) {
@@ -61,8 +64,6 @@ route_partial_kernel(const uint16_t *__restrict__ x, const float *__restrict__ w
     const int e = blockIdx.x * kRouteCols + lane;
     const int h0 = blockIdx.y * kRouteRows;
     const int hw = h0 + warp * kRowsPerWarp;
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
-        hdr[kHdrRouteTicket] = 0;
 
     float w[kRowsPerWarp];
 #pragma unroll
@@ -70,11 +71,15 @@ route_partial_kernel(const uint16_t *__restrict__ x, const float *__restrict__ w
         const int h = hw + i;
         w[i] = (e < E && h < H) ? __ldg(wr + (size_t)h * E + e) : 0.0f;
     }
+    pdl_wait();
+    pdl_trigger();
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+        hdr[kHdrRouteTicket] = 0;
 
     for (int t0 = 0; t0 < T; t0 += kTok) {
         const int tn = min(kTok, T - t0);
         __syncthreads();
-        // 8 tokens x 512 rows of bf16 = 512 chunks of 8 elements, two per thread
+        // tn tokens x 512 rows of bf16 in chunks of 8 elements, two per thread
 #pragma unroll
         for (int i = threadIdx.x; i < kTok * kRouteRows / 8; i += kRouteThreads) {
             const int tt = i / (kRouteRows / 8), h8 = (i % (kRouteRows / 8)) * 8;
@@ -89,28 +94,35 @@ route_partial_kernel(const uint16_t *__restrict__ x, const float *__restrict__ w
             }
         }
         __syncthreads();
-#pragma unroll 1
-        for (int tt = 0; tt < kTok; ++tt) {
+        for (int tt = 0; tt < tn; ++tt) {
             const float *xr = &xs[tt][warp * kRowsPerWarp];
-            float p, s;
-            two_prod(xr[0], w[0], p, s);
+            float p[4], q4[4];
 #pragma unroll
-            for (int i = 1; i < kRowsPerWarp; ++i) {
-                float hp, r, q;
-                two_prod(xr[i], w[i], hp, r);
-                two_sum(p, hp, p, q);
-                s = __fadd_rn(s, __fadd_rn(q, r));
+            for (int c = 0; c < 4; ++c)
+                two_prod(xr[c], w[c], p[c], q4[c]);
+#pragma unroll
+            for (int i = 4; i < kRowsPerWarp; i += 4) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float hp, r, q;
+                    two_prod(xr[i + c], w[i + c], hp, r);
+                    two_sum(p[c], hp, p[c], q);
+                    q4[c] = __fadd_rn(q4[c], __fadd_rn(q, r));
+                }
             }
-            red[warp][tt][lane] = make_float2(p, s);
+            pair_add(p[0], q4[0], p[1], q4[1]);
+            pair_add(p[2], q4[2], p[3], q4[3]);
+            pair_add(p[0], q4[0], p[2], q4[2]);
+            red[warp][tt][lane] = make_float2(p[0], q4[0]);
         }
         __syncthreads();
         const int tt = warp;   // one warp per token of the chunk
         if (tt < tn && e < E) {
-            float p = red[0][tt][lane].x, s = red[0][tt][lane].y;
+            float p = red[0][tt][lane].x, q = red[0][tt][lane].y;
 #pragma unroll
             for (int w2 = 1; w2 < kWarps; ++w2)
-                pair_add(p, s, red[w2][tt][lane].x, red[w2][tt][lane].y);
-            part[((size_t)blockIdx.y * T + t0 + tt) * E + e] = make_float2(p, s);
+                pair_add(p, q, red[w2][tt][lane].x, red[w2][tt][lane].y);
+            part[((size_t)blockIdx.y * T + t0 + tt) * E + e] = make_float2(p, q);
         }
     }
 }
@@ -122,7 +134,8 @@ route_partial_kernel(const uint16_t *__restrict__ x, const float *__restrict__ w
 // by (expert, entry), the ascending list of active experts, the passes (runs
 // of up to kPassTokens entries of one expert) and the reset of the down-kernel
 // row-block counters.
-__device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const GroupOut &o, uint32_t *hdr) {
+__device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const GroupOut &o, uint32_t *hdr,
+                            bool ids_in_smem = false) {
     __shared__ int cnt[kMaxExperts];
     __shared__ int cursor[kMaxExperts];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -134,8 +147,9 @@ __device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const
         o.counters[i] = 0;
     __syncthreads();
     int bad = 0;
+    auto id_at = [&](int i) { return ids_in_smem ? ids[i] : __ldcg(ids + i); };
     for (int i = tid; i < n; i += blockDim.x) {
-        const int e = __ldcg(ids + i);
+        const int e = id_at(i);
         if (e < 0 || e >= n_tot)
             bad = 1;
         else
@@ -213,7 +227,7 @@ __device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const
         // stable scatter in entry order, 32 entries at a time
         for (int base = 0; base < n; base += 32) {
             const int i = base + lane;
-            const int e = i < n ? __ldcg(ids + i) : -1;
+            const int e = i < n ? id_at(i) : -1;
             const unsigned same = __match_any_sync(0xffffffffu, e);
             if (i < n) {
                 const int pos = cursor[e] + __popc(same & ((1u << lane) - 1u));
@@ -232,17 +246,19 @@ __device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const
 
 __global__ void __launch_bounds__(kGroupThreads)
 group_kernel(const int32_t *ids, int T, int kps, int n_tot, GroupOut o, uint32_t *hdr) {
+    pdl_wait();
+    pdl_trigger();
     group_block(ids, T, kps, n_tot, o, hdr);
 }
 
 // ------------------------------------------------------- top-k + shared slot
 
 // One CTA per token.  All threads sum the partial pairs of the experts in a
-// fixed order (loads of one expert issued together) and add the bias; warp 0
-// selects the top k (warp-wide argmax over (hi, lo, -index)), writes ids and
-// softmax weights and the shared slot.  With do_group, the CTA also writes
-// the f16 copy of its token's x, and the last CTA to finish (atomic ticket)
-// groups all tokens.
+// fixed order (the loads of one expert issued together) and add the bias;
+// then warp 0 selects the top k (warp-wide argmax over (hi, lo, -index)) and
+// writes ids, softmax weights and the shared slot while, with do_group, warps
+// 1..7 write the f16 copy of the token's x.  With do_group the last CTA to
+// finish (atomic ticket; the only CTA when T = 1) groups all tokens.
 __global__ void __launch_bounds__(256)
 route_finish_kernel(const float2 *__restrict__ part, int nh, const float *__restrict__ bias, int T, int E, int k,
                     int has_shared, float shared_weight, int32_t *__restrict__ ids_out, float *__restrict__ w_out,
@@ -250,9 +266,12 @@ route_finish_kernel(const float2 *__restrict__ part, int nh, const float *__rest
                     __half *x16, float *xundo) {
     extern __shared__ float2 L[];   // [E] normalised (hi, lo) logits
     __shared__ int last_cta;
+    __shared__ int sids[kMaxSlots];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x;
     const int kps = k + has_shared;
+    pdl_wait();
+    pdl_trigger();
 
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         float p = 0.0f, s = 0.0f;
@@ -261,6 +280,7 @@ route_finish_kernel(const float2 *__restrict__ part, int nh, const float *__rest
         for (int c = 0; c < 16; ++c)             // issue the loads of all chunks first
             if (c < nh)
                 v[c] = part[((size_t)c * T + t) * E + e];
+        const float b = bias ? bias[e] : 0.0f;
 #pragma unroll
         for (int c = 0; c < 16; ++c)
             if (c < nh)
@@ -269,14 +289,11 @@ route_finish_kernel(const float2 *__restrict__ part, int nh, const float *__rest
             const float2 u = part[((size_t)c * T + t) * E + e];
             pair_add(p, s, u.x, u.y);
         }
-        if (bias)
-            pair_add(p, s, bias[e], 0.0f);
+        pair_add(p, s, b, 0.0f);
         float hi, lo;
         two_sum(p, s, hi, lo);
         L[e] = make_float2(hi, lo);
     }
-    if (do_group && x16)
-        convert_x_row(x, t, H, x16, xundo);
     __syncthreads();
 
     if (warp == 0) {
@@ -327,18 +344,27 @@ route_finish_kernel(const float2 *__restrict__ part, int nh, const float *__rest
         if (lane < k) {
             ids_out[(size_t)t * kps + lane] = sel_id;
             w_out[(size_t)t * kps + lane] = sel_num / denom;
+            sids[lane] = sel_id;
         }
         if (has_shared && lane == k) {
             ids_out[(size_t)t * kps + k] = E;
             w_out[(size_t)t * kps + k] = shared_weight;
+            sids[k] = E;
         }
+    } else if (do_group && x16) {
+        convert_x_row(x, t, H, x16, xundo, 1, 7, 1);
     }
     if (!do_group)
         return;
+    __syncthreads();
+    if (gridDim.x == 1) {                        // a single token: group from shared memory
+        group_block(sids, T, kps, E + has_shared, go, hdr, true);
+        return;
+    }
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
-        const unsigned ticket = gridDim.x == 1 ? 0u : atomicAdd(hdr + kHdrRouteTicket, 1u);
+        const unsigned ticket = atomicAdd(hdr + kHdrRouteTicket, 1u);
         last_cta = ticket == gridDim.x - 1;
     }
     __syncthreads();
@@ -360,8 +386,7 @@ cudaError_t launch_route(const uint16_t *x, const float *wr, const float *bias, 
     float2 *part = ws_at<float2>(ws, L.route_part);
     const int nh = (H + kRouteRows - 1) / kRouteRows;
     dim3 g1((E + kRouteCols - 1) / kRouteCols, nh);
-    route_partial_kernel<<<g1, kRouteThreads, 0, stream>>>(x, wr, T, H, E, part, hdr);
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_pdl(route_partial_kernel, g1, dim3(kRouteThreads), 0, stream, x, wr, T, H, E, part, hdr);
     if (err != cudaSuccess)
         return err;
     if (ev_after_partial &&
@@ -370,15 +395,13 @@ cudaError_t launch_route(const uint16_t *x, const float *wr, const float *bias, 
     const size_t smem = (size_t)E * sizeof(float2);
     __half *x16 = do_group ? ws_at<__half>(ws, L.x16) : nullptr;
     float *xundo = do_group ? ws_at<float>(ws, L.xundo) : nullptr;
-    route_finish_kernel<<<T, 256, smem, stream>>>(part, nh, bias, T, E, k, has_shared, shared_weight, ids, w, hdr,
-                                                  do_group ? 1 : 0, go, x, H, x16, xundo);
-    return cudaGetLastError();
+    return launch_pdl(route_finish_kernel, dim3(T), dim3(256), smem, stream, part, nh, bias, T, E, k, has_shared,
+                      shared_weight, ids, w, hdr, do_group ? 1 : 0, go, x, H, x16, xundo);
 }
 
 cudaError_t launch_group(const int32_t *ids, int T, int kps, int n_tot, const GroupOut &go, uint32_t *hdr,
                          cudaStream_t stream) {
-    group_kernel<<<1, kGroupThreads, 0, stream>>>(ids, T, kps, n_tot, go, hdr);
-    return cudaGetLastError();
+    return launch_pdl(group_kernel, dim3(1), dim3(kGroupThreads), 0, stream, ids, T, kps, n_tot, go, hdr);
 }
 
 }  // namespace moe
