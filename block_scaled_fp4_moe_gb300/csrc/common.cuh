@@ -23,7 +23,8 @@ constexpr int kPassEntries = 4;       // entries per down pass (hi and lo f16 te
 constexpr int kFfnWarps = 12;         // warps per expert-FFN CTA (one CTA per SM)
 constexpr int kFfnBatch = 8;          // steps per batch of loads (two batches in flight)
 constexpr int kTargetWarps = 152 * kFfnWarps;
-constexpr int kMaxKChunks = 8;        // K-chunks per row block (partial sums per output)
+constexpr int kMaxKChunks = 16;       // K-chunks per row block (partial sums per output)
+constexpr size_t kAlignedPartialBudget = 64u << 20;   // partial-sum bytes allowed for one-batch K-chunks
 constexpr int kWindowBudget = 200 * 1024;   // shared memory for an FFN CTA's activation window
 enum FfnMode { kFfnGateUp = 0, kFfnDown = 1 };
 constexpr int kMaxExperts = 1025;     // E + S (E <= 1024)
@@ -58,10 +59,16 @@ inline int max_passes(int T, int kps, int n_tot, int cap = kPassTokens) {
     return (int)((entries + cap - 1) / cap + na + 1);
 }
 
-// Split of a row block's K/64 steps into K-chunks: the smallest divisor of
-// `steps` that gives a full grid (kTargetWarps warps) about eight units per
-// warp.  A function of the shapes only, so every call agrees on it.
-inline int pick_kchunks(int steps, long long units_no_split) {
+// Split of a row block's K/64 steps into K-chunks, a function of the shapes
+// only so that every call agrees on it.  When K is a multiple of 512 and the
+// partial sums stay small, K-chunks of exactly kFfnBatch steps: then a unit
+// is one batch of loads and the streaming loop needs no per-step bookkeeping.
+// Otherwise the smallest divisor of `steps` that gives a full grid
+// (kTargetWarps warps) about eight units per warp.
+inline int pick_kchunks(int steps, long long units_no_split, size_t partial_bytes_per_chunk) {
+    if (steps % kFfnBatch == 0 && steps / kFfnBatch <= kMaxKChunks &&
+        partial_bytes_per_chunk * (steps / kFfnBatch) <= kAlignedPartialBudget)
+        return steps / kFfnBatch;
     const long long target = 8LL * kTargetWarps;
     int best = 1;
     for (int d = 1; d <= steps && d <= kMaxKChunks; ++d) {
@@ -87,8 +94,8 @@ struct WsLayout {
         const int nh = (H + kRouteRows - 1) / kRouteRows;
         // largest possible number of (expert, <= 8 tokens) passes, without splits
         const long long active = entries < (size_t)n_tot ? (long long)entries : n_tot;
-        L.n_kc_gu = pick_kchunks(H / 64, active * (I / 8));
-        L.n_kc_dn = pick_kchunks(I / 64, active * (H / 16));
+        L.n_kc_gu = pick_kchunks(H / 64, active * (I / 8), entries * 2 * (size_t)I * sizeof(float));
+        L.n_kc_dn = pick_kchunks(I / 64, active * (H / 16), entries * (size_t)H * sizeof(float));
         size_t o = kHdrWords * sizeof(uint32_t);
         auto take = [&](size_t bytes) { o = align_up(o, 256); size_t r = o; o += bytes; return r; };
         L.route_part = take((size_t)nh * T * E * 2 * sizeof(float));

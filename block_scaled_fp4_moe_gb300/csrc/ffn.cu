@@ -172,7 +172,7 @@ __device__ __noinline__ void write_partials(const FfnArgs *a, float a0, float a1
 // WIN: the B operand (x16 rows for gate/up, h16 hi/lo rows for down) of the
 // CTA's passes is first copied to a shared-memory window; otherwise it is read
 // from global memory.
-template <int MODE, int NW, int S, bool WIN>
+template <int MODE, int NW, int S, bool WIN, bool ALIGNED>
 __global__ void __launch_bounds__(NW * 32, 1) ffn_kernel(const __grid_constant__ FfnArgs a) {
     extern __shared__ __align__(16) int cache[];
     __half *win = reinterpret_cast<__half *>(reinterpret_cast<uint8_t *>(cache) + a.win_offset);
@@ -298,9 +298,7 @@ __global__ void __launch_bounds__(NW * 32, 1) ffn_kernel(const __grid_constant__
 
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     // one 16 x 64 step: decode, two (or four) MMAs per 32-element block, block scales
-    auto step = [&](const uint4 q, const uint32_t s) {
-        const int *pc = cc.pc;
-        const __half *bp = bbase + cc.bk;
+    auto step_at = [&](const uint4 q, const uint32_t s, const __half *bp) {
         const uint4 b0 = load_b(bp);
         const uint4 b1 = load_b(bp + 32);
         uint32_t pa[4], qa[4];
@@ -326,6 +324,10 @@ __global__ void __launch_bounds__(NW * 32, 1) ffn_kernel(const __grid_constant__
         acc[1] = fmaf(d[1], sg1, acc[1]);
         acc[2] = fmaf(d[2], sh1, acc[2]);
         acc[3] = fmaf(d[3], sh1, acc[3]);
+    };
+    auto step = [&](const uint4 q, const uint32_t s) {
+        const int *pc = cc.pc;
+        step_at(q, s, bbase + cc.bk);
         return pc;
     };
     auto consume = [&](const uint4 (&q)[S], const uint32_t (&sc)[S], long long f_first) {
@@ -344,6 +346,40 @@ __global__ void __launch_bounds__(NW * 32, 1) ffn_kernel(const __grid_constant__
         }
     };
 
+    if (ALIGNED) {
+        // every unit is exactly one batch of S steps: straight-line code, the
+        // next unit's loads in flight while the current one is computed
+        auto consume_unit = [&](const uint4 (&q)[S], const uint32_t (&sc)[S]) {
+            const int rb = cc.rb, kc = cc.kc;
+            const int *pc = cc.pc;
+            const __half *bp = bbase + cc.bk;
+#pragma unroll
+            for (int j = 0; j < S; ++j) {
+                step_at(q[j], sc[j], bp + 64 * j);
+            }
+            write_partials<MODE>(&a, acc[0], acc[1], acc[2], acc[3], pc[1], pc[2], rb, kc, lane);
+            acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
+        };
+        const long long nu = ue - ub;
+        for (long long u = 0; u < nu; u += 2) {
+            if (u + 1 < nu)
+                issue(bq[1], bs[1], (u + 1) * S);
+            consume_unit(bq[0], bs[0]);
+            for (int j = 0; j < S; ++j)
+                wk.advance(cc);
+            if (u + 1 >= nu)
+                break;
+            wk.locate(cc);
+            if (u + 2 < nu)
+                issue(bq[0], bs[0], (u + 2) * S);
+            consume_unit(bq[1], bs[1]);
+            for (int j = 0; j < S; ++j)
+                wk.advance(cc);
+            if (u + 2 < nu)
+                wk.locate(cc);
+        }
+        return;
+    }
     for (long long f0 = 0; f0 < F; f0 += 2 * S) {
         issue(bq[1], bs[1], f0 + S);             // no-op past the end
         consume(bq[0], bs[0], f0);
@@ -374,10 +410,10 @@ hfin_kernel(const float *__restrict__ part, int n_kc, int n_entries, int I, cons
     const float *base = part + (size_t)r * 2 * I;
     const size_t kstride = (size_t)n_entries * 2 * I;
     float mx = 0.0f;
-    for (int j0 = threadIdx.x; j0 < I; j0 += 4 * blockDim.x) {
-        float gv[4][kMaxKChunks], uv[4][kMaxKChunks];
+    for (int j0 = threadIdx.x; j0 < I; j0 += 2 * blockDim.x) {
+        float gv[2][kMaxKChunks], uv[2][kMaxKChunks];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
             const int j = j0 + q * blockDim.x;
 #pragma unroll
             for (int kc = 0; kc < kMaxKChunks; ++kc) {
@@ -388,7 +424,7 @@ hfin_kernel(const float *__restrict__ part, int n_kc, int n_entries, int I, cons
             }
         }
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
             const int j = j0 + q * blockDim.x;
             if (j < I) {
                 float G = 0.0f, U = 0.0f;
@@ -456,16 +492,16 @@ combine_kernel(const float *__restrict__ part, int n_kc, int n_entries, const in
         return;
     const size_t kstride = (size_t)n_entries * H;
     float s = 0.0f;
-    for (int s0 = 0; s0 < kps; s0 += 12) {
-        float v[12][kMaxKChunks];
+    for (int s0 = 0; s0 < kps; s0 += 4) {
+        float v[4][kMaxKChunks];
 #pragma unroll
-        for (int i = 0; i < 12; ++i)
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int kc = 0; kc < kMaxKChunks; ++kc)
                 if (s0 + i < kps && kc < n_kc)
                     v[i][kc] = part[(size_t)spos[s0 + i] * H + n + kc * kstride];
 #pragma unroll
-        for (int i = 0; i < 12; ++i) {
+        for (int i = 0; i < 4; ++i) {
             if (s0 + i < kps) {
                 float a = 0.0f;
 #pragma unroll
@@ -505,7 +541,7 @@ __global__ void selftest_decode_kernel(const uint8_t *codes, uint16_t *out, int 
 
 bool ffn_shape_supported(int H, int I) { return H > 0 && I > 0 && H % 64 == 0 && I % 64 == 0 && I <= 16384; }
 
-template <int MODE, bool WIN>
+template <int MODE, bool WIN, bool ALIGNED>
 static cudaError_t launch_one(const FfnArgs &a, int grid, size_t smem, cudaStream_t stream) {
     constexpr int NW = kFfnWarps, D = kFfnBatch;
     static std::atomic<int> set_bytes[64];
@@ -514,13 +550,20 @@ static cudaError_t launch_one(const FfnArgs &a, int grid, size_t smem, cudaStrea
     if (err != cudaSuccess)
         return err;
     if (smem > 48 * 1024 && set_bytes[dev & 63].load() < (int)smem) {
-        err = cudaFuncSetAttribute(ffn_kernel<MODE, NW, D, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        err = cudaFuncSetAttribute(ffn_kernel<MODE, NW, D, WIN, ALIGNED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    (int)smem);
         if (err != cudaSuccess)
             return err;
         set_bytes[dev & 63].store((int)smem);
     }
-    return launch_pdl(ffn_kernel<MODE, NW, D, WIN>, dim3(grid), dim3(NW * 32), smem, stream, a);
+    return launch_pdl(ffn_kernel<MODE, NW, D, WIN, ALIGNED>, dim3(grid), dim3(NW * 32), smem, stream, a);
+}
+
+template <int MODE, bool WIN>
+static cudaError_t launch_aligned(const FfnArgs &a, int grid, size_t smem, cudaStream_t stream) {
+    if (a.steps / a.n_kc == kFfnBatch)
+        return launch_one<MODE, WIN, true>(a, grid, smem, stream);
+    return launch_one<MODE, WIN, false>(a, grid, smem, stream);
 }
 
 // Chooses the shared-memory window when the B rows a CTA can need fit.
@@ -531,9 +574,9 @@ static cudaError_t launch_mode(FfnArgs &a, int grid, int cache_passes, int windo
     a.win_row = a.b_row + 32;
     const size_t win_bytes = (size_t)window_rows * a.win_row * sizeof(__half);
     if (cache_bytes + win_bytes <= (size_t)kWindowBudget)
-        return launch_one<MODE, true>(a, grid, cache_bytes + win_bytes, stream);
+        return launch_aligned<MODE, true>(a, grid, cache_bytes + win_bytes, stream);
     a.win_row = a.b_row;
-    return launch_one<MODE, false>(a, grid, cache_bytes, stream);
+    return launch_aligned<MODE, false>(a, grid, cache_bytes, stream);
 }
 
 cudaError_t launch_ffn(const FfnProblem &pr, void *ws, const WsLayout &L, int num_sms, cudaStream_t stream,
