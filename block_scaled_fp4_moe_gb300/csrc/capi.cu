@@ -2,6 +2,7 @@
 // workspace layout and the launch sequence on the caller's stream.
 #include <atomic>
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -139,6 +140,44 @@ moe_status_t layer_forward(const uint16_t *x, const float *router_w, const float
         return MOE_ERR_CUDA;
     if (ev && cudaEventRecord(ev[4], stream) != cudaSuccess)
         return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+// ------------------------------------------------------------ static scratch
+
+// Scratch of moe_layer_forward_noalloc.  Every device that loads the library
+// keeps this array until the process exits; its size bounds the problem sizes
+// that entry point accepts.
+constexpr size_t kStaticScratchBytes = 16u << 20;
+__device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+std::atomic<uintptr_t> g_static_addr[64];
+std::mutex g_static_mu;
+
+// Device address of the static scratch on the current device.  The first call
+// on a device looks it up (the host-side name of the array is not a device
+// address) and clears its header on `stream`.
+moe_status_t static_scratch(void **out, cudaStream_t stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= 64)
+        return MOE_ERR_UNSUPPORTED_DEVICE;
+    uintptr_t p = g_static_addr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        std::lock_guard<std::mutex> lock(g_static_mu);
+        p = g_static_addr[dev].load(std::memory_order_acquire);
+        if (!p) {
+            void *ptr = nullptr;
+            if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr)
+                return MOE_ERR_CUDA;
+            if (cudaMemsetAsync(ptr, 0, kHdrWords * sizeof(uint32_t), stream) != cudaSuccess)
+                return MOE_ERR_CUDA;
+            p = reinterpret_cast<uintptr_t>(ptr);
+            g_static_addr[dev].store(p, std::memory_order_release);
+        }
+    }
+    *out = reinterpret_cast<void *>(p);
     return MOE_OK;
 }
 
@@ -288,6 +327,28 @@ moe_status_t moe_layer_forward(const uint16_t *x, const float *router_w, const f
                                cudaStream_t stream) {
     return layer_forward(x, router_w, logit_bias, T, top_k, bank, shared_weight, y, topk_ids_out, topk_w_out, ws,
                          ws_bytes, nullptr, stream);
+}
+
+moe_status_t moe_layer_forward_noalloc(const uint16_t *x, const float *router_w, const float *logit_bias, int T,
+                                      int top_k, const moe_mxfp4_bank_t *bank, float shared_weight, uint16_t *y,
+                                      int32_t *topk_ids_out, float *topk_w_out, cudaStream_t stream) {
+    moe_status_t st = check_bank(bank);
+    if (st != MOE_OK)
+        return st;
+    if ((st = check_routing_shape(T, bank->hidden, bank->num_experts, top_k, bank->has_shared)) != MOE_OK)
+        return st;
+    const WsLayout L = WsLayout::make(T, bank->hidden, bank->inter, bank->num_experts, top_k, bank->has_shared);
+    if (L.total > kStaticScratchBytes)
+        return MOE_ERR_WORKSPACE_TOO_SMALL;     // more scratch than the built-in array holds
+    if (T == 0)
+        return MOE_OK;
+    if (!x || !router_w || !y)
+        return MOE_ERR_INVALID_ARG;
+    void *ws = nullptr;
+    if ((st = static_scratch(&ws, stream)) != MOE_OK)
+        return st;
+    return layer_forward(x, router_w, logit_bias, T, top_k, bank, shared_weight, y, topk_ids_out, topk_w_out, ws,
+                         kStaticScratchBytes, nullptr, stream);
 }
 
 moe_status_t moe_layer_forward_profiled(const uint16_t *x, const float *router_w, const float *logit_bias, int T,

@@ -179,6 +179,28 @@ moe_status_t moe_layer_forward(const uint16_t *x, const float *router_w, const f
                                size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * The whole layer without a caller-provided workspace.  The pages have no
+ * counterpart of this call; it exists for callers that cannot allocate device
+ * memory themselves, such as plugins whose host application owns every device
+ * allocation, or runtimes whose device-memory budget is fixed at start-up.
+ * Its scratch is one array of 16 MiB compiled into the library, which every
+ * GPU that loads the library holds until the process exits; problem sizes
+ * whose workspace (moe_workspace_size) exceeds it are rejected with
+ * MOE_ERR_WORKSPACE_TOO_SMALL.  The call allocates nothing (no cudaMalloc or
+ * cudaFree).  The first call on a device looks up the array's device address
+ * and clears its header; make that first call before any stream capture.
+ * All calls on a device share the array and it keeps the last call's
+ * contents: calls that overlap on the GPU (other streams, other host threads)
+ * race and must be serialised by the caller.  Arguments and outputs as in
+ * moe_layer_forward.  A device-side routing error leaves y untouched; it is
+ * recorded in the array's status word, which this call does not report.
+ */
+moe_status_t moe_layer_forward_noalloc(const uint16_t *x, const float *router_w, const float *logit_bias,
+                                       int T, int top_k, const moe_mxfp4_bank_t *bank,
+                                       float shared_weight, uint16_t *y, int32_t *topk_ids_out,
+                                       float *topk_w_out, cudaStream_t stream);
+
+/*
  * The whole layer with the activations in HOST memory: copies x_host [T,H]
  * to the workspace, runs moe_layer_forward, copies y back to y_host [T,H]
  * and waits for the stream.  x_host / y_host should be pinned
