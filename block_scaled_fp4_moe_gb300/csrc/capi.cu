@@ -123,6 +123,24 @@ moe_status_t layer_forward(const uint16_t *x, const float *router_w, const float
     (void)cudaGetLastError();
     if (T == 0)
         return MOE_OK;
+    if (T <= kFusedMaxTokens && fused_plan(T, H, I, E, top_k, S, sms).ok) {
+        // decode-sized T: the whole layer in one cooperative launch
+        if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        const FusedProblem fp{x, router_w, logit_bias, bank, shared_weight, y, ids_out, w_out, T, top_k};
+        const cudaError_t ferr = launch_fused(fp, ws, L, sms, stream);
+        if (ferr == cudaSuccess) {
+            for (int i = 1; ev && i < 5; ++i)
+                if (cudaEventRecord(ev[i], stream) != cudaSuccess)
+                    return MOE_ERR_CUDA;
+            return MOE_OK;
+        }
+        // not all CTAs can be resident (e.g. a partitioned device): use the
+        // multi-launch sequence below
+        if (ferr != cudaErrorCooperativeLaunchTooLarge)
+            return MOE_ERR_CUDA;
+        (void)cudaGetLastError();
+    }
     int32_t *ids = ids_out ? ids_out : ws_at<int32_t>(ws, L.topk_ids);
     float *w = w_out ? w_out : ws_at<float>(ws, L.topk_w);
     const GroupOut go = group_out_for(ws, L, H);
@@ -171,7 +189,7 @@ moe_status_t static_scratch(void **out, cudaStream_t stream) {
             void *ptr = nullptr;
             if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr)
                 return MOE_ERR_CUDA;
-            if (cudaMemsetAsync(ptr, 0, kHdrWords * sizeof(uint32_t), stream) != cudaSuccess)
+            if (cudaMemsetAsync(ptr, 0, kHeaderBytes, stream) != cudaSuccess)
                 return MOE_ERR_CUDA;
             p = reinterpret_cast<uintptr_t>(ptr);
             g_static_addr[dev].store(p, std::memory_order_release);
@@ -222,7 +240,7 @@ moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) 
         return MOE_ERR_MISALIGNED;
     if (ws_bytes < kHdrWords * sizeof(uint32_t))
         return MOE_ERR_WORKSPACE_TOO_SMALL;
-    return from_cuda(cudaMemsetAsync(ws, 0, kHdrWords * sizeof(uint32_t), stream));
+    return from_cuda(cudaMemsetAsync(ws, 0, ws_bytes < kHeaderBytes ? ws_bytes : kHeaderBytes, stream));
 }
 
 moe_status_t moe_route_topk(const uint16_t *x, const float *router_w, const float *logit_bias, int T, int H, int E,

@@ -30,6 +30,10 @@ enum FfnMode { kFfnGateUp = 0, kFfnDown = 1 };
 constexpr int kMaxExperts = 1025;     // E + S (E <= 1024)
 constexpr int kMaxSlots = 32;         // k + S
 constexpr int kMaxTokens = 4096;
+constexpr int kFusedWarps = 12;       // warps per CTA of the single-launch layer kernel
+constexpr int kFusedMaxTokens = 8;    // token counts the single-launch kernel takes
+constexpr int kFusedGridTarget = 152; // CTAs the router tiling is cut for (one per SM)
+constexpr size_t kFusedSmemBudget = 200 * 1024;
 
 // header words of the workspace
 enum HeaderWord : int {
@@ -39,8 +43,22 @@ enum HeaderWord : int {
     kHdrNumActive = 3,
     kHdrNumPasses = 4,
     kHdrNumPasses4 = 5,
+    kHdrBarrier = 6,      // grid-barrier arrivals of the fused layer kernel
+    kHdrDone = 7,         // CTAs of the fused layer kernel that have finished
+    kHdrAbort = 8,        // set when a fused-kernel wait gave up
+    kHdrStamps = 16,      // 16 x u64 phase timestamps of the fused kernel (words 16..47)
     kHdrWords = 64
 };
+
+// The header words are followed by one arrival counter per 16-row tile of
+// the output (H / 16 <= 4096), used by the fused kernel's combine (zero at
+// moe_workspace_init, and every call leaves them at zero), then by per-CTA
+// phase-end times of the fused kernel (diagnostics, 4 x u64 per CTA).
+constexpr size_t kTileCounterOffset = kHdrWords * sizeof(uint32_t);
+constexpr int kMaxTileCounters = 4096;
+constexpr size_t kCtaStampOffset = kTileCounterOffset + kMaxTileCounters * sizeof(uint32_t);
+constexpr int kFusedMaxCtaStamps = 256;
+constexpr size_t kHeaderBytes = kCtaStampOffset + kFusedMaxCtaStamps * 4 * sizeof(unsigned long long);
 
 // A pass: up to kPassTokens consecutive entries of one expert's group.
 struct Pass {
@@ -50,7 +68,7 @@ struct Pass {
     int32_t pad;
 };
 
-inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Upper bound on the passes of capacity `cap` over T*kps entries.
 inline int max_passes(int T, int kps, int n_tot, int cap = kPassTokens) {
@@ -81,10 +99,23 @@ inline int pick_kchunks(int steps, long long units_no_split, size_t partial_byte
     return best;
 }
 
+// Router tiles of the single-launch kernel: groups of 32 experts x chunks of
+// `rows` router rows (a multiple of 8), about one tile per CTA.
+inline void fused_router_tiling(int H, int E, int *groups, int *chunks, int *rows) {
+    *groups = (E + 31) / 32;
+    int target = kFusedGridTarget / *groups;
+    if (target < 1)
+        target = 1;
+    int r = (H + target - 1) / target;
+    r = (r + 7) / 8 * 8;
+    *rows = r;
+    *chunks = (H + r - 1) / r;
+}
+
 // Offsets (bytes) of the workspace regions for one problem size.
 struct WsLayout {
     size_t route_part, topk_ids, topk_w, offsets, sorted_tok, sorted_slot, inv_pos, active, passes, passes4, x16, xundo,
-        gpart, h16, hundo, ypart, counters, xstage, ystage, total;
+        gpart, h16, hundo, ypart, counters, xstage, ystage, fz_rpart, fz_xmax, fz_h32, fz_yent, total;
     int n_kc_gu, n_kc_dn;
 
     static WsLayout make(int T, int H, int I, int E, int k, int S) {
@@ -96,7 +127,7 @@ struct WsLayout {
         const long long active = entries < (size_t)n_tot ? (long long)entries : n_tot;
         L.n_kc_gu = pick_kchunks(H / 64, active * (I / 8), entries * 2 * (size_t)I * sizeof(float));
         L.n_kc_dn = pick_kchunks(I / 64, active * (H / 16), entries * (size_t)H * sizeof(float));
-        size_t o = kHdrWords * sizeof(uint32_t);
+        size_t o = kHeaderBytes;
         auto take = [&](size_t bytes) { o = align_up(o, 256); size_t r = o; o += bytes; return r; };
         L.route_part = take((size_t)nh * T * E * 2 * sizeof(float));
         L.topk_ids = take(entries * sizeof(int32_t));
@@ -117,6 +148,14 @@ struct WsLayout {
         L.counters = take(256);
         L.xstage = take((size_t)T * H * sizeof(uint16_t));
         L.ystage = take((size_t)T * H * sizeof(uint16_t));
+        if (T <= kFusedMaxTokens) {          // single-launch kernel
+            int g, ch, r;
+            fused_router_tiling(H, E, &g, &ch, &r);
+            L.fz_rpart = take((size_t)ch * T * E * sizeof(float2));
+            L.fz_xmax = take((size_t)ch * T * sizeof(float));
+            L.fz_h32 = take(entries * (size_t)I * sizeof(float));
+            L.fz_yent = take(entries * (size_t)H * sizeof(float));
+        }
         L.total = align_up(o, 256);
         return L;
     }
@@ -198,12 +237,12 @@ __device__ __forceinline__ void named_barrier_sync(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
-// D = A(16x16 f16, row) * B(16x8 f16, col) + C, fp32 accumulate.
+// D = A(16x16 f16, row) * B(16x8 f16, col) + C, fp32 accumulate.  Not
+// volatile: independent MMAs may be interleaved by the compiler.
 __device__ __forceinline__ void mma_m16n8k16_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                  uint32_t a3, uint32_t b0, uint32_t b1,
                                                  const float (&c)[4]) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%10,%11,%12,%13};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]),
@@ -242,6 +281,70 @@ __device__ __forceinline__ int f16_shift_for_max(float m) {
     frexpf(m, &e);          // m = f * 2^e, 0.5 <= f < 1
     int s = 15 - e;
     return s < -126 ? -126 : (s > 126 ? 126 : s);
+}
+
+// ------------------------------------------------- error-free arithmetic
+
+// p + e = a * b exactly (one FMA).
+__device__ __forceinline__ void two_prod(float a, float b, float &p, float &e) {
+    p = __fmul_rn(a, b);
+    e = __fmaf_rn(a, b, -p);
+}
+
+// s + e = a + b exactly (Knuth's branch-free TwoSum).
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = __fadd_rn(a, b);
+    float z = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, z)), __fsub_rn(b, z));
+}
+
+// (p, s) += (p2, s2) for unevaluated sums p + s.
+__device__ __forceinline__ void pair_add(float &p, float &s, float p2, float s2) {
+    float q;
+    two_sum(p, p2, p, q);
+    s = __fadd_rn(s, __fadd_rn(s2, q));
+}
+
+// ------------------------------------------------------ weight streaming
+
+constexpr int kStepBytes = 544;          // one 16 x 64 tile of the repacked bank: 512 B codes + 32 B exponents
+
+__device__ __forceinline__ uint4 ld_stream16(const void *p, uint64_t policy) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(policy));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_stream4(const void *p, uint64_t policy) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(policy));
+    return v;
+}
+
+// A word of four E8M0 exponents [s0 s1 s2 s3] (s0 in the low byte) ->
+// 2^(s-127) of each in fp32, via the sm_100-family conversion of exponent
+// pairs to bf16 (exact for 0..254; 0 gives the subnormal 2^-127) and the
+// exact widening of bf16 to fp32.
+__device__ __forceinline__ void e8m0x4_to_f32(uint32_t s, float &f0, float &f1, float &f2, float &f3) {
+    uint32_t lo, hi;
+    asm("{\n\t.reg .b16 a, b;\n\t"
+        "mov.b32 {a, b}, %2;\n\t"
+        "cvt.rn.bf16x2.ue8m0x2 %0, a;\n\t"
+        "cvt.rn.bf16x2.ue8m0x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(s));
+    f0 = __uint_as_float(lo << 16);
+    f1 = __uint_as_float(lo & 0xFFFF0000u);
+    f2 = __uint_as_float(hi << 16);
+    f3 = __uint_as_float(hi & 0xFFFF0000u);
+}
+
+// Byte k of a word of E8M0 exponents -> 2^(s-127) in fp32 (s = 0: 2^-127).
+__device__ __forceinline__ float e8m0_byte(uint32_t w, int k) {
+    const uint32_t top = __byte_perm(w, 0u, 0x0444u | ((uint32_t)k << 12));   // s << 24
+    return __uint_as_float(max(top >> 1, 0x00400000u));
 }
 
 }  // namespace moe

@@ -34,7 +34,6 @@
 
 namespace moe {
 
-constexpr int kStepBytes = 544;          // one 16 x 64 tile: 512 B codes + 32 B exponents
 constexpr int kCacheInts = 20;           // per cached pass: expert, begin, count, pad, boff[8], boff_lo[8]
 
 struct FfnArgs {
@@ -57,26 +56,6 @@ struct FfnArgs {
     int win_offset;              // byte offset of the activation window in shared memory
     int win_row;                 // window row stride in elements (B row length + 32)
 };
-
-__device__ __forceinline__ uint4 ld_stream16(const void *p, uint64_t policy) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p), "l"(policy));
-    return v;
-}
-
-__device__ __forceinline__ uint32_t ld_stream4(const void *p, uint64_t policy) {
-    uint32_t v;
-    asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(policy));
-    return v;
-}
-
-// Byte k of a word of E8M0 exponents -> 2^(s-127) in fp32 (s = 0: 2^-127).
-__device__ __forceinline__ float e8m0_byte(uint32_t w, int k) {
-    const uint32_t top = __byte_perm(w, 0u, 0x0444u | ((uint32_t)k << 12));   // s << 24
-    return __uint_as_float(max(top >> 1, 0x00400000u));
-}
 
 // Position of one warp in its list of units, one 64-element step at a time.
 struct Cursor {

@@ -1,0 +1,1070 @@
+// fused.cu -- the whole MoE layer as one persistent kernel for decode-sized
+// token counts (T <= 8), sm_103a.
+//
+// At a few tokens the layer is a chain of small dependent steps around two
+// weight streams (GLM-5.2 on B300, d9249.github.io, "What it sets out to
+// solve": decode is bound by streaming the active expert weights; the pages'
+// kernel sections name launch gaps and too few CTAs as what kept the first
+// batch-1 GEMMs at a quarter of peak).  Here one cooperative launch of one CTA
+// per SM runs the chain, with two grid-wide waits:
+//
+//  R  router partial dot products (Dot2, error-free) over tiles of the router
+//     matrix; meanwhile the shared expert's gate/up weights, which every token
+//     uses, are prefetched into L2.
+//  -- grid wait 1
+//  T  every CTA sums the partials, selects the top k of each token (shared
+//     expert as slot k), groups the (token, slot) entries by expert and
+//     converts x to f16, all in its own shared memory (the same arithmetic
+//     in every CTA, so every CTA holds the same routing).
+//  G  gate/up: each CTA streams a contiguous range of whole 16-row blocks of
+//     the active experts; its warps split the range's 64-element steps, sum
+//     their partial results in shared memory in warp order and write
+//     h = silu(gate) * up in fp32.  Before the second wait each warp already
+//     issues the loads of its first down batch.
+//  -- grid wait 2
+//  D  down: each CTA converts the h rows of its entries to f16 hi + lo terms
+//     (per-entry power-of-two scale), streams whole 16-row blocks of H, and
+//     writes the per-entry outputs Y.  A per-tile arrival counter tells the
+//     CTA that delivers the last entry of a 16-row output tile to combine that
+//     tile: y = bf16(sum over slots in order of w * Y).  No CTA waits there.
+//
+// Waits spin on a counter in the workspace with a time limit; a wait that runs
+// out records MOE_ERR_DEVICE_TIMEOUT and every CTA leaves without writing y.
+// The cooperative launch guarantees that all CTAs are resident, so a wait can
+// only end that way through a fault elsewhere.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+struct FusedArgs {
+    const uint16_t *x;           // [T, H] bf16
+    const float *wr;             // [H, E] router
+    const float *bias;           // [E] or null
+    const uint8_t *gu, *dn;      // packed gate/up and down sections
+    uint16_t *y;                 // [T, H] bf16
+    int32_t *ids_out;            // [T, kps] or null
+    float *w_out;                // [T, kps] or null
+    uint32_t *hdr;               // workspace header
+    uint32_t *tile_ctr;          // [H / 16] arrival counters
+    float2 *rpart;               // [r_chunks][T][E] router partial pairs
+    float *xmax;                 // [r_chunks][T] max |x| over each router row chunk
+    float *h32;                  // [entries][I] h in sorted entry order
+    float *yent;                 // [entries][H] per-entry outputs
+    unsigned long long *cstamps; // [grid][4] per-CTA phase-end times (diagnostics)
+    int T, H, E, k, S, I;
+    float shared_weight;
+    int r_groups, r_chunks, r_rows;   // router tiles: 32 experts x r_rows rows
+    unsigned gu_unit, dn_unit;        // bytes of one packed row block
+    int xwin_row, hwin_row;           // window row strides (elements)
+    int win_entries;                  // entries the down window holds
+    int off_hundo, off_b;             // dynamic shared-memory offsets (bytes)
+};
+
+namespace {
+
+constexpr int NW = kFusedWarps;
+constexpr int NT = NW * 32;
+constexpr int SB = 8;                 // steps per batch of loads
+constexpr int NBUF = 2;               // register buffers of one batch; NBUF - 1 batches stay in flight
+constexpr int kBatchBytes = SB * kStepBytes;
+constexpr int kMaxEntries = kFusedMaxTokens * kMaxSlots;
+constexpr unsigned long long kWaitLimitNs = 200ull * 1000 * 1000;
+constexpr int kL2AheadDown = 16;     // batches a warp asks L2 for before the wait that precedes the down phase
+constexpr int kL2Ahead = 0;          // batches a warp asks L2 for ahead of its register loads (0: none)
+constexpr bool kL2PerLane = false;   // ask per 128-byte line from every lane instead of one bulk request
+
+// Routing results every CTA derives for itself in phase T.
+struct RouteState {
+    int n_gu, n_dn, bad, n_comb;
+    int n_cand[kFusedMaxTokens];   // top-k candidates per token
+    float xundo[kFusedMaxTokens];  // 2^-s of token t's f16 scaling
+    float xscale[kFusedMaxTokens]; // 2^s
+    int sel_id[kMaxEntries];       // entry t*kps+s -> expert
+    float sel_w[kMaxEntries];      // entry -> combine weight
+    int inv_pos[kMaxEntries];      // entry -> sorted position
+    int sorted_ent[kMaxEntries];   // sorted position -> entry
+    int sorted_tok[kMaxEntries];   // sorted position -> token
+    int gsize[kMaxEntries];        // size of the group starting at a sorted position (else 0)
+    Pass pgu[kMaxEntries];         // gate/up passes: one per active expert (T <= 8)
+    Pass pdn[kMaxEntries];         // down passes of <= 4 entries
+};
+
+// The kernel's shared memory: the dynamic region (windows, scratch) and the
+// routing state, declared here so that every function addresses them as
+// shared memory.
+extern __shared__ __align__(16) uint8_t fz_smem[];
+__shared__ RouteState fz_rs;
+
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void stamp(const FusedArgs &a, int i) {
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        reinterpret_cast<unsigned long long *>(a.hdr + kHdrStamps)[i] = globaltimer_ns();
+}
+
+__device__ __forceinline__ void cta_stamp(const FusedArgs &a, int i) {
+    if (threadIdx.x == 0 && blockIdx.x < kFusedMaxCtaStamps)
+        a.cstamps[blockIdx.x * 4 + i] = globaltimer_ns();
+}
+
+// Grid-wide wait in two halves.  grid_arrive: after every thread's earlier
+// writes (each thread fences its own), one arrival per CTA on the counter.
+// grid_wait: until `target` (= waits so far x CTAs) arrivals are counted.
+// Work that needs nobody else's results can run in between.  A wait gives up
+// after kWaitLimitNs (or when another CTA's wait gave up) and returns false.
+__device__ void grid_arrive(const FusedArgs &a) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0)
+        atomicAdd(a.hdr + kHdrBarrier, 1u);
+}
+
+__device__ bool grid_wait(const FusedArgs &a, unsigned target) {
+    __shared__ int ok;
+    if (threadIdx.x == 0) {
+        const unsigned long long t0 = globaltimer_ns();
+        int r = 1;
+        while (ld_acquire_u32(a.hdr + kHdrBarrier) < target) {
+            if (ld_acquire_u32(a.hdr + kHdrAbort)) {
+                r = 0;
+                break;
+            }
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                record_status(a.hdr, MOE_ERR_DEVICE_TIMEOUT);
+                atomicExch(a.hdr + kHdrAbort, 1u);
+                r = 0;
+                break;
+            }
+        }
+        __threadfence();
+        ok = r;
+    }
+    __syncthreads();
+    return ok != 0;
+}
+
+// ------------------------------------------------------------- phase R
+
+// Router tile (32 experts x r_rows rows): each warp pulls its rows (every
+// NW-th row) into L1 while the tile's x rows are staged, then accumulates one
+// Dot2 pair per token and lane (expert); the CTA sums the warps' pairs in warp
+// order.  CTAs of expert group 0 also record max |x| of their rows per token.
+__device__ void phase_router(const FusedArgs &a, uint8_t *smB) {
+    __shared__ unsigned xm[kFusedMaxTokens];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int T = a.T, H = a.H, E = a.E;
+    float *xs = reinterpret_cast<float *>(smB);                                  // [T][r_rows]
+    float2 *red = reinterpret_cast<float2 *>(smB + align_up(T * a.r_rows * 4, 16));   // [NW][T][32]
+    const int tiles = a.r_groups * a.r_chunks;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+        const int gi = tile % a.r_groups, ci = tile / a.r_groups;
+        const int r0 = ci * a.r_rows, nr = min(H - r0, a.r_rows);
+        const int e0 = gi * 32, e1 = min(E, e0 + 32);       // experts [e0, e1) of this tile
+        const int nrw = nr > warp ? (nr - warp + NW - 1) / NW : 0;
+        const float *wrow = a.wr + (size_t)(r0 + warp) * E;  // this warp's first row
+        const size_t wstride = (size_t)NW * E;
+        for (int j = lane; j < nrw; j += 32) {
+            prefetch_l1(wrow + j * wstride + e0);
+            prefetch_l1(wrow + j * wstride + e1 - 1);
+        }
+        __syncthreads();
+        if (threadIdx.x < kFusedMaxTokens)
+            xm[threadIdx.x] = 0u;
+        __syncthreads();
+        for (int i = threadIdx.x; i < T * (nr / 8); i += NT) {
+            const int t = i / (nr / 8), c8 = i - t * (nr / 8);
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)t * H + r0) + c8);
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+            float *d = xs + t * a.r_rows + c8 * 8;
+            float m = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                d[2 * j] = __uint_as_float(w4[j] << 16);
+                d[2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
+                m = fmaxf(m, fmaxf(fabsf(d[2 * j]), fabsf(d[2 * j + 1])));
+            }
+            if (gi == 0)
+                atomicMax(&xm[t], __float_as_uint(m));
+        }
+        __syncthreads();
+        stamp(a, 8);
+        if (gi == 0 && threadIdx.x < T)
+            a.xmax[ci * T + threadIdx.x] = __uint_as_float(xm[threadIdx.x]);
+        const bool live = e0 + lane < e1;
+        for (int t = 0; t < T; ++t) {
+            const float *xr = xs + t * a.r_rows + warp;
+            float p = 0.0f, q = 0.0f;
+#pragma unroll 4
+            for (int j = 0; j < nrw; ++j) {
+                const float w = live ? __ldg(wrow + j * wstride + e0 + lane) : 0.0f;
+                float hp, er, s;
+                two_prod(xr[j * NW], w, hp, er);
+                two_sum(p, hp, p, s);
+                q = __fadd_rn(q, __fadd_rn(s, er));
+            }
+            red[(warp * T + t) * 32 + lane] = make_float2(p, q);
+        }
+        __syncthreads();
+        for (int t = warp; t < T; t += NW) {
+            float P = red[t * 32 + lane].x, Q = red[t * 32 + lane].y;
+            for (int w2 = 1; w2 < NW; ++w2) {
+                const float2 v = red[(w2 * T + t) * 32 + lane];
+                pair_add(P, Q, v.x, v.y);
+            }
+            if (live)
+                a.rpart[((size_t)ci * T + t) * E + e0 + lane] = make_float2(P, Q);
+        }
+    }
+}
+
+// The shared expert's gate/up weights do not depend on the routing: pull
+// this CTA's slice of them into L2 while the router runs.
+__device__ void prefetch_shared_expert(const FusedArgs &a) {
+    if (!a.S || threadIdx.x != 0)
+        return;
+    const size_t total = (size_t)(a.I / 8) * a.gu_unit;
+    const uint8_t *base = a.gu + (size_t)a.E * total;
+    const size_t piece = align_up((total + gridDim.x - 1) / gridDim.x, 16);
+    const size_t lo = (size_t)blockIdx.x * piece;
+    const size_t hi = lo + piece < total ? lo + piece : total;
+    for (size_t o = lo; o < hi; o += 16384) {
+        const size_t n = hi - o < 16384 ? hi - o : 16384;
+        prefetch_l2(base + o, (uint32_t)n);
+    }
+}
+
+// ------------------------------------------------------------- phase T
+
+// x -> window rows in f16, x[t] scaled by 2^s[t] so that max |x[t]| lies in
+// [2^14, 2^15) (rs.xundo[t] = 2^-s[t]); run by the `nthr` threads numbered
+// `lt` = 0.. of the warps that do not select experts.
+__device__ void x_to_window(const FusedArgs &a, const RouteState &rs, __half *xwin, int lt, int nthr) {
+    const int H = a.H, n8 = H / 8, total = a.T * n8;
+    for (int i0 = lt; i0 < total; i0 += 4 * nthr) {
+        uint4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = i0 + j * nthr;
+            if (i < total) {
+                const int t = i / n8, c = i - t * n8;
+                v[j] = __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)t * H) + c);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = i0 + j * nthr;
+            if (i < total) {
+                const int t = i / n8, c = i - t * n8;
+                const float sc = rs.xscale[t];
+                const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+                uint32_t o[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    __half2 h2 = __floats2half2_rn(__uint_as_float(w4[k] << 16) * sc,
+                                                   __uint_as_float(w4[k] & 0xFFFF0000u) * sc);
+                    o[k] = *reinterpret_cast<uint32_t *>(&h2);
+                }
+                *reinterpret_cast<uint4 *>(xwin + (size_t)t * a.xwin_row + 8 * c) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    }
+}
+
+// Order key of a normalised logit pair (hi, lo): larger value -> larger key.
+// lo is below half an ulp of hi, so (hi, lo) order is the order of the sums.
+__device__ __forceinline__ unsigned long long logit_key(float hi, float lo) {
+    auto mono = [](float v) -> uint32_t {
+        const uint32_t b = __float_as_uint(v);
+        return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    };
+    return ((unsigned long long)mono(hi) << 32) | mono(lo);
+}
+
+__device__ __forceinline__ float unkey_half(uint32_t m) {
+    return __uint_as_float((m & 0x80000000u) ? (m & 0x7FFFFFFFu) : ~m);
+}
+
+// Returns false when the routing selected an invalid expert (non-finite
+// logits); every CTA reaches the same answer.
+__device__ bool phase_route(const FusedArgs &a, RouteState &rs, uint8_t *smA, uint8_t *smB) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    const int T = a.T, E = a.E, k = a.k, kps = a.k + a.S, n = T * kps, n_tot = a.E + a.S;
+    const int Ep = (E + 31) & ~31;                  // experts padded to whole groups of 32
+    const int cmax = (Ep / 32) * k;                  // top-k candidates per token at most
+    unsigned long long *key = reinterpret_cast<unsigned long long *>(smB);          // [T][Ep]
+    int *cand = reinterpret_cast<int *>(smB + (size_t)T * Ep * sizeof(unsigned long long));   // [T][cmax]
+    // logits: S consecutive threads share one logit's chunk partials and
+    // combine their sums in a fixed tree order
+    int S = 1;
+    while (S < 8 && 2 * S * T * E <= NT)
+        S *= 2;
+    const int cps = (a.r_chunks + S - 1) / S;
+    for (int i0 = 0; i0 < T * E * S; i0 += NT) {
+        const int i = i0 + tid, item = i / S, part = i - item * S;
+        const bool live = item < T * E;
+        const int t = live ? item / E : 0, e = live ? item - t * E : 0;
+        const int c_lo = part * cps, c_hi = min(a.r_chunks, c_lo + cps);
+        float P = 0.0f, Q = 0.0f;
+        for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+            float2 v[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                if (live && c0 + c < c_hi)
+                    v[c] = __ldcg(a.rpart + ((size_t)(c0 + c) * T + t) * E + e);
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                if (live && c0 + c < c_hi)
+                    pair_add(P, Q, v[c].x, v[c].y);
+        }
+        for (int d = 1; d < S; d *= 2) {            // S divides 32: groups stay inside a warp
+            const float oP = __shfl_xor_sync(0xffffffffu, P, d), oQ = __shfl_xor_sync(0xffffffffu, Q, d);
+            if ((part & d) == 0)
+                pair_add(P, Q, oP, oQ);
+        }
+        if (live && part == 0) {
+            pair_add(P, Q, a.bias ? __ldg(a.bias + e) : 0.0f, 0.0f);
+            float hi, lo;
+            two_sum(P, Q, hi, lo);
+            if (!isfinite(hi))
+                rs.bad = 1;                          // non-finite router logits
+            key[t * Ep + e] = logit_key(hi, lo);
+        }
+    }
+    for (int i = tid; i < T * (Ep - E); i += NT)     // padding sorts below every real key
+        key[(i / (Ep - E)) * Ep + E + i % (Ep - E)] = 0ull;
+    // per-token f16 scale of x from the router tiles' maxima (the last warps,
+    // which have the fewest logits to sum)
+    if (warp >= NW - T) {
+        const int t = warp - (NW - T);
+        float m = 0.0f;
+        for (int c = lane; c < a.r_chunks; c += 32)
+            m = fmaxf(m, __ldcg(a.xmax + c * T + t));
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1)
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+        if (lane == 0) {
+            const int sh = f16_shift_for_max(m);
+            rs.xundo[t] = exp2i(-sh);
+            rs.xscale[t] = exp2i(sh);
+        }
+    }
+    __syncthreads();
+    stamp(a, 9);
+    // top k: an expert ranked k or lower inside its group of 32 cannot be in
+    // the top k, so the slots are the ranks among the group survivors; order
+    // is (key descending, index ascending)
+    for (int i = tid; i < T * Ep; i += NT) {
+        const int t = i / Ep, e = i - t * Ep;
+        const unsigned long long *g = key + t * Ep + (e & ~31);
+        const unsigned long long my = g[e & 31];
+        int r = 0;
+#pragma unroll 8
+        for (int j = 0; j < 32; ++j) {
+            const unsigned long long o = g[j];
+            r += (o > my) | ((o == my) & (j < (e & 31)));
+        }
+        if (e < E && r < k)
+            cand[t * cmax + atomicAdd(&rs.n_cand[t], 1)] = e;
+    }
+    __syncthreads();
+    for (int i = tid; i < T * cmax; i += NT) {
+        const int t = i / cmax, c = i - t * cmax, nc = rs.n_cand[t];
+        if (c >= nc)
+            continue;
+        const int e = cand[t * cmax + c];
+        const unsigned long long my = key[t * Ep + e];
+        int r = 0;
+        for (int j = 0; j < nc; ++j) {
+            const int oe = cand[t * cmax + j];
+            const unsigned long long o = key[t * Ep + oe];
+            r += (o > my) | ((o == my) & (oe < e));
+        }
+        if (r < k)
+            rs.sel_id[t * kps + r] = e;
+    }
+    __syncthreads();
+    if (warp < T) {
+        // softmax over the kept logits, relative to the largest; the
+        // denominator is summed in slot order
+        const int t = warp;
+        float ex = 0.0f;
+        int id = 0;
+        if (lane < k) {
+            id = rs.sel_id[t * kps + lane];
+            const unsigned long long k0 = key[t * Ep + rs.sel_id[t * kps]], kr = key[t * Ep + id];
+            const float h0 = unkey_half((uint32_t)(k0 >> 32)), l0 = unkey_half((uint32_t)k0);
+            const float hr = unkey_half((uint32_t)(kr >> 32)), lr = unkey_half((uint32_t)kr);
+            ex = expf(__fadd_rn(__fsub_rn(hr, h0), __fsub_rn(lr, l0)));
+        }
+        float denom = 0.0f;
+        for (int r = 0; r < k; ++r)
+            denom += __shfl_sync(0xffffffffu, ex, r);
+        if (lane < k) {
+            const float w = ex / denom;
+            rs.sel_w[t * kps + lane] = w;
+            if (blockIdx.x == 0) {
+                if (a.ids_out)
+                    a.ids_out[t * kps + lane] = id;
+                if (a.w_out)
+                    a.w_out[t * kps + lane] = w;
+            }
+        }
+        if (a.S && lane == k) {
+            rs.sel_id[t * kps + k] = E;
+            rs.sel_w[t * kps + k] = a.shared_weight;
+            if (blockIdx.x == 0) {
+                if (a.ids_out)
+                    a.ids_out[t * kps + k] = E;
+                if (a.w_out)
+                    a.w_out[t * kps + k] = a.shared_weight;
+            }
+        }
+    } else {
+        x_to_window(a, rs, reinterpret_cast<__half *>(smA), tid - 32 * T, NT - 32 * T);
+    }
+    __syncthreads();
+    stamp(a, 10);
+    if (tid < n && (unsigned)rs.sel_id[tid] >= (unsigned)n_tot)
+        rs.bad = 1;
+    __syncthreads();
+    if (rs.bad) {
+        if (blockIdx.x == 0 && tid == 0)
+            record_status(a.hdr, MOE_ERR_DEVICE_ASSERT);
+        return false;
+    }
+    // sorted position of entry i: entries with a smaller expert, or the same
+    // expert and a smaller index, come first
+    if (tid < n) {
+        const int ei = rs.sel_id[tid];
+        int pos = 0;
+        for (int j = 0; j < n; ++j) {
+            const int ej = rs.sel_id[j];
+            pos += (ej < ei) || (ej == ei && j < tid);
+        }
+        rs.inv_pos[tid] = pos;
+        rs.sorted_ent[pos] = tid;
+        rs.sorted_tok[pos] = tid / kps;
+    }
+    __syncthreads();
+    if (tid < n) {
+        const int ex = rs.sel_id[rs.sorted_ent[tid]];
+        int size = 0;
+        if (tid == 0 || rs.sel_id[rs.sorted_ent[tid - 1]] != ex) {
+            size = 1;
+            while (tid + size < n && rs.sel_id[rs.sorted_ent[tid + size]] == ex)
+                ++size;
+        }
+        rs.gsize[tid] = size;
+    }
+    __syncthreads();
+    if (tid < n && rs.gsize[tid] > 0) {
+        int gi = 0, di = 0;
+        for (int j = 0; j < tid; ++j) {
+            const int s = rs.gsize[j];
+            gi += s > 0;
+            di += (s + kPassEntries - 1) / kPassEntries;
+        }
+        const int size = rs.gsize[tid], ex = rs.sel_id[rs.sorted_ent[tid]];
+        rs.pgu[gi] = Pass{ex, tid, size, 0};
+        for (int q = 0; q * kPassEntries < size; ++q)
+            rs.pdn[di + q] = Pass{ex, tid + q * kPassEntries, min(kPassEntries, size - q * kPassEntries), 0};
+    }
+    if (tid == 0) {
+        int gi = 0, di = 0;
+        for (int j = 0; j < n; ++j) {
+            const int s = rs.gsize[j];
+            gi += s > 0;
+            di += (s + kPassEntries - 1) / kPassEntries;
+        }
+        rs.n_gu = gi;
+        rs.n_dn = di;
+    }
+    __syncthreads();
+    return true;
+}
+
+// ------------------------------------------------------- streaming (G, D)
+
+struct UnitCursor {
+    int ul, bi;      // CTA-local unit, batch within the unit
+    int P, rb;       // pass and row block of the unit
+};
+
+__device__ __forceinline__ void cursor_set(UnitCursor &c, long long u0, int b, int nb, int upe) {
+    c.ul = b / nb;
+    c.bi = b - c.ul * nb;
+    const long long u = u0 + c.ul;
+    c.P = (int)(u / upe);
+    c.rb = (int)(u - (long long)c.P * upe);
+}
+
+__device__ __forceinline__ void cursor_next(UnitCursor &c, int nb, int upe) {
+    if (++c.bi == nb) {
+        c.bi = 0;
+        ++c.ul;
+        if (++c.rb == upe) {
+            c.rb = 0;
+            ++c.P;
+        }
+    }
+}
+
+// Warp owning CTA-local batch b when Bc batches are split over NW warps as
+// [w*Bc/NW, (w+1)*Bc/NW).
+__device__ __forceinline__ int warp_of_batch(long long b, long long Bc) { return (int)(((b + 1) * NW - 1) / Bc); }
+
+struct Phase {
+    const uint8_t *sec;      // packed section
+    unsigned unit_bytes;     // bytes of one row block
+    int upe;                 // row blocks per expert
+    int steps;               // 64-element steps per row block
+    int nb;                  // batches per row block
+    const Pass *passes;
+    const __half *win;       // activation window in shared memory
+    int win_row;
+    int e_lo;                // down: first entry of the window
+    const float *hundo;      // down: per window entry, undoes the h scaling
+};
+
+template <bool FULL>
+__device__ __forceinline__ void load_batch(uint4 (&q)[SB], uint32_t (&s)[SB], const Phase &ph, const UnitCursor &c,
+                                           int lane, uint64_t pol) {
+    const uint8_t *p = ph.sec + ((size_t)ph.passes[c.P].expert * ph.upe + c.rb) * ph.unit_bytes +
+                       (size_t)c.bi * kBatchBytes;
+    const int ns = FULL ? SB : min(SB, ph.steps - c.bi * SB);
+#pragma unroll
+    for (int j = 0; j < SB; ++j) {
+        if (FULL || j < ns) {
+            q[j] = ld_stream16(p + j * kStepBytes + lane * 16, pol);
+            s[j] = ld_stream4(p + j * kStepBytes + 512 + (lane >> 2) * 4, pol);
+        }
+    }
+}
+
+// Ask L2 for a whole batch ahead of its register loads.
+__device__ __forceinline__ void prefetch_batch(const Phase &ph, const UnitCursor &c, int lane, bool per_lane) {
+    const uint8_t *p = ph.sec + ((size_t)ph.passes[c.P].expert * ph.upe + c.rb) * ph.unit_bytes +
+                       (size_t)c.bi * kBatchBytes;
+    const int bytes = min(SB, ph.steps - c.bi * SB) * kStepBytes;
+    if (per_lane) {
+        for (int o = lane * 128; o < bytes; o += 32 * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p + o));
+    } else if (lane == 0) {
+        prefetch_l2(p, (uint32_t)bytes);
+    }
+}
+
+// One 16 x 64 step: decode, two MMAs per 32-element block, block scales.
+__device__ __forceinline__ void step_mma(const uint4 q, const uint32_t s, const __half *bp, float (&acc)[4]) {
+    const uint4 b0 = *reinterpret_cast<const uint4 *>(bp);
+    const uint4 b1 = *reinterpret_cast<const uint4 *>(bp + 32);
+    uint32_t pa[4], qa[4];
+    const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    float d[4], e[4];
+    float sg0, sg1, sh0, sh1;       // rows g / g+8, blocks 2q / 2q+1
+    e8m0x4_to_f32(s, sg0, sg1, sh0, sh1);
+    decode_e2m1x8(q.x, pa);
+    decode_e2m1x8(q.y, qa);
+    mma_m16n8k16_f16(d, pa[0], qa[0], pa[1], qa[1], b0.x, b0.y, zero);
+    mma_m16n8k16_f16(d, pa[2], qa[2], pa[3], qa[3], b0.z, b0.w, d);
+    decode_e2m1x8(q.z, pa);
+    decode_e2m1x8(q.w, qa);
+    mma_m16n8k16_f16(e, pa[0], qa[0], pa[1], qa[1], b1.x, b1.y, zero);
+    mma_m16n8k16_f16(e, pa[2], qa[2], pa[3], qa[3], b1.z, b1.w, e);
+    acc[0] = fmaf(d[0], sg0, acc[0]);
+    acc[1] = fmaf(d[1], sg0, acc[1]);
+    acc[2] = fmaf(d[2], sh0, acc[2]);
+    acc[3] = fmaf(d[3], sh0, acc[3]);
+    acc[0] = fmaf(e[0], sg1, acc[0]);
+    acc[1] = fmaf(e[1], sg1, acc[1]);
+    acc[2] = fmaf(e[2], sh1, acc[2]);
+    acc[3] = fmaf(e[3], sh1, acc[3]);
+}
+
+template <bool FULL>
+__device__ __forceinline__ void compute_batch(const uint4 (&q)[SB], const uint32_t (&s)[SB], const Phase &ph,
+                                              const UnitCursor &c, const __half *bp, float (&acc)[4]) {
+    const int ns = FULL ? SB : min(SB, ph.steps - c.bi * SB);
+    const __half *b = bp + c.bi * (SB * 64);
+#pragma unroll
+    for (int j = 0; j < SB; ++j)
+        if (FULL || j < ns)
+            step_mma(q[j], s[j], b + 64 * j, acc);
+}
+
+// This lane's B-operand pointer at the start of the unit under the cursor:
+// gate/up reads the x row of the pass's token in MMA column g; down reads
+// the hi (columns 0..3) or lo (4..7) row of the pass's entry g % 4.
+__device__ __forceinline__ const __half *unit_bptr(int mode, const Phase &ph, const RouteState &rs,
+                                                   const UnitCursor &c, int lane) {
+    const Pass ps = ph.passes[c.P];
+    const int g = lane >> 2, cc = lane & 3;
+    const int row = mode == kFfnGateUp ? rs.sorted_tok[ps.begin + min(g, ps.count - 1)]
+                                       : 2 * (ps.begin + min(g & 3, ps.count - 1) - ph.e_lo) + (g >> 2);
+    return ph.win + (size_t)row * ph.win_row + 8 * cc;
+}
+
+// A unit's sums are complete: write h = silu(gate) * up (gate/up) or the
+// per-entry outputs Y (down) of its real columns.
+__device__ __forceinline__ void finish_unit(int mode, const FusedArgs *a, const RouteState *rs, const Pass *passes,
+                                         int e_lo, const float *hundo, int P, int rb, float a0, float a1, float a2,
+                                         float a3) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    const Pass ps = passes[P];
+    if (mode == kFfnGateUp) {
+        const float acc[4] = {a0, a1, a2, a3};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int n = 2 * c + h;
+            if (n < ps.count) {
+                const float xu = rs->xundo[rs->sorted_tok[ps.begin + n]];
+                const float G = acc[h] * xu, U = acc[2 + h] * xu;
+                a->h32[(size_t)(ps.begin + n) * a->I + 8 * rb + g] = G / (1.0f + expf(-G)) * U;
+            }
+        }
+    } else {
+        float y[4] = {a0, a1, a2, a3};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)   // add the lo column n+4 to the hi column n
+            y[i] += __shfl_xor_sync(0xffffffffu, y[i], 2);
+        if (c < 2) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int n = 2 * c + h;
+                if (n < ps.count) {
+                    const int e = ps.begin + n;
+                    const float u = hundo[e - e_lo];
+                    float *dst = a->yent + (size_t)e * a->H + 16 * rb;
+                    dst[g] = y[h] * u;
+                    dst[g + 8] = y[2 + h] * u;
+                }
+            }
+        }
+    }
+}
+
+// h rows of window entries -> f16 hi + lo rows, scaled per entry by 2^s with
+// max|h| in [2^14, 2^15); one warp per entry.
+__device__ void h_to_window(const FusedArgs &a, int e_lo, int n_win, int win_row, __half *win, float *hundo) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, I = a.I;
+    for (int ew = warp; ew < n_win; ew += NW) {
+        const float4 *src = reinterpret_cast<const float4 *>(a.h32 + (size_t)(e_lo + ew) * I);
+        float m = 0.0f;
+        for (int i = lane; i < I / 4; i += 32) {
+            const float4 v = __ldcg(src + i);
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1)
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
+        const int sh = f16_shift_for_max(m);
+        const float sc = exp2i(sh);
+        __half *hi = win + (size_t)(2 * ew) * win_row, *lo = hi + win_row;
+        for (int i = lane; i < I / 4; i += 32) {
+            const float4 v = __ldcg(src + i);
+            const float vv[4] = {v.x * sc, v.y * sc, v.z * sc, v.w * sc};
+            __half hv[4], lv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                hv[j] = __float2half_rn(vv[j]);
+                lv[j] = __float2half_rn(vv[j] - __half2float(hv[j]));
+            }
+            *reinterpret_cast<uint2 *>(hi + 4 * i) = *reinterpret_cast<const uint2 *>(hv);
+            *reinterpret_cast<uint2 *>(lo + 4 * i) = *reinterpret_cast<const uint2 *>(lv);
+        }
+        if (lane == 0)
+            hundo[ew] = exp2i(-sh);
+    }
+}
+
+// Rows [16 rb, 16 rb + 16) of y for every token, from the per-entry outputs.
+__device__ void combine_tile(const FusedArgs &a, const RouteState &rs, int rb, int lane) {
+    const int kps = a.k + a.S, T = a.T, H = a.H;
+    for (int i = lane; i < T * 16; i += 32) {
+        const int t = i >> 4, r = 16 * rb + (i & 15);
+        float v[kMaxSlots];
+#pragma unroll
+        for (int s = 0; s < kMaxSlots; ++s)
+            if (s < kps)
+                v[s] = __ldcg(a.yent + (size_t)rs.inv_pos[t * kps + s] * H + r);
+        float acc = 0.0f;
+#pragma unroll
+        for (int s = 0; s < kMaxSlots; ++s)
+            if (s < kps)
+                acc = fmaf(rs.sel_w[t * kps + s], v[s], acc);
+        const __nv_bfloat16 bv = __float2bfloat16_rn(acc);
+        a.y[(size_t)t * H + r] = *reinterpret_cast<const uint16_t *>(&bv);
+    }
+}
+
+// One streaming phase, shared by gate/up and down so that the down phase runs
+// the code the gate/up phase has just brought into the instruction cache.
+// Each CTA takes a contiguous range of whole row-block units; its warps take
+// contiguous ranges of the range's batches.  A warp finishes the units it
+// streams completely; units shared between warps leave partial sums in slot
+// 2*warp (the warp's first unit) or 2*warp+1 (its last unit), which the warp
+// holding the unit's last batch adds up in warp order.  The first batch is
+// issued before anything else; for the down phase that is before the wait for
+// every CTA's h.  Returns false when that wait gave up.
+template <bool FULL>
+__device__ __forceinline__ bool stream_phase(const FusedArgs *ap, int mode) {
+    const FusedArgs &a = *ap;
+    RouteState &rs = fz_rs;
+    uint8_t *smem = fz_smem;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int G = gridDim.x;
+    const uint64_t pol = l2_evict_first_policy();
+    float *hundo = reinterpret_cast<float *>(smem + a.off_hundo);
+    float *slots = reinterpret_cast<float *>(smem + a.off_b);
+    int *comb = reinterpret_cast<int *>(smem + a.off_b + 2 * NW * 32 * 4 * sizeof(float));
+    const bool down = mode == kFfnDown;
+    Phase ph;
+    ph.sec = down ? a.dn : a.gu;
+    ph.unit_bytes = down ? a.dn_unit : a.gu_unit;
+    ph.upe = down ? a.H / 16 : a.I / 8;
+    ph.steps = down ? a.I / 64 : a.H / 64;
+    ph.nb = (ph.steps + SB - 1) / SB;
+    ph.passes = down ? rs.pdn : rs.pgu;
+    ph.win = reinterpret_cast<const __half *>(smem);
+    ph.win_row = down ? a.hwin_row : a.xwin_row;
+    ph.e_lo = 0;
+    ph.hundo = hundo;
+    const long long U = (long long)(down ? rs.n_dn : rs.n_gu) * ph.upe;
+    const long long u0 = (long long)blockIdx.x * U / G, u1 = (long long)(blockIdx.x + 1) * U / G;
+    const long long Bc = (u1 - u0) * ph.nb;
+    const int bw0 = (int)((long long)warp * Bc / NW), bw1 = (int)((long long)(warp + 1) * Bc / NW);
+    uint4 q[NBUF][SB];
+    uint32_t s[NBUF][SB];
+    UnitCursor cc, lc, pc;
+    int lb = bw0;                         // next batch to load into registers
+    int pb = bw0;                         // next batch to ask L2 for
+    if (bw0 < bw1) {
+        cursor_set(cc, u0, bw0, ph.nb, ph.upe);
+        lc = cc;
+#pragma unroll
+        for (int i = 0; i < NBUF - 1; ++i) {
+            if (lb < bw1) {
+                load_batch<FULL>(q[i], s[i], ph, lc, lane, pol);
+                cursor_next(lc, ph.nb, ph.upe);
+                ++lb;
+            }
+        }
+        pc = lc;
+        pb = lb;
+        for (int i = 0; i < kL2Ahead && pb < bw1; ++i, ++pb) {
+            prefetch_batch(ph, pc, lane, kL2PerLane);
+            cursor_next(pc, ph.nb, ph.upe);
+        }
+        if (down) {                       // L2 fetches the next batches while the CTAs wait
+            UnitCursor pc = lc;
+            for (int i = 0, pb = lb; i < kL2AheadDown && pb < bw1; ++i, ++pb) {
+                prefetch_batch(ph, pc, lane, false);
+                cursor_next(pc, ph.nb, ph.upe);
+            }
+        }
+    }
+    if (down) {
+        if (!grid_wait(a, 2u * G))
+            return false;
+        stamp(a, 5);
+        cta_stamp(a, 1);
+        if (u1 > u0) {
+            const int P0 = (int)(u0 / ph.upe), P1 = (int)((u1 - 1) / ph.upe);
+            ph.e_lo = rs.pdn[P0].begin;
+            const int n_win = rs.pdn[P1].begin + rs.pdn[P1].count - ph.e_lo;
+            if (n_win > a.win_entries) {           // cannot happen for the sizes the host admits
+                if (threadIdx.x == 0)
+                    record_status(a.hdr, MOE_ERR_DEVICE_ASSERT);
+                return true;
+            }
+            h_to_window(a, ph.e_lo, n_win, ph.win_row, reinterpret_cast<__half *>(smem), hundo);
+        }
+        __syncthreads();
+    }
+    if (bw0 < bw1) {
+        const int ul_first = cc.ul;
+        const __half *bp = unit_bptr(mode, ph, rs, cc, lane);
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        int b = bw0;
+        auto end_batch = [&]() {
+            const bool unit_end = cc.bi == ph.nb - 1;
+            const bool range_end = b + 1 == bw1;
+            if (unit_end || range_end) {
+                if (unit_end && cc.ul * ph.nb >= bw0) {
+                    finish_unit(mode, &a, &rs, ph.passes, ph.e_lo, ph.hundo, cc.P, cc.rb, acc[0], acc[1], acc[2],
+                                acc[3]);
+                } else {
+                    const int slot = cc.ul == ul_first ? 2 * warp : 2 * warp + 1;
+                    *reinterpret_cast<float4 *>(slots + (slot * 32 + lane) * 4) =
+                        make_float4(acc[0], acc[1], acc[2], acc[3]);
+                }
+                acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
+            }
+            cursor_next(cc, ph.nb, ph.upe);
+            if (cc.bi == 0 && !range_end)
+                bp = unit_bptr(mode, ph, rs, cc, lane);
+        };
+        // ring of NBUF register buffers: buffer i holds batch b; the load of
+        // batch b + NBUF - 1 goes into the buffer consumed last
+        bool more = true;
+        while (more) {
+#pragma unroll
+            for (int i = 0; i < NBUF; ++i) {
+                if (lb < bw1) {
+                    load_batch<FULL>(q[(i + NBUF - 1) % NBUF], s[(i + NBUF - 1) % NBUF], ph, lc, lane, pol);
+                    cursor_next(lc, ph.nb, ph.upe);
+                    ++lb;
+                    if (kL2Ahead > 0 && pb < bw1) {
+                        prefetch_batch(ph, pc, lane, kL2PerLane);
+                        cursor_next(pc, ph.nb, ph.upe);
+                        ++pb;
+                    }
+                }
+                compute_batch<FULL>(q[i], s[i], ph, cc, bp, acc);
+                end_batch();
+                if (++b >= bw1) {
+                    more = false;
+                    break;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    cta_stamp(a, down ? 2 : 0);
+    // units shared between warps, finished by the warp holding the last batch
+    if (bw0 < bw1 && Bc > 0) {
+        const long long ul = bw0 / ph.nb;
+        const long long ue = min((ul + 1) * ph.nb, Bc) - 1;
+        if (ul * ph.nb != bw0 && ue < bw1) {
+            const int wf = warp_of_batch(ul * ph.nb, Bc);
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            for (int w = wf; w <= warp; ++w) {
+                const long long wb0 = (long long)w * Bc / NW, wb1 = (long long)(w + 1) * Bc / NW;
+                if (wb0 >= wb1)
+                    continue;
+                const int slot = wb0 / ph.nb == ul ? 2 * w : 2 * w + 1;
+                const float4 v = *reinterpret_cast<const float4 *>(slots + (slot * 32 + lane) * 4);
+                acc[0] += v.x;
+                acc[1] += v.y;
+                acc[2] += v.z;
+                acc[3] += v.w;
+            }
+            const long long u = u0 + ul;
+            const int P = (int)(u / ph.upe), rb = (int)(u - (long long)P * ph.upe);
+            finish_unit(mode, &a, &rs, ph.passes, ph.e_lo, ph.hundo, P, rb, acc[0], acc[1], acc[2], acc[3]);
+        }
+    }
+    if (!down)
+        return true;
+    // every entry output of this CTA is written: count them into the tiles
+    // and combine the tiles this CTA completes
+    __threadfence();
+    if (threadIdx.x == 0)
+        rs.n_comb = 0;
+    __syncthreads();
+    const int kps = a.k + a.S;
+    for (long long i = threadIdx.x; i < u1 - u0; i += NT) {
+        const long long u = u0 + i;
+        const int P = (int)(u / ph.upe), rb = (int)(u - (long long)P * ph.upe);
+        const unsigned cnt = (unsigned)rs.pdn[P].count;
+        const unsigned old = atomicAdd(a.tile_ctr + rb, cnt);
+        if (old + cnt == (unsigned)(a.T * kps))
+            comb[atomicAdd(&rs.n_comb, 1)] = rb;
+    }
+    __syncthreads();
+    __threadfence();
+    for (int i = warp; i < rs.n_comb; i += NW) {
+        combine_tile(a, rs, comb[i], lane);
+        if (lane == 0)
+            a.tile_ctr[comb[i]] = 0;
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <bool FULL>
+__global__ void __launch_bounds__(NT, 1) fused_layer_kernel(const __grid_constant__ FusedArgs a) {
+    uint8_t *smem = fz_smem;
+    RouteState &rs = fz_rs;
+    const int G = gridDim.x;
+
+    stamp(a, 0);
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        reinterpret_cast<unsigned long long *>(a.hdr + kHdrStamps)[12] = clock64();
+    if (threadIdx.x < kFusedMaxTokens)           // ordered before phase T by the waits' barriers
+        rs.n_cand[threadIdx.x] = 0;
+    if (threadIdx.x == 0)
+        rs.bad = 0;
+    prefetch_shared_expert(a);
+    phase_router(a, smem + a.off_b);
+    stamp(a, 1);
+    grid_arrive(a);
+    bool ok = grid_wait(a, (unsigned)G);
+    stamp(a, 2);
+    if (ok)
+        ok = phase_route(a, rs, smem, smem + a.off_b);
+    stamp(a, 3);
+    if (ok) {
+        // gate/up, then down: one copy of the streaming code runs both
+#pragma unroll 1
+        for (int mode = kFfnGateUp; mode <= kFfnDown; ++mode) {
+            if (mode == kFfnDown) {
+                stamp(a, 4);
+                grid_arrive(a);
+            }
+            if (!stream_phase<FULL>(&a, mode))
+                break;
+        }
+        stamp(a, 6);
+        if (blockIdx.x == 0 && threadIdx.x == 0)
+            reinterpret_cast<unsigned long long *>(a.hdr + kHdrStamps)[13] = clock64();
+    }
+    // the last CTA to leave resets the wait counters for the next call
+    __syncthreads();
+    cta_stamp(a, 3);
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(a.hdr + kHdrDone, 1u) == (unsigned)G - 1) {
+            a.hdr[kHdrBarrier] = 0;
+            a.hdr[kHdrAbort] = 0;
+            a.hdr[kHdrDone] = 0;
+            reinterpret_cast<unsigned long long *>(a.hdr + kHdrStamps)[7] = globaltimer_ns();
+            __threadfence();
+        }
+    }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- host side
+
+FusedPlan fused_plan(int T, int H, int I, int E, int k, int S, int grid) {
+    FusedPlan p{};
+    p.ok = false;
+    if (T < 1 || T > kFusedMaxTokens || grid < 1 || H / 16 > kMaxTileCounters || H % 64 || I % 64)
+        return p;
+    const int kps = k + S, n = T * kps, n_tot = E + S;
+    fused_router_tiling(H, E, &p.r_groups, &p.r_chunks, &p.r_rows);
+    p.xwin_row = H + 32;
+    p.hwin_row = I + 32;
+    // down units a CTA can own, and the entries their passes can span
+    const int active = n < n_tot ? n : n_tot;
+    const long long max_pdn = (n + (long long)(kPassEntries - 1) * active) / kPassEntries;
+    const int upe_dn = H / 16;
+    const long long nu_dn = (max_pdn * upe_dn + grid - 1) / grid;
+    const long long spanned = (nu_dn + upe_dn - 1) / upe_dn + 1;
+    long long we = spanned * kPassEntries;
+    if (we > n)
+        we = n;
+    p.win_entries = (int)we;
+    const size_t a_x = (size_t)T * p.xwin_row * 2;
+    const size_t a_h = (size_t)p.win_entries * 2 * p.hwin_row * 2;
+    const size_t szA = align_up(a_x > a_h ? a_x : a_h, 16);
+    p.off_hundo = szA;
+    const size_t sz_hundo = align_up((size_t)p.win_entries * sizeof(float), 16);
+    p.off_b = p.off_hundo + sz_hundo;
+    const int Ep = (E + 31) / 32 * 32;
+    const size_t b_logits = (size_t)T * Ep * sizeof(unsigned long long) + (size_t)T * (Ep / 32) * k * sizeof(int);
+    const size_t b_router = align_up((size_t)T * p.r_rows * 4, 16) + (size_t)kFusedWarps * T * 32 * sizeof(float2);
+    const size_t b_slots = (size_t)2 * kFusedWarps * 32 * 4 * sizeof(float) + (size_t)(nu_dn + 1) * sizeof(int);
+    size_t szB = b_logits;
+    if (b_router > szB)
+        szB = b_router;
+    if (b_slots > szB)
+        szB = b_slots;
+    p.smem = p.off_b + align_up(szB, 16);
+    p.ok = p.smem <= kFusedSmemBudget;
+    return p;
+}
+
+template <bool FULL>
+static cudaError_t launch_fused_t(const FusedArgs &args, int grid, size_t smem, cudaStream_t stream) {
+    static std::atomic<int> set_bytes[64];
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess)
+        return err;
+    if (set_bytes[dev & 63].load() < (int)smem) {
+        err = cudaFuncSetAttribute(fused_layer_kernel<FULL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess)
+            return err;
+        set_bytes[dev & 63].store((int)smem);
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(NT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fused_layer_kernel<FULL>, args);
+}
+
+cudaError_t launch_fused(const FusedProblem &pr, void *ws, const WsLayout &L, int num_sms, cudaStream_t stream) {
+    const moe_mxfp4_bank_t &b = *pr.bank;
+    const int H = b.hidden, I = b.inter, E = b.num_experts, S = b.has_shared;
+    const FusedPlan plan = fused_plan(pr.T, H, I, E, pr.top_k, S, num_sms);
+    if (!plan.ok)
+        return cudaErrorInvalidValue;
+    const PackedLayout PL = packed_layout(H, I, E + S);
+    FusedArgs a{};
+    a.x = pr.x;
+    a.wr = pr.router_w;
+    a.bias = pr.bias;
+    a.gu = b.packed + PL.gu_offset;
+    a.dn = b.packed + PL.dn_offset;
+    a.y = pr.y;
+    a.ids_out = pr.ids_out;
+    a.w_out = pr.w_out;
+    a.hdr = ws_at<uint32_t>(ws, 0);
+    a.tile_ctr = ws_at<uint32_t>(ws, kTileCounterOffset);
+    a.rpart = ws_at<float2>(ws, L.fz_rpart);
+    a.xmax = ws_at<float>(ws, L.fz_xmax);
+    a.cstamps = ws_at<unsigned long long>(ws, kCtaStampOffset);
+    a.h32 = ws_at<float>(ws, L.fz_h32);
+    a.yent = ws_at<float>(ws, L.fz_yent);
+    a.T = pr.T;
+    a.H = H;
+    a.E = E;
+    a.k = pr.top_k;
+    a.S = S;
+    a.I = I;
+    a.shared_weight = pr.shared_weight;
+    a.r_groups = plan.r_groups;
+    a.r_chunks = plan.r_chunks;
+    a.r_rows = plan.r_rows;
+    a.gu_unit = (unsigned)PL.gu_unit_bytes;
+    a.dn_unit = (unsigned)PL.dn_unit_bytes;
+    a.xwin_row = plan.xwin_row;
+    a.hwin_row = plan.hwin_row;
+    a.win_entries = plan.win_entries;
+    a.off_hundo = (int)plan.off_hundo;
+    a.off_b = (int)plan.off_b;
+    if (H % (64 * SB) == 0 && I % (64 * SB) == 0)
+        return launch_fused_t<true>(a, num_sms, plan.smem, stream);
+    return launch_fused_t<false>(a, num_sms, plan.smem, stream);
+}
+
+}  // namespace moe

@@ -66,6 +66,29 @@ cudaError_t launch_ffn(const FfnProblem &p, void *ws, const WsLayout &L, int num
 // f16 copy of x with per-token power-of-two scaling (x16, xundo regions).
 cudaError_t launch_x16(const uint16_t *x, int T, int H, void *ws, const WsLayout &L, cudaStream_t stream);
 
+// The whole layer in one cooperative launch for T <= kFusedMaxTokens (fused.cu).
+struct FusedProblem {
+    const uint16_t *x;
+    const float *router_w;
+    const float *bias;
+    const moe_mxfp4_bank_t *bank;
+    float shared_weight;
+    uint16_t *y;
+    int32_t *ids_out;        // nullable
+    float *w_out;            // nullable
+    int T, top_k;
+};
+
+// Shared-memory plan of the single-launch kernel; ok = the shape fits.
+struct FusedPlan {
+    bool ok;
+    int r_groups, r_chunks, r_rows;
+    int xwin_row, hwin_row, win_entries;
+    size_t off_hundo, off_b, smem;
+};
+FusedPlan fused_plan(int T, int H, int I, int E, int k, int S, int grid);
+cudaError_t launch_fused(const FusedProblem &p, void *ws, const WsLayout &L, int num_sms, cudaStream_t stream);
+
 // Byte offsets inside a repacked bank (pack.cu).
 struct PackedLayout {
     size_t gu_unit_bytes, dn_unit_bytes, gu_offset, dn_offset, total;

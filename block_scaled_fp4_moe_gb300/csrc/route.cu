@@ -21,26 +21,6 @@
 
 namespace moe {
 
-// --------------------------------------------------- error-free arithmetic
-
-__device__ __forceinline__ void two_prod(float a, float b, float &p, float &e) {
-    p = __fmul_rn(a, b);
-    e = __fmaf_rn(a, b, -p);
-}
-
-__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
-    s = __fadd_rn(a, b);
-    float z = __fsub_rn(s, a);
-    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, z)), __fsub_rn(b, z));
-}
-
-// (p, s) += (p2, s2) for unevaluated sums p + s.
-__device__ __forceinline__ void pair_add(float &p, float &s, float p2, float s2) {
-    float q;
-    two_sum(p, p2, p, q);
-    s = __fadd_rn(s, __fadd_rn(s2, q));
-}
-
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
 // ------------------------------------------------------------ router GEMV

@@ -56,8 +56,14 @@
  * caller-supplied topk_ids (or produced from non-finite router logits) is
  * found on the device: it is recorded in a status word inside the workspace,
  * the remaining kernels of the call do no work and leave y untouched, and
- * moe_check_device_status reports and clears the word.  No kernel waits on
- * another CTA or on a flag, so no call can hang the device.
+ * moe_check_device_status reports and clears the word.
+ *
+ * Waits: for T <= 8, moe_layer_forward runs the whole layer as one
+ * cooperative launch (all CTAs resident at once) whose CTAs wait twice for
+ * one another on a counter in the workspace.  Each wait gives up after
+ * 200 ms: the call then records MOE_ERR_DEVICE_TIMEOUT, leaves y untouched,
+ * and the workspace must be re-initialised (moe_workspace_init) before its
+ * next use.  No other kernel waits on another CTA or on a flag.
  */
 #ifndef MOE_FP4_H
 #define MOE_FP4_H
@@ -77,7 +83,7 @@ typedef enum {
     MOE_ERR_MISALIGNED = 3,         /* a pointer breaks its alignment rule */
     MOE_ERR_WORKSPACE_TOO_SMALL = 4,/* ws_bytes < moe_workspace_size(...) */
     MOE_ERR_CUDA = 5,               /* a CUDA runtime call or launch failed */
-    MOE_ERR_DEVICE_TIMEOUT = 6,     /* reserved: the kernels contain no device-side waits */
+    MOE_ERR_DEVICE_TIMEOUT = 6,     /* a device-side wait gave up (see Waits) */
     MOE_ERR_DEVICE_ASSERT = 7,      /* device-side input check failed */
     MOE_ERR_UNSUPPORTED_DEVICE = 8  /* current device is not sm_103 */
 } moe_status_t;
@@ -121,13 +127,15 @@ moe_status_t moe_pack_bank(const moe_mxfp4_bank_t *bank, void *packed, size_t pa
 
 /* Bytes of device workspace the calls below need for these sizes (a caller
  * may pass a larger one).  The workspace carries no state between calls
- * except its header (the device status word). */
+ * except its header: the device status word and the counters of the
+ * single-launch layer kernel, which every completed call leaves at zero. */
 size_t moe_workspace_size(int T, int H, int I, int E, int top_k, int has_shared);
 
-/* Clears the workspace header (status word) on `stream`.
- * Call it once on a newly allocated workspace before its first use (a
- * zero-filled workspace needs no call).  ws: device pointer, 256-byte
- * aligned; ws_bytes at least 256. */
+/* Clears the workspace header (status word, counters and diagnostics, the
+ * first 24,832 bytes or ws_bytes if smaller) on `stream`.  Call it once on a newly
+ * allocated workspace before its first use (a zero-filled workspace needs no
+ * call), and after a call that reported MOE_ERR_DEVICE_TIMEOUT.  ws: device
+ * pointer, 256-byte aligned; ws_bytes at least 256. */
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
@@ -171,7 +179,10 @@ moe_status_t moe_expert_ffn_mxfp4(const uint16_t *x, const int32_t *topk_ids, co
 
 /*
  * The whole layer a1..a6.  topk_ids_out / topk_w_out [T, top_k+S] are
- * optional (NULL: kept in the workspace).
+ * optional (NULL: not returned).  For T <= 8 (and shapes whose staging fits
+ * in shared memory) the layer is one cooperative kernel launch; otherwise a
+ * sequence of six launches.  Both compute the same definition; they may
+ * differ in the last bits of y through a different fp32 summation order.
  */
 moe_status_t moe_layer_forward(const uint16_t *x, const float *router_w, const float *logit_bias,
                                int T, int top_k, const moe_mxfp4_bank_t *bank, float shared_weight,
@@ -217,7 +228,8 @@ moe_status_t moe_layer_forward_hostio(const uint16_t *x_host, const float *route
  * Diagnostic form of moe_layer_forward: records events[0] before the first
  * kernel, events[1] after the router GEMV, events[2] after top-k/grouping,
  * events[3] after gate/up + h finalize and events[4] after down + combine, so
- * n_events must be 5.  Events are created by the caller.
+ * n_events must be 5.  Events are created by the caller.  When the layer runs
+ * as one launch (T <= 8), events[1..4] are all recorded after it.
  */
 moe_status_t moe_layer_forward_profiled(const uint16_t *x, const float *router_w,
                                         const float *logit_bias, int T, int top_k,
