@@ -13,9 +13,14 @@ that no step finds its weights in L2 (L * touched bytes > 2.5 x L2).  Steps
 are replayed from a CUDA graph; W warm-up steps precede the K timed ones.
 
 Extra JSON keys:
-  roofline      the dominant kernel (gate/up + SiLU*up) timed by CUDA events
-                inside a graph replay of the same steps, against the measured
-                HBM copy bandwidth; traffic from the committed ncu capture.
+  roofline      the dominant kernel against the measured HBM copy bandwidth:
+                for T <= 8 the layer is one kernel (algorithmic bytes of the
+                whole layer / its CUDA-event duration); otherwise the gate/up
+                kernel with its h finalize.  traffic from the committed ncu
+                summary of that kernel.
+  kernel_us     per-kernel CUDA-event times of eagerly queued calls;
+  phase_us      for the single-launch kernel, its phases from the kernel's
+                own timestamps (first CTA's view).
   cpu_baseline  the FP64 oracle on this host, a bounded sample.
   e2e           the same metric through moe_layer_forward_hostio, with the
                 pinned host->device copy of x and the device->host copy of y
@@ -47,9 +52,13 @@ from block_scaled_fp4_moe_gb300 import inputs  # noqa: E402
 METRIC = "MoE layer µs/call and effective HBM TB/s (% of 8 TB/s) at T=1/4/16 tokens"
 PAGES_ROOFLINE_TBS = 8.0
 DEFAULT_CONFIG = "glm_t1"
-# dram__bytes_read.sum + dram__bytes_write.sum per gate/up launch, glm_t1,
-# from profiles/ffn_gateup_glm_t1.md (None until captured for this kernel).
-GATEUP_TRAFFIC_BYTES = {}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the kernel the
+# roofline object names, from the committed ncu summaries under profiles/
+# (absent: not captured for the current kernel).
+TRAFFIC_BYTES = {
+    # profiles/launches_glm_t1.md: 116,215,424 read + 346,944 written
+    ("glm_t1", "fused_layer_kernel"): 116562368,
+}
 
 
 def touched_bytes(cfg: inputs.MoEConfig, n_experts: int) -> dict:
@@ -298,8 +307,12 @@ def run_mine(args, cfg):
 
     # ---- per-kernel times: the same steps launched eagerly with events between
     # the kernels, queued behind a bounded sleep kernel so that the GPU runs
-    # them back to back (no host gaps inside the measured intervals)
+    # them back to back (no host gaps inside the measured intervals).  When a
+    # call is a single launch, events 1..4 all follow it: ev0 -> ev4 is the
+    # kernel, and its phases come from the kernel's own timestamps.
+    launches = moe.moe_layer_launches(cfg.T, base, cfg.top_k)
     kern = {"router": [], "topk_group": [], "gateup_hfin": [], "down_combine": []}
+    whole = []
     n_prof = min(max(steps, n_layers), 400)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_prof)]
     with torch.cuda.stream(stream):
@@ -316,8 +329,20 @@ def run_mine(args, cfg):
     for i in range(n_prof):
         for j, name in enumerate(kern):
             kern[name].append(evs[i][j].elapsed_time(evs[i][j + 1]) * 1e3)
-    kernel_source = "cuda events between the kernels of eagerly queued steps"
-    kern_us = {k: statistics.median(v) for k, v in kern.items()}
+        whole.append(evs[i][0].elapsed_time(evs[i][4]) * 1e3)
+    phases = None
+    if launches == 1:
+        kern_us = {"fused_layer_kernel": statistics.median(whole)}
+        kernel_source = "cuda events around each eagerly queued single-launch call"
+        samples = []
+        for i in range(min(64, 4 * n_layers)):
+            moe.moe_layer_forward(xd, routers[i % n_layers], bd, cfg.top_k, banks[i % n_layers], 1.0, y, ws=ws,
+                                  stream=stream)
+            samples.append(moe.moe_read_phase_times(ws, stream=stream))
+        phases = {k: statistics.median(s_[k] for s_ in samples) for k in moe.PHASE_NAMES}
+    else:
+        kernel_source = "cuda events between the kernels of eagerly queued steps"
+        kern_us = {k: statistics.median(v) for k, v in kern.items()}
 
     # ---- end to end through host buffers
     xh = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -336,7 +361,15 @@ def run_mine(args, cfg):
 
     peaks = read_peaks()
     peak = peaks.get("hbm_gbs")
-    gate_gbs = b["gateup"] / (kern_us["gateup_hfin"] * 1e-6) / 1e9
+    if launches == 1:
+        # one launch per step: its average duration inside the timed graph
+        # replay is the step time
+        roof_kernel, roof_bytes = "fused_layer_kernel (the whole layer)", b["total"]
+        roof_us = per_call * 1e6
+    else:
+        roof_kernel, roof_bytes = "ffn_kernel<gate/up> (+ h finalize)", b["gateup"]
+        roof_us = kern_us["gateup_hfin"]
+    achieved = roof_bytes / (roof_us * 1e-6) / 1e9
     line = None
     if rank == 0:
         cpu = time_oracle(cfg, budget_s=args.cpu_budget)
@@ -351,20 +384,21 @@ def run_mine(args, cfg):
                        "bytes_per_call": b["total"], "router_bytes_not_counted": b["router"],
                        "l2": f"inputs larger than L2: steps rotate over {n_layers} weight copies "
                              f"({n_layers} x {b['total'] / 1e6:.1f} MB vs L2 {l2 / 1e6:.0f} MB)",
-                       "launch": "cuda graph replay, 4 kernels per call", "parallelism": f"replicas x{world}"},
-            "kernel_us": kern_us, "kernel_timing": kernel_source,
-            "roofline": {"bound": "hbm", "kernel": "ffn_kernel<gate/up> (+ h finalize)", "achieved": gate_gbs,
+                       "launch": f"cuda graph replay, {launches} kernel launch(es) per call",
+                       "parallelism": f"replicas x{world}"},
+            "kernel_us": kern_us, "kernel_timing": kernel_source, "phase_us": phases,
+            "roofline": {"bound": "hbm", "kernel": roof_kernel, "achieved": achieved,
                          "peak": peak if peak else 6800.0, "unit": "GB/s",
                          "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak else "fallback",
-                         "frac": gate_gbs / (peak if peak else 6800.0),
-                         "traffic": GATEUP_TRAFFIC_BYTES.get(cfg.name),
-                         "algorithmic_bytes": b["gateup"]},
+                         "frac": achieved / (peak if peak else 6800.0),
+                         "traffic": TRAFFIC_BYTES.get((cfg.name, roof_kernel.split()[0])),
+                         "algorithmic_bytes": roof_bytes},
             "cpu_baseline": {"value": cpu["tbs"], "unit": "TB/s", "cores": cpu["cores"], "kind": "oracle",
                              "sample": cpu["sample"]},
             "e2e": {"value": world * b["total"] / e2e_per_call / 1e12, "unit": "TB/s",
                     "us_per_call": e2e_per_call * 1e6,
                     "h2d_bytes_per_step": cfg.T * cfg.H * 2, "d2h_bytes_per_step": cfg.T * cfg.H * 2},
-            "gpu_launches": 4 * steps,
+            "gpu_launches": launches * steps,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -415,6 +415,32 @@ moe_status_t moe_layer_forward_hostio(const uint16_t *x_host, const float *route
     return from_cuda(cudaStreamSynchronize(stream));
 }
 
+int moe_layer_launches(int T, int H, int I, int E, int top_k, int has_shared) {
+    if (T < 0 || H <= 0 || I <= 0 || E <= 0 || top_k <= 0 || (has_shared != 0 && has_shared != 1))
+        return -1;
+    if (T == 0)
+        return 0;
+    int sms = 0;
+    if (current_device_sms(&sms) != MOE_OK)
+        return -1;
+    return (T <= kFusedMaxTokens && fused_plan(T, H, I, E, top_k, has_shared, sms).ok) ? 1 : 6;
+}
+
+moe_status_t moe_read_phase_times(void *ws, float *out_us, int n_out, cudaStream_t stream) {
+    if (!ws || !out_us || n_out < 8)
+        return MOE_ERR_INVALID_ARG;
+    unsigned long long st[8];
+    const uint32_t *hdr = ws_at<uint32_t>(ws, 0);
+    if (cudaMemcpyAsync(st, hdr + kHdrStamps, sizeof st, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    for (int i = 0; i < 6; ++i)
+        out_us[i] = (float)((double)(long long)(st[i + 1] - st[i]) * 1e-3);
+    out_us[6] = (float)((double)(long long)(st[7] - st[6]) * 1e-3);
+    out_us[7] = (float)((double)(long long)(st[7] - st[0]) * 1e-3);
+    return MOE_OK;
+}
+
 moe_status_t moe_check_device_status(void *ws, cudaStream_t stream) {
     if (!ws)
         return MOE_ERR_INVALID_ARG;
@@ -441,6 +467,21 @@ moe_status_t moe_selftest_decode_e2m1(const uint8_t *codes, uint16_t *out, int n
     if (n == 0)
         return MOE_OK;
     return from_cuda(launch_selftest_decode(codes, out, n, stream));
+}
+
+moe_status_t moe_selftest_wait_timeout(void *ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!ws)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(ws, 256))
+        return MOE_ERR_MISALIGNED;
+    if (ws_bytes < kHeaderBytes)
+        return MOE_ERR_WORKSPACE_TOO_SMALL;
+    int sms = 0;
+    moe_status_t st = current_device_sms(&sms);
+    if (st != MOE_OK)
+        return st;
+    (void)cudaGetLastError();
+    return from_cuda(launch_wait_selftest(ws_at<uint32_t>(ws, 0), stream));
 }
 
 const char *moe_status_string(moe_status_t s) {

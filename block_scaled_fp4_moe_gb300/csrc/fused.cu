@@ -953,7 +953,32 @@ __global__ void __launch_bounds__(NT, 1) fused_layer_kernel(const __grid_constan
     }
 }
 
+// Self-test of the bounded grid wait: one CTA arrives and waits for an
+// arrival that never comes; the wait gives up after kWaitLimitNs, records
+// MOE_ERR_DEVICE_TIMEOUT, and the CTA leaves the way the layer kernel does.
+__global__ void wait_selftest_kernel(const __grid_constant__ FusedArgs a) {
+    grid_arrive(a);
+    grid_wait(a, gridDim.x + 1u);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(a.hdr + kHdrDone, 1u) == gridDim.x - 1) {
+            a.hdr[kHdrBarrier] = 0;
+            a.hdr[kHdrAbort] = 0;
+            a.hdr[kHdrDone] = 0;
+            __threadfence();
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_wait_selftest(uint32_t *hdr, cudaStream_t stream) {
+    FusedArgs a{};
+    a.hdr = hdr;
+    wait_selftest_kernel<<<1, 32, 0, stream>>>(a);
+    return cudaGetLastError();
+}
 
 // ---------------------------------------------------------------- host side
 

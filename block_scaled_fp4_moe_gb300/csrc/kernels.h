@@ -88,6 +88,7 @@ struct FusedPlan {
 };
 FusedPlan fused_plan(int T, int H, int I, int E, int k, int S, int grid);
 cudaError_t launch_fused(const FusedProblem &p, void *ws, const WsLayout &L, int num_sms, cudaStream_t stream);
+cudaError_t launch_wait_selftest(uint32_t *hdr, cudaStream_t stream);
 
 // Byte offsets inside a repacked bank (pack.cu).
 struct PackedLayout {

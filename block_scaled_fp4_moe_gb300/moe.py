@@ -71,6 +71,9 @@ def lib() -> C.CDLL:
                     "moe_layer_forward_noalloc": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, p, p]),
                     "moe_layer_forward_profiled": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, s, p, i, p]),
                     "moe_check_device_status": (i, [p, p]),
+                    "moe_layer_launches": (i, [i, i, i, i, i, i]),
+                    "moe_read_phase_times": (i, [p, p, i, p]),
+                    "moe_selftest_wait_timeout": (i, [p, s, p]),
                     "moe_selftest_decode_e2m1": (i, [p, p, i, p]),
                     "moe_status_string": (C.c_char_p, [i]),
                 }
@@ -85,7 +88,8 @@ def lib() -> C.CDLL:
 def exported_symbols() -> list[str]:
     return ["moe_workspace_size", "moe_workspace_init", "moe_packed_bank_size", "moe_pack_bank", "moe_route_topk", "moe_group_tokens", "moe_expert_ffn_mxfp4",
             "moe_layer_forward", "moe_layer_forward_hostio", "moe_layer_forward_noalloc", "moe_layer_forward_profiled",
-            "moe_check_device_status", "moe_selftest_decode_e2m1", "moe_status_string"]
+            "moe_layer_launches", "moe_read_phase_times", "moe_check_device_status", "moe_selftest_decode_e2m1", "moe_selftest_wait_timeout",
+            "moe_status_string"]
 
 
 def moe_status_string(status: int) -> str:
@@ -275,8 +279,29 @@ def moe_layer_forward_hostio(x_host, router_w, logit_bias, top_k, bank: MXFP4Ban
            "moe_layer_forward_hostio")
 
 
+def moe_layer_launches(T, bank: MXFP4Bank, top_k) -> int:
+    """Kernel launches one moe_layer_forward call makes (1: single launch)."""
+    return int(lib().moe_layer_launches(T, bank.hidden, bank.inter, bank.num_experts, top_k, bank.has_shared))
+
+
+PHASE_NAMES = ("router", "wait1", "route", "gateup", "wait2", "down_combine", "tail", "total")
+
+
+def moe_read_phase_times(ws, stream=None) -> dict:
+    """Phase durations (us) of the last single-launch call on `ws`."""
+    out = (C.c_float * 8)()
+    _check(lib().moe_read_phase_times(_ptr(ws, torch.uint8, "ws"), C.cast(out, C.c_void_p), 8, _stream(stream)),
+           "moe_read_phase_times")
+    return dict(zip(PHASE_NAMES, [float(v) for v in out]))
+
+
 def moe_check_device_status(ws, stream=None) -> int:
     return int(lib().moe_check_device_status(_ptr(ws, torch.uint8, "ws"), _stream(stream)))
+
+
+def moe_selftest_wait_timeout(ws, stream=None) -> None:
+    _check(lib().moe_selftest_wait_timeout(_ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)),
+           "moe_selftest_wait_timeout")
 
 
 def moe_selftest_decode_e2m1(codes, out, stream=None) -> None:

@@ -225,6 +225,34 @@ moe_status_t moe_layer_forward_hostio(const uint16_t *x_host, const float *route
                                       cudaStream_t stream);
 
 /*
+ * Self-test of the device-side wait limit: launches one CTA that waits on
+ * the workspace's grid-wait counter for an arrival that never comes.  After
+ * the 200 ms limit the wait gives up and records MOE_ERR_DEVICE_TIMEOUT in
+ * the status word (read it with moe_check_device_status); the counters are
+ * left at zero, so the workspace stays usable.  ws_bytes >= 24,832.
+ */
+moe_status_t moe_selftest_wait_timeout(void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Number of kernel launches moe_layer_forward makes for these sizes on the
+ * current device: 1 when the layer runs as one cooperative launch, 6 for the
+ * multi-launch sequence, 0 for T = 0, -1 on invalid sizes or when the device
+ * cannot be queried.  Host-only; enqueues nothing.
+ */
+int moe_layer_launches(int T, int H, int I, int E, int top_k, int has_shared);
+
+/*
+ * Diagnostic: the phase durations (microseconds, from the GPU's global timer)
+ * of the last single-launch layer call that used `ws`, as seen by its first
+ * CTA: out_us[0] router partials, [1] first grid wait, [2] top-k and
+ * grouping, [3] gate/up, [4] second grid wait, [5] down and combine, [6] time
+ * from the first CTA's end to the last CTA's end, [7] whole kernel.
+ * n_out >= 8.  Synchronises `stream`.  Values are meaningless after a
+ * multi-launch call.
+ */
+moe_status_t moe_read_phase_times(void *ws, float *out_us, int n_out, cudaStream_t stream);
+
+/*
  * Diagnostic form of moe_layer_forward: records events[0] before the first
  * kernel, events[1] after the router GEMV, events[2] after top-k/grouping,
  * events[3] after gate/up + h finalize and events[4] after down + combine, so

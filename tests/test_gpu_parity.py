@@ -268,3 +268,31 @@ def test_layer_full_size(name, banks):
     assert np.all(np.isfinite(yall))
     del p
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------- single-launch kernel
+
+
+def test_device_wait_limit_reports_timeout_and_workspace_stays_usable():
+    """A grid wait that nothing completes gives up after its limit; the
+    status word says so and the same workspace then runs a correct layer."""
+    p = random_problem(T=2, H=1024, E=16, k=4, I=512, seed=21)
+    ws = p.workspace()
+    moe.moe_selftest_wait_timeout(ws)
+    assert moe.moe_check_device_status(ws) == moe.MOE_ERR_DEVICE_TIMEOUT
+    out = p.forward(ws)
+    r = p.oracle_route()
+    np.testing.assert_array_equal(out["ids"], r["ids"])
+    check_output(out["y"], p.oracle_tokens(r, np.arange(p.T))["y"], "after a timed-out wait")
+
+
+def test_launch_count_and_phase_times():
+    p = random_problem(T=1, H=1024, E=16, k=4, I=512, seed=22)
+    assert moe.moe_layer_launches(1, p.bank, p.top_k) == 1
+    assert moe.moe_layer_launches(8, p.bank, p.top_k) == 1
+    assert moe.moe_layer_launches(9, p.bank, p.top_k) == 6
+    assert moe.moe_layer_launches(0, p.bank, p.top_k) == 0
+    out = p.forward()
+    ph = moe.moe_read_phase_times(out["ws"])
+    assert all(v >= 0.0 for v in ph.values()), ph
+    assert 0.0 < ph["total"] < 1e5, ph
