@@ -50,13 +50,9 @@ enum HeaderWord : int {
     kHdrWords = 64
 };
 
-// The header words are followed by one arrival counter per 16-row tile of
-// the output (H / 16 <= 4096), used by the fused kernel's combine (zero at
-// moe_workspace_init, and every call leaves them at zero), then by per-CTA
-// phase-end times of the fused kernel (diagnostics, 4 x u64 per CTA).
-constexpr size_t kTileCounterOffset = kHdrWords * sizeof(uint32_t);
-constexpr int kMaxTileCounters = 4096;
-constexpr size_t kCtaStampOffset = kTileCounterOffset + kMaxTileCounters * sizeof(uint32_t);
+// The header words are followed by per-CTA phase-end times of the fused
+// kernel (diagnostics, 4 x u64 per CTA).
+constexpr size_t kCtaStampOffset = kHdrWords * sizeof(uint32_t);
 constexpr int kFusedMaxCtaStamps = 256;
 constexpr size_t kHeaderBytes = kCtaStampOffset + kFusedMaxCtaStamps * 4 * sizeof(unsigned long long);
 

@@ -6,7 +6,7 @@
 // solve": decode is bound by streaming the active expert weights; the pages'
 // kernel sections name launch gaps and too few CTAs as what kept the first
 // batch-1 GEMMs at a quarter of peak).  Here one cooperative launch of one CTA
-// per SM runs the chain, with two grid-wide waits:
+// per SM runs the chain, with three grid-wide waits:
 //
 //  R  router partial dot products (Dot2, error-free) over tiles of the router
 //     matrix; meanwhile the shared expert's gate/up weights, which every token
@@ -24,9 +24,10 @@
 //  -- grid wait 2
 //  D  down: each CTA converts the h rows of its entries to f16 hi + lo terms
 //     (per-entry power-of-two scale), streams whole 16-row blocks of H, and
-//     writes the per-entry outputs Y.  A per-tile arrival counter tells the
-//     CTA that delivers the last entry of a 16-row output tile to combine that
-//     tile: y = bf16(sum over slots in order of w * Y).  No CTA waits there.
+//     writes the per-entry outputs Y.
+//  -- grid wait 3
+//  C  every CTA combines an equal share of the outputs:
+//     y = bf16(sum over slots in order of w * Y).
 //
 // Waits spin on a counter in the workspace with a time limit; a wait that runs
 // out records MOE_ERR_DEVICE_TIMEOUT and every CTA leaves without writing y.
@@ -51,7 +52,6 @@ struct FusedArgs {
     int32_t *ids_out;            // [T, kps] or null
     float *w_out;                // [T, kps] or null
     uint32_t *hdr;               // workspace header
-    uint32_t *tile_ctr;          // [H / 16] arrival counters
     float2 *rpart;               // [r_chunks][T][E] router partial pairs
     float *xmax;                 // [r_chunks][T] max |x| over each router row chunk
     float *h32;                  // [entries][I] h in sorted entry order
@@ -81,7 +81,7 @@ constexpr bool kL2PerLane = false;   // ask per 128-byte line from every lane in
 
 // Routing results every CTA derives for itself in phase T.
 struct RouteState {
-    int n_gu, n_dn, bad, n_comb;
+    int n_gu, n_dn, bad, pad;
     int n_cand[kFusedMaxTokens];   // top-k candidates per token
     float xundo[kFusedMaxTokens];  // 2^-s of token t's f16 scaling
     float xscale[kFusedMaxTokens]; // 2^s
@@ -695,26 +695,6 @@ __device__ void h_to_window(const FusedArgs &a, int e_lo, int n_win, int win_row
     }
 }
 
-// Rows [16 rb, 16 rb + 16) of y for every token, from the per-entry outputs.
-__device__ void combine_tile(const FusedArgs &a, const RouteState &rs, int rb, int lane) {
-    const int kps = a.k + a.S, T = a.T, H = a.H;
-    for (int i = lane; i < T * 16; i += 32) {
-        const int t = i >> 4, r = 16 * rb + (i & 15);
-        float v[kMaxSlots];
-#pragma unroll
-        for (int s = 0; s < kMaxSlots; ++s)
-            if (s < kps)
-                v[s] = __ldcg(a.yent + (size_t)rs.inv_pos[t * kps + s] * H + r);
-        float acc = 0.0f;
-#pragma unroll
-        for (int s = 0; s < kMaxSlots; ++s)
-            if (s < kps)
-                acc = fmaf(rs.sel_w[t * kps + s], v[s], acc);
-        const __nv_bfloat16 bv = __float2bfloat16_rn(acc);
-        a.y[(size_t)t * H + r] = *reinterpret_cast<const uint16_t *>(&bv);
-    }
-}
-
 // One streaming phase, shared by gate/up and down so that the down phase runs
 // the code the gate/up phase has just brought into the instruction cache.
 // Each CTA takes a contiguous range of whole row-block units; its warps take
@@ -734,7 +714,6 @@ __device__ __forceinline__ bool stream_phase(const FusedArgs *ap, int mode) {
     const uint64_t pol = l2_evict_first_policy();
     float *hundo = reinterpret_cast<float *>(smem + a.off_hundo);
     float *slots = reinterpret_cast<float *>(smem + a.off_b);
-    int *comb = reinterpret_cast<int *>(smem + a.off_b + 2 * NW * 32 * 4 * sizeof(float));
     const bool down = mode == kFfnDown;
     Phase ph;
     ph.sec = down ? a.dn : a.gu;
@@ -872,31 +851,30 @@ __device__ __forceinline__ bool stream_phase(const FusedArgs *ap, int mode) {
             finish_unit(mode, &a, &rs, ph.passes, ph.e_lo, ph.hundo, P, rb, acc[0], acc[1], acc[2], acc[3]);
         }
     }
-    if (!down)
-        return true;
-    // every entry output of this CTA is written: count them into the tiles
-    // and combine the tiles this CTA completes
-    __threadfence();
-    if (threadIdx.x == 0)
-        rs.n_comb = 0;
-    __syncthreads();
-    const int kps = a.k + a.S;
-    for (long long i = threadIdx.x; i < u1 - u0; i += NT) {
-        const long long u = u0 + i;
-        const int P = (int)(u / ph.upe), rb = (int)(u - (long long)P * ph.upe);
-        const unsigned cnt = (unsigned)rs.pdn[P].count;
-        const unsigned old = atomicAdd(a.tile_ctr + rb, cnt);
-        if (old + cnt == (unsigned)(a.T * kps))
-            comb[atomicAdd(&rs.n_comb, 1)] = rb;
-    }
-    __syncthreads();
-    __threadfence();
-    for (int i = warp; i < rs.n_comb; i += NW) {
-        combine_tile(a, rs, comb[i], lane);
-        if (lane == 0)
-            a.tile_ctr[comb[i]] = 0;
-    }
     return true;
+}
+
+// y = bf16(sum over slots, in slot order, of w * Y) for this CTA's equal
+// share of the T x H outputs, after every CTA's per-entry outputs Y are
+// written (third grid wait).  All loads of a thread are issued first.
+__device__ void combine_share(const FusedArgs &a, const RouteState &rs) {
+    const int kps = a.k + a.S, TH = a.T * a.H, G = gridDim.x;
+    const int o0 = (int)((long long)blockIdx.x * TH / G), o1 = (int)((long long)(blockIdx.x + 1) * TH / G);
+    for (int o = o0 + threadIdx.x; o < o1; o += NT) {
+        const int t = o / a.H, hcol = o - t * a.H;
+        float v[kMaxSlots];
+#pragma unroll
+        for (int s = 0; s < kMaxSlots; ++s)
+            if (s < kps)
+                v[s] = __ldcg(a.yent + (size_t)rs.inv_pos[t * kps + s] * a.H + hcol);
+        float acc = 0.0f;
+#pragma unroll
+        for (int s = 0; s < kMaxSlots; ++s)
+            if (s < kps)
+                acc = fmaf(rs.sel_w[t * kps + s], v[s], acc);
+        const __nv_bfloat16 bv = __float2bfloat16_rn(acc);
+        a.y[o] = *reinterpret_cast<const uint16_t *>(&bv);
+    }
 }
 
 // ---------------------------------------------------------------- kernel
@@ -931,8 +909,16 @@ __global__ void __launch_bounds__(NT, 1) fused_layer_kernel(const __grid_constan
                 stamp(a, 4);
                 grid_arrive(a);
             }
-            if (!stream_phase<FULL>(&a, mode))
+            if (!stream_phase<FULL>(&a, mode)) {
+                ok = false;
                 break;
+            }
+        }
+        // every CTA's per-entry outputs, then the combine
+        if (ok) {
+            grid_arrive(a);
+            if (grid_wait(a, 3u * G))
+                combine_share(a, rs);
         }
         stamp(a, 6);
         if (blockIdx.x == 0 && threadIdx.x == 0)
@@ -985,7 +971,7 @@ cudaError_t launch_wait_selftest(uint32_t *hdr, cudaStream_t stream) {
 FusedPlan fused_plan(int T, int H, int I, int E, int k, int S, int grid) {
     FusedPlan p{};
     p.ok = false;
-    if (T < 1 || T > kFusedMaxTokens || grid < 1 || H / 16 > kMaxTileCounters || H % 64 || I % 64)
+    if (T < 1 || T > kFusedMaxTokens || grid < 1 || H % 64 || I % 64)
         return p;
     const int kps = k + S, n = T * kps, n_tot = E + S;
     fused_router_tiling(H, E, &p.r_groups, &p.r_chunks, &p.r_rows);
@@ -1064,7 +1050,6 @@ cudaError_t launch_fused(const FusedProblem &pr, void *ws, const WsLayout &L, in
     a.ids_out = pr.ids_out;
     a.w_out = pr.w_out;
     a.hdr = ws_at<uint32_t>(ws, 0);
-    a.tile_ctr = ws_at<uint32_t>(ws, kTileCounterOffset);
     a.rpart = ws_at<float2>(ws, L.fz_rpart);
     a.xmax = ws_at<float>(ws, L.fz_xmax);
     a.cstamps = ws_at<unsigned long long>(ws, kCtaStampOffset);

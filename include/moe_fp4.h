@@ -59,11 +59,12 @@
  * moe_check_device_status reports and clears the word.
  *
  * Waits: for T <= 8, moe_layer_forward runs the whole layer as one
- * cooperative launch (all CTAs resident at once) whose CTAs wait twice for
- * one another on a counter in the workspace.  Each wait gives up after
- * 200 ms: the call then records MOE_ERR_DEVICE_TIMEOUT, leaves y untouched,
- * and the workspace must be re-initialised (moe_workspace_init) before its
- * next use.  No other kernel waits on another CTA or on a flag.
+ * cooperative launch (all CTAs resident at once) whose CTAs wait three times
+ * for one another on a counter in the workspace.  Each wait gives up after
+ * 200 ms (the cooperative launch makes that happen only after a fault
+ * elsewhere): the call then records MOE_ERR_DEVICE_TIMEOUT and y is
+ * undefined; the counters are reset when the kernel ends, so the workspace
+ * stays usable.  No other kernel waits on another CTA or on a flag.
  */
 #ifndef MOE_FP4_H
 #define MOE_FP4_H
@@ -132,7 +133,7 @@ moe_status_t moe_pack_bank(const moe_mxfp4_bank_t *bank, void *packed, size_t pa
 size_t moe_workspace_size(int T, int H, int I, int E, int top_k, int has_shared);
 
 /* Clears the workspace header (status word, counters and diagnostics, the
- * first 24,832 bytes or ws_bytes if smaller) on `stream`.  Call it once on a newly
+ * first 8,448 bytes or ws_bytes if smaller) on `stream`.  Call it once on a newly
  * allocated workspace before its first use (a zero-filled workspace needs no
  * call), and after a call that reported MOE_ERR_DEVICE_TIMEOUT.  ws: device
  * pointer, 256-byte aligned; ws_bytes at least 256. */
@@ -229,7 +230,7 @@ moe_status_t moe_layer_forward_hostio(const uint16_t *x_host, const float *route
  * the workspace's grid-wait counter for an arrival that never comes.  After
  * the 200 ms limit the wait gives up and records MOE_ERR_DEVICE_TIMEOUT in
  * the status word (read it with moe_check_device_status); the counters are
- * left at zero, so the workspace stays usable.  ws_bytes >= 24,832.
+ * left at zero, so the workspace stays usable.  ws_bytes >= 8,448.
  */
 moe_status_t moe_selftest_wait_timeout(void *ws, size_t ws_bytes, cudaStream_t stream);
 
