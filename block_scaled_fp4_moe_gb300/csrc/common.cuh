@@ -43,11 +43,11 @@ enum HeaderWord : int {
     kHdrNumActive = 3,
     kHdrNumPasses = 4,
     kHdrNumPasses4 = 5,
-    kHdrBarrier = 6,      // grid-barrier arrivals of the fused layer kernel
-    kHdrDone = 7,         // CTAs of the fused layer kernel that have finished
-    kHdrAbort = 8,        // set when a fused-kernel wait gave up
-    kHdrStamps = 16,      // 16 x u64 phase timestamps of the fused kernel (words 16..47)
-    kHdrWords = 64
+    kHdrBarrier = 32,     // grid-wait arrivals of the fused layer kernel (own 128-byte line)
+    kHdrAbort = 33,       // set when a fused-kernel wait gave up
+    kHdrDone = 34,        // CTAs of the fused layer kernel that have finished
+    kHdrStamps = 64,      // 16 x u64 phase timestamps of the fused kernel (words 64..95)
+    kHdrWords = 128
 };
 
 // The header words are followed by per-CTA phase-end times of the fused

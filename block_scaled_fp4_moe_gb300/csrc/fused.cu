@@ -75,9 +75,6 @@ constexpr int NBUF = 2;               // register buffers of one batch; NBUF - 1
 constexpr int kBatchBytes = SB * kStepBytes;
 constexpr int kMaxEntries = kFusedMaxTokens * kMaxSlots;
 constexpr unsigned long long kWaitLimitNs = 200ull * 1000 * 1000;
-constexpr int kL2AheadDown = 16;     // batches a warp asks L2 for before the wait that precedes the down phase
-constexpr int kL2Ahead = 0;          // batches a warp asks L2 for ahead of its register loads (0: none)
-constexpr bool kL2PerLane = false;   // ask per 128-byte line from every lane instead of one bulk request
 
 // Routing results every CTA derives for itself in phase T.
 struct RouteState {
@@ -125,16 +122,18 @@ __device__ __forceinline__ void cta_stamp(const FusedArgs &a, int i) {
         a.cstamps[blockIdx.x * 4 + i] = globaltimer_ns();
 }
 
-// Grid-wide wait in two halves.  grid_arrive: after every thread's earlier
-// writes (each thread fences its own), one arrival per CTA on the counter.
-// grid_wait: until `target` (= waits so far x CTAs) arrivals are counted.
-// Work that needs nobody else's results can run in between.  A wait gives up
-// after kWaitLimitNs (or when another CTA's wait gave up) and returns false.
+// Grid-wide wait in two halves.  grid_arrive: after the CTA barrier, one
+// thread fences (cumulative: it orders the writes the barrier ordered before
+// it) and arrives on the counter.  grid_wait: until `target` (= waits so far
+// x CTAs) arrivals are counted.  Work that needs nobody else's results can
+// run in between.  A wait gives up after kWaitLimitNs (or when another CTA's
+// wait gave up) and returns false.
 __device__ void grid_arrive(const FusedArgs &a) {
-    __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
+        __threadfence();
         atomicAdd(a.hdr + kHdrBarrier, 1u);
+    }
 }
 
 __device__ bool grid_wait(const FusedArgs &a, unsigned target) {
@@ -142,7 +141,10 @@ __device__ bool grid_wait(const FusedArgs &a, unsigned target) {
     if (threadIdx.x == 0) {
         const unsigned long long t0 = globaltimer_ns();
         int r = 1;
-        while (ld_acquire_u32(a.hdr + kHdrBarrier) < target) {
+        for (unsigned it = 0; ld_acquire_u32(a.hdr + kHdrBarrier) < target; ++it) {
+            __nanosleep(32);              // let the arrivals through to the counter's line
+            if ((it & 15) != 15)
+                continue;
             if (ld_acquire_u32(a.hdr + kHdrAbort)) {
                 r = 0;
                 break;
@@ -559,19 +561,6 @@ __device__ __forceinline__ void load_batch(uint4 (&q)[SB], uint32_t (&s)[SB], co
     }
 }
 
-// Ask L2 for a whole batch ahead of its register loads.
-__device__ __forceinline__ void prefetch_batch(const Phase &ph, const UnitCursor &c, int lane, bool per_lane) {
-    const uint8_t *p = ph.sec + ((size_t)ph.passes[c.P].expert * ph.upe + c.rb) * ph.unit_bytes +
-                       (size_t)c.bi * kBatchBytes;
-    const int bytes = min(SB, ph.steps - c.bi * SB) * kStepBytes;
-    if (per_lane) {
-        for (int o = lane * 128; o < bytes; o += 32 * 128)
-            asm volatile("prefetch.global.L2 [%0];" ::"l"(p + o));
-    } else if (lane == 0) {
-        prefetch_l2(p, (uint32_t)bytes);
-    }
-}
-
 // One 16 x 64 step: decode, two MMAs per 32-element block, block scales.
 __device__ __forceinline__ void step_mma(const uint4 q, const uint32_t s, const __half *bp, float (&acc)[4]) {
     const uint4 b0 = *reinterpret_cast<const uint4 *>(bp);
@@ -732,9 +721,8 @@ __device__ __forceinline__ bool stream_phase(const FusedArgs *ap, int mode) {
     const int bw0 = (int)((long long)warp * Bc / NW), bw1 = (int)((long long)(warp + 1) * Bc / NW);
     uint4 q[NBUF][SB];
     uint32_t s[NBUF][SB];
-    UnitCursor cc, lc, pc;
+    UnitCursor cc, lc;
     int lb = bw0;                         // next batch to load into registers
-    int pb = bw0;                         // next batch to ask L2 for
     if (bw0 < bw1) {
         cursor_set(cc, u0, bw0, ph.nb, ph.upe);
         lc = cc;
@@ -744,19 +732,6 @@ __device__ __forceinline__ bool stream_phase(const FusedArgs *ap, int mode) {
                 load_batch<FULL>(q[i], s[i], ph, lc, lane, pol);
                 cursor_next(lc, ph.nb, ph.upe);
                 ++lb;
-            }
-        }
-        pc = lc;
-        pb = lb;
-        for (int i = 0; i < kL2Ahead && pb < bw1; ++i, ++pb) {
-            prefetch_batch(ph, pc, lane, kL2PerLane);
-            cursor_next(pc, ph.nb, ph.upe);
-        }
-        if (down) {                       // L2 fetches the next batches while the CTAs wait
-            UnitCursor pc = lc;
-            for (int i = 0, pb = lb; i < kL2AheadDown && pb < bw1; ++i, ++pb) {
-                prefetch_batch(ph, pc, lane, false);
-                cursor_next(pc, ph.nb, ph.upe);
             }
         }
     }
@@ -811,11 +786,6 @@ __device__ __forceinline__ bool stream_phase(const FusedArgs *ap, int mode) {
                     load_batch<FULL>(q[(i + NBUF - 1) % NBUF], s[(i + NBUF - 1) % NBUF], ph, lc, lane, pol);
                     cursor_next(lc, ph.nb, ph.upe);
                     ++lb;
-                    if (kL2Ahead > 0 && pb < bw1) {
-                        prefetch_batch(ph, pc, lane, kL2PerLane);
-                        cursor_next(pc, ph.nb, ph.upe);
-                        ++pb;
-                    }
                 }
                 compute_batch<FULL>(q[i], s[i], ph, cc, bp, acc);
                 end_batch();
@@ -916,9 +886,13 @@ __global__ void __launch_bounds__(NT, 1) fused_layer_kernel(const __grid_constan
         }
         // every CTA's per-entry outputs, then the combine
         if (ok) {
+            stamp(a, 11);
+            cta_stamp(a, 3);
             grid_arrive(a);
-            if (grid_wait(a, 3u * G))
+            if (grid_wait(a, 3u * G)) {
+                stamp(a, 14);
                 combine_share(a, rs);
+            }
         }
         stamp(a, 6);
         if (blockIdx.x == 0 && threadIdx.x == 0)
@@ -926,7 +900,6 @@ __global__ void __launch_bounds__(NT, 1) fused_layer_kernel(const __grid_constan
     }
     // the last CTA to leave resets the wait counters for the next call
     __syncthreads();
-    cta_stamp(a, 3);
     if (threadIdx.x == 0) {
         __threadfence();
         if (atomicAdd(a.hdr + kHdrDone, 1u) == (unsigned)G - 1) {

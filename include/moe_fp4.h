@@ -133,10 +133,10 @@ moe_status_t moe_pack_bank(const moe_mxfp4_bank_t *bank, void *packed, size_t pa
 size_t moe_workspace_size(int T, int H, int I, int E, int top_k, int has_shared);
 
 /* Clears the workspace header (status word, counters and diagnostics, the
- * first 8,448 bytes or ws_bytes if smaller) on `stream`.  Call it once on a newly
+ * first 8,704 bytes or ws_bytes if smaller) on `stream`.  Call it once on a newly
  * allocated workspace before its first use (a zero-filled workspace needs no
  * call), and after a call that reported MOE_ERR_DEVICE_TIMEOUT.  ws: device
- * pointer, 256-byte aligned; ws_bytes at least 256. */
+ * pointer, 256-byte aligned; ws_bytes at least 512. */
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
@@ -230,7 +230,7 @@ moe_status_t moe_layer_forward_hostio(const uint16_t *x_host, const float *route
  * the workspace's grid-wait counter for an arrival that never comes.  After
  * the 200 ms limit the wait gives up and records MOE_ERR_DEVICE_TIMEOUT in
  * the status word (read it with moe_check_device_status); the counters are
- * left at zero, so the workspace stays usable.  ws_bytes >= 8,448.
+ * left at zero, so the workspace stays usable.  ws_bytes >= 8,704.
  */
 moe_status_t moe_selftest_wait_timeout(void *ws, size_t ws_bytes, cudaStream_t stream);
 
