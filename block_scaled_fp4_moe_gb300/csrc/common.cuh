@@ -111,7 +111,7 @@ inline void fused_router_tiling(int H, int E, int *groups, int *chunks, int *row
 // Offsets (bytes) of the workspace regions for one problem size.
 struct WsLayout {
     size_t route_part, topk_ids, topk_w, offsets, sorted_tok, sorted_slot, inv_pos, active, passes, passes4, x16, xundo,
-        gpart, h16, hundo, ypart, counters, xstage, ystage, fz_rpart, fz_xmax, fz_h32, fz_yent, total;
+        gpart, h16, hundo, ypart, counters, xstage, ystage, fz_rpart, fz_h32, fz_yent, total;
     int n_kc_gu, n_kc_dn;
 
     static WsLayout make(int T, int H, int I, int E, int k, int S) {
@@ -148,7 +148,6 @@ struct WsLayout {
             int g, ch, r;
             fused_router_tiling(H, E, &g, &ch, &r);
             L.fz_rpart = take((size_t)ch * T * E * sizeof(float2));
-            L.fz_xmax = take((size_t)ch * T * sizeof(float));
             L.fz_h32 = take(entries * (size_t)I * sizeof(float));
             L.fz_yent = take(entries * (size_t)H * sizeof(float));
         }

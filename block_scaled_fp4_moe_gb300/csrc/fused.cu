@@ -53,7 +53,6 @@ struct FusedArgs {
     float *w_out;                // [T, kps] or null
     uint32_t *hdr;               // workspace header
     float2 *rpart;               // [r_chunks][T][E] router partial pairs
-    float *xmax;                 // [r_chunks][T] max |x| over each router row chunk
     float *h32;                  // [entries][I] h in sorted entry order
     float *yent;                 // [entries][H] per-entry outputs
     unsigned long long *cstamps; // [grid][4] per-CTA phase-end times (diagnostics)
@@ -168,9 +167,8 @@ __device__ bool grid_wait(const FusedArgs &a, unsigned target) {
 // Router tile (32 experts x r_rows rows): each warp pulls its rows (every
 // NW-th row) into L1 while the tile's x rows are staged, then accumulates one
 // Dot2 pair per token and lane (expert); the CTA sums the warps' pairs in warp
-// order.  CTAs of expert group 0 also record max |x| of their rows per token.
+// order.
 __device__ void phase_router(const FusedArgs &a, uint8_t *smB) {
-    __shared__ unsigned xm[kFusedMaxTokens];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int T = a.T, H = a.H, E = a.E;
     float *xs = reinterpret_cast<float *>(smB);                                  // [T][r_rows]
@@ -188,28 +186,19 @@ __device__ void phase_router(const FusedArgs &a, uint8_t *smB) {
             prefetch_l1(wrow + j * wstride + e1 - 1);
         }
         __syncthreads();
-        if (threadIdx.x < kFusedMaxTokens)
-            xm[threadIdx.x] = 0u;
-        __syncthreads();
         for (int i = threadIdx.x; i < T * (nr / 8); i += NT) {
             const int t = i / (nr / 8), c8 = i - t * (nr / 8);
             const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)t * H + r0) + c8);
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
             float *d = xs + t * a.r_rows + c8 * 8;
-            float m = 0.0f;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 d[2 * j] = __uint_as_float(w4[j] << 16);
                 d[2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
-                m = fmaxf(m, fmaxf(fabsf(d[2 * j]), fabsf(d[2 * j + 1])));
             }
-            if (gi == 0)
-                atomicMax(&xm[t], __float_as_uint(m));
         }
         __syncthreads();
         stamp(a, 8);
-        if (gi == 0 && threadIdx.x < T)
-            a.xmax[ci * T + threadIdx.x] = __uint_as_float(xm[threadIdx.x]);
         const bool live = e0 + lane < e1;
         for (int t = 0; t < T; ++t) {
             const float *xr = xs + t * a.r_rows + warp;
@@ -255,24 +244,55 @@ __device__ void prefetch_shared_expert(const FusedArgs &a) {
 
 // ------------------------------------------------------------- phase T
 
-// x -> window rows in f16, x[t] scaled by 2^s[t] so that max |x[t]| lies in
-// [2^14, 2^15) (rs.xundo[t] = 2^-s[t]); run by the `nthr` threads numbered
-// `lt` = 0.. of the warps that do not select experts.
-__device__ void x_to_window(const FusedArgs &a, const RouteState &rs, __half *xwin, int lt, int nthr) {
+// x -> the f16 window: x[t] scaled by 2^s[t] so that max |x[t]| lies in
+// [2^14, 2^15) (rs.xundo[t] = 2^-s[t]).  Every CTA reads all of x itself, so
+// this needs nobody else's results; the kernel runs it while it waits for the
+// other CTAs' router partials.
+__device__ void x_window_local(const FusedArgs &a, RouteState &rs, __half *xwin) {
+    __shared__ unsigned xm[kFusedMaxTokens];
     const int H = a.H, n8 = H / 8, total = a.T * n8;
-    for (int i0 = lt; i0 < total; i0 += 4 * nthr) {
+    if (threadIdx.x < kFusedMaxTokens)
+        xm[threadIdx.x] = 0u;
+    __syncthreads();
+    for (int i0 = threadIdx.x; i0 < total; i0 += 4 * NT) {
         uint4 v[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int i = i0 + j * nthr;
-            if (i < total) {
-                const int t = i / n8, c = i - t * n8;
-                v[j] = __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)t * H) + c);
-            }
+            const int i = i0 + j * NT;
+            if (i < total)
+                v[j] = __ldg(reinterpret_cast<const uint4 *>(a.x) + i);
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int i = i0 + j * nthr;
+            const int i = i0 + j * NT;
+            if (i < total) {
+                const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+                float m = 0.0f;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    m = fmaxf(m, fmaxf(fabsf(__uint_as_float(w4[k] << 16)), fabsf(__uint_as_float(w4[k] & 0xFFFF0000u))));
+                atomicMax(&xm[i / n8], __float_as_uint(m));
+            }
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < a.T) {
+        const int sh = f16_shift_for_max(__uint_as_float(xm[threadIdx.x]));
+        rs.xundo[threadIdx.x] = exp2i(-sh);
+        rs.xscale[threadIdx.x] = exp2i(sh);
+    }
+    __syncthreads();
+    for (int i0 = threadIdx.x; i0 < total; i0 += 4 * NT) {
+        uint4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = i0 + j * NT;
+            if (i < total)
+                v[j] = __ldg(reinterpret_cast<const uint4 *>(a.x) + i);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int i = i0 + j * NT;
             if (i < total) {
                 const int t = i / n8, c = i - t * n8;
                 const float sc = rs.xscale[t];
@@ -352,22 +372,6 @@ __device__ bool phase_route(const FusedArgs &a, RouteState &rs, uint8_t *smA, ui
     }
     for (int i = tid; i < T * (Ep - E); i += NT)     // padding sorts below every real key
         key[(i / (Ep - E)) * Ep + E + i % (Ep - E)] = 0ull;
-    // per-token f16 scale of x from the router tiles' maxima (the last warps,
-    // which have the fewest logits to sum)
-    if (warp >= NW - T) {
-        const int t = warp - (NW - T);
-        float m = 0.0f;
-        for (int c = lane; c < a.r_chunks; c += 32)
-            m = fmaxf(m, __ldcg(a.xmax + c * T + t));
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1)
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, d));
-        if (lane == 0) {
-            const int sh = f16_shift_for_max(m);
-            rs.xundo[t] = exp2i(-sh);
-            rs.xscale[t] = exp2i(sh);
-        }
-    }
     __syncthreads();
     stamp(a, 9);
     // top k: an expert ranked k or lower inside its group of 32 cannot be in
@@ -439,8 +443,6 @@ __device__ bool phase_route(const FusedArgs &a, RouteState &rs, uint8_t *smA, ui
                     a.w_out[t * kps + k] = a.shared_weight;
             }
         }
-    } else {
-        x_to_window(a, rs, reinterpret_cast<__half *>(smA), tid - 32 * T, NT - 32 * T);
     }
     __syncthreads();
     stamp(a, 10);
@@ -451,6 +453,53 @@ __device__ bool phase_route(const FusedArgs &a, RouteState &rs, uint8_t *smA, ui
         if (blockIdx.x == 0 && tid == 0)
             record_status(a.hdr, MOE_ERR_DEVICE_ASSERT);
         return false;
+    }
+    if (n <= 32) {
+        // one warp: entry `lane` -> sorted position, group starts and sizes,
+        // passes, with shuffles and ballots only
+        if (warp == 0) {
+            const unsigned full = 0xffffffffu;
+            const int ei = lane < n ? rs.sel_id[lane] : 0x7fffffff;
+            int pos = 0;
+            for (int j = 0; j < n; ++j) {
+                const int ej = __shfl_sync(full, ei, j);
+                pos += (ej < ei) | ((ej == ei) & (j < lane));
+            }
+            if (lane < n) {
+                rs.inv_pos[lane] = pos;
+                rs.sorted_ent[pos] = lane;
+                rs.sorted_tok[pos] = lane / kps;
+            }
+            __syncwarp();
+            const int ex = lane < n ? rs.sel_id[rs.sorted_ent[lane]] : -1;
+            const int prev = __shfl_up_sync(full, ex, 1);
+            const bool start = lane < n && (lane == 0 || prev != ex);
+            const unsigned starts = __ballot_sync(full, start);
+            const unsigned later = lane == 31 ? 0u : starts & ~((2u << lane) - 1u);
+            const int next = later ? __ffs(later) - 1 : n;
+            const int size = start ? next - lane : 0;
+            const int gi = __popc(starts & ((1u << lane) - 1u));
+            const int d4 = (size + kPassEntries - 1) / kPassEntries;
+            int incl = d4;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(full, incl, d);
+                if (lane >= d)
+                    incl += y;
+            }
+            if (start) {
+                const int di = incl - d4;
+                rs.pgu[gi] = Pass{ex, lane, size, 0};
+                for (int q = 0; q < d4; ++q)
+                    rs.pdn[di + q] = Pass{ex, lane + q * kPassEntries, min(kPassEntries, size - q * kPassEntries), 0};
+            }
+            if (lane == 31) {
+                rs.n_gu = __popc(starts);
+                rs.n_dn = incl;
+            }
+        }
+        __syncthreads();
+        return true;
     }
     // sorted position of entry i: entries with a smaller expert, or the same
     // expert and a smaller index, come first
@@ -866,6 +915,7 @@ __global__ void __launch_bounds__(NT, 1) fused_layer_kernel(const __grid_constan
     phase_router(a, smem + a.off_b);
     stamp(a, 1);
     grid_arrive(a);
+    x_window_local(a, rs, reinterpret_cast<__half *>(smem));
     bool ok = grid_wait(a, (unsigned)G);
     stamp(a, 2);
     if (ok)
@@ -1024,7 +1074,6 @@ cudaError_t launch_fused(const FusedProblem &pr, void *ws, const WsLayout &L, in
     a.w_out = pr.w_out;
     a.hdr = ws_at<uint32_t>(ws, 0);
     a.rpart = ws_at<float2>(ws, L.fz_rpart);
-    a.xmax = ws_at<float>(ws, L.fz_xmax);
     a.cstamps = ws_at<unsigned long long>(ws, kCtaStampOffset);
     a.h32 = ws_at<float>(ws, L.fz_h32);
     a.yent = ws_at<float>(ws, L.fz_yent);
