@@ -226,6 +226,25 @@ __device__ void phase_router(const FusedArgs &a, uint8_t *smB) {
     }
 }
 
+// This CTA's first router tile into L1 (read-only data: may run before the
+// previous kernel on the stream has finished).
+__device__ void prefetch_router_tile(const FusedArgs &a) {
+    const int tile = blockIdx.x;
+    if (tile >= a.r_groups * a.r_chunks)
+        return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gi = tile % a.r_groups, ci = tile / a.r_groups;
+    const int r0 = ci * a.r_rows, nr = min(a.H - r0, a.r_rows);
+    const int e0 = gi * 32, e1 = min(a.E, e0 + 32);
+    const int nrw = nr > warp ? (nr - warp + NW - 1) / NW : 0;
+    const float *wrow = a.wr + (size_t)(r0 + warp) * a.E;
+    const size_t wstride = (size_t)NW * a.E;
+    for (int j = lane; j < nrw; j += 32) {
+        prefetch_l1(wrow + j * wstride + e0);
+        prefetch_l1(wrow + j * wstride + e1 - 1);
+    }
+}
+
 // The shared expert's gate/up weights do not depend on the routing: pull
 // this CTA's slice of them into L2 while the router runs.
 __device__ void prefetch_shared_expert(const FusedArgs &a) {
@@ -904,6 +923,13 @@ __global__ void __launch_bounds__(NT, 1) fused_layer_kernel(const __grid_constan
     RouteState &rs = fz_rs;
     const int G = gridDim.x;
 
+    // read-only prefetches, then wait until the previous kernel on the stream
+    // has completed (its outputs and the workspace are then ours); the next
+    // kernel may be scheduled from here on
+    prefetch_shared_expert(a);
+    prefetch_router_tile(a);
+    pdl_wait();
+    pdl_trigger();
     stamp(a, 0);
     if (blockIdx.x == 0 && threadIdx.x == 0)
         reinterpret_cast<unsigned long long *>(a.hdr + kHdrStamps)[12] = clock64();
@@ -911,7 +937,6 @@ __global__ void __launch_bounds__(NT, 1) fused_layer_kernel(const __grid_constan
         rs.n_cand[threadIdx.x] = 0;
     if (threadIdx.x == 0)
         rs.bad = 0;
-    prefetch_shared_expert(a);
     phase_router(a, smem + a.off_b);
     stamp(a, 1);
     grid_arrive(a);
@@ -1048,11 +1073,13 @@ static cudaError_t launch_fused_t(const FusedArgs &args, int grid, size_t smem, 
     cfg.blockDim = dim3(NT);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, fused_layer_kernel<FULL>, args);
 }
 
