@@ -25,10 +25,11 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_
 
 // ------------------------------------------------------------ router GEMV
 
-// Grid (ceil(E/32), ceil(H/512)); CTA (bx, by) owns experts [32bx, 32bx+32)
-// (one per lane) and router rows [512by, 512by+512) (64 per warp, summed in
-// four interleaved Dot2 chains for instruction-level parallelism) for all T
-// tokens, and writes the partial pairs part[by][t][e].  The router weights do
+// Grid (ceil(E/32), ceil(H/512), ceil(T/8)); CTA (bx, by, bz) owns experts
+// [32bx, 32bx+32) (one per lane), router rows [512by, 512by+512) (64 per
+// warp, summed in four interleaved Dot2 chains for instruction-level
+// parallelism) and tokens [8bz, 8bz+8), and writes the partial pairs
+// part[by][t][e].  The router weights do
 // not depend on earlier kernels, so they are loaded before the wait on the
 // preceding grid.
 __global__ void __launch_bounds__(kRouteThreads)
@@ -53,10 +54,10 @@ route_partial_kernel(const uint16_t *__restrict__ x, const float *__restrict__ w
     }
     pdl_wait();
     pdl_trigger();
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0)
         hdr[kHdrRouteTicket] = 0;
 
-    for (int t0 = 0; t0 < T; t0 += kTok) {
+    for (int t0 = blockIdx.z * kTok; t0 < T && t0 < (int)(blockIdx.z + 1) * kTok; t0 += kTok) {
         const int tn = min(kTok, T - t0);
         __syncthreads();
         // tn tokens x 512 rows of bf16 in chunks of 8 elements, two per thread
@@ -365,7 +366,7 @@ cudaError_t launch_route(const uint16_t *x, const float *wr, const float *bias, 
     uint32_t *hdr = ws_at<uint32_t>(ws, 0);
     float2 *part = ws_at<float2>(ws, L.route_part);
     const int nh = (H + kRouteRows - 1) / kRouteRows;
-    dim3 g1((E + kRouteCols - 1) / kRouteCols, nh);
+    dim3 g1((E + kRouteCols - 1) / kRouteCols, nh, (T + 7) / 8);   // one CTA per 8 tokens of a tile
     cudaError_t err = launch_pdl(route_partial_kernel, g1, dim3(kRouteThreads), 0, stream, x, wr, T, H, E, part, hdr);
     if (err != cudaSuccess)
         return err;
