@@ -47,6 +47,7 @@ enum HeaderWord : int {
     kHdrAbort = 33,       // set when a fused-kernel wait gave up
     kHdrDone = 34,        // CTAs of the fused layer kernel that have finished
     kHdrStamps = 64,      // 16 x u64 phase timestamps of the fused kernel (words 64..95)
+    kHdrRouterTickets = 96,   // fused kernel: router tiles done per group of 32 experts (words 96..127)
     kHdrWords = 128
 };
 
@@ -95,11 +96,20 @@ inline int pick_kchunks(int steps, long long units_no_split, size_t partial_byte
     return best;
 }
 
+// Copies of the router partials the single-launch kernel writes when every
+// CTA sums them (CTAs read copy blockIdx % kRouterCopies).
+constexpr int kRouterCopies = 4;
+
 // Router tiles of the single-launch kernel: groups of 32 experts x chunks of
-// `rows` router rows (a multiple of 8), about one tile per CTA.
+// `rows` router rows (a multiple of 8), about one tile per CTA; a tile's weight
+// lines (rows x 128 B, pulled into L1 ahead of use) stay within 96 KB.
 inline void fused_router_tiling(int H, int E, int *groups, int *chunks, int *rows) {
     *groups = (E + 31) / 32;
     int target = kFusedGridTarget / *groups;
+    const int max_rows = 768;
+    const int min_target = (H + max_rows - 1) / max_rows;
+    if (target < min_target)
+        target = min_target;
     if (target < 1)
         target = 1;
     int r = (H + target - 1) / target;
@@ -147,7 +157,7 @@ struct WsLayout {
         if (T <= kFusedMaxTokens) {          // single-launch kernel
             int g, ch, r;
             fused_router_tiling(H, E, &g, &ch, &r);
-            L.fz_rpart = take((size_t)ch * T * E * sizeof(float2));
+            L.fz_rpart = take((size_t)kRouterCopies * ch * T * E * sizeof(float2));
             L.fz_h32 = take(entries * (size_t)I * sizeof(float));
             L.fz_yent = take(entries * (size_t)H * sizeof(float));
         }

@@ -52,13 +52,14 @@ struct FusedArgs {
     int32_t *ids_out;            // [T, kps] or null
     float *w_out;                // [T, kps] or null
     uint32_t *hdr;               // workspace header
-    float2 *rpart;               // [r_chunks][T][E] router partial pairs
+    float2 *rpart;               // [kRouterCopies][r_chunks][T][E] router partial pairs
     float *h32;                  // [entries][I] h in sorted entry order
     float *yent;                 // [entries][H] per-entry outputs
     unsigned long long *cstamps; // [grid][4] per-CTA phase-end times (diagnostics)
     int T, H, E, k, S, I;
     float shared_weight;
     int r_groups, r_chunks, r_rows;   // router tiles: 32 experts x r_rows rows
+    int r_final;                 // 1: the router phase sums each group's chunks (else every CTA does)
     unsigned gu_unit, dn_unit;        // bytes of one packed row block
     int xwin_row, hwin_row;           // window row strides (elements)
     int win_entries;                  // entries the down window holds
@@ -78,7 +79,6 @@ constexpr unsigned long long kWaitLimitNs = 200ull * 1000 * 1000;
 // Routing results every CTA derives for itself in phase T.
 struct RouteState {
     int n_gu, n_dn, bad, pad;
-    int n_cand[kFusedMaxTokens];   // top-k candidates per token
     float xundo[kFusedMaxTokens];  // 2^-s of token t's f16 scaling
     float xscale[kFusedMaxTokens]; // 2^s
     int sel_id[kMaxEntries];       // entry t*kps+s -> expert
@@ -122,16 +122,18 @@ __device__ __forceinline__ void cta_stamp(const FusedArgs &a, int i) {
 }
 
 // Grid-wide wait in two halves.  grid_arrive: after the CTA barrier, one
-// thread fences (cumulative: it orders the writes the barrier ordered before
-// it) and arrives on the counter.  grid_wait: until `target` (= waits so far
+// thread issues a release fence (cumulative: it covers the writes the barrier
+// ordered before it) and adds its arrival to the counter.  grid_wait: until `target` (= waits so far
 // x CTAs) arrivals are counted.  Work that needs nobody else's results can
 // run in between.  A wait gives up after kWaitLimitNs (or when another CTA's
 // wait gave up) and returns false.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ void grid_arrive(const FusedArgs &a) {
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(a.hdr + kHdrBarrier, 1u);
+        fence_acq_rel_gpu();
+        asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(a.hdr + kHdrBarrier) : "memory");
     }
 }
 
@@ -155,8 +157,7 @@ __device__ bool grid_wait(const FusedArgs &a, unsigned target) {
                 break;
             }
         }
-        __threadfence();
-        ok = r;
+        ok = r;                           // the acquiring load orders what follows the barrier below
     }
     __syncthreads();
     return ok != 0;
@@ -164,15 +165,135 @@ __device__ bool grid_wait(const FusedArgs &a, unsigned target) {
 
 // ------------------------------------------------------------- phase R
 
+// Dot2 sums of one warp's rows of a router tile for TT token columns (x rows
+// staged as xs[row][TT], zero past T): each weight is loaded once and feeds TT
+// independent compensated sums.  The weights come in register batches of B
+// rows, the next batch in flight while the current one is summed.
+template <int TT>
+__device__ __forceinline__ void router_row(const float *xs, int row, float wv, float (&p)[kFusedMaxTokens],
+                                           float (&q)[kFusedMaxTokens]) {
+    const float *xr = xs + (size_t)row * TT;
+    float xv[TT];
+    if (TT == 1) {
+        xv[0] = xr[0];
+    } else if (TT == 2) {
+        const float2 v = *reinterpret_cast<const float2 *>(xr);
+        xv[0] = v.x;
+        xv[1 % TT] = v.y;
+    } else {
+#pragma unroll
+        for (int h = 0; h < TT / 4; ++h) {
+            const float4 v = *reinterpret_cast<const float4 *>(xr + 4 * h);
+            xv[(4 * h) % TT] = v.x;
+            xv[(4 * h + 1) % TT] = v.y;
+            xv[(4 * h + 2) % TT] = v.z;
+            xv[(4 * h + 3) % TT] = v.w;
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+        float hp, er, s;
+        two_prod(xv[t], wv, hp, er);
+        two_sum(p[t], hp, p[t], s);
+        q[t] = __fadd_rn(q[t], __fadd_rn(s, er));
+    }
+}
+
+template <int TT, int B>
+__device__ __forceinline__ void router_load(float (&w)[B], const float *wp, size_t wstride, int j0, int nrw,
+                                            bool live) {
+#pragma unroll
+    for (int u = 0; u < B; ++u)
+        w[u] = live && j0 + u < nrw ? __ldg(wp + (size_t)(j0 + u) * wstride) : 0.0f;
+}
+
+template <int TT, int B>
+__device__ __forceinline__ void router_sum(const float (&w)[B], const float *xs, int j0, int nrw,
+                                           float (&p)[kFusedMaxTokens], float (&q)[kFusedMaxTokens]) {
+    const int warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int u = 0; u < B; ++u)
+        if (j0 + u < nrw)
+            router_row<TT>(xs, (j0 + u) * NW + warp, w[u], p, q);
+}
+
+template <int TT>
+__device__ __forceinline__ void router_rows(const float *xs, const float *wp, size_t wstride, int nrw, bool live,
+                                            float (&p)[kFusedMaxTokens], float (&q)[kFusedMaxTokens]) {
+    constexpr int B = TT <= 2 ? 8 : 4;
+    float wa[B], wb[B];
+    router_load<TT, B>(wa, wp, wstride, 0, nrw, live);
+#pragma unroll 1
+    for (int j0 = 0; j0 < nrw; j0 += 2 * B) {
+        router_load<TT, B>(wb, wp, wstride, j0 + B, nrw, live);
+        router_sum<TT, B>(wa, xs, j0, nrw, p, q);
+        router_load<TT, B>(wa, wp, wstride, j0 + 2 * B, nrw, live);
+        router_sum<TT, B>(wb, xs, j0 + B, nrw, p, q);
+    }
+}
+
+// The CTA that completes the last chunk of an expert group sums the group's
+// chunk partials in chunk order (the chunk range split into parts that are
+// then added in part order) and leaves the logit pairs in chunk 0's slots.
+// Every CTA's partial writes are released before its ticket; the last CTA
+// acquires them after its own.
+__device__ void router_finish_group(const FusedArgs &a, int gi, float2 *red) {
+    __shared__ int last;
+    const int tid = threadIdx.x, T = a.T, E = a.E, chunks = a.r_chunks;
+    __syncthreads();
+    if (tid == 0) {
+        fence_acq_rel_gpu();                       // release this CTA's partials
+        const unsigned tk = atomicAdd(a.hdr + kHdrRouterTickets + gi, 1u);
+        last = tk == (unsigned)chunks - 1u;
+        if (last) {
+            fence_acq_rel_gpu();                   // acquire the other CTAs' partials
+            a.hdr[kHdrRouterTickets + gi] = 0u;    // ready for the next launch
+        }
+    }
+    __syncthreads();
+    if (!last)
+        return;
+    const int e0 = gi * 32, ne = min(E, e0 + 32) - e0, items = T * 32;
+    const int parts = max(1, NT / items), cpp = (chunks + parts - 1) / parts;
+    const int item = tid / parts, part = tid - item * parts, t = item >> 5, el = item & 31;
+    const bool live = item < items && el < ne;
+    float P = 0.0f, Q = 0.0f;
+    if (live) {
+        const float2 *src = a.rpart + (size_t)t * E + e0 + el;
+        const size_t cstride = (size_t)T * E;
+        const int c_lo = part * cpp, c_hi = min(chunks, c_lo + cpp);
+        for (int c0 = c_lo; c0 < c_hi; c0 += 16) {
+            float2 v[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                if (c0 + c < c_hi)
+                    v[c] = __ldcg(src + (size_t)(c0 + c) * cstride);
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+                if (c0 + c < c_hi)
+                    pair_add(P, Q, v[c].x, v[c].y);
+        }
+    }
+    if (item < items)
+        red[tid] = make_float2(P, Q);
+    __syncthreads();
+    if (live && part == 0) {
+        for (int q = 1; q < parts; ++q)
+            pair_add(P, Q, red[tid + q].x, red[tid + q].y);
+        a.rpart[(size_t)t * E + e0 + el] = make_float2(P, Q);
+    }
+}
+
 // Router tile (32 experts x r_rows rows): each warp pulls its rows (every
 // NW-th row) into L1 while the tile's x rows are staged, then accumulates one
 // Dot2 pair per token and lane (expert); the CTA sums the warps' pairs in warp
 // order.
-__device__ void phase_router(const FusedArgs &a, uint8_t *smB) {
+__device__ void phase_router(const FusedArgs &a, uint8_t *sm) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int T = a.T, H = a.H, E = a.E;
-    float *xs = reinterpret_cast<float *>(smB);                                  // [T][r_rows]
-    float2 *red = reinterpret_cast<float2 *>(smB + align_up(T * a.r_rows * 4, 16));   // [NW][T][32]
+    const int TT = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;      // token columns of the x rows
+    float *xs = reinterpret_cast<float *>(sm);                                    // [r_rows][TT]
+    float2 *red = reinterpret_cast<float2 *>(sm + align_up(TT * a.r_rows * 4, 16));   // [NW][T][32]
     const int tiles = a.r_groups * a.r_chunks;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         const int gi = tile % a.r_groups, ci = tile / a.r_groups;
@@ -186,33 +307,39 @@ __device__ void phase_router(const FusedArgs &a, uint8_t *smB) {
             prefetch_l1(wrow + j * wstride + e1 - 1);
         }
         __syncthreads();
-        for (int i = threadIdx.x; i < T * (nr / 8); i += NT) {
-            const int t = i / (nr / 8), c8 = i - t * (nr / 8);
-            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)t * H + r0) + c8);
+        for (int i = threadIdx.x; i < TT * (nr / 8); i += NT) {
+            const int c8 = i / TT, t = i - c8 * TT;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (t < T)
+                v = __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)t * H + r0) + c8);
             const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-            float *d = xs + t * a.r_rows + c8 * 8;
+            float *d = xs + (size_t)c8 * 8 * TT + t;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                d[2 * j] = __uint_as_float(w4[j] << 16);
-                d[2 * j + 1] = __uint_as_float(w4[j] & 0xFFFF0000u);
+                d[(2 * j) * TT] = __uint_as_float(w4[j] << 16);
+                d[(2 * j + 1) * TT] = __uint_as_float(w4[j] & 0xFFFF0000u);
             }
         }
         __syncthreads();
         stamp(a, 8);
         const bool live = e0 + lane < e1;
-        for (int t = 0; t < T; ++t) {
-            const float *xr = xs + t * a.r_rows + warp;
-            float p = 0.0f, q = 0.0f;
-#pragma unroll 4
-            for (int j = 0; j < nrw; ++j) {
-                const float w = live ? __ldg(wrow + j * wstride + e0 + lane) : 0.0f;
-                float hp, er, s;
-                two_prod(xr[j * NW], w, hp, er);
-                two_sum(p, hp, p, s);
-                q = __fadd_rn(q, __fadd_rn(s, er));
-            }
-            red[(warp * T + t) * 32 + lane] = make_float2(p, q);
-        }
+        float p[kFusedMaxTokens], q[kFusedMaxTokens];
+#pragma unroll
+        for (int t = 0; t < kFusedMaxTokens; ++t)
+            p[t] = q[t] = 0.0f;
+        const float *w0 = wrow + e0 + lane;
+        if (TT == 1)
+            router_rows<1>(xs, w0, wstride, nrw, live, p, q);
+        else if (TT == 2)
+            router_rows<2>(xs, w0, wstride, nrw, live, p, q);
+        else if (TT == 4)
+            router_rows<4>(xs, w0, wstride, nrw, live, p, q);
+        else
+            router_rows<8>(xs, w0, wstride, nrw, live, p, q);
+#pragma unroll
+        for (int t = 0; t < kFusedMaxTokens; ++t)
+            if (t < T)
+                red[(warp * T + t) * 32 + lane] = make_float2(p[t], q[t]);
         __syncthreads();
         for (int t = warp; t < T; t += NW) {
             float P = red[t * 32 + lane].x, Q = red[t * 32 + lane].y;
@@ -220,9 +347,20 @@ __device__ void phase_router(const FusedArgs &a, uint8_t *smB) {
                 const float2 v = red[(w2 * T + t) * 32 + lane];
                 pair_add(P, Q, v.x, v.y);
             }
-            if (live)
-                a.rpart[((size_t)ci * T + t) * E + e0 + lane] = make_float2(P, Q);
+            if (live) {
+                const size_t o = ((size_t)ci * T + t) * E + e0 + lane;
+                if (a.r_final) {
+                    a.rpart[o] = make_float2(P, Q);
+                } else {
+                    const size_t copy = (size_t)a.r_chunks * T * E;
+#pragma unroll
+                    for (int r = 0; r < kRouterCopies; ++r)
+                        a.rpart[o + r * copy] = make_float2(P, Q);
+                }
+            }
         }
+        if (a.r_final)
+            router_finish_group(a, gi, red);
     }
 }
 
@@ -343,17 +481,33 @@ __device__ __forceinline__ float unkey_half(uint32_t m) {
     return __uint_as_float((m & 0x80000000u) ? (m & 0x7FFFFFFFu) : ~m);
 }
 
-// Returns false when the routing selected an invalid expert (non-finite
-// logits); every CTA reaches the same answer.
-__device__ bool phase_route(const FusedArgs &a, RouteState &rs, uint8_t *smA, uint8_t *smB) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-    const int T = a.T, E = a.E, k = a.k, kps = a.k + a.S, n = T * kps, n_tot = a.E + a.S;
-    const int Ep = (E + 31) & ~31;                  // experts padded to whole groups of 32
-    const int cmax = (Ep / 32) * k;                  // top-k candidates per token at most
-    unsigned long long *key = reinterpret_cast<unsigned long long *>(smB);          // [T][Ep]
-    int *cand = reinterpret_cast<int *>(smB + (size_t)T * Ep * sizeof(unsigned long long));   // [T][cmax]
-    // logits: S consecutive threads share one logit's chunk partials and
-    // combine their sums in a fixed tree order
+// Order key of logit + bias from its (P, Q) pair.
+__device__ __forceinline__ void put_key(const FusedArgs &a, RouteState &rs, unsigned long long *key, int t, int e,
+                                        float P, float Q) {
+    pair_add(P, Q, a.bias ? __ldg(a.bias + e) : 0.0f, 0.0f);
+    float hi, lo;
+    two_sum(P, Q, hi, lo);
+    if (!isfinite(hi))
+        rs.bad = 1;                                  // non-finite router logits
+    key[t * ((a.E + 31) & ~31) + e] = logit_key(hi, lo);
+}
+
+// Logit keys.  With r_final the router phase left each logit's pair in chunk
+// 0's slot.  Otherwise every CTA sums the chunk pairs itself, from one of
+// kRouterCopies copies (spreading the CTAs' reads of the same lines): S
+// consecutive threads share a logit's chunks, each summing its range in chunk
+// order, and combine in a fixed tree.
+__device__ void route_logits(const FusedArgs &a, RouteState &rs, unsigned long long *key) {
+    const int tid = threadIdx.x, T = a.T, E = a.E;
+    if (a.r_final) {
+#pragma unroll 4
+        for (int i = tid; i < T * E; i += NT) {
+            const float2 v = __ldcg(a.rpart + i);
+            put_key(a, rs, key, i / E, i % E, v.x, v.y);
+        }
+        return;
+    }
+    const float2 *src = a.rpart + (size_t)(blockIdx.x % kRouterCopies) * a.r_chunks * T * E;
     int S = 1;
     while (S < 8 && 2 * S * T * E <= NT)
         S *= 2;
@@ -369,7 +523,7 @@ __device__ bool phase_route(const FusedArgs &a, RouteState &rs, uint8_t *smA, ui
 #pragma unroll
             for (int c = 0; c < 16; ++c)
                 if (live && c0 + c < c_hi)
-                    v[c] = __ldcg(a.rpart + ((size_t)(c0 + c) * T + t) * E + e);
+                    v[c] = __ldcg(src + ((size_t)(c0 + c) * T + t) * E + e);
 #pragma unroll
             for (int c = 0; c < 16; ++c)
                 if (live && c0 + c < c_hi)
@@ -380,22 +534,30 @@ __device__ bool phase_route(const FusedArgs &a, RouteState &rs, uint8_t *smA, ui
             if ((part & d) == 0)
                 pair_add(P, Q, oP, oQ);
         }
-        if (live && part == 0) {
-            pair_add(P, Q, a.bias ? __ldg(a.bias + e) : 0.0f, 0.0f);
-            float hi, lo;
-            two_sum(P, Q, hi, lo);
-            if (!isfinite(hi))
-                rs.bad = 1;                          // non-finite router logits
-            key[t * Ep + e] = logit_key(hi, lo);
-        }
+        if (live && part == 0)
+            put_key(a, rs, key, t, e, P, Q);
     }
-    for (int i = tid; i < T * (Ep - E); i += NT)     // padding sorts below every real key
+}
+
+// Returns false when the routing selected an invalid expert (non-finite
+// logits); every CTA reaches the same answer.
+__device__ bool phase_route(const FusedArgs &a, RouteState &rs, uint8_t *smA, uint8_t *smB) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    const int T = a.T, E = a.E, k = a.k, kps = a.k + a.S, n = T * kps, n_tot = a.E + a.S;
+    const int Ep = (E + 31) & ~31;                  // experts padded to whole groups of 32
+    const int cmax = (Ep / 32) * k;                  // sorted group lists: k entries per group
+    unsigned long long *key = reinterpret_cast<unsigned long long *>(smB);          // [T][Ep]
+    unsigned long long *ckey = key + (size_t)T * Ep;                                  // [T][cmax]
+    int *cand = reinterpret_cast<int *>(ckey + (size_t)T * cmax);                     // [T][cmax]
+    route_logits(a, rs, key);
+    for (int i = tid; i < T * (Ep - E); i += NT)     // padding ranks below every real key
         key[(i / (Ep - E)) * Ep + E + i % (Ep - E)] = 0ull;
     __syncthreads();
     stamp(a, 9);
-    // top k: an expert ranked k or lower inside its group of 32 cannot be in
-    // the top k, so the slots are the ranks among the group survivors; order
-    // is (key descending, index ascending)
+    // top k, stage 1: an expert ranked k or lower inside its group of 32
+    // cannot be in the top k; the group's first k ranks fill its sorted list
+    // (order: key descending, index ascending; padding carries index
+    // 0x7fffffff and key 0 and never reaches the top k)
     for (int i = tid; i < T * Ep; i += NT) {
         const int t = i / Ep, e = i - t * Ep;
         const unsigned long long *g = key + t * Ep + (e & ~31);
@@ -406,48 +568,59 @@ __device__ bool phase_route(const FusedArgs &a, RouteState &rs, uint8_t *smA, ui
             const unsigned long long o = g[j];
             r += (o > my) | ((o == my) & (j < (e & 31)));
         }
-        if (e < E && r < k)
-            cand[t * cmax + atomicAdd(&rs.n_cand[t], 1)] = e;
-    }
-    __syncthreads();
-    for (int i = tid; i < T * cmax; i += NT) {
-        const int t = i / cmax, c = i - t * cmax, nc = rs.n_cand[t];
-        if (c >= nc)
-            continue;
-        const int e = cand[t * cmax + c];
-        const unsigned long long my = key[t * Ep + e];
-        int r = 0;
-        for (int j = 0; j < nc; ++j) {
-            const int oe = cand[t * cmax + j];
-            const unsigned long long o = key[t * Ep + oe];
-            r += (o > my) | ((o == my) & (oe < e));
+        if (r < k) {
+            const int slot = t * cmax + (e >> 5) * k + r;
+            ckey[slot] = my;
+            cand[slot] = e < E ? e : 0x7fffffff;
         }
-        if (r < k)
-            rs.sel_id[t * kps + r] = e;
     }
     __syncthreads();
+    // stage 2, one warp per token: lane g holds the head of group g's list;
+    // each round takes the largest head (key, then lower index), and its lane
+    // moves to the next entry of its list.  Slot r gets the r-th largest
+    // logit.  The softmax over the kept logits is taken relative to the
+    // largest, its denominator summed in slot order.
     if (warp < T) {
-        // softmax over the kept logits, relative to the largest; the
-        // denominator is summed in slot order
-        const int t = warp;
+        const unsigned full = 0xffffffffu;
+        const int t = warp, G = Ep >> 5;
+        const unsigned long long *ck = ckey + t * cmax;
+        const int *ce = cand + t * cmax;
+        int pos = 0;
+        unsigned long long hk = lane < G ? ck[lane * k] : 0ull;
+        unsigned he = lane < G ? (unsigned)ce[lane * k] : 0xffffffffu;
+        unsigned long long myk = 0ull;
+        int myid = -1;
+        for (int r = 0; r < k; ++r) {
+            const uint32_t hh = (uint32_t)(hk >> 32), mh = __reduce_max_sync(full, hh);
+            const uint32_t ml = __reduce_max_sync(full, hh == mh ? (uint32_t)hk : 0u);
+            const unsigned we = __reduce_min_sync(full, (hh == mh && (uint32_t)hk == ml) ? he : 0xffffffffu);
+            if (lane == r) {
+                myk = ((unsigned long long)mh << 32) | ml;
+                myid = (int)we;
+            }
+            if (lane < G && he == we && we < (unsigned)E) {
+                ++pos;
+                hk = pos < k ? ck[lane * k + pos] : 0ull;
+                he = pos < k ? (unsigned)ce[lane * k + pos] : 0xffffffffu;
+            }
+        }
+        const unsigned long long k0 = __shfl_sync(full, myk, 0);
         float ex = 0.0f;
-        int id = 0;
         if (lane < k) {
-            id = rs.sel_id[t * kps + lane];
-            const unsigned long long k0 = key[t * Ep + rs.sel_id[t * kps]], kr = key[t * Ep + id];
             const float h0 = unkey_half((uint32_t)(k0 >> 32)), l0 = unkey_half((uint32_t)k0);
-            const float hr = unkey_half((uint32_t)(kr >> 32)), lr = unkey_half((uint32_t)kr);
+            const float hr = unkey_half((uint32_t)(myk >> 32)), lr = unkey_half((uint32_t)myk);
             ex = expf(__fadd_rn(__fsub_rn(hr, h0), __fsub_rn(lr, l0)));
         }
         float denom = 0.0f;
         for (int r = 0; r < k; ++r)
-            denom += __shfl_sync(0xffffffffu, ex, r);
+            denom += __shfl_sync(full, ex, r);
         if (lane < k) {
             const float w = ex / denom;
+            rs.sel_id[t * kps + lane] = myid;
             rs.sel_w[t * kps + lane] = w;
             if (blockIdx.x == 0) {
                 if (a.ids_out)
-                    a.ids_out[t * kps + lane] = id;
+                    a.ids_out[t * kps + lane] = myid;
                 if (a.w_out)
                     a.w_out[t * kps + lane] = w;
             }
@@ -933,11 +1106,9 @@ __global__ void __launch_bounds__(NT, 1) fused_layer_kernel(const __grid_constan
     stamp(a, 0);
     if (blockIdx.x == 0 && threadIdx.x == 0)
         reinterpret_cast<unsigned long long *>(a.hdr + kHdrStamps)[12] = clock64();
-    if (threadIdx.x < kFusedMaxTokens)           // ordered before phase T by the waits' barriers
-        rs.n_cand[threadIdx.x] = 0;
     if (threadIdx.x == 0)
         rs.bad = 0;
-    phase_router(a, smem + a.off_b);
+    phase_router(a, smem);                  // nothing else lives in shared memory yet
     stamp(a, 1);
     grid_arrive(a);
     x_window_local(a, rs, reinterpret_cast<__half *>(smem));
@@ -1023,6 +1194,10 @@ FusedPlan fused_plan(int T, int H, int I, int E, int k, int S, int grid) {
         return p;
     const int kps = k + S, n = T * kps, n_tot = E + S;
     fused_router_tiling(H, E, &p.r_groups, &p.r_chunks, &p.r_rows);
+    // past ~48 KB of chunk pairs per CTA, summing each group once in the
+    // router phase (a ticket and one more dependent step) beats every CTA
+    // reading them all
+    p.r_final = (long long)T * E * p.r_chunks * 8 > 48 * 1024;
     p.xwin_row = H + 32;
     p.hwin_row = I + 32;
     // down units a CTA can own, and the entries their passes can span
@@ -1042,15 +1217,17 @@ FusedPlan fused_plan(int T, int H, int I, int E, int k, int S, int grid) {
     const size_t sz_hundo = align_up((size_t)p.win_entries * sizeof(float), 16);
     p.off_b = p.off_hundo + sz_hundo;
     const int Ep = (E + 31) / 32 * 32;
-    const size_t b_logits = (size_t)T * Ep * sizeof(unsigned long long) + (size_t)T * (Ep / 32) * k * sizeof(int);
-    const size_t b_router = align_up((size_t)T * p.r_rows * 4, 16) + (size_t)kFusedWarps * T * 32 * sizeof(float2);
+    const size_t b_logits = (size_t)T * Ep * sizeof(unsigned long long) +
+                            (size_t)T * (Ep / 32) * k * (sizeof(unsigned long long) + sizeof(int));
+    const int TT = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
+    const size_t b_router = align_up((size_t)TT * p.r_rows * 4, 16) + (size_t)kFusedWarps * T * 32 * sizeof(float2);
     const size_t b_slots = (size_t)2 * kFusedWarps * 32 * 4 * sizeof(float) + (size_t)(nu_dn + 1) * sizeof(int);
     size_t szB = b_logits;
-    if (b_router > szB)
-        szB = b_router;
     if (b_slots > szB)
         szB = b_slots;
     p.smem = p.off_b + align_up(szB, 16);
+    if (b_router > p.smem)                  // the router phase runs first and may use all of it
+        p.smem = align_up(b_router, 16);
     p.ok = p.smem <= kFusedSmemBudget;
     return p;
 }
@@ -1114,6 +1291,7 @@ cudaError_t launch_fused(const FusedProblem &pr, void *ws, const WsLayout &L, in
     a.r_groups = plan.r_groups;
     a.r_chunks = plan.r_chunks;
     a.r_rows = plan.r_rows;
+    a.r_final = plan.r_final ? 1 : 0;
     a.gu_unit = (unsigned)PL.gu_unit_bytes;
     a.dn_unit = (unsigned)PL.dn_unit_bytes;
     a.xwin_row = plan.xwin_row;

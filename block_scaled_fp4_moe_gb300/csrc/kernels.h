@@ -83,6 +83,7 @@ struct FusedProblem {
 struct FusedPlan {
     bool ok;
     int r_groups, r_chunks, r_rows;
+    bool r_final;
     int xwin_row, hwin_row, win_entries;
     size_t off_hundo, off_b, smem;
 };

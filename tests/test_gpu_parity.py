@@ -182,6 +182,28 @@ def test_layer_small_shapes(case):
     compare_all(p, str(case))
 
 
+@pytest.mark.parametrize("T", [1, 4, 8, 13])
+def test_layer_exact_logit_ties_go_to_the_lower_index(T):
+    # duplicated router columns give bit-identical logits: four experts tie
+    # for the first slots across both groups of 32, and three more tie at the
+    # k-th slot, so the cut falls inside a tie (lower indices win)
+    p = random_problem(T=T, H=1024, E=64, k=6, I=512, seed=31 + T, bias=False)
+    rng = np.random.default_rng(7)
+    base = inputs.bf16_bits_to_f32(p.x[0])
+    x = base[None, :] + 0.1 * rng.standard_normal((T, p.H)).astype(np.float32)
+    p.x = inputs.f32_to_bf16_bits(x.astype(np.float32))
+    p.xd = dev_bf16(p.x)
+    v = (0.02 * np.sign(base)).astype(np.float32)
+    for e in (3, 17, 35, 50):
+        p.wr[:, e] = 3.0 * v
+    for e in (8, 40, 41):
+        p.wr[:, e] = 1.5 * v
+    p.wrd = torch.from_numpy(p.wr).cuda()
+    r = p.oracle_route()
+    assert (r["ids"][:, :6] == np.array([3, 17, 35, 50, 8, 40])).all()
+    compare_all(p, f"ties T={T}")
+
+
 def test_layer_tiny_workload_against_fixture():
     cfg = inputs.CONFIGS["tiny"]
     p = Problem.from_config(cfg)
