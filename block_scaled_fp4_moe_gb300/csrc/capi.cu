@@ -91,6 +91,8 @@ GroupOut group_out_for(void *ws, const WsLayout &L, int H) {
     go.num_active = nullptr;
     go.passes = ws_at<Pass>(ws, L.passes);
     go.passes4 = ws_at<Pass>(ws, L.passes4);
+    go.passesw = ws_at<Pass>(ws, L.passesw);
+    go.passesw4 = ws_at<Pass>(ws, L.passesw4);
     go.counters = ws_at<uint32_t>(ws, L.counters);
     go.n_counters = 0;
     return go;
@@ -299,6 +301,8 @@ moe_status_t moe_group_tokens(const int32_t *topk_ids, int T, int k_plus_s, int 
     go.num_active = num_active;
     go.passes = nullptr;
     go.passes4 = nullptr;
+    go.passesw = nullptr;
+    go.passesw4 = nullptr;
     go.counters = nullptr;
     go.n_counters = 0;
     return from_cuda(launch_group(topk_ids, T, k_plus_s, n_experts_total, go, ws_at<uint32_t>(ws, 0), stream));

@@ -19,6 +19,8 @@ constexpr int kRouteCols = 32;        // router experts per CTA (one per lane)
 constexpr int kRouteThreads = 256;
 constexpr int kGroupThreads = 256;
 constexpr int kPassTokens = 8;        // MMA N: tokens per gate/up pass
+constexpr int kWidePassTokens = 32;   // tiled kernels (large T): four MMA column groups per decoded tile
+constexpr int kWidePassEntries = 16;  //   down: 16 entries x (hi, lo)
 constexpr int kPassEntries = 4;       // entries per down pass (hi and lo f16 terms fill N = 8)
 constexpr int kFfnWarps = 12;         // warps per expert-FFN CTA (one CTA per SM)
 constexpr int kFfnBatch = 8;          // steps per batch of loads (two batches in flight)
@@ -43,6 +45,8 @@ enum HeaderWord : int {
     kHdrNumActive = 3,
     kHdrNumPasses = 4,
     kHdrNumPasses4 = 5,
+    kHdrNumPassesW = 6,   // wide passes (<= kWidePassTokens) of the tiled gate/up kernel
+    kHdrNumPassesW4 = 7,  // wide passes (<= kWidePassEntries) of the tiled down kernel
     kHdrBarrier = 32,     // grid-wait arrivals of the fused layer kernel (own 128-byte line)
     kHdrAbort = 33,       // set when a fused-kernel wait gave up
     kHdrDone = 34,        // CTAs of the fused layer kernel that have finished
@@ -120,7 +124,8 @@ inline void fused_router_tiling(int H, int E, int *groups, int *chunks, int *row
 
 // Offsets (bytes) of the workspace regions for one problem size.
 struct WsLayout {
-    size_t route_part, topk_ids, topk_w, offsets, sorted_tok, sorted_slot, inv_pos, active, passes, passes4, x16, xundo,
+    size_t route_part, topk_ids, topk_w, offsets, sorted_tok, sorted_slot, inv_pos, active, passes, passes4, passesw,
+        passesw4, x16, xundo,
         gpart, h16, hundo, ypart, counters, xstage, ystage, fz_rpart, fz_h32, fz_yent, total;
     int n_kc_gu, n_kc_dn;
 
@@ -145,6 +150,8 @@ struct WsLayout {
         L.active = take((size_t)n_tot * sizeof(int32_t));
         L.passes = take((size_t)max_passes(T, kps, n_tot) * sizeof(Pass));
         L.passes4 = take((size_t)max_passes(T, kps, n_tot, kPassEntries) * sizeof(Pass));
+        L.passesw = take((size_t)max_passes(T, kps, n_tot, kWidePassTokens) * sizeof(Pass));
+        L.passesw4 = take((size_t)max_passes(T, kps, n_tot, kWidePassEntries) * sizeof(Pass));
         L.x16 = take((size_t)T * H * 2);
         L.xundo = take((size_t)T * sizeof(float));
         L.gpart = take((size_t)L.n_kc_gu * entries * 2 * I * sizeof(float));
@@ -313,6 +320,15 @@ __device__ __forceinline__ void pair_add(float &p, float &s, float p2, float s2)
 // ------------------------------------------------------ weight streaming
 
 constexpr int kStepBytes = 544;          // one 16 x 64 tile of the repacked bank: 512 B codes + 32 B exponents
+
+// 16-byte asynchronous copy global -> shared (L2 only), and its group fences.
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 __device__ __forceinline__ uint4 ld_stream16(const void *p, uint64_t policy) {
     uint4 v;

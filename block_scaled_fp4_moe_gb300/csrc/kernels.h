@@ -15,6 +15,8 @@ struct GroupOut {
     int32_t *num_active;   // [1] nullable (the header always gets it)
     Pass *passes;          // nullable: passes of <= 8 entries (gate/up)
     Pass *passes4;         // with passes: passes of <= 4 entries (down)
+    Pass *passesw;         // with passes: wide passes of <= kWidePassTokens (tiled gate/up)
+    Pass *passesw4;        // with passes: wide passes of <= kWidePassEntries (tiled down)
     uint32_t *counters;    // down-kernel row-block counters to zero
     int n_counters;
 };

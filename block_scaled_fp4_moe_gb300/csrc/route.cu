@@ -143,6 +143,8 @@ __device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const
             hdr[kHdrNumActive] = 0;
             hdr[kHdrNumPasses] = 0;
             hdr[kHdrNumPasses4] = 0;
+            hdr[kHdrNumPassesW] = 0;
+            hdr[kHdrNumPassesW4] = 0;
             if (o.num_active)
                 *o.num_active = 0;
         }
@@ -150,7 +152,13 @@ __device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const
     }
 
     if (warp == 0) {
-        int run = 0, na = 0, np = 0, np4 = 0;
+        // pass lists: caps kPassTokens (gate/up), kPassEntries (down) and the
+        // wide caps of the tiled kernels
+        constexpr int NL = 4;
+        const int caps[NL] = {kPassTokens, kPassEntries, kWidePassTokens, kWidePassEntries};
+        Pass *const lists[NL] = {o.passes, o.passes4, o.passesw, o.passesw4};
+        int run = 0, na = 0;
+        int np[NL] = {0, 0, 0, 0};
         for (int base = 0; base < n_tot; base += 32) {
             const int e = base + lane;
             const int v = e < n_tot ? cnt[e] : 0;
@@ -164,43 +172,38 @@ __device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const
             const int excl = run + incl - v;
             const unsigned act = __ballot_sync(0xffffffffu, v > 0);
             const int rank = __popc(act & ((1u << lane) - 1u));
-            // passes of up to kPassTokens (gate/up) and kPassEntries (down) entries
-            const int npass = (v + kPassTokens - 1) / kPassTokens;
-            const int npass4 = (v + kPassEntries - 1) / kPassEntries;
-            int pincl = npass, pincl4 = npass4;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, pincl, d);
-                const int y4 = __shfl_up_sync(0xffffffffu, pincl4, d);
-                if (lane >= d) {
-                    pincl += y;
-                    pincl4 += y4;
-                }
-            }
-            const int pexcl = np + pincl - npass, pexcl4 = np4 + pincl4 - npass4;
             if (e < n_tot) {
                 cursor[e] = excl;
                 o.offsets[e] = excl;
                 if (v > 0)
                     o.active[na + rank] = e;
-                if (o.passes) {
-                    for (int p = 0; p < npass; ++p)
-                        o.passes[pexcl + p] = Pass{e, excl + p * kPassTokens, min(kPassTokens, v - p * kPassTokens), 0};
-                    for (int p = 0; p < npass4; ++p)
-                        o.passes4[pexcl4 + p] =
-                            Pass{e, excl + p * kPassEntries, min(kPassEntries, v - p * kPassEntries), 0};
+            }
+#pragma unroll
+            for (int li = 0; li < NL; ++li) {
+                const int npass = (v + caps[li] - 1) / caps[li];
+                int pincl = npass;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, pincl, d);
+                    if (lane >= d)
+                        pincl += y;
                 }
+                const int pexcl = np[li] + pincl - npass;
+                if (o.passes && e < n_tot)
+                    for (int p = 0; p < npass; ++p)
+                        lists[li][pexcl + p] = Pass{e, excl + p * caps[li], min(caps[li], v - p * caps[li]), 0};
+                np[li] += __shfl_sync(0xffffffffu, pincl, 31);
             }
             run += __shfl_sync(0xffffffffu, incl, 31);
-            np += __shfl_sync(0xffffffffu, pincl, 31);
-            np4 += __shfl_sync(0xffffffffu, pincl4, 31);
             na += __popc(act);
         }
         if (lane == 0) {
             o.offsets[n_tot] = run;
             hdr[kHdrNumActive] = na;
-            hdr[kHdrNumPasses] = np;
-            hdr[kHdrNumPasses4] = np4;
+            hdr[kHdrNumPasses] = np[0];
+            hdr[kHdrNumPasses4] = np[1];
+            hdr[kHdrNumPassesW] = np[2];
+            hdr[kHdrNumPassesW4] = np[3];
             if (o.num_active)
                 *o.num_active = na;
         }
