@@ -385,7 +385,7 @@ __global__ void __launch_bounds__(NW * 32, 1) ffn_kernel(const __grid_constant__
 constexpr int kTileWarps = 12;
 constexpr int kTiledMinTokens = 32;              // T from which the tiled kernels run
 constexpr int kTileCols = 32;                    // B columns: 4 MMA column groups
-constexpr int kTileRow = 8 * 64 + 8;             // B tile row stride in halves (512 + pad)
+constexpr int kTileRow = 8 * 64 + 32;            // B tile row stride in halves: 1088 B, rows g and g+1 on disjoint bank quads
 constexpr size_t kTileSmem = (size_t)2 * kTileCols * kTileRow * sizeof(__half);
 
 struct TiledArgs {
