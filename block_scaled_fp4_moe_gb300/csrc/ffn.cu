@@ -404,6 +404,52 @@ struct TiledArgs {
     const float *bundo;          // down: per-entry factor that undoes the h scaling
 };
 
+// The sums of row block u of pass ps are complete: gate/up writes the gate
+// and up sums of its real tokens; down adds each lo column to its hi column,
+// undoes the entry's h scaling and writes the entries' outputs.
+template <int MODE>
+__device__ __forceinline__ void tiled_epilogue(const TiledArgs &a, const Pass &ps, int ncg, int u,
+                                               const float (&acc)[4][4]) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
+    if (MODE == kFfnGateUp) {
+#pragma unroll
+        for (int cg = 0; cg < 4; ++cg) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int n = 8 * cg + 2 * c + h;
+                if (cg < ncg && n < ps.count) {
+                    float *dst = a.part + (size_t)(ps.begin + n) * 2 * a.out_len + 8 * u + g;
+                    dst[0] = acc[cg][h];                      // gate row
+                    dst[a.out_len] = acc[cg][2 + h];          // up row
+                }
+            }
+        }
+    } else {
+#pragma unroll
+        for (int cg = 0; cg < 4; ++cg) {
+            if (cg < ncg) {
+                float y[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)                  // add the lo column to the hi column
+                    y[i] = acc[cg][i] + __shfl_xor_sync(0xffffffffu, acc[cg][i], 2);
+                if (c < 2) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int n = 4 * cg + 2 * c + h;
+                        if (n < ps.count) {
+                            const int e = ps.begin + n;
+                            const float un = a.bundo[e];
+                            float *dst = a.part + (size_t)e * a.out_len + 16 * u;
+                            dst[g] = y[h] * un;
+                            dst[g + 8] = y[2 + h] * un;
+                        }
+                    }
+                }
+            }
+        }
+    }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kTileWarps * 32, 1) ffn_tiled_kernel(const __grid_constant__ TiledArgs a) {
     extern __shared__ __align__(16) uint8_t tsm[];
@@ -527,42 +573,137 @@ __global__ void __launch_bounds__(kTileWarps * 32, 1) ffn_tiled_kernel(const __g
         }
         if (!active)
             continue;
-        if (MODE == kFfnGateUp) {
+        tiled_epilogue<MODE>(a, ps, ncg, u, acc);
+    }
+}
+
+// Whole-K variant (the down projection, K = I): the pass's B rows over all of
+// K fit in shared memory, so they are copied once per item and every warp
+// streams several row blocks back to back (a ring of two register batches
+// running across row blocks), with no barrier inside the stream.  An item is
+// a pass and kKfUnits row blocks, kKfUnits / kTileWarps per warp.
+constexpr int kKfUnitsPerWarp = 4;
+constexpr int kKfUnits = kKfUnitsPerWarp * kTileWarps;
+
+inline size_t kfull_smem(int K) { return (size_t)kTileCols * (K + 32) * sizeof(__half); }
+
+template <int MODE>
+__global__ void __launch_bounds__(kTileWarps * 32, 1) ffn_tiled_kfull_kernel(const __grid_constant__ TiledArgs a) {
+    extern __shared__ __align__(16) uint8_t tsm[];
+    __half *win = reinterpret_cast<__half *>(tsm);             // [kTileCols][K + 32]
+    __shared__ int brow[kTileCols];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, c = lane & 3;
+    pdl_wait();
+    pdl_trigger();
+    const int K = a.b_row, wrow = K + 32;
+    const int n_passes = *reinterpret_cast<const volatile int *>(a.hdr + a.passes_word);
+    const int n_rg = (a.upe + kKfUnits - 1) / kKfUnits;
+    const long long n_items = (long long)n_passes * n_rg;
+    const int nkc = a.steps / 8;
+    const uint64_t pol = l2_evict_first_policy();
+    for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const int P = (int)(item / n_rg), rg = (int)(item - (long long)P * n_rg);
+        const Pass ps = a.passes[P];
+        const int ncg = MODE == kFfnGateUp ? (ps.count + 7) >> 3 : (ps.count + 3) >> 2;
+        __syncthreads();
+        if (threadIdx.x < kTileCols) {
+            const int col = threadIdx.x;
+            int row;
+            if (MODE == kFfnGateUp) {
+                row = a.sorted_tok[ps.begin + (col < ps.count ? col : 0)];
+            } else {
+                const int j = 4 * (col >> 3) + (col & 3);
+                row = 2 * (ps.begin + (j < ps.count ? j : 0)) + ((col >> 2) & 1);
+            }
+            brow[col] = row * K;
+        }
+        __syncthreads();
+        // this warp's row blocks: rg * kKfUnits + warp + kTileWarps * j
+        int nu = 0;
+        while (nu < kKfUnitsPerWarp && rg * kKfUnits + warp + kTileWarps * nu < a.upe)
+            ++nu;
+        const int nbat = nu * nkc;
+        const uint8_t *ebase = a.packed + (size_t)ps.expert * a.upe * a.unit_bytes;
+        auto load = [&](int b, uint4 (&qq)[8], uint32_t (&ss)[8]) {
+            const int j = b / nkc, kc = b - j * nkc;
+            const int u = rg * kKfUnits + warp + kTileWarps * j;
+            const uint8_t *p = ebase + (size_t)u * a.unit_bytes + (size_t)kc * 8 * kStepBytes;
 #pragma unroll
-            for (int cg = 0; cg < 4; ++cg) {
+            for (int s = 0; s < 8; ++s) {
+                qq[s] = ld_stream16(p + s * kStepBytes + lane * 16, pol);
+                ss[s] = ld_stream4(p + s * kStepBytes + 512 + g * 4, pol);
+            }
+        };
+        uint4 q[2][8];
+        uint32_t s[2][8];
+        if (nbat > 0)
+            load(0, q[0], s[0]);              // weights first, then the window copy
+        const int rows = 8 * ncg;
+        for (int i = threadIdx.x; i < rows * (K / 8); i += blockDim.x) {
+            const int r = i / (K / 8), k8 = i - r * (K / 8);
+            cp_async16(win + r * wrow + k8 * 8, a.b16 + brow[r] + k8 * 8);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncthreads();
+        float acc[4][4];
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int n = 8 * cg + 2 * c + h;
-                    if (cg < ncg && n < ps.count) {
-                        float *dst = a.part + (size_t)(ps.begin + n) * 2 * a.out_len + 8 * u + g;
-                        dst[0] = acc[cg][h];                      // gate row
-                        dst[a.out_len] = acc[cg][2 + h];          // up row
+        for (int cg = 0; cg < 4; ++cg)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                acc[cg][i] = 0.0f;
+        const __half *wb = win + g * wrow + 8 * c;
+        auto compute = [&](const uint4 (&qq)[8], const uint32_t (&ss)[8], int b) {
+            const int j = b / nkc, kc = b - j * nkc;
+            const __half *tb = wb + kc * 512;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                uint32_t pa0[4], qa0[4], pa1[4], qa1[4];
+                decode_e2m1x8(qq[t].x, pa0);
+                decode_e2m1x8(qq[t].y, qa0);
+                decode_e2m1x8(qq[t].z, pa1);
+                decode_e2m1x8(qq[t].w, qa1);
+                float sg0, sg1, sh0, sh1;
+                e8m0x4_to_f32(ss[t], sg0, sg1, sh0, sh1);
+                const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+                for (int cg = 0; cg < 4; ++cg) {
+                    if (cg < ncg) {
+                        const __half *bp = tb + cg * 8 * wrow + 64 * t;
+                        const uint4 b0 = *reinterpret_cast<const uint4 *>(bp);
+                        const uint4 b1 = *reinterpret_cast<const uint4 *>(bp + 32);
+                        float d[4], e[4];
+                        mma_m16n8k16_f16(d, pa0[0], qa0[0], pa0[1], qa0[1], b0.x, b0.y, zero);
+                        mma_m16n8k16_f16(d, pa0[2], qa0[2], pa0[3], qa0[3], b0.z, b0.w, d);
+                        mma_m16n8k16_f16(e, pa1[0], qa1[0], pa1[1], qa1[1], b1.x, b1.y, zero);
+                        mma_m16n8k16_f16(e, pa1[2], qa1[2], pa1[3], qa1[3], b1.z, b1.w, e);
+                        acc[cg][0] = fmaf(d[0], sg0, fmaf(e[0], sg1, acc[cg][0]));
+                        acc[cg][1] = fmaf(d[1], sg0, fmaf(e[1], sg1, acc[cg][1]));
+                        acc[cg][2] = fmaf(d[2], sh0, fmaf(e[2], sh1, acc[cg][2]));
+                        acc[cg][3] = fmaf(d[3], sh0, fmaf(e[3], sh1, acc[cg][3]));
                     }
                 }
             }
-        } else {
+            if (kc == nkc - 1) {              // the row block is complete
+                const int u = rg * kKfUnits + warp + kTileWarps * j;
+                tiled_epilogue<MODE>(a, ps, ncg, u, acc);
 #pragma unroll
-            for (int cg = 0; cg < 4; ++cg) {
-                if (cg < ncg) {
-                    float y[4];
+                for (int cg = 0; cg < 4; ++cg)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)                  // add the lo column to the hi column
-                        y[i] = acc[cg][i] + __shfl_xor_sync(0xffffffffu, acc[cg][i], 2);
-                    if (c < 2) {
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int n = 4 * cg + 2 * c + h;
-                            if (n < ps.count) {
-                                const int e = ps.begin + n;
-                                const float un = a.bundo[e];
-                                float *dst = a.part + (size_t)e * a.out_len + 16 * u;
-                                dst[g] = y[h] * un;
-                                dst[g + 8] = y[2 + h] * un;
-                            }
-                        }
-                    }
-                }
+                    for (int i = 0; i < 4; ++i)
+                        acc[cg][i] = 0.0f;
             }
+        };
+        for (int b = 0; b < nbat; b += 2) {
+            if (b + 1 < nbat)
+                load(b + 1, q[1], s[1]);
+            compute(q[0], s[0], b);
+            if (b + 1 >= nbat)
+                break;
+            if (b + 2 < nbat)
+                load(b + 2, q[0], s[0]);
+            compute(q[1], s[1], b + 1);
         }
     }
 }
@@ -818,8 +959,20 @@ static cudaError_t launch_ffn_tiled(const FfnProblem &pr, void *ws, const WsLayo
     d.part = ws_at<float>(ws, L.ypart);
     d.out_len = H;
     d.bundo = ws_at<float>(ws, L.hundo);
-    if ((err = launch_pdl(ffn_tiled_kernel<kFfnDown>, dim3(num_sms), dim3(kTileWarps * 32), kTileSmem, stream,
-                          d)) != cudaSuccess)
+    const size_t ksm = kfull_smem(I);
+    if (ksm <= 200 * 1024) {                // the pass's h rows over all of I fit: whole-K items
+        static std::atomic<int> kset{0};
+        if (kset.load() < (int)ksm) {
+            if ((err = cudaFuncSetAttribute(ffn_tiled_kfull_kernel<kFfnDown>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ksm)) != cudaSuccess)
+                return err;
+            kset.store((int)ksm);
+        }
+        err = launch_pdl(ffn_tiled_kfull_kernel<kFfnDown>, dim3(num_sms), dim3(kTileWarps * 32), ksm, stream, d);
+    } else {
+        err = launch_pdl(ffn_tiled_kernel<kFfnDown>, dim3(num_sms), dim3(kTileWarps * 32), kTileSmem, stream, d);
+    }
+    if (err != cudaSuccess)
         return err;
     return launch_pdl(combine_kernel, dim3(T * ((H + 255) / 256)), dim3(256), 0, stream,
                       (const float *)ws_at<float>(ws, L.ypart), 1, entries,
