@@ -585,7 +585,7 @@ __global__ void __launch_bounds__(kTileWarps * 32, 1) ffn_tiled_kernel(const __g
 constexpr int kKfUnitsPerWarp = 4;
 constexpr int kKfUnits = kKfUnitsPerWarp * kTileWarps;
 
-inline size_t kfull_smem(int K) { return (size_t)kTileCols * (K + 32) * sizeof(__half); }
+inline size_t kfull_smem(int K, int cols) { return (size_t)cols * (K + 32) * sizeof(__half); }
 
 template <int MODE>
 __global__ void __launch_bounds__(kTileWarps * 32, 1) ffn_tiled_kfull_kernel(const __grid_constant__ TiledArgs a) {
@@ -929,8 +929,22 @@ static cudaError_t launch_ffn_tiled(const FfnProblem &pr, void *ws, const WsLayo
     g.hdr = hdr;
     g.part = ws_at<float>(ws, L.gpart);
     g.out_len = I;
-    if ((err = launch_pdl(ffn_tiled_kernel<kFfnGateUp>, dim3(num_sms), dim3(kTileWarps * 32), kTileSmem, stream,
-                          g)) != cudaSuccess)
+    const size_t gsm = kfull_smem(H, kWidePassEntries);
+    if (gsm <= 200 * 1024) {                // 16 tokens' x rows over all of H fit: whole-K items
+        g.passes = ws_at<Pass>(ws, L.passesw4);
+        g.passes_word = kHdrNumPassesW4;
+        static std::atomic<int> gset{0};
+        if (gset.load() < (int)gsm) {
+            if ((err = cudaFuncSetAttribute(ffn_tiled_kfull_kernel<kFfnGateUp>,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsm)) != cudaSuccess)
+                return err;
+            gset.store((int)gsm);
+        }
+        err = launch_pdl(ffn_tiled_kfull_kernel<kFfnGateUp>, dim3(num_sms), dim3(kTileWarps * 32), gsm, stream, g);
+    } else {
+        err = launch_pdl(ffn_tiled_kernel<kFfnGateUp>, dim3(num_sms), dim3(kTileWarps * 32), kTileSmem, stream, g);
+    }
+    if (err != cudaSuccess)
         return err;
     const size_t hsmem = (size_t)I * sizeof(float);
     if (hsmem > 48 * 1024 &&
@@ -959,7 +973,7 @@ static cudaError_t launch_ffn_tiled(const FfnProblem &pr, void *ws, const WsLayo
     d.part = ws_at<float>(ws, L.ypart);
     d.out_len = H;
     d.bundo = ws_at<float>(ws, L.hundo);
-    const size_t ksm = kfull_smem(I);
+    const size_t ksm = kfull_smem(I, kTileCols);
     if (ksm <= 200 * 1024) {                // the pass's h rows over all of I fit: whole-K items
         static std::atomic<int> kset{0};
         if (kset.load() < (int)ksm) {
