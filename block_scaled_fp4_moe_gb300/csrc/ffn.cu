@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(NW * 32, 1) ffn_kernel(const __grid_constant__
 // once (K-chunk count 1 in the partial layouts of hfin and combine).
 
 constexpr int kTileWarps = 12;
-constexpr int kTiledMinTokens = 32;              // T from which the tiled kernels run
+constexpr int kTiledMinTokens = 9;               // T from which the tiled kernels run
 constexpr int kTileCols = 32;                    // B columns: 4 MMA column groups
 constexpr int kTileRow = 8 * 64 + 32;            // B tile row stride in halves: 1088 B, rows g and g+1 on disjoint bank quads
 constexpr size_t kTileSmem = (size_t)2 * kTileCols * kTileRow * sizeof(__half);
@@ -581,9 +581,8 @@ __global__ void __launch_bounds__(kTileWarps * 32, 1) ffn_tiled_kernel(const __g
 // K fit in shared memory, so they are copied once per item and every warp
 // streams several row blocks back to back (a ring of two register batches
 // running across row blocks), with no barrier inside the stream.  An item is
-// a pass and kKfUnits row blocks, kKfUnits / kTileWarps per warp.
+// a pass and up to kKfUnitsPerWarp row blocks per warp.
 constexpr int kKfUnitsPerWarp = 4;
-constexpr int kKfUnits = kKfUnitsPerWarp * kTileWarps;
 
 inline size_t kfull_smem(int K, int cols) { return (size_t)cols * (K + 32) * sizeof(__half); }
 
@@ -598,7 +597,12 @@ __global__ void __launch_bounds__(kTileWarps * 32, 1) ffn_tiled_kfull_kernel(con
     pdl_trigger();
     const int K = a.b_row, wrow = K + 32;
     const int n_passes = *reinterpret_cast<const volatile int *>(a.hdr + a.passes_word);
-    const int n_rg = (a.upe + kKfUnits - 1) / kKfUnits;
+    // row blocks per warp and item: up to kKfUnitsPerWarp, fewer when there
+    // are too few items to give every CTA about two
+    const int rg1 = (a.upe + kTileWarps - 1) / kTileWarps;
+    const int upw = max(1, min(kKfUnitsPerWarp, (int)((long long)n_passes * rg1 / (2 * gridDim.x))));
+    const int rgu = upw * kTileWarps;
+    const int n_rg = (a.upe + rgu - 1) / rgu;
     const long long n_items = (long long)n_passes * n_rg;
     const int nkc = a.steps / 8;
     const uint64_t pol = l2_evict_first_policy();
@@ -619,15 +623,15 @@ __global__ void __launch_bounds__(kTileWarps * 32, 1) ffn_tiled_kfull_kernel(con
             brow[col] = row * K;
         }
         __syncthreads();
-        // this warp's row blocks: rg * kKfUnits + warp + kTileWarps * j
+        // this warp's row blocks: rg * rgu + warp + kTileWarps * j
         int nu = 0;
-        while (nu < kKfUnitsPerWarp && rg * kKfUnits + warp + kTileWarps * nu < a.upe)
+        while (nu < upw && rg * rgu + warp + kTileWarps * nu < a.upe)
             ++nu;
         const int nbat = nu * nkc;
         const uint8_t *ebase = a.packed + (size_t)ps.expert * a.upe * a.unit_bytes;
         auto load = [&](int b, uint4 (&qq)[8], uint32_t (&ss)[8]) {
             const int j = b / nkc, kc = b - j * nkc;
-            const int u = rg * kKfUnits + warp + kTileWarps * j;
+            const int u = rg * rgu + warp + kTileWarps * j;
             const uint8_t *p = ebase + (size_t)u * a.unit_bytes + (size_t)kc * 8 * kStepBytes;
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
@@ -686,7 +690,7 @@ __global__ void __launch_bounds__(kTileWarps * 32, 1) ffn_tiled_kfull_kernel(con
                 }
             }
             if (kc == nkc - 1) {              // the row block is complete
-                const int u = rg * kKfUnits + warp + kTileWarps * j;
+                const int u = rg * rgu + warp + kTileWarps * j;
                 tiled_epilogue<MODE>(a, ps, ncg, u, acc);
 #pragma unroll
                 for (int cg = 0; cg < 4; ++cg)
