@@ -269,8 +269,15 @@ def run_mine(args, cfg):
     stream = torch.cuda.Stream(device=dev)
 
     def step(i, s):
-        moe.moe_layer_forward(xd, routers[i % n_layers], bd, cfg.top_k, banks[i % n_layers], 1.0, y, ws=ws,
-                              stream=s)
+        if args.chain:
+            # a chain of layers: each call names the next one, whose router and
+            # shared expert it prefetches into L2 once its own streams are done
+            j = (i + 1) % n_layers
+            moe.moe_layer_forward_next(xd, routers[i % n_layers], bd, cfg.top_k, banks[i % n_layers], 1.0, y,
+                                       ws=ws, next_router_w=routers[j], next_bank=banks[j], stream=s)
+        else:
+            moe.moe_layer_forward(xd, routers[i % n_layers], bd, cfg.top_k, banks[i % n_layers], 1.0, y, ws=ws,
+                                  stream=s)
 
     # graph of one rotation over all layers
     with torch.cuda.stream(stream):
@@ -397,7 +404,9 @@ def run_mine(args, cfg):
                        "bytes_per_call": b["total"], "router_bytes_not_counted": b["router"],
                        "l2": f"inputs larger than L2: steps rotate over {n_layers} weight copies "
                              f"({n_layers} x {b['total'] / 1e6:.1f} MB vs L2 {l2 / 1e6:.0f} MB)",
-                       "launch": f"cuda graph replay, {launches} kernel launch(es) per call",
+                       "launch": f"cuda graph replay, {launches} kernel launch(es) per call" +
+                                 (", layers chained (moe_layer_forward_next: the next layer's router and shared "
+                                  "expert prefetched into L2)" if args.chain else ""),
                        "parallelism": f"replicas x{world}"},
             "kernel_us": kern_us, "kernel_timing": kernel_source, "phase_us": phases,
             "roofline": {"bound": "hbm", "kernel": roof_kernel, "achieved": achieved,
@@ -452,6 +461,9 @@ def main():
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=list(inputs.CONFIGS))
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--chain", action=argparse.BooleanOptionalAction, default=False,
+                    help="time the calls as a chain of layers that prefetch the next layer's router and shared "
+                         "expert (moe_layer_forward_next)")
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="profiling mode: run this many plain layer calls on one weight copy and exit")
     args = ap.parse_args()

@@ -101,7 +101,8 @@ GroupOut group_out_for(void *ws, const WsLayout &L, int H) {
 // Shared body of the full-layer entry points.
 moe_status_t layer_forward(const uint16_t *x, const float *router_w, const float *logit_bias, int T, int top_k,
                            const moe_mxfp4_bank_t *bank, float shared_weight, uint16_t *y, int32_t *ids_out,
-                           float *w_out, void *ws, size_t ws_bytes, cudaEvent_t *ev, cudaStream_t stream) {
+                           float *w_out, void *ws, size_t ws_bytes, cudaEvent_t *ev, cudaStream_t stream,
+                           const float *next_router_w = nullptr, const moe_mxfp4_bank_t *next_bank = nullptr) {
     moe_status_t st = check_bank(bank);
     if (st != MOE_OK)
         return st;
@@ -129,7 +130,24 @@ moe_status_t layer_forward(const uint16_t *x, const float *router_w, const float
         // decode-sized T: the whole layer in one cooperative launch
         if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess)
             return MOE_ERR_CUDA;
-        const FusedProblem fp{x, router_w, logit_bias, bank, shared_weight, y, ids_out, w_out, T, top_k};
+        FusedProblem fp{x, router_w, logit_bias, bank, shared_weight, y, ids_out, w_out, T, top_k,
+                        nullptr, 0, nullptr, nullptr, 0, 0};
+        if (next_bank && next_bank->hidden > 0 && next_bank->num_experts > 0 && next_bank->inter > 0) {
+            const int nH = next_bank->hidden, nI = next_bank->inter, nE = next_bank->num_experts;
+            if (next_router_w) {
+                fp.next_router = next_router_w;
+                fp.next_router_bytes = (size_t)nH * nE * sizeof(float);
+            }
+            if (next_bank->has_shared && next_bank->packed && nH % 64 == 0 && nI % 64 == 0) {
+                const PackedLayout NL = packed_layout(nH, nI, nE + 1);
+                fp.next_shared_gu = next_bank->packed + NL.gu_offset +
+                                    (size_t)nE * NL.gu_units_per_expert * NL.gu_unit_bytes;
+                fp.next_shared_gu_bytes = (size_t)NL.gu_units_per_expert * NL.gu_unit_bytes;
+                fp.next_shared_dn = next_bank->packed + NL.dn_offset +
+                                    (size_t)nE * NL.dn_units_per_expert * NL.dn_unit_bytes;
+                fp.next_shared_dn_bytes = (size_t)NL.dn_units_per_expert * NL.dn_unit_bytes;
+            }
+        }
         const cudaError_t ferr = launch_fused(fp, ws, L, sms, stream);
         if (ferr == cudaSuccess) {
             for (int i = 1; ev && i < 5; ++i)
@@ -349,6 +367,19 @@ moe_status_t moe_layer_forward(const uint16_t *x, const float *router_w, const f
                                cudaStream_t stream) {
     return layer_forward(x, router_w, logit_bias, T, top_k, bank, shared_weight, y, topk_ids_out, topk_w_out, ws,
                          ws_bytes, nullptr, stream);
+}
+
+moe_status_t moe_layer_forward_next(const uint16_t *x, const float *router_w, const float *logit_bias, int T,
+                                    int top_k, const moe_mxfp4_bank_t *bank, float shared_weight, uint16_t *y,
+                                    int32_t *topk_ids_out, float *topk_w_out, void *ws, size_t ws_bytes,
+                                    const float *next_router_w, const moe_mxfp4_bank_t *next_bank,
+                                    cudaStream_t stream) {
+    if (next_bank && check_bank(next_bank) != MOE_OK)
+        return MOE_ERR_INVALID_ARG;
+    if (next_router_w && !aligned(next_router_w, 4))
+        return MOE_ERR_MISALIGNED;
+    return layer_forward(x, router_w, logit_bias, T, top_k, bank, shared_weight, y, topk_ids_out, topk_w_out, ws,
+                         ws_bytes, nullptr, stream, next_router_w, next_bank);
 }
 
 moe_status_t moe_layer_forward_noalloc(const uint16_t *x, const float *router_w, const float *logit_bias, int T,

@@ -64,6 +64,8 @@ struct FusedArgs {
     int xwin_row, hwin_row;           // window row strides (elements)
     int win_entries;                  // entries the down window holds
     int off_hundo, off_b;             // dynamic shared-memory offsets (bytes)
+    const uint8_t *next_pf[3];        // next layer: router, shared gate/up, shared down (nullable)
+    size_t next_pf_bytes[3];
 };
 
 namespace {
@@ -475,6 +477,26 @@ __device__ __forceinline__ unsigned long long logit_key(float hi, float lo) {
         return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
     };
     return ((unsigned long long)mono(hi) << 32) | mono(lo);
+}
+
+// The next layer's router weights and shared expert into L2: this CTA's
+// slice of each region, issued once its own weight streams are done.
+__device__ void prefetch_next_layer(const FusedArgs &a) {
+    if (threadIdx.x != 0)
+        return;
+    for (int r = 0; r < 3; ++r) {
+        const uint8_t *base = a.next_pf[r];
+        const size_t total = a.next_pf_bytes[r];
+        if (!base || total == 0 || (reinterpret_cast<uintptr_t>(base) & 15))   // bulk prefetches want 16-byte alignment
+            continue;
+        const size_t piece = align_up((total + gridDim.x - 1) / gridDim.x, 16);
+        const size_t lo = (size_t)blockIdx.x * piece;
+        const size_t hi = lo + piece < total ? lo + piece : total;
+        for (size_t o = lo; o + 16 <= hi; o += 16384) {
+            const size_t n = hi - o < 16384 ? (hi - o) & ~(size_t)15 : 16384;
+            prefetch_l2(base + o, (uint32_t)n);
+        }
+    }
 }
 
 __device__ __forceinline__ float unkey_half(uint32_t m) {
@@ -1134,6 +1156,7 @@ __global__ void __launch_bounds__(NT, 1) fused_layer_kernel(const __grid_constan
         if (ok) {
             stamp(a, 11);
             cta_stamp(a, 3);
+            prefetch_next_layer(a);
             grid_arrive(a);
             if (grid_wait(a, 3u * G)) {
                 stamp(a, 14);
@@ -1299,6 +1322,12 @@ cudaError_t launch_fused(const FusedProblem &pr, void *ws, const WsLayout &L, in
     a.win_entries = plan.win_entries;
     a.off_hundo = (int)plan.off_hundo;
     a.off_b = (int)plan.off_b;
+    a.next_pf[0] = static_cast<const uint8_t *>(pr.next_router);
+    a.next_pf_bytes[0] = pr.next_router_bytes;
+    a.next_pf[1] = static_cast<const uint8_t *>(pr.next_shared_gu);
+    a.next_pf_bytes[1] = pr.next_shared_gu_bytes;
+    a.next_pf[2] = static_cast<const uint8_t *>(pr.next_shared_dn);
+    a.next_pf_bytes[2] = pr.next_shared_dn_bytes;
     if (H % (64 * SB) == 0 && I % (64 * SB) == 0)
         return launch_fused_t<true>(a, num_sms, plan.smem, stream);
     return launch_fused_t<false>(a, num_sms, plan.smem, stream);

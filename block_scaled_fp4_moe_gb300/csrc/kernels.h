@@ -79,6 +79,11 @@ struct FusedProblem {
     int32_t *ids_out;        // nullable
     float *w_out;            // nullable
     int T, top_k;
+    // L2 prefetch hint for the next layer (nullable; sizes in bytes)
+    const void *next_router;
+    size_t next_router_bytes;
+    const void *next_shared_gu, *next_shared_dn;
+    size_t next_shared_gu_bytes, next_shared_dn_bytes;
 };
 
 // Shared-memory plan of the single-launch kernel; ok = the shape fits.

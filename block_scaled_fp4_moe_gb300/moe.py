@@ -69,6 +69,8 @@ def lib() -> C.CDLL:
                     "moe_layer_forward": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, p, p, s, p]),
                     "moe_layer_forward_hostio": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, s, p]),
                     "moe_layer_forward_noalloc": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, p, p]),
+                    "moe_layer_forward_next": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, p, p, s, p,
+                                                   C.POINTER(_Bank), p]),
                     "moe_layer_forward_profiled": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, s, p, i, p]),
                     "moe_check_device_status": (i, [p, p]),
                     "moe_layer_launches": (i, [i, i, i, i, i, i]),
@@ -87,7 +89,8 @@ def lib() -> C.CDLL:
 
 def exported_symbols() -> list[str]:
     return ["moe_workspace_size", "moe_workspace_init", "moe_packed_bank_size", "moe_pack_bank", "moe_route_topk", "moe_group_tokens", "moe_expert_ffn_mxfp4",
-            "moe_layer_forward", "moe_layer_forward_hostio", "moe_layer_forward_noalloc", "moe_layer_forward_profiled",
+            "moe_layer_forward", "moe_layer_forward_hostio", "moe_layer_forward_next", "moe_layer_forward_noalloc",
+            "moe_layer_forward_profiled",
             "moe_layer_launches", "moe_read_phase_times", "moe_check_device_status", "moe_selftest_decode_e2m1", "moe_selftest_wait_timeout",
             "moe_status_string"]
 
@@ -237,6 +240,23 @@ def moe_layer_forward(x, router_w, logit_bias, top_k, bank: MXFP4Bank, shared_we
                                    _ptr(topk_ids_out, torch.int32, "topk_ids_out"),
                                    _ptr(topk_w_out, torch.float32, "topk_w_out"), _ptr(ws, torch.uint8, "ws"),
                                    ws.numel(), _stream(stream)), "moe_layer_forward")
+
+
+def moe_layer_forward_next(x, router_w, logit_bias, top_k, bank: MXFP4Bank, shared_weight, y, topk_ids_out=None,
+                           topk_w_out=None, ws=None, next_router_w=None, next_bank: "MXFP4Bank | None" = None,
+                           stream=None):
+    """moe_layer_forward plus the next layer's router weights and bank as an L2 prefetch hint."""
+    T = x.shape[0]
+    b = bank.c_struct()
+    nb = next_bank.c_struct() if next_bank is not None else None
+    _check(lib().moe_layer_forward_next(_ptr(x, torch.bfloat16, "x"), _ptr(router_w, torch.float32, "router_w"),
+                                        _ptr(logit_bias, torch.float32, "logit_bias"), T, top_k, C.byref(b),
+                                        float(shared_weight), _ptr(y, torch.bfloat16, "y"),
+                                        _ptr(topk_ids_out, torch.int32, "topk_ids_out"),
+                                        _ptr(topk_w_out, torch.float32, "topk_w_out"), _ptr(ws, torch.uint8, "ws"),
+                                        ws.numel(), _ptr(next_router_w, torch.float32, "next_router_w"),
+                                        C.byref(nb) if nb is not None else None, _stream(stream)),
+           "moe_layer_forward_next")
 
 
 def moe_layer_forward_noalloc(x, router_w, logit_bias, top_k, bank: MXFP4Bank, shared_weight, y, topk_ids_out=None,

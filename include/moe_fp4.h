@@ -191,6 +191,27 @@ moe_status_t moe_layer_forward(const uint16_t *x, const float *router_w, const f
                                size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * One layer of a chain of MoE layers: moe_layer_forward, plus a hint naming
+ * the layer that runs next on the same stream (next_router_w [H', E'] and
+ * next_bank; either may be NULL).  When the layer runs as one launch (T <= 8)
+ * its CTAs, once their last expert weights have been streamed, ask L2 to hold
+ * the next layer's router weights and its shared expert (gate/up and down),
+ * so that the next layer's router phase and shared expert read L2 instead of
+ * HBM.  The hint changes no result: outputs are bit-identical to
+ * moe_layer_forward.  It moves no data the next layer would not read anyway;
+ * with T > 8 it is ignored.  The motivation is the cost the pages put on
+ * operator and layer boundaries: the execution gap between operators (the
+ * 1T-model article, section 1, "the problem") and the runtime row of the
+ * GLM-5.2-on-B300 article's table of optimisation axes (launch, graph and
+ * synchronisation overhead).
+ */
+moe_status_t moe_layer_forward_next(const uint16_t *x, const float *router_w, const float *logit_bias,
+                                    int T, int top_k, const moe_mxfp4_bank_t *bank, float shared_weight,
+                                    uint16_t *y, int32_t *topk_ids_out, float *topk_w_out, void *ws,
+                                    size_t ws_bytes, const float *next_router_w,
+                                    const moe_mxfp4_bank_t *next_bank, cudaStream_t stream);
+
+/*
  * The whole layer without a caller-provided workspace.  The pages have no
  * counterpart of this call; it exists for callers that cannot allocate device
  * memory themselves, such as plugins whose host application owns every device

@@ -230,6 +230,24 @@ def test_layer_is_deterministic_and_entry_points_agree():
     np.testing.assert_array_equal(yh.view(torch.int16).numpy().view(np.uint16), a["y"])
 
 
+@pytest.mark.parametrize("T", [1, 4, 13])
+def test_chained_layer_hint_changes_nothing(T):
+    p = random_problem(T=T, H=1024, E=16, k=4, I=512, seed=40 + T)
+    q = random_problem(T=T, H=1024, E=16, k=4, I=512, seed=90 + T)    # the layer that runs next
+    a = p.forward()
+    for nr, nb in ((q.wrd, q.bank), (None, q.bank), (q.wrd, None), (None, None)):
+        ws = p.workspace()
+        y = torch.full((p.T, p.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+        ids = torch.full((p.T, p.kps), -1, dtype=torch.int32, device="cuda")
+        w = torch.full((p.T, p.kps), float("nan"), dtype=torch.float32, device="cuda")
+        moe.moe_layer_forward_next(p.xd, p.wrd, p.bd, p.top_k, p.bank, p.shared_weight, y, ids, w, ws,
+                                   next_router_w=nr, next_bank=nb)
+        assert moe.moe_check_device_status(ws) == 0
+        np.testing.assert_array_equal(host_bits(y), a["y"])
+        np.testing.assert_array_equal(ids.cpu().numpy(), a["ids"])
+        np.testing.assert_array_equal(w.cpu().numpy(), a["w"])
+
+
 def test_zero_tokens_is_a_noop():
     p = random_problem(T=1, H=1024, E=16, k=4, I=512)
     y = torch.empty((0, p.H), dtype=torch.bfloat16, device="cuda")
