@@ -21,6 +21,9 @@ Extra JSON keys:
   kernel_us     per-kernel CUDA-event times of eagerly queued calls;
   phase_us      for the single-launch kernel, its phases from the kernel's
                 own timestamps (first CTA's view).
+  l2_scrubbed_single_call  64 calls, each after writing a buffer of 4x the L2
+                size (not timed) and bracketed alone by CUDA events: median,
+                p10, p90.
   cpu_baseline  the FP64 oracle on this host, a bounded sample.
   e2e           the same metric through moe_layer_forward_hostio, with the
                 pinned host->device copy of x and the device->host copy of y
@@ -364,6 +367,25 @@ def run_mine(args, cfg):
         kernel_source = "cuda events between the kernels of eagerly queued steps"
         kern_us = {k: statistics.median(v) for k, v in kern.items()}
 
+    # ---- single calls after an L2 scrub: before each of 64 calls a buffer of
+    # 4x the L2 size is written (not timed), then events bracket the call alone
+    scrub = torch.empty(4 * l2 // 4, dtype=torch.float32, device=dev)
+    cold = []
+    ce = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(64)]
+    with torch.cuda.stream(stream):
+        for i, (e0, e1) in enumerate(ce):
+            scrub.fill_(float(i))
+            e0.record(stream)
+            moe.moe_layer_forward(xd, routers[i % n_layers], bd, cfg.top_k, banks[i % n_layers], 1.0, y, ws=ws,
+                                  stream=stream)
+            e1.record(stream)
+    stream.synchronize()
+    cold = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in ce)
+    scrubbed = {"median_us": statistics.median(cold), "p10_us": cold[len(cold) // 10],
+                "p90_us": cold[(9 * len(cold)) // 10], "calls": len(cold),
+                "median_tbs": b["total"] / (statistics.median(cold) * 1e-6) / 1e12}
+    del scrub
+
     # ---- end to end through host buffers
     xh = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
     yh = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
@@ -409,6 +431,7 @@ def run_mine(args, cfg):
                                   "expert prefetched into L2)" if args.chain else ""),
                        "parallelism": f"replicas x{world}"},
             "kernel_us": kern_us, "kernel_timing": kernel_source, "phase_us": phases,
+            "l2_scrubbed_single_call": scrubbed,
             "roofline": {"bound": "hbm", "kernel": roof_kernel, "achieved": achieved,
                          "peak": peak if peak else 6800.0, "unit": "GB/s",
                          "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak else "fallback",
