@@ -169,6 +169,8 @@ SMALL = [
     dict(T=13, H=1024, E=16, k=4, I=512),          # more tokens than one pass
     dict(T=40, H=1024, E=6, k=3, I=512),           # experts hold up to 40 tokens
     dict(T=80, H=1024, E=4, k=2, I=512),           # several wide passes per expert (tiled kernels)
+    dict(T=33, H=1536, E=12, k=3, I=1024, has_shared=0),   # tiled kernels without a shared expert
+    dict(T=9, H=1024, E=16, k=8, I=512),           # first T of the multi-launch path
     dict(T=5, H=1024, E=16, k=4, I=512, has_shared=0),
     dict(T=9, H=320, E=5, k=5, I=192),             # block-mode scales, k == E
     dict(T=2, H=2048, E=4, k=2, I=2048),
