@@ -60,6 +60,7 @@ struct FusedArgs {
     float shared_weight;
     int r_groups, r_chunks, r_rows;   // router tiles: 32 experts x r_rows rows
     int r_final;                 // 1: the router phase sums each group's chunks (else every CTA does)
+    int r_vec;                   // 1: router rows are 16-byte aligned (E % 4 == 0): asynchronous tile copies
     unsigned gu_unit, dn_unit;        // bytes of one packed row block
     int xwin_row, hwin_row;           // window row strides (elements)
     int win_entries;                  // entries the down window holds
@@ -103,6 +104,10 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t *p) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+__device__ __forceinline__ void prefetch_l2_line(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_l1(const void *p) {
@@ -206,7 +211,7 @@ __device__ __forceinline__ void router_load(float (&w)[B], const float *wp, size
                                             bool live) {
 #pragma unroll
     for (int u = 0; u < B; ++u)
-        w[u] = live && j0 + u < nrw ? __ldg(wp + (size_t)(j0 + u) * wstride) : 0.0f;
+        w[u] = live && j0 + u < nrw ? wp[(size_t)(j0 + u) * wstride] : 0.0f;
 }
 
 template <int TT, int B>
@@ -294,21 +299,33 @@ __device__ void phase_router(const FusedArgs &a, uint8_t *sm) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int T = a.T, H = a.H, E = a.E;
     const int TT = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;      // token columns of the x rows
-    float *xs = reinterpret_cast<float *>(sm);                                    // [r_rows][TT]
-    float2 *red = reinterpret_cast<float2 *>(sm + align_up(TT * a.r_rows * 4, 16));   // [NW][T][32]
+    float *wt = reinterpret_cast<float *>(sm);                                    // [r_rows][32] weights
+    float *xs = reinterpret_cast<float *>(sm + (size_t)a.r_rows * 128);          // [r_rows][TT]
+    float2 *red = reinterpret_cast<float2 *>(sm + (size_t)a.r_rows * 128 + align_up(TT * a.r_rows * 4, 16));
     const int tiles = a.r_groups * a.r_chunks;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
         const int gi = tile % a.r_groups, ci = tile / a.r_groups;
         const int r0 = ci * a.r_rows, nr = min(H - r0, a.r_rows);
         const int e0 = gi * 32, e1 = min(E, e0 + 32);       // experts [e0, e1) of this tile
         const int nrw = nr > warp ? (nr - warp + NW - 1) / NW : 0;
-        const float *wrow = a.wr + (size_t)(r0 + warp) * E;  // this warp's first row
-        const size_t wstride = (size_t)NW * E;
-        for (int j = lane; j < nrw; j += 32) {
-            prefetch_l1(wrow + j * wstride + e0);
-            prefetch_l1(wrow + j * wstride + e1 - 1);
+        __syncthreads();                                     // the previous tile's readers are done
+        // the tile's weights into shared memory, all rows at once: 16-byte
+        // asynchronous copies when rows are 16-byte aligned, else words
+        if (a.r_vec) {
+            const int nch = (e1 - e0) >> 2;                  // 16-byte chunks per row
+            for (int i = threadIdx.x; i < nr * 8; i += NT) {
+                const int row = i >> 3, ch = i & 7;
+                if (ch < nch)
+                    cp_async16(wt + row * 32 + 4 * ch, a.wr + (size_t)(r0 + row) * E + e0 + 4 * ch);
+            }
+            cp_async_commit();
+        } else {
+            for (int i = threadIdx.x; i < nr * 32; i += NT) {
+                const int row = i >> 5, col = i & 31;
+                if (e0 + col < e1)
+                    wt[row * 32 + col] = __ldg(a.wr + (size_t)(r0 + row) * E + e0 + col);
+            }
         }
-        __syncthreads();
         for (int i = threadIdx.x; i < TT * (nr / 8); i += NT) {
             const int c8 = i / TT, t = i - c8 * TT;
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -322,6 +339,8 @@ __device__ void phase_router(const FusedArgs &a, uint8_t *sm) {
                 d[(2 * j + 1) * TT] = __uint_as_float(w4[j] & 0xFFFF0000u);
             }
         }
+        if (a.r_vec)
+            cp_async_wait<0>();
         __syncthreads();
         stamp(a, 8);
         const bool live = e0 + lane < e1;
@@ -329,7 +348,8 @@ __device__ void phase_router(const FusedArgs &a, uint8_t *sm) {
 #pragma unroll
         for (int t = 0; t < kFusedMaxTokens; ++t)
             p[t] = q[t] = 0.0f;
-        const float *w0 = wrow + e0 + lane;
+        const float *w0 = wt + warp * 32 + lane;             // this warp's rows: warp, warp + NW, ...
+        const size_t wstride = (size_t)NW * 32;
         if (TT == 1)
             router_rows<1>(xs, w0, wstride, nrw, live, p, q);
         else if (TT == 2)
@@ -366,8 +386,8 @@ __device__ void phase_router(const FusedArgs &a, uint8_t *sm) {
     }
 }
 
-// This CTA's first router tile into L1 (read-only data: may run before the
-// previous kernel on the stream has finished).
+// This CTA's first router tile into L2 (a hint on read-only data: may run
+// before the previous kernel on the stream has finished).
 __device__ void prefetch_router_tile(const FusedArgs &a) {
     const int tile = blockIdx.x;
     if (tile >= a.r_groups * a.r_chunks)
@@ -380,8 +400,8 @@ __device__ void prefetch_router_tile(const FusedArgs &a) {
     const float *wrow = a.wr + (size_t)(r0 + warp) * a.E;
     const size_t wstride = (size_t)NW * a.E;
     for (int j = lane; j < nrw; j += 32) {
-        prefetch_l1(wrow + j * wstride + e0);
-        prefetch_l1(wrow + j * wstride + e1 - 1);
+        prefetch_l2_line(wrow + j * wstride + e0);
+        prefetch_l2_line(wrow + j * wstride + e1 - 1);
     }
 }
 
@@ -1243,7 +1263,8 @@ FusedPlan fused_plan(int T, int H, int I, int E, int k, int S, int grid) {
     const size_t b_logits = (size_t)T * Ep * sizeof(unsigned long long) +
                             (size_t)T * (Ep / 32) * k * (sizeof(unsigned long long) + sizeof(int));
     const int TT = T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8;
-    const size_t b_router = align_up((size_t)TT * p.r_rows * 4, 16) + (size_t)kFusedWarps * T * 32 * sizeof(float2);
+    const size_t b_router = (size_t)p.r_rows * 128 + align_up((size_t)TT * p.r_rows * 4, 16) +
+                            (size_t)kFusedWarps * T * 32 * sizeof(float2);
     const size_t b_slots = (size_t)2 * kFusedWarps * 32 * 4 * sizeof(float) + (size_t)(nu_dn + 1) * sizeof(int);
     size_t szB = b_logits;
     if (b_slots > szB)
@@ -1315,6 +1336,7 @@ cudaError_t launch_fused(const FusedProblem &pr, void *ws, const WsLayout &L, in
     a.r_chunks = plan.r_chunks;
     a.r_rows = plan.r_rows;
     a.r_final = plan.r_final ? 1 : 0;
+    a.r_vec = (E % 4 == 0 && (reinterpret_cast<uintptr_t>(pr.router_w) & 15) == 0) ? 1 : 0;
     a.gu_unit = (unsigned)PL.gu_unit_bytes;
     a.dn_unit = (unsigned)PL.dn_unit_bytes;
     a.xwin_row = plan.xwin_row;
