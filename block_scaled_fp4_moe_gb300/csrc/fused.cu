@@ -89,7 +89,6 @@ struct RouteState {
     int inv_pos[kMaxEntries];      // entry -> sorted position
     int sorted_ent[kMaxEntries];   // sorted position -> entry
     int sorted_tok[kMaxEntries];   // sorted position -> token
-    int gsize[kMaxEntries];        // size of the group starting at a sorted position (else 0)
     Pass pgu[kMaxEntries];         // gate/up passes: one per active expert (T <= 8)
     Pass pdn[kMaxEntries];         // down passes of <= 4 entries
 };
@@ -749,38 +748,70 @@ __device__ bool phase_route(const FusedArgs &a, RouteState &rs, uint8_t *smA, ui
         rs.sorted_tok[pos] = tid / kps;
     }
     __syncthreads();
-    if (tid < n) {
-        const int ex = rs.sel_id[rs.sorted_ent[tid]];
+    // by sorted position p = tid: group starts from one ballot per warp; the
+    // group's size from the next start (this warp, else the first later warp
+    // holding one); group and down-pass indices from per-warp counts
+    {
+        __shared__ int wstarts[NW], wfirst[NW], wd4[NW];
+        const unsigned full = 0xffffffffu;
+        const int p = tid;
+        int ex = -1;
+        bool start = false;
+        if (p < n) {
+            ex = rs.sel_id[rs.sorted_ent[p]];
+            start = p == 0 || rs.sel_id[rs.sorted_ent[p - 1]] != ex;
+        }
+        const unsigned sm = __ballot_sync(full, start);
+        if (lane == 0) {
+            wstarts[warp] = __popc(sm);
+            wfirst[warp] = sm ? 32 * warp + __ffs(sm) - 1 : 0x7fffffff;
+        }
+        __syncthreads();
         int size = 0;
-        if (tid == 0 || rs.sel_id[rs.sorted_ent[tid - 1]] != ex) {
-            size = 1;
-            while (tid + size < n && rs.sel_id[rs.sorted_ent[tid + size]] == ex)
-                ++size;
+        if (start) {
+            const unsigned later = lane == 31 ? 0u : sm & ~((2u << lane) - 1u);
+            int next = n;
+            if (later) {
+                next = 32 * warp + __ffs(later) - 1;
+            } else {
+                for (int w = warp + 1; w < NW; ++w)
+                    if (wfirst[w] != 0x7fffffff) {
+                        next = wfirst[w];
+                        break;
+                    }
+            }
+            size = next - p;
         }
-        rs.gsize[tid] = size;
-    }
-    __syncthreads();
-    if (tid < n && rs.gsize[tid] > 0) {
-        int gi = 0, di = 0;
-        for (int j = 0; j < tid; ++j) {
-            const int s = rs.gsize[j];
-            gi += s > 0;
-            di += (s + kPassEntries - 1) / kPassEntries;
+        const int d4 = (size + kPassEntries - 1) / kPassEntries;
+        int incl = d4;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(full, incl, d);
+            if (lane >= d)
+                incl += y;
         }
-        const int size = rs.gsize[tid], ex = rs.sel_id[rs.sorted_ent[tid]];
-        rs.pgu[gi] = Pass{ex, tid, size, 0};
-        for (int q = 0; q * kPassEntries < size; ++q)
-            rs.pdn[di + q] = Pass{ex, tid + q * kPassEntries, min(kPassEntries, size - q * kPassEntries), 0};
-    }
-    if (tid == 0) {
-        int gi = 0, di = 0;
-        for (int j = 0; j < n; ++j) {
-            const int s = rs.gsize[j];
-            gi += s > 0;
-            di += (s + kPassEntries - 1) / kPassEntries;
+        if (lane == 31)
+            wd4[warp] = incl;
+        __syncthreads();
+        if (start) {
+            int gi = __popc(sm & ((1u << lane) - 1u)), di = incl - d4;
+            for (int w = 0; w < warp; ++w) {
+                gi += wstarts[w];
+                di += wd4[w];
+            }
+            rs.pgu[gi] = Pass{ex, p, size, 0};
+            for (int q = 0; q * kPassEntries < size; ++q)
+                rs.pdn[di + q] = Pass{ex, p + q * kPassEntries, min(kPassEntries, size - q * kPassEntries), 0};
         }
-        rs.n_gu = gi;
-        rs.n_dn = di;
+        if (tid == 0) {
+            int gi = 0, di = 0;
+            for (int w = 0; w < NW; ++w) {
+                gi += wstarts[w];
+                di += wd4[w];
+            }
+            rs.n_gu = gi;
+            rs.n_dn = di;
+        }
     }
     __syncthreads();
     return true;
