@@ -109,10 +109,6 @@ __device__ __forceinline__ void prefetch_l2_line(const void *p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
 }
 
-__device__ __forceinline__ void prefetch_l1(const void *p) {
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
-}
-
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
