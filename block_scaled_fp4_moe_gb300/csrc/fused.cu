@@ -599,11 +599,24 @@ __device__ bool phase_route(const FusedArgs &a, RouteState &rs, uint8_t *smA, ui
         const int t = i / Ep, e = i - t * Ep;
         const unsigned long long *g = key + t * Ep + (e & ~31);
         const unsigned long long my = g[e & 31];
-        int r = 0;
+        // rank by the high words, two keys per 16-byte load; a key sharing
+        // the high word (besides the own one) sends the item to the full
+        // 64-bit comparison with the index rule
+        const uint4 *g4 = reinterpret_cast<const uint4 *>(g);
+        const uint32_t myhi = (uint32_t)(my >> 32);
+        int r = 0, eq = 0;
 #pragma unroll 8
-        for (int j = 0; j < 32; ++j) {
-            const unsigned long long o = g[j];
-            r += (o > my) | ((o == my) & (j < (e & 31)));
+        for (int j2 = 0; j2 < 16; ++j2) {
+            const uint4 w = g4[j2];                 // key 2j2: (x lo, y hi), key 2j2+1: (z lo, w hi)
+            r += (w.y > myhi) + (w.w > myhi);
+            eq += (w.y == myhi) + (w.w == myhi);
+        }
+        if (eq > 1) {
+            r = 0;
+            for (int j = 0; j < 32; ++j) {
+                const unsigned long long o = g[j];
+                r += (o > my) | ((o == my) & (j < (e & 31)));
+            }
         }
         if (r < k) {
             const int slot = t * cmax + (e >> 5) * k + r;
