@@ -237,6 +237,10 @@ group_kernel(const int32_t *ids, int T, int kps, int n_tot, GroupOut o, uint32_t
 
 // ------------------------------------------------------- top-k + shared slot
 
+// Entries the grouping CTA copies into shared memory (32 KB: with the static
+// arrays this stays under the 48 KB that need no opt-in).
+constexpr int kGroupSmemIds = 8 * 1024;
+
 // One CTA per token.  All threads sum the partial pairs of the experts in a
 // fixed order (the loads of one expert issued together) and add the bias;
 // then warp 0 selects the top k (warp-wide argmax over (hi, lo, -index)) and
@@ -355,7 +359,18 @@ route_finish_kernel(const float2 *__restrict__ part, int nh, const float *__rest
     if (!last_cta)
         return;
     __threadfence();
-    group_block(ids_out, T, kps, E + has_shared, go, hdr);
+    const int n = T * kps;
+    if (n <= kGroupSmemIds) {
+        // every token's ids into shared memory first: the grouping then reads
+        // them without a global round trip per step
+        int *sm_ids = reinterpret_cast<int *>(L);
+        for (int i = threadIdx.x; i < n; i += blockDim.x)
+            sm_ids[i] = __ldcg(ids_out + i);
+        __syncthreads();
+        group_block(sm_ids, T, kps, E + has_shared, go, hdr, true);
+    } else {
+        group_block(ids_out, T, kps, E + has_shared, go, hdr);
+    }
     if (threadIdx.x == 0)
         hdr[kHdrRouteTicket] = 0;
 }
@@ -376,7 +391,10 @@ cudaError_t launch_route(const uint16_t *x, const float *wr, const float *bias, 
     if (ev_after_partial &&
         (err = cudaEventRecord(ev_after_partial, stream)) != cudaSuccess)
         return err;
-    const size_t smem = (size_t)E * sizeof(float2);
+    const size_t n_ids = (size_t)T * (k + has_shared);
+    size_t smem = (size_t)E * sizeof(float2);
+    if (do_group && T > 1 && n_ids <= (size_t)kGroupSmemIds && n_ids * sizeof(int) > smem)
+        smem = n_ids * sizeof(int);
     __half *x16 = do_group ? ws_at<__half>(ws, L.x16) : nullptr;
     float *xundo = do_group ? ws_at<float>(ws, L.xundo) : nullptr;
     return launch_pdl(route_finish_kernel, dim3(T), dim3(256), smem, stream, part, nh, bias, T, E, k, has_shared,
