@@ -63,6 +63,14 @@ def lib():
         L.oracle_expert_token.argtypes = [p, p, p, p, i, i, p, p, p]
         L.oracle_moe_tokens.restype = None
         L.oracle_moe_tokens.argtypes = [p, i, i, i, p, p, p, p, p, p, p, i, p, p, p]
+        L.oracle_moe_tokens_act.restype = None
+        L.oracle_moe_tokens_act.argtypes = [p, i, i, i, p, p, p, p, p, p, p, i, p, p, p, i]
+        L.oracle_e4m3_value.restype = d
+        L.oracle_e4m3_value.argtypes = [i]
+        L.oracle_e4m3_round.restype = i
+        L.oracle_e4m3_round.argtypes = [d]
+        L.oracle_mxfp8_quantize.restype = None
+        L.oracle_mxfp8_quantize.argtypes = [p, i, p, p, p]
         L.oracle_num_threads.restype = i
         L.oracle_num_threads.argtypes = []
         L.oracle_bf16_round_array.restype = None
@@ -104,6 +112,26 @@ def bf16_round_array(v: np.ndarray) -> np.ndarray:
     out = np.empty(v.shape, dtype=np.uint16)
     lib().oracle_bf16_round_array(_ptr(v), v.size, _ptr(out))
     return out
+
+
+def e4m3_value(code: int) -> float:
+    return lib().oracle_e4m3_value(int(code))
+
+
+def e4m3_round(v: float) -> int:
+    return int(lib().oracle_e4m3_round(float(v)))
+
+
+def mxfp8_quantize(v: np.ndarray) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """MXFP8 (OCP MX v1.0) of a vector whose length is a multiple of 32:
+    (E4M3 codes, E8M0 scale bytes, dequantised values)."""
+    v = np.ascontiguousarray(v, dtype=np.float64).ravel()
+    assert v.size % 32 == 0
+    codes = np.empty(v.size, dtype=np.uint8)
+    scales = np.empty(v.size // 32, dtype=np.uint8)
+    deq = np.empty(v.size, dtype=np.float64)
+    lib().oracle_mxfp8_quantize(_ptr(v), v.size, _ptr(codes), _ptr(scales), _ptr(deq))
+    return codes, scales, deq
 
 
 def decode_row(codes: np.ndarray, scales: np.ndarray, K: int) -> np.ndarray:
@@ -170,13 +198,19 @@ def expert_token(expert: Mapping[str, np.ndarray], x_row: np.ndarray) -> tuple[n
 ExpertSource = Callable[[int], Mapping[str, np.ndarray]]
 
 
+ACTIVATIONS = ("exact", "mxfp8")
+
+
 def moe_tokens(x: np.ndarray, ids: np.ndarray, w: np.ndarray, experts: ExpertSource,
-               tokens=None, want_h: bool = False, want_slots: bool = False) -> dict[str, np.ndarray]:
+               tokens=None, want_h: bool = False, want_slots: bool = False,
+               act: str = "exact") -> dict[str, np.ndarray]:
     """Expert FFNs + weighted combine for the listed tokens (default: all).
 
     ``experts(e)`` returns expert e's packed arrays; only experts that the
-    listed tokens select are requested.
+    listed tokens select are requested.  ``act="mxfp8"``: x and h enter
+    their projections MXFP8-quantised (the live-quantisation variant).
     """
+    assert act in ACTIVATIONS
     x = np.ascontiguousarray(x, dtype=np.uint16)
     ids = np.ascontiguousarray(ids, dtype=np.int32)
     w = np.ascontiguousarray(w, dtype=np.float64)
@@ -197,8 +231,9 @@ def moe_tokens(x: np.ndarray, ids: np.ndarray, w: np.ndarray, experts: ExpertSou
     y = np.empty((n, H), dtype=np.float64)
     hs = np.empty((n, kps, I), dtype=np.float64) if want_h else None
     ys = np.empty((n, kps, H), dtype=np.float64) if want_slots else None
-    lib().oracle_moe_tokens(_ptr(x), H, I, kps, _ptr(ids), _ptr(w), ptrs["w13"], ptrs["s13"],
-                            ptrs["w2"], ptrs["s2"], _ptr(tokens), n, _ptr(y), _ptr(hs), _ptr(ys))
+    lib().oracle_moe_tokens_act(_ptr(x), H, I, kps, _ptr(ids), _ptr(w), ptrs["w13"], ptrs["s13"],
+                                ptrs["w2"], ptrs["s2"], _ptr(tokens), n, _ptr(y), _ptr(hs), _ptr(ys),
+                                1 if act == "mxfp8" else 0)
     out = {"y": y, "tokens": tokens}
     if want_h:
         out["h"] = hs
@@ -209,10 +244,11 @@ def moe_tokens(x: np.ndarray, ids: np.ndarray, w: np.ndarray, experts: ExpertSou
 
 def layer_forward(x: np.ndarray, wr: np.ndarray, bias: np.ndarray | None, top_k: int,
                   experts: ExpertSource, has_shared: int = 1, shared_weight: float = 1.0,
-                  tokens=None, want_h: bool = False, want_slots: bool = False) -> dict[str, np.ndarray]:
+                  tokens=None, want_h: bool = False, want_slots: bool = False,
+                  act: str = "exact") -> dict[str, np.ndarray]:
     """Whole layer: routing for all tokens, FFNs + combine for ``tokens``."""
     r = route(x, wr, bias, top_k, has_shared, shared_weight)
-    out = moe_tokens(x, r["ids"], r["w"], experts, tokens, want_h, want_slots)
+    out = moe_tokens(x, r["ids"], r["w"], experts, tokens, want_h, want_slots, act)
     out.update(r)
     out["y_bf16"] = bf16_round_array(out["y"])
     return out

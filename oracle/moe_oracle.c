@@ -43,6 +43,11 @@
  * Precision: every product x*w is exact in double (8-bit x 24-bit and 8-bit x
  * 3-bit significands); sums are plain left-to-right double sums.
  *
+ * MXFP8 activation mode (oracle_moe_tokens_act with mx = 1): x[t] is
+ * MXFP8-quantised (OCP MX v1.0, E4M3 elements, blocks of 32 along H) before
+ * the gate/up projection and h before the down projection; everything else
+ * as above.  Pins: tests/test_oracle_mxfp8_pins.py.
+ *
  * Parity pins (tests/test_oracle_pins.py): exhaustive E2M1 table and E8M0
  * exponents against the OCP bit-field definitions, a brute-force tiny layer
  * (top-k by enumerating every k-subset, dense numpy matmuls), a closed form
@@ -132,6 +137,97 @@ void oracle_decode_row(const uint8_t *codes, const uint8_t *scales, int K, doubl
 {
     for (int c = 0; c < K; ++c)
         out[c] = oracle_e2m1_value(row_code(codes, c)) * oracle_e8m0_value(scales[c / 32]);
+}
+
+/* ------------------------------------------------- MXFP8 activations */
+/*
+ * The live-activation-quantisation variant (GLM-5.2 on B300, d9249.github.io,
+ * section 1 of its kernel part: FP8 activations quantised right before the
+ * GEMM).  The page names FP8 but neither the element format nor the block
+ * size; the reading taken here is MXFP8 of the OCP Microscaling v1.0 spec,
+ * the same block structure as the MXFP4 weights: E4M3 elements, one E8M0
+ * scale per 32 consecutive values along the reduction axis.
+ *
+ * E4M3 (OCP 8-bit floating point): 1 sign, 4 exponent bits with bias 7,
+ * 3 mantissa bits; exponent field 0 holds subnormals m/8 * 2^-6; S.1111.111
+ * is NaN; there are no infinities, so the largest magnitude is 1.75 * 2^8 =
+ * 448.
+ */
+double oracle_e4m3_value(int b)
+{
+    int sign = (b >> 7) & 1, ex = (b >> 3) & 15, m = b & 7;
+    double v;
+    if (ex == 15 && m == 7)
+        return NAN;
+    if (ex == 0)
+        v = ldexp((double)m, -9);              /* m/8 * 2^-6 */
+    else
+        v = ldexp(8.0 + m, ex - 10);           /* (1 + m/8) * 2^(ex-7) */
+    return sign ? -v : v;
+}
+
+/* Nearest E4M3 code to v, ties to even, magnitudes above 448 saturated to
+ * 448 (the OCP MX conversion clamps to the element's largest normal). */
+int oracle_e4m3_round(double v)
+{
+    int sign = signbit(v) ? 0x80 : 0;
+    double a = fabs(v);
+    if (isnan(v))
+        return 0x7F;
+    if (a >= 448.0)
+        return sign | 0x7E;
+    if (a == 0.0)
+        return sign;
+    int e;
+    (void)frexp(a, &e);                        /* a = f * 2^e, 0.5 <= f < 1 */
+    int q = e - 4;                             /* weight of the last of 4 significant bits */
+    if (q < -9)
+        q = -9;                                /* subnormal quantum */
+    double r = ldexp(nearbyint(ldexp(a, -q)), q);   /* ties to even */
+    /* encode r (exactly representable; at most 448 after the clamp above,
+     * since 448 < a < 448 + 16 rounds to 448) */
+    if (r < ldexp(1.0, -6))
+        return sign | (int)ldexp(r, 9);        /* subnormal: m = r / 2^-9 */
+    (void)frexp(r, &e);
+    int ex = e - 1 + 7;                         /* r = (1 + m/8) * 2^(e-1) */
+    int m = (int)(ldexp(r, 4 - e) - 8.0);
+    return sign | (ex << 3) | m;
+}
+
+/*
+ * OCP MX v1.0 conversion of n values (n a multiple of 32) to MXFP8: for
+ * each block of 32, the shared exponent is floor(log2(max |v|)) minus the
+ * largest exponent of E4M3 (8), kept inside E8M0's range [-127, 127] (an
+ * all-zero block takes -127); the scale byte is that exponent + 127 and
+ * each element is E4M3-rounded v / 2^exponent.  deq (nullable) receives the
+ * dequantised values code * 2^exponent.
+ */
+void oracle_mxfp8_quantize(const double *v, int n, uint8_t *codes, uint8_t *scales, double *deq)
+{
+    for (int b = 0; b < n / 32; ++b) {
+        const double *vb = v + 32 * b;
+        double amax = 0.0;
+        for (int i = 0; i < 32; ++i)
+            if (fabs(vb[i]) > amax)
+                amax = fabs(vb[i]);
+        int se = -127;
+        if (amax > 0.0) {
+            int e;
+            (void)frexp(amax, &e);             /* floor(log2(amax)) = e - 1 */
+            se = e - 1 - 8;
+            if (se < -127)
+                se = -127;
+            if (se > 127)
+                se = 127;
+        }
+        scales[b] = (uint8_t)(se + 127);
+        for (int i = 0; i < 32; ++i) {
+            int c = oracle_e4m3_round(ldexp(vb[i], -se));
+            codes[32 * b + i] = (uint8_t)c;
+            if (deq)
+                deq[32 * b + i] = ldexp(oracle_e4m3_value(c), se);
+        }
+    }
 }
 
 /* ----------------------------------------------------------------- router */
@@ -264,13 +360,15 @@ int oracle_group(const int32_t *ids, int T, int kps, int n_tot, int32_t *offsets
 /*
  * One expert on one token.  w13 [2I][H/2] (gate rows then up rows), s13
  * [2I][H/32], w2 [H][I/2], s2 [H][I/32].  x [H] in double.
- * h_out [I] (nullable), y_out [H].
+ * h_out [I] (nullable), y_out [H].  With mx, h enters the down projection
+ * MXFP8-quantised (blocks of 32 along I); h_out keeps the unquantised h.
  */
-void oracle_expert_token(const uint8_t *w13, const uint8_t *s13, const uint8_t *w2,
+static void expert_token(const uint8_t *w13, const uint8_t *s13, const uint8_t *w2,
                          const uint8_t *s2, int H, int I, const double *x,
-                         double *h_out, double *y_out)
+                         double *h_out, double *y_out, int mx)
 {
     double *h = malloc(sizeof(double) * (size_t)I);
+    double *hq = malloc(sizeof(double) * (size_t)I);
 #pragma omp parallel for schedule(static)
     for (int j = 0; j < I; ++j) {
         double *row = malloc(sizeof(double) * (size_t)H);
@@ -284,19 +382,35 @@ void oracle_expert_token(const uint8_t *w13, const uint8_t *s13, const uint8_t *
         h[j] = g / (1.0 + exp(-g)) * u;
         free(row);
     }
+    if (mx) {
+        uint8_t *codes = malloc((size_t)I), *scales = malloc((size_t)I / 32);
+        oracle_mxfp8_quantize(h, I, codes, scales, hq);
+        free(codes);
+        free(scales);
+    } else {
+        memcpy(hq, h, sizeof(double) * (size_t)I);
+    }
 #pragma omp parallel for schedule(static)
     for (int n = 0; n < H; ++n) {
         double *row = malloc(sizeof(double) * (size_t)I);
         double acc = 0.0;
         oracle_decode_row(w2 + (size_t)n * (I / 2), s2 + (size_t)n * (I / 32), I, row);
         for (int j = 0; j < I; ++j)
-            acc += row[j] * h[j];
+            acc += row[j] * hq[j];
         y_out[n] = acc;
         free(row);
     }
     if (h_out)
         memcpy(h_out, h, sizeof(double) * (size_t)I);
     free(h);
+    free(hq);
+}
+
+void oracle_expert_token(const uint8_t *w13, const uint8_t *s13, const uint8_t *w2,
+                         const uint8_t *s2, int H, int I, const double *x,
+                         double *h_out, double *y_out)
+{
+    expert_token(w13, s13, w2, s2, H, I, x, h_out, y_out, 0);
 }
 
 /*
@@ -304,11 +418,13 @@ void oracle_expert_token(const uint8_t *w13, const uint8_t *s13, const uint8_t *
  * Expert e's arrays are w13[e], s13[e], w2[e], s2[e] (per-expert pointers, so
  * a caller may supply only the experts its tokens touch).
  * y [n_tokens][H]; hs [n_tokens][kps][I] and ys [n_tokens][kps][H] nullable.
+ * mx = 1: MXFP8 activations -- x[t] is quantised (blocks of 32 along H)
+ * before the gate/up projection and each h before the down projection.
  */
-void oracle_moe_tokens(const uint16_t *x, int H, int I, int kps, const int32_t *ids,
-                       const double *w, const uint8_t *const *w13, const uint8_t *const *s13,
-                       const uint8_t *const *w2, const uint8_t *const *s2,
-                       const int32_t *tokens, int n_tokens, double *y, double *hs, double *ys)
+void oracle_moe_tokens_act(const uint16_t *x, int H, int I, int kps, const int32_t *ids,
+                           const double *w, const uint8_t *const *w13, const uint8_t *const *s13,
+                           const uint8_t *const *w2, const uint8_t *const *s2,
+                           const int32_t *tokens, int n_tokens, double *y, double *hs, double *ys, int mx)
 {
     double *xt = malloc(sizeof(double) * (size_t)H);
     double *yslot = malloc(sizeof(double) * (size_t)H);
@@ -316,13 +432,19 @@ void oracle_moe_tokens(const uint16_t *x, int H, int I, int kps, const int32_t *
         int t = tokens[i];
         for (int c = 0; c < H; ++c)
             xt[c] = oracle_bf16_value(x[(size_t)t * H + c]);
+        if (mx) {
+            uint8_t *codes = malloc((size_t)H), *scales = malloc((size_t)H / 32);
+            oracle_mxfp8_quantize(xt, H, codes, scales, xt);
+            free(codes);
+            free(scales);
+        }
         double *yt = y + (size_t)i * H;
         for (int c = 0; c < H; ++c)
             yt[c] = 0.0;
         for (int s = 0; s < kps; ++s) {
             int e = ids[(size_t)t * kps + s];
             double *hdst = hs ? hs + ((size_t)i * kps + s) * I : NULL;
-            oracle_expert_token(w13[e], s13[e], w2[e], s2[e], H, I, xt, hdst, yslot);
+            expert_token(w13[e], s13[e], w2[e], s2[e], H, I, xt, hdst, yslot, mx);
             if (ys)
                 memcpy(ys + ((size_t)i * kps + s) * H, yslot, sizeof(double) * (size_t)H);
             double ws = w[(size_t)t * kps + s];
@@ -332,6 +454,14 @@ void oracle_moe_tokens(const uint16_t *x, int H, int I, int kps, const int32_t *
     }
     free(xt);
     free(yslot);
+}
+
+void oracle_moe_tokens(const uint16_t *x, int H, int I, int kps, const int32_t *ids,
+                       const double *w, const uint8_t *const *w13, const uint8_t *const *s13,
+                       const uint8_t *const *w2, const uint8_t *const *s2,
+                       const int32_t *tokens, int n_tokens, double *y, double *hs, double *ys)
+{
+    oracle_moe_tokens_act(x, H, I, kps, ids, w, w13, s13, w2, s2, tokens, n_tokens, y, hs, ys, 0);
 }
 
 /* bf16 rounding of a whole array (the layer's output format). */
