@@ -2,6 +2,7 @@
 // workspace layout and the launch sequence on the caller's stream.
 #include <atomic>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -223,6 +224,22 @@ moe_status_t static_scratch(void **out, cudaStream_t stream) {
 
 extern "C" {
 
+size_t moe_workspace_offset(int T, int H, int I, int E, int top_k, int has_shared, const char *region) {
+    if (!region || T < 0 || H <= 0 || I <= 0 || E <= 0 || top_k <= 0 || (has_shared != 0 && has_shared != 1))
+        return (size_t)-1;
+    const WsLayout L = WsLayout::make(T, H, I, E, top_k, has_shared);
+    const struct {
+        const char *name;
+        size_t off;
+    } regions[] = {{"topk_ids", L.topk_ids}, {"topk_w", L.topk_w}, {"inv_pos", L.inv_pos},
+                   {"sorted_tok", L.sorted_tok}, {"mx_xq", L.mx_xq}, {"mx_xs", L.mx_xs},
+                   {"mx_h32", L.mx_h32}, {"mx_hq", L.mx_hq}, {"mx_hs", L.mx_hs}, {"mx_y", L.mx_y}};
+    for (const auto &r : regions)
+        if (std::strcmp(r.name, region) == 0)
+            return r.off;
+    return (size_t)-1;
+}
+
 size_t moe_workspace_size(int T, int H, int I, int E, int top_k, int has_shared) {
     if (T < 0 || H <= 0 || I <= 0 || E <= 0 || top_k <= 0 || (has_shared != 0 && has_shared != 1))
         return 0;
@@ -380,6 +397,48 @@ moe_status_t moe_layer_forward_next(const uint16_t *x, const float *router_w, co
         return MOE_ERR_MISALIGNED;
     return layer_forward(x, router_w, logit_bias, T, top_k, bank, shared_weight, y, topk_ids_out, topk_w_out, ws,
                          ws_bytes, nullptr, stream, next_router_w, next_bank);
+}
+
+moe_status_t moe_layer_forward_mxfp8(const uint16_t *x, const float *router_w, const float *logit_bias, int T,
+                                     int top_k, const moe_mxfp4_bank_t *bank, float shared_weight, uint16_t *y,
+                                     int32_t *topk_ids_out, float *topk_w_out, void *ws, size_t ws_bytes,
+                                     cudaStream_t stream) {
+    moe_status_t st = check_bank_dims(bank);
+    if (st != MOE_OK)
+        return st;
+    if (!bank->w13 || !bank->s13 || !bank->w2 || !bank->s2)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(bank->w13, 16) || !aligned(bank->w2, 16) || !aligned(bank->s13, 4) || !aligned(bank->s2, 4))
+        return MOE_ERR_MISALIGNED;
+    const int H = bank->hidden, I = bank->inter, E = bank->num_experts, S = bank->has_shared;
+    if (!mx8_shape_supported(H, I))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if ((st = check_routing_shape(T, H, E, top_k, S)) != MOE_OK ||
+        (st = check_ffn_extent(T, top_k + S, H, I)) != MOE_OK)
+        return st;
+    if (T == 0)
+        return MOE_OK;
+    if (!x || !router_w || !y || !ws)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(y, 16) || !aligned(ws, 256) || !aligned(router_w, 4) ||
+        !aligned(logit_bias, 4) || !aligned(topk_ids_out, 4) || !aligned(topk_w_out, 4))
+        return MOE_ERR_MISALIGNED;
+    const WsLayout L = WsLayout::make(T, H, I, E, top_k, S);
+    if (ws_bytes < L.total)
+        return MOE_ERR_WORKSPACE_TOO_SMALL;
+    int sms = 0;
+    if ((st = current_device_sms(&sms)) != MOE_OK)
+        return st;
+    (void)cudaGetLastError();
+    int32_t *ids = topk_ids_out ? topk_ids_out : ws_at<int32_t>(ws, L.topk_ids);
+    float *w = topk_w_out ? topk_w_out : ws_at<float>(ws, L.topk_w);
+    const GroupOut go = group_out_for(ws, L, H);
+    cudaError_t err = launch_route(x, router_w, logit_bias, T, H, E, top_k, S, shared_weight, ids, w, ws, L, true, go,
+                                   stream);
+    if (err != cudaSuccess)
+        return MOE_ERR_CUDA;
+    const Mx8Problem pr{x, bank, w, y, T, top_k + S};
+    return from_cuda(launch_mx8_ffn(pr, ws, L, stream));
 }
 
 moe_status_t moe_layer_forward_noalloc(const uint16_t *x, const float *router_w, const float *logit_bias, int T,

@@ -126,7 +126,8 @@ inline void fused_router_tiling(int H, int E, int *groups, int *chunks, int *row
 struct WsLayout {
     size_t route_part, topk_ids, topk_w, offsets, sorted_tok, sorted_slot, inv_pos, active, passes, passes4, passesw,
         passesw4, x16, xundo,
-        gpart, h16, hundo, ypart, counters, xstage, ystage, fz_rpart, fz_h32, fz_yent, total;
+        gpart, h16, hundo, ypart, counters, xstage, ystage, fz_rpart, fz_h32, fz_yent, mx_xq, mx_xs, mx_h32, mx_hq,
+        mx_hs, mx_y, total;
     int n_kc_gu, n_kc_dn;
 
     static WsLayout make(int T, int H, int I, int E, int k, int S) {
@@ -168,6 +169,13 @@ struct WsLayout {
             L.fz_h32 = take(entries * (size_t)I * sizeof(float));
             L.fz_yent = take(entries * (size_t)H * sizeof(float));
         }
+        // MXFP8 variant: quantised x and h, fp32 h and per-entry outputs
+        L.mx_xq = take((size_t)T * H);
+        L.mx_xs = take((size_t)T * (H / 32));
+        L.mx_h32 = take(entries * (size_t)I * sizeof(float));
+        L.mx_hq = take(entries * (size_t)I);
+        L.mx_hs = take(entries * (size_t)(I / 32));
+        L.mx_y = take(entries * (size_t)H * sizeof(float));
         L.total = align_up(o, 256);
         return L;
     }

@@ -1075,6 +1075,12 @@ cudaError_t launch_ffn(const FfnProblem &pr, void *ws, const WsLayout &L, int nu
                       (const uint32_t *)hdr);
 }
 
+cudaError_t launch_combine(const float *yent, int entries, const int32_t *inv_pos, const float *topk_w, int T, int kps,
+                           int H, uint16_t *y, const uint32_t *hdr, cudaStream_t stream) {
+    return launch_pdl(combine_kernel, dim3(T * ((H + 255) / 256)), dim3(256), 0, stream, yent, 1, entries, inv_pos,
+                      topk_w, T, kps, H, y, hdr);
+}
+
 cudaError_t launch_x16(const uint16_t *x, int T, int H, void *ws, const WsLayout &L, cudaStream_t stream) {
     return launch_pdl(x16_kernel, dim3(T), dim3(256), 0, stream, x, H, ws_at<__half>(ws, L.x16),
                       ws_at<float>(ws, L.xundo));

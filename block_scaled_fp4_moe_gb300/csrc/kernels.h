@@ -64,6 +64,22 @@ struct FfnProblem {
 
 cudaError_t launch_ffn(const FfnProblem &p, void *ws, const WsLayout &L, int num_sms, cudaStream_t stream,
                        cudaEvent_t ev_after_gateup);
+// y = bf16(sum over slots of w * Y), Y [entries][H] in sorted entry order.
+cudaError_t launch_combine(const float *yent, int entries, const int32_t *inv_pos, const float *topk_w, int T, int kps,
+                           int H, uint16_t *y, const uint32_t *hdr, cudaStream_t stream);
+
+// MXFP8 live-activation-quantisation variant (mx8.cu): after routing and
+// grouping, x and h are quantised to MXFP8 and both projections run as
+// block-scaled tcgen05 MMAs on the canonical bank arrays.
+struct Mx8Problem {
+    const uint16_t *x;       // [T, H] bf16
+    const moe_mxfp4_bank_t *bank;
+    const float *topk_w;     // [T, kps]
+    uint16_t *y;             // [T, H] bf16
+    int T, kps;
+};
+bool mx8_shape_supported(int H, int I);
+cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cudaStream_t stream);
 
 // f16 copy of x with per-token power-of-two scaling (x16, xundo regions).
 cudaError_t launch_x16(const uint16_t *x, int T, int H, void *ws, const WsLayout &L, cudaStream_t stream);

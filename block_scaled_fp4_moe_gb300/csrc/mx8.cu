@@ -1,0 +1,408 @@
+// mx8.cu -- the MXFP8 live-activation-quantisation variant of the layer, sm_103a.
+//
+// GLM-5.2 on B300 (d9249.github.io), kernel section 1: FP8 activation
+// quantisation fused in front of the GEMM, and section 2: tcgen05 with the
+// accumulators and scale handling in tensor memory (TMEM) instead of
+// registers.  Here x (per token, along H) and h (per entry, along I) are
+// quantised to MXFP8 -- E4M3 elements, one E8M0 scale per 32, the OCP MX v1.0
+// conversion -- and both projections run as block-scaled tensor-core MMAs,
+// `tcgen05.mma.kind::mxf8f6f4.block_scale`: A = MXFP4 weights read as E2M1 by
+// the tensor core, B = the MXFP8 activations, both block scales applied by the
+// hardware, fp32 accumulators in TMEM.  The weights are read from the
+// canonical bank arrays (w13, s13, w2, s2); no decode instruction runs.
+//
+// Launches: routing + grouping (route.cu), x quantisation, gate/up GEMM
+// (writes h = silu(g) * u in fp32), h quantisation, down GEMM (per-entry
+// outputs Y), combine (ffn.cu's combine_kernel).
+//
+// GEMM CTA: 128 weight rows x one pass of <= 16 entries (MMA M = 128,
+// N = 16), K in stages of 128 (four MMAs of K = 32).  A 4-buffer ring of
+// cp.async copies stages the operands into shared memory in the canonical
+// K-major no-swizzle layout: core matrices of 8 rows x 16 bytes, adjacent in
+// K 128 bytes apart, 8-row groups 1,024 bytes apart.  An E2M1 operand of
+// kind::mxf8f6f4 occupies a 16-byte slot per 16 elements with the 8 bytes of
+// codes in the low half.  Scale factors go into TMEM with tcgen05.st: row r
+// of A at lane r % 32 (in every 32-lane quarter), column base + r / 32;
+// column n of B at lane n; byte j of a 32-bit cell is the scale of the
+// stage's K block j, selected by the MMA's scale-factor id.  Scale-factor
+// regions start on 32-column (A) and 16-column (B) boundaries of the CTA's
+// 256-column allocation (two CTAs per SM).
+#include <cuda_bf16.h>
+
+#include <atomic>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+namespace {
+
+constexpr int kMxThreads = 128;
+constexpr int kMxN = 16;                       // MMA N: entries of one pass
+constexpr int kMxStageK = 128;                 // K elements per stage
+constexpr int kMxStages = 4;                   // ring buffers; loads run kMxStages - 2 stages ahead
+constexpr int kMxLbo = 128;                    // bytes between core matrices adjacent in K
+constexpr int kMxSbo = 8 * 128;                // bytes between 8-row groups (8 K slots of 16 B)
+constexpr int kMxABytes = 128 * kMxStageK;     // 128 rows x 8 slots x 16 B
+constexpr int kMxBBytes = kMxN * kMxStageK;    // 16 rows x 128 E4M3
+constexpr int kMxSfaBytes = 128 * 4;
+constexpr int kMxSfbBytes = kMxN * 4;
+constexpr int kMxStageBytes = kMxABytes + kMxBBytes + kMxSfaBytes + kMxSfbBytes;
+constexpr int kMxTmemCols = 256;               // D: columns 0..15; scale factors on aligned columns
+constexpr int kMxColSfa = 32;                  // SFA of buffer b: 4 columns at 32 + 32 b
+constexpr int kMxColSfb = 192;                 // SFB of buffer b: 1 column at 192 + 16 b
+constexpr unsigned long long kMxWaitLimitNs = 200ull * 1000 * 1000;
+constexpr size_t kMxSmem = (size_t)kMxStages * kMxStageBytes + 64;
+
+static_assert(kMxColSfa + 32 * (kMxStages - 1) + 4 <= kMxColSfb && kMxColSfb + 16 * kMxStages <= kMxTmemCols,
+              "TMEM columns");
+static_assert((size_t)128 * 17 * 4 <= (size_t)kMxStageBytes, "epilogue buffer fits a stage");
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Shared-memory matrix descriptor: start, leading (K) and stride (8-row)
+// byte offsets, the fixed 0b001 at bits 46-48, no swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+    uint64_t d = (uint64_t)((addr & 0x3FFFF) >> 4);
+    d |= (uint64_t)(kMxLbo >> 4) << 16;
+    d |= (uint64_t)(kMxSbo >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with block scaling: A E2M1 (5),
+// B E4M3 (0), both K-major, N >> 3 at bit 17, UE8M0 scales (bit 23),
+// M >> 4 at bit 24; scale-factor ids (byte of the TMEM cell) of B at bits
+// 4-5 and of A at bits 29-30.
+__host__ __device__ constexpr uint32_t mx_idesc(int sf_id) {
+    return ((uint32_t)(sf_id & 3) << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(kMxN >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(128 >> 4) << 24) | ((uint32_t)(sf_id & 3) << 29);
+}
+
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16s(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait until the barrier's phase with this parity has completed; false after
+// kMxWaitLimitNs.
+__device__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try(bar, parity))
+        if (globaltimer_ns() - t0 > kMxWaitLimitNs)
+            return false;
+    return true;
+}
+
+struct MxGemmArgs {
+    const uint8_t *w;           // E2M1 codes [n_tot][rows][K/2]
+    const uint8_t *wsc;         // E8M0 scales [n_tot][rows][K/32]
+    const uint8_t *aq;          // E4M3 activations [act_rows][K]
+    const uint8_t *asc;         // E8M0 scales [act_rows][K/32]
+    const Pass *passes;         // passes of <= 16 entries
+    const int32_t *sorted_tok;  // gate/up: entry -> activation row (token); down: null (row = entry)
+    float *out;                 // gate/up: h [entries][I]; down: Y [entries][H]
+    uint32_t *hdr;
+    int rows;                   // weight rows per expert: 2I (gate/up) or H (down)
+    int K;                      // H (gate/up) or I (down)
+    int half;                   // gate/up: I (up rows start there); down: 0
+    int out_ld;                 // I (gate/up) or H (down)
+    int n_tot;                  // experts in the bank
+    int act_rows;               // rows of aq: T (gate/up) or entries (down)
+    int entries;                // T * (k + S)
+};
+
+// ------------------------------------------------------------------ GEMM
+
+template <bool GATEUP>
+__global__ void __launch_bounds__(kMxThreads, 1) mx8_gemm_kernel(const __grid_constant__ MxGemmArgs a) {
+    extern __shared__ __align__(1024) uint8_t mx_smem[];
+    __shared__ uint32_t s_taddr;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_wait();
+    pdl_trigger();
+    const int n_pass = (int)*reinterpret_cast<const volatile uint32_t *>(a.hdr + kHdrNumPassesW4);
+    if ((int)blockIdx.y >= n_pass)
+        return;
+    const Pass ps = a.passes[blockIdx.y];
+    const int tile = blockIdx.x;
+    // the pass and its activation rows must lie inside the buffers
+    {
+        int bad = ps.expert < 0 || ps.expert >= a.n_tot || ps.count < 1 || ps.count > kMxN || ps.begin < 0 ||
+                  ps.begin + ps.count > a.entries;
+        if (!bad && tid < ps.count) {
+            const int row = GATEUP ? a.sorted_tok[ps.begin + tid] : ps.begin + tid;
+            bad = row < 0 || row >= a.act_rows;
+        }
+        if (__syncthreads_or(bad)) {
+            if (tid == 0)
+                record_status(a.hdr, MOE_ERR_DEVICE_ASSERT);
+            return;
+        }
+    }
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(mx_smem + (size_t)kMxStages * kMxStageBytes);
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&s_taddr)),
+                     "n"(kMxTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (tid == 0) {
+        for (int b = 0; b < kMxStages; ++b)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(mbar + b)));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = s_taddr;
+
+    // this thread's copies: A rows (tid / 8) + 16 i, 8-byte slot tid % 8;
+    // B row tid / 8, 16-byte slot tid % 8; SFA row tid; SFB row tid (< 16)
+    const int K2 = a.K / 2, K32 = a.K / 32;
+    const uint8_t *wexp = a.w + (size_t)ps.expert * a.rows * K2;
+    const uint8_t *sexp = a.wsc + (size_t)ps.expert * a.rows * K32;
+    auto wrow = [&](int r) { return GATEUP ? (r < 64 ? tile * 64 + r : a.half + tile * 64 + r - 64) : tile * 128 + r; };
+    auto arow = [&](int n) {
+        const int e = ps.begin + min(n, ps.count - 1);
+        return GATEUP ? a.sorted_tok[e] : e;
+    };
+    const int slot = tid & 7, r0 = tid >> 3;
+    const uint8_t *asrc = a.aq + (size_t)arow(r0) * a.K + slot * 16;
+    const uint8_t *sfa_src = sexp + (size_t)wrow(tid) * K32;
+    const uint8_t *sfb_src = a.asc + (size_t)arow(tid & 15) * K32;
+    const uint32_t sbase = smem_addr(mx_smem);
+    const int nst = a.K / kMxStageK;
+
+    auto issue = [&](int s) {
+        const uint32_t st = sbase + (uint32_t)((s % kMxStages) * kMxStageBytes);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = r0 + 16 * i;
+            cp_async8(st + (uint32_t)((r >> 3) * kMxSbo + slot * kMxLbo + (r & 7) * 16),
+                      wexp + (size_t)wrow(r) * K2 + s * (kMxStageK / 2) + slot * 8);
+        }
+        cp_async16s(st + kMxABytes + (uint32_t)((r0 >> 3) * kMxSbo + slot * kMxLbo + (r0 & 7) * 16),
+                    asrc + (size_t)s * kMxStageK);
+        cp_async4(st + kMxABytes + kMxBBytes + tid * 4, sfa_src + s * 4);
+        if (tid < kMxN)
+            cp_async4(st + kMxABytes + kMxBBytes + kMxSfaBytes + tid * 4, sfb_src + s * 4);
+    };
+
+    bool ok = true;
+#pragma unroll
+    for (int s = 0; s < kMxStages - 2; ++s) {
+        if (s < nst)
+            issue(s);
+        cp_async_commit();
+    }
+    for (int s = 0; s < nst; ++s) {
+        // refill the buffer that the MMAs of stage s - 2 read
+        if (s >= 2)
+            ok = ok && mbar_wait(smem_addr(mbar + (s - 2) % kMxStages), ((s - 2) / kMxStages) & 1);
+        if (ok && s + kMxStages - 2 < nst)
+            issue(s + kMxStages - 2);
+        cp_async_commit();
+        cp_async_wait<kMxStages - 2>();
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (__syncthreads_or(!ok))
+            break;
+        // scale factors of stage s into this buffer's TMEM columns, every quarter
+        const int b = s % kMxStages;
+        const uint8_t *st = mx_smem + (size_t)b * kMxStageBytes;
+        const uint32_t *sfa = reinterpret_cast<const uint32_t *>(st + kMxABytes + kMxBBytes);
+        const uint32_t *sfb = sfa + 128;
+        const uint32_t colA = (uint32_t)(kMxColSfa + 32 * b), colB = (uint32_t)(kMxColSfb + 16 * b);
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(tmem + lane_base + colA),
+                     "r"(sfa[lane]), "r"(sfa[lane + 32]), "r"(sfa[lane + 64]), "r"(sfa[lane + 96])
+                     : "memory");
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(tmem + lane_base + colB),
+                     "r"(sfb[lane & 15])
+                     : "memory");
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncthreads();
+        if (tid == 0) {
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t sa = sbase + (uint32_t)(b * kMxStageBytes), sb = sa + kMxABytes;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint64_t ad = smem_desc(sa + j * 2 * kMxLbo), bd = smem_desc(sb + j * 2 * kMxLbo);
+                const uint32_t acc = (s > 0 || j > 0) ? 1u : 0u;
+                asm volatile(
+                    "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                    "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n}\n"
+                    ::"r"(tmem), "l"(ad), "l"(bd), "r"(mx_idesc(j)), "r"(acc), "r"(tmem + colA), "r"(tmem + colB)
+                    : "memory");
+            }
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                             smem_addr(mbar + b))
+                         : "memory");
+        }
+    }
+    if (ok)
+        ok = mbar_wait(smem_addr(mbar + (nst - 1) % kMxStages), ((nst - 1) / kMxStages) & 1);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    ok = !__syncthreads_or(!ok);
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (!ok) {
+        if (tid == 0)
+            record_status(a.hdr, MOE_ERR_DEVICE_TIMEOUT);
+    } else {
+        uint32_t v[16];
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+            : "r"(tmem + ((uint32_t)(warp * 32) << 16)));
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        const int r = tid;                  // MMA row = TMEM lane
+        if (GATEUP) {
+            // rows 0..63 hold g, 64..127 the matching u: pass u through shared memory
+            float *ub = reinterpret_cast<float *>(mx_smem);
+            if (r >= 64)
+                for (int n = 0; n < kMxN; ++n)
+                    ub[(r - 64) * 17 + n] = __uint_as_float(v[n]);
+            __syncthreads();
+            if (r < 64) {
+                for (int n = 0; n < ps.count; ++n) {
+                    const float g = __uint_as_float(v[n]), u = ub[r * 17 + n];
+                    a.out[(size_t)(ps.begin + n) * a.out_ld + tile * 64 + r] = g / (1.0f + expf(-g)) * u;
+                }
+            }
+        } else {
+            for (int n = 0; n < ps.count; ++n)
+                a.out[(size_t)(ps.begin + n) * a.out_ld + tile * 128 + r] = __uint_as_float(v[n]);
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kMxTmemCols));
+}
+
+// ------------------------------------------------------------ quantisation
+
+__device__ __forceinline__ float load_act(const uint16_t *p) {
+    return __uint_as_float((uint32_t)*p << 16);   // bf16
+}
+__device__ __forceinline__ float load_act(const float *p) { return __ldcg(p); }
+
+// MXFP8 (OCP MX v1.0) of rows x cols values, one warp per block of 32: the
+// shared exponent is floor(log2(max |v|)) - 8 (E4M3's largest exponent),
+// kept in [-127, 127], -127 for an all-zero block; each element is v / 2^e
+// rounded to E4M3, ties to even, saturating at 448.  v / 2^e is exact in
+// fp32, so the codes are those of the exact quotient.
+template <typename In>
+__global__ void __launch_bounds__(256) mx8_quant_kernel(const In *__restrict__ in, int rows, int cols,
+                                                        uint8_t *__restrict__ codes, uint8_t *__restrict__ scales) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const long long blk = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const int per_row = cols / 32;
+    if (blk >= (long long)rows * per_row)
+        return;
+    const size_t i = (size_t)blk * 32 + lane;
+    const float v = load_act(in + i);
+    const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
+    const int ef = (int)(amax >> 23);           // biased exponent of max |v| (0: zero or subnormal)
+    int se = ef == 0 ? -127 : ef - 127 - 8;
+    se = max(-127, min(127, se));
+    const float q = v * exp2i(-se);             // -se <= 127: a normal power of two
+    uint16_t pair;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.0f), "f"(q));
+    codes[i] = (uint8_t)(pair & 0xFF);
+    if (lane == 0)
+        scales[blk] = (uint8_t)(se + 127);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ host
+
+bool mx8_shape_supported(int H, int I) { return H > 0 && I > 0 && H % 128 == 0 && I % 128 == 0; }
+
+cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cudaStream_t stream) {
+    const moe_mxfp4_bank_t &b = *p.bank;
+    const int H = b.hidden, I = b.inter, T = p.T, kps = p.kps;
+    const int entries = T * kps;
+    const int n_tot = b.num_experts + b.has_shared;
+    const int max_pass = max_passes(T, kps, n_tot, kWidePassEntries);
+    uint32_t *hdr = ws_at<uint32_t>(ws, 0);
+    uint8_t *xq = ws_at<uint8_t>(ws, L.mx_xq), *xs = ws_at<uint8_t>(ws, L.mx_xs);
+    uint8_t *hq = ws_at<uint8_t>(ws, L.mx_hq), *hs = ws_at<uint8_t>(ws, L.mx_hs);
+    float *h32 = ws_at<float>(ws, L.mx_h32), *yent = ws_at<float>(ws, L.mx_y);
+    static std::atomic<int> attr_set{0};
+    if (!attr_set.load()) {
+        cudaError_t err;
+        if ((err = cudaFuncSetAttribute(mx8_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kMxSmem)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(mx8_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kMxSmem)) != cudaSuccess)
+            return err;
+        attr_set.store(1);
+    }
+    const int xblocks = T * (H / 32), hblocks = entries * (I / 32);
+    cudaError_t err = launch_pdl(mx8_quant_kernel<uint16_t>, dim3((xblocks + 7) / 8), dim3(256), 0, stream, p.x, T, H,
+                                 xq, xs);
+    if (err != cudaSuccess)
+        return err;
+    MxGemmArgs g{};
+    g.w = b.w13;
+    g.wsc = b.s13;
+    g.aq = xq;
+    g.asc = xs;
+    g.passes = ws_at<Pass>(ws, L.passesw4);
+    g.sorted_tok = ws_at<int32_t>(ws, L.sorted_tok);
+    g.out = h32;
+    g.hdr = hdr;
+    g.rows = 2 * I;
+    g.K = H;
+    g.half = I;
+    g.out_ld = I;
+    g.n_tot = n_tot;
+    g.act_rows = T;
+    g.entries = entries;
+    if ((err = launch_pdl(mx8_gemm_kernel<true>, dim3(I / 64, max_pass), dim3(kMxThreads), kMxSmem, stream, g)) !=
+        cudaSuccess)
+        return err;
+    if ((err = launch_pdl(mx8_quant_kernel<float>, dim3((hblocks + 7) / 8), dim3(256), 0, stream, (const float *)h32,
+                          entries, I, hq, hs)) != cudaSuccess)
+        return err;
+    MxGemmArgs d = g;
+    d.w = b.w2;
+    d.wsc = b.s2;
+    d.aq = hq;
+    d.asc = hs;
+    d.sorted_tok = nullptr;
+    d.out = yent;
+    d.rows = H;
+    d.K = I;
+    d.half = 0;
+    d.out_ld = H;
+    d.act_rows = entries;
+    if ((err = launch_pdl(mx8_gemm_kernel<false>, dim3(H / 128, max_pass), dim3(kMxThreads), kMxSmem, stream, d)) !=
+        cudaSuccess)
+        return err;
+    return launch_combine(yent, entries, ws_at<int32_t>(ws, L.inv_pos), p.topk_w, T, kps, H, p.y, hdr, stream);
+}
+
+}  // namespace moe

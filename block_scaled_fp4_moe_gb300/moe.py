@@ -60,6 +60,7 @@ def lib() -> C.CDLL:
                 p, i, f, s = C.c_void_p, C.c_int, C.c_float, C.c_size_t
                 sig = {
                     "moe_workspace_size": (s, [i, i, i, i, i, i]),
+                    "moe_workspace_offset": (s, [i, i, i, i, i, i, C.c_char_p]),
                     "moe_workspace_init": (i, [p, s, p]),
                     "moe_packed_bank_size": (s, [i, i, i, i]),
                     "moe_pack_bank": (i, [C.POINTER(_Bank), p, s, p]),
@@ -71,6 +72,7 @@ def lib() -> C.CDLL:
                     "moe_layer_forward_noalloc": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, p, p]),
                     "moe_layer_forward_next": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, p, p, s, p,
                                                    C.POINTER(_Bank), p]),
+                    "moe_layer_forward_mxfp8": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, p, p, s, p]),
                     "moe_layer_forward_profiled": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, s, p, i, p]),
                     "moe_check_device_status": (i, [p, p]),
                     "moe_layer_launches": (i, [i, i, i, i, i, i]),
@@ -88,9 +90,9 @@ def lib() -> C.CDLL:
 
 
 def exported_symbols() -> list[str]:
-    return ["moe_workspace_size", "moe_workspace_init", "moe_packed_bank_size", "moe_pack_bank", "moe_route_topk", "moe_group_tokens", "moe_expert_ffn_mxfp4",
-            "moe_layer_forward", "moe_layer_forward_hostio", "moe_layer_forward_next", "moe_layer_forward_noalloc",
-            "moe_layer_forward_profiled",
+    return ["moe_workspace_size", "moe_workspace_offset", "moe_workspace_init", "moe_packed_bank_size", "moe_pack_bank", "moe_route_topk", "moe_group_tokens", "moe_expert_ffn_mxfp4",
+            "moe_layer_forward", "moe_layer_forward_hostio", "moe_layer_forward_mxfp8", "moe_layer_forward_next",
+            "moe_layer_forward_noalloc", "moe_layer_forward_profiled",
             "moe_layer_launches", "moe_read_phase_times", "moe_check_device_status", "moe_selftest_decode_e2m1", "moe_selftest_wait_timeout",
             "moe_status_string"]
 
@@ -183,6 +185,13 @@ def moe_packed_bank_size(H: int, I: int, E: int, has_shared: int) -> int:
     return int(lib().moe_packed_bank_size(H, I, E, has_shared))
 
 
+def moe_workspace_offset(T: int, H: int, I: int, E: int, top_k: int, has_shared: int, region: str) -> int:
+    off = int(lib().moe_workspace_offset(T, H, I, E, top_k, has_shared, region.encode()))
+    if off == (1 << 64) - 1:
+        raise KeyError(region)
+    return off
+
+
 def moe_workspace_size(T: int, H: int, I: int, E: int, top_k: int, has_shared: int) -> int:
     return int(lib().moe_workspace_size(T, H, I, E, top_k, has_shared))
 
@@ -257,6 +266,19 @@ def moe_layer_forward_next(x, router_w, logit_bias, top_k, bank: MXFP4Bank, shar
                                         ws.numel(), _ptr(next_router_w, torch.float32, "next_router_w"),
                                         C.byref(nb) if nb is not None else None, _stream(stream)),
            "moe_layer_forward_next")
+
+
+def moe_layer_forward_mxfp8(x, router_w, logit_bias, top_k, bank: MXFP4Bank, shared_weight, y, topk_ids_out=None,
+                            topk_w_out=None, ws=None, stream=None):
+    """The MXFP8 live-activation-quantisation variant (needs the bank's canonical arrays)."""
+    T = x.shape[0]
+    b = bank.c_struct()
+    _check(lib().moe_layer_forward_mxfp8(_ptr(x, torch.bfloat16, "x"), _ptr(router_w, torch.float32, "router_w"),
+                                         _ptr(logit_bias, torch.float32, "logit_bias"), T, top_k, C.byref(b),
+                                         float(shared_weight), _ptr(y, torch.bfloat16, "y"),
+                                         _ptr(topk_ids_out, torch.int32, "topk_ids_out"),
+                                         _ptr(topk_w_out, torch.float32, "topk_w_out"), _ptr(ws, torch.uint8, "ws"),
+                                         ws.numel(), _stream(stream)), "moe_layer_forward_mxfp8")
 
 
 def moe_layer_forward_noalloc(x, router_w, logit_bias, top_k, bank: MXFP4Bank, shared_weight, y, topk_ids_out=None,

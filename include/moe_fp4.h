@@ -132,6 +132,16 @@ moe_status_t moe_pack_bank(const moe_mxfp4_bank_t *bank, void *packed, size_t pa
  * single-launch layer kernel, which every completed call leaves at zero. */
 size_t moe_workspace_size(int T, int H, int I, int E, int top_k, int has_shared);
 
+/*
+ * Diagnostics: byte offset inside the workspace of a named region of the
+ * T-token layout ("topk_ids", "topk_w", "inv_pos", "sorted_tok", and the
+ * MXFP8 variant's "mx_xq" [T][H] E4M3 codes of x, "mx_xs" [T][H/32] their
+ * E8M0 scales, "mx_h32" [T*(k+S)][I] fp32 h, "mx_hq" / "mx_hs" its MXFP8
+ * codes and scales, "mx_y" [T*(k+S)][H] fp32 per-entry outputs; entry rows in
+ * grouped order).  (size_t)-1 for an unknown name or invalid sizes.
+ */
+size_t moe_workspace_offset(int T, int H, int I, int E, int top_k, int has_shared, const char *region);
+
 /* Clears the workspace header (status word, counters and diagnostics, the
  * first 8,704 bytes or ws_bytes if smaller) on `stream`.  Call it once on a newly
  * allocated workspace before its first use (a zero-filled workspace needs no
@@ -210,6 +220,32 @@ moe_status_t moe_layer_forward_next(const uint16_t *x, const float *router_w, co
                                     uint16_t *y, int32_t *topk_ids_out, float *topk_w_out, void *ws,
                                     size_t ws_bytes, const float *next_router_w,
                                     const moe_mxfp4_bank_t *next_bank, cudaStream_t stream);
+
+/*
+ * The MXFP8 live-activation-quantisation variant of the layer (the pages'
+ * live FP8 activation quantisation in front of the GEMM and its tcgen05/TMEM
+ * path: GLM-5.2 on B300, d9249.github.io, kernel sections 1 and 2).  Routing
+ * and grouping are those of moe_layer_forward (bit-identical ids and
+ * weights).  Then x[t] (blocks of 32 along H) and each entry's h (blocks of
+ * 32 along I) are converted to MXFP8 -- E4M3 elements with one E8M0 scale per
+ * block, the OCP MX v1.0 conversion: shared exponent floor(log2(max|v|)) - 8,
+ * elements rounded to nearest even and saturated at 448 -- and both
+ * projections run as block-scaled tensor-core MMAs with the MXFP4 weights.
+ * This is a different, lossier definition than moe_layer_forward: y differs
+ * from it by the activation quantisation (a few 1e-2 of max|y| at the
+ * shapes tested), and it is compared against its own oracle mode.
+ *
+ * Reads the canonical bank arrays w13, s13, w2, s2 (non-NULL; w13 and w2
+ * 16-byte aligned, s13 and s2 4-byte aligned); `packed` is not used.
+ * H and I must be multiples of 128 (MOE_ERR_UNSUPPORTED_SHAPE).  Workspace:
+ * moe_workspace_size(T, ...) bytes, as for moe_layer_forward.  Seven
+ * launches (two of routing, two quantisations, two GEMMs, the combine);
+ * asynchronous on `stream`, graph-capturable.
+ */
+moe_status_t moe_layer_forward_mxfp8(const uint16_t *x, const float *router_w, const float *logit_bias,
+                                     int T, int top_k, const moe_mxfp4_bank_t *bank, float shared_weight,
+                                     uint16_t *y, int32_t *topk_ids_out, float *topk_w_out, void *ws,
+                                     size_t ws_bytes, cudaStream_t stream);
 
 /*
  * The whole layer without a caller-provided workspace.  The pages have no
