@@ -399,16 +399,43 @@ moe_status_t moe_layer_forward_next(const uint16_t *x, const float *router_w, co
                          ws_bytes, nullptr, stream, next_router_w, next_bank);
 }
 
-moe_status_t moe_layer_forward_mxfp8(const uint16_t *x, const float *router_w, const float *logit_bias, int T,
-                                     int top_k, const moe_mxfp4_bank_t *bank, float shared_weight, uint16_t *y,
-                                     int32_t *topk_ids_out, float *topk_w_out, void *ws, size_t ws_bytes,
-                                     cudaStream_t stream) {
+size_t moe_packed_mx_bank_size(int H, int I, int E, int has_shared) {
+    if (E <= 0 || (has_shared != 0 && has_shared != 1) || !mx8_shape_supported(H, I))
+        return 0;
+    return mx8_packed_size(H, I, E + has_shared);
+}
+
+moe_status_t moe_pack_bank_mx(const moe_mxfp4_bank_t *bank, void *packed_mx, size_t packed_mx_bytes,
+                              cudaStream_t stream) {
     moe_status_t st = check_bank_dims(bank);
     if (st != MOE_OK)
         return st;
-    if (!bank->w13 || !bank->s13 || !bank->w2 || !bank->s2)
+    if (!mx8_shape_supported(bank->hidden, bank->inter))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!bank->w13 || !bank->s13 || !bank->w2 || !bank->s2 || !packed_mx)
         return MOE_ERR_INVALID_ARG;
-    if (!aligned(bank->w13, 16) || !aligned(bank->w2, 16) || !aligned(bank->s13, 4) || !aligned(bank->s2, 4))
+    if (!aligned(bank->w13, 16) || !aligned(bank->w2, 16) || !aligned(bank->s13, 4) || !aligned(bank->s2, 4) ||
+        !aligned(packed_mx, 256))
+        return MOE_ERR_MISALIGNED;
+    if (packed_mx_bytes < mx8_packed_size(bank->hidden, bank->inter, bank->num_experts + bank->has_shared))
+        return MOE_ERR_WORKSPACE_TOO_SMALL;
+    int sms = 0;
+    if ((st = current_device_sms(&sms)) != MOE_OK)
+        return st;
+    (void)cudaGetLastError();
+    return from_cuda(launch_mx8_pack(*bank, static_cast<uint8_t *>(packed_mx), stream));
+}
+
+moe_status_t moe_layer_forward_mxfp8(const uint16_t *x, const float *router_w, const float *logit_bias, int T,
+                                     int top_k, const moe_mxfp4_bank_t *bank, const void *packed_mx,
+                                     float shared_weight, uint16_t *y, int32_t *topk_ids_out, float *topk_w_out,
+                                     void *ws, size_t ws_bytes, cudaStream_t stream) {
+    moe_status_t st = check_bank_dims(bank);
+    if (st != MOE_OK)
+        return st;
+    if (!packed_mx)
+        return MOE_ERR_INVALID_ARG;
+    if (!aligned(packed_mx, 256))
         return MOE_ERR_MISALIGNED;
     const int H = bank->hidden, I = bank->inter, E = bank->num_experts, S = bank->has_shared;
     if (!mx8_shape_supported(H, I))
@@ -437,7 +464,7 @@ moe_status_t moe_layer_forward_mxfp8(const uint16_t *x, const float *router_w, c
                                    stream);
     if (err != cudaSuccess)
         return MOE_ERR_CUDA;
-    const Mx8Problem pr{x, bank, w, y, T, top_k + S};
+    const Mx8Problem pr{x, bank, static_cast<const uint8_t *>(packed_mx), w, y, T, top_k + S};
     return from_cuda(launch_mx8_ffn(pr, ws, L, stream));
 }
 

@@ -74,11 +74,14 @@ cudaError_t launch_combine(const float *yent, int entries, const int32_t *inv_po
 struct Mx8Problem {
     const uint16_t *x;       // [T, H] bf16
     const moe_mxfp4_bank_t *bank;
+    const uint8_t *packed_mx;   // stage-ordered bank (launch_mx8_pack)
     const float *topk_w;     // [T, kps]
     uint16_t *y;             // [T, H] bf16
     int T, kps;
 };
 bool mx8_shape_supported(int H, int I);
+size_t mx8_packed_size(int H, int I, int n_tot);
+cudaError_t launch_mx8_pack(const moe_mxfp4_bank_t &b, uint8_t *out, cudaStream_t stream);
 cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cudaStream_t stream);
 
 // f16 copy of x with per-token power-of-two scaling (x16, xundo regions).

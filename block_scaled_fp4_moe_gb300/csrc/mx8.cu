@@ -16,15 +16,26 @@
 // outputs Y), combine (ffn.cu's combine_kernel).
 //
 // GEMM CTA: 128 weight rows x one pass of <= 16 entries (MMA M = 128,
-// N = 16), K in stages of 128 (four MMAs of K = 32).  A 4-buffer ring of
-// cp.async copies stages the operands into shared memory in the canonical
+// N = 16), K in stages of 128 (four MMAs of K = 32).  Every operand of a
+// stage is loaded into registers kMxRegStages stages ahead and then stored
+// into a 3-buffer shared-memory ring in the canonical
 // K-major no-swizzle layout: core matrices of 8 rows x 16 bytes, adjacent in
 // K 128 bytes apart, 8-row groups 1,024 bytes apart.  An E2M1 operand of
 // kind::mxf8f6f4 occupies a 16-byte slot per 16 elements with the 8 bytes of
 // codes in the low half.  Scale factors go into TMEM with tcgen05.st: row r
 // of A at lane r % 32 (in every 32-lane quarter), column base + r / 32;
 // column n of B at lane n; byte j of a 32-bit cell is the scale of the
-// stage's K block j, selected by the MMA's scale-factor id.  Scale-factor
+// stage's K block j, selected by the MMA's scale-factor id.
+//
+// The GEMMs read a stage-ordered copy of the bank (moe_pack_bank_mx): per
+// (expert, 128-row tile, K stage) one contiguous block of 8,704 bytes: the
+// codes in the order of the shared-memory image ([8-row group][16-byte slot]
+// [row], 8 bytes each, at half the image's stride) except that within a
+// group pieces w and w + 32 sit side by side, then the 128 rows' four scale
+// bytes.  A stage is one linear 8.5 KB read (instead of 64 bytes from each
+// of 128 rows), streamed through registers kMxRegStages stages ahead; a
+// 16-byte chunk then holds two pieces whose slots are 32 apart, so the
+// 8-byte shared stores of a warp cover 32 consecutive slots.  Scale-factor
 // regions start on 32-column (A) and 16-column (B) boundaries of the CTA's
 // 256-column allocation (two CTAs per SM).
 #include <cuda_bf16.h>
@@ -40,7 +51,8 @@ namespace {
 constexpr int kMxThreads = 128;
 constexpr int kMxN = 16;                       // MMA N: entries of one pass
 constexpr int kMxStageK = 128;                 // K elements per stage
-constexpr int kMxStages = 4;                   // ring buffers; loads run kMxStages - 2 stages ahead
+constexpr int kMxStages = 3;                   // shared-memory ring buffers
+constexpr int kMxRegStages = 6;                // stages of operands in flight in registers
 constexpr int kMxLbo = 128;                    // bytes between core matrices adjacent in K
 constexpr int kMxSbo = 8 * 128;                // bytes between 8-row groups (8 K slots of 16 B)
 constexpr int kMxABytes = 128 * kMxStageK;     // 128 rows x 8 slots x 16 B
@@ -50,9 +62,12 @@ constexpr int kMxSfbBytes = kMxN * 4;
 constexpr int kMxStageBytes = kMxABytes + kMxBBytes + kMxSfaBytes + kMxSfbBytes;
 constexpr int kMxTmemCols = 256;               // D: columns 0..15; scale factors on aligned columns
 constexpr int kMxColSfa = 32;                  // SFA of buffer b: 4 columns at 32 + 32 b
-constexpr int kMxColSfb = 192;                 // SFB of buffer b: 1 column at 192 + 16 b
+constexpr int kMxColSfb = 176;                 // SFB of buffer b: 1 column at 176 + 16 b
+constexpr int kMxBlockBytes = 8192 + 512;      // one stage of a 128-row tile in the stage-ordered bank
 constexpr unsigned long long kMxWaitLimitNs = 200ull * 1000 * 1000;
-constexpr size_t kMxSmem = (size_t)kMxStages * kMxStageBytes + 64;
+// at least 80 KB, so that no more than two CTAs (2 x 256 TMEM columns) share an SM
+constexpr size_t kMxSmemNeed = (size_t)kMxStages * kMxStageBytes + 64;
+constexpr size_t kMxSmem = kMxSmemNeed > 80 * 1024 ? kMxSmemNeed : 80 * 1024;
 
 static_assert(kMxColSfa + 32 * (kMxStages - 1) + 4 <= kMxColSfb && kMxColSfb + 16 * kMxStages <= kMxTmemCols,
               "TMEM columns");
@@ -79,16 +94,6 @@ __host__ __device__ constexpr uint32_t mx_idesc(int sf_id) {
            ((uint32_t)(128 >> 4) << 24) | ((uint32_t)(sf_id & 3) << 29);
 }
 
-__device__ __forceinline__ void cp_async8(uint32_t dst, const void *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async16s(uint32_t dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
@@ -112,17 +117,15 @@ __device__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 }
 
 struct MxGemmArgs {
-    const uint8_t *w;           // E2M1 codes [n_tot][rows][K/2]
-    const uint8_t *wsc;         // E8M0 scales [n_tot][rows][K/32]
+    const uint8_t *blocks;      // section of the stage-ordered bank: [n_tot][tiles][K/128] blocks
     const uint8_t *aq;          // E4M3 activations [act_rows][K]
     const uint8_t *asc;         // E8M0 scales [act_rows][K/32]
     const Pass *passes;         // passes of <= 16 entries
     const int32_t *sorted_tok;  // gate/up: entry -> activation row (token); down: null (row = entry)
     float *out;                 // gate/up: h [entries][I]; down: Y [entries][H]
     uint32_t *hdr;
-    int rows;                   // weight rows per expert: 2I (gate/up) or H (down)
+    int tiles;                  // 128-row tiles per expert: I/64 (gate/up) or H/128 (down)
     int K;                      // H (gate/up) or I (down)
-    int half;                   // gate/up: I (up rows start there); down: 0
     int out_ld;                 // I (gate/up) or H (down)
     int n_tot;                  // experts in the bank
     int act_rows;               // rows of aq: T (gate/up) or entries (down)
@@ -157,7 +160,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx8_gemm_kernel(const __grid_co
             return;
         }
     }
-    uint64_t *mbar = reinterpret_cast<uint64_t *>(mx_smem + (size_t)kMxStages * kMxStageBytes);
+    uint64_t *mbar = reinterpret_cast<uint64_t *>(mx_smem + (size_t)kMxStages * kMxStageBytes);   // kMxStages barriers
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&s_taddr)),
                      "n"(kMxTmemCols));
@@ -173,56 +176,83 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx8_gemm_kernel(const __grid_co
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = s_taddr;
 
-    // this thread's copies: A rows (tid / 8) + 16 i, 8-byte slot tid % 8;
-    // B row tid / 8, 16-byte slot tid % 8; SFA row tid; SFB row tid (< 16)
-    const int K2 = a.K / 2, K32 = a.K / 32;
-    const uint8_t *wexp = a.w + (size_t)ps.expert * a.rows * K2;
-    const uint8_t *sexp = a.wsc + (size_t)ps.expert * a.rows * K32;
-    auto wrow = [&](int r) { return GATEUP ? (r < 64 ? tile * 64 + r : a.half + tile * 64 + r - 64) : tile * 128 + r; };
+    // this thread's copies: 8-byte code pieces tid + 128 i of the stage's
+    // block, 16 bytes of its scales (tid < 32); B row tid / 8, 16-byte slot
+    // tid % 8; SFB row tid (< 16)
+    const int K32 = a.K / 32;
+    const int nst = a.K / kMxStageK;
+    const uint8_t *wblk = a.blocks + ((size_t)ps.expert * a.tiles + tile) * nst * kMxBlockBytes;
     auto arow = [&](int n) {
         const int e = ps.begin + min(n, ps.count - 1);
         return GATEUP ? a.sorted_tok[e] : e;
     };
     const int slot = tid & 7, r0 = tid >> 3;
     const uint8_t *asrc = a.aq + (size_t)arow(r0) * a.K + slot * 16;
-    const uint8_t *sfa_src = sexp + (size_t)wrow(tid) * K32;
     const uint8_t *sfb_src = a.asc + (size_t)arow(tid & 15) * K32;
     const uint32_t sbase = smem_addr(mx_smem);
-    const int nst = a.K / kMxStageK;
 
-    auto issue = [&](int s) {
-        const uint32_t st = sbase + (uint32_t)((s % kMxStages) * kMxStageBytes);
+    // every operand of a stage arrives through registers, kMxRegStages
+    // stages ahead.  Weight codes: 16-byte chunk c = tid + 128 i (i < 4) of
+    // the block holds the pieces q0 = 64 (c / 32) + c % 32 and q0 + 32 of the
+    // shared-memory image (so each 8-byte store of a warp covers 32
+    // consecutive slots); weight scales: chunks of threads 0..31; activation
+    // codes: 16 bytes of row tid / 8, slot tid % 8; activation scales: 4 bytes
+    // of row tid (< 16).
+    const uint64_t pol = l2_evict_first_policy();
+    uint4 rq[kMxRegStages][4];
+    uint4 rsf[kMxRegStages];
+    uint4 rb[kMxRegStages];
+    uint32_t rsb[kMxRegStages];
+    auto load_stage = [&](int s, uint4(&q)[4], uint4 &sf, uint4 &bq, uint32_t &sb) {
+        const uint8_t *blk = wblk + (size_t)s * kMxBlockBytes;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = r0 + 16 * i;
-            cp_async8(st + (uint32_t)((r >> 3) * kMxSbo + slot * kMxLbo + (r & 7) * 16),
-                      wexp + (size_t)wrow(r) * K2 + s * (kMxStageK / 2) + slot * 8);
-        }
-        cp_async16s(st + kMxABytes + (uint32_t)((r0 >> 3) * kMxSbo + slot * kMxLbo + (r0 & 7) * 16),
-                    asrc + (size_t)s * kMxStageK);
-        cp_async4(st + kMxABytes + kMxBBytes + tid * 4, sfa_src + s * 4);
+        for (int i = 0; i < 4; ++i)
+            q[i] = ld_stream16(blk + 16 * (tid + kMxThreads * i), pol);
+        if (tid < 32)
+            sf = ld_stream16(blk + 8192 + 16 * tid, pol);
+        bq = __ldg(reinterpret_cast<const uint4 *>(asrc + (size_t)s * kMxStageK));
         if (tid < kMxN)
-            cp_async4(st + kMxABytes + kMxBBytes + kMxSfaBytes + tid * 4, sfb_src + s * 4);
+            sb = __ldg(reinterpret_cast<const uint32_t *>(sfb_src + s * 4));
+    };
+    auto store_stage = [&](int s, const uint4(&q)[4], const uint4 &sf, const uint4 &bq, uint32_t sb) {
+        uint8_t *st = mx_smem + (size_t)(s % kMxStages) * kMxStageBytes;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int c = tid + kMxThreads * i;
+            const int q0 = 64 * (c >> 5) + (c & 31);
+            *reinterpret_cast<uint2 *>(st + 16 * q0) = make_uint2(q[i].x, q[i].y);
+            *reinterpret_cast<uint2 *>(st + 16 * (q0 + 32)) = make_uint2(q[i].z, q[i].w);
+        }
+        if (tid < 32)
+            *reinterpret_cast<uint4 *>(st + kMxABytes + kMxBBytes + 16 * tid) = sf;
+        *reinterpret_cast<uint4 *>(st + kMxABytes + (r0 >> 3) * kMxSbo + slot * kMxLbo + (r0 & 7) * 16) = bq;
+        if (tid < kMxN)
+            *reinterpret_cast<uint32_t *>(st + kMxABytes + kMxBBytes + kMxSfaBytes + 4 * tid) = sb;
     };
 
     bool ok = true;
 #pragma unroll
-    for (int s = 0; s < kMxStages - 2; ++s) {
-        if (s < nst)
-            issue(s);
-        cp_async_commit();
-    }
-    for (int s = 0; s < nst; ++s) {
-        // refill the buffer that the MMAs of stage s - 2 read
-        if (s >= 2)
-            ok = ok && mbar_wait(smem_addr(mbar + (s - 2) % kMxStages), ((s - 2) / kMxStages) & 1);
-        if (ok && s + kMxStages - 2 < nst)
-            issue(s + kMxStages - 2);
-        cp_async_commit();
-        cp_async_wait<kMxStages - 2>();
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        if (__syncthreads_or(!ok))
+    for (int k = 0; k < kMxRegStages; ++k)
+        if (k < nst)
+            load_stage(k, rq[k], rsf[k], rb[k], rsb[k]);
+    for (int s0 = 0; s0 < nst && ok; s0 += kMxRegStages) {
+#pragma unroll
+        for (int k = 0; k < kMxRegStages; ++k) {
+        const int s = s0 + k;
+        if (s >= nst)
             break;
+        // shared buffer s % kMxStages was read by the MMAs of stage s - kMxStages
+        if (s >= kMxStages)
+            ok = ok && mbar_wait(smem_addr(mbar + (s - kMxStages) % kMxStages), ((s - kMxStages) / kMxStages) & 1);
+        if (ok)
+            store_stage(s, rq[k], rsf[k], rb[k], rsb[k]);
+        if (s + kMxRegStages < nst)
+            load_stage(s + kMxRegStages, rq[k], rsf[k], rb[k], rsb[k]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (__syncthreads_or(!ok)) {
+            ok = false;
+            break;
+        }
         // scale factors of stage s into this buffer's TMEM columns, every quarter
         const int b = s % kMxStages;
         const uint8_t *st = mx_smem + (size_t)b * kMxStageBytes;
@@ -256,10 +286,10 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx8_gemm_kernel(const __grid_co
                              smem_addr(mbar + b))
                          : "memory");
         }
+        }
     }
     if (ok)
         ok = mbar_wait(smem_addr(mbar + (nst - 1) % kMxStages), ((nst - 1) / kMxStages) & 1);
-    asm volatile("cp.async.wait_all;" ::: "memory");
     ok = !__syncthreads_or(!ok);
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     if (!ok) {
@@ -334,9 +364,58 @@ __global__ void __launch_bounds__(256) mx8_quant_kernel(const In *__restrict__ i
         scales[blk] = (uint8_t)(se + 127);
 }
 
+// Stage-ordered copy of one section of the bank: one thread per 8-byte code
+// piece (q < 1024) or 4-byte scale word (q >= 1024) of a block.  Tile rows:
+// gate/up (half = I) rows 0..63 are gate rows 64t.., rows 64..127 the up rows
+// I + 64t..; down (half = 0) rows 128t...
+__global__ void __launch_bounds__(256) mx8_pack_kernel(const uint8_t *__restrict__ w, const uint8_t *__restrict__ sc,
+                                                       int n_tot, int rows, int K, int tiles, int half,
+                                                       uint8_t *__restrict__ out) {
+    const int nst = K / kMxStageK, K2 = K / 2, K32 = K / 32;
+    const long long items = (long long)n_tot * tiles * nst * 1152;
+    for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < items;
+         it += (long long)gridDim.x * blockDim.x) {
+        const long long blk = it / 1152;
+        const int q = (int)(it - blk * 1152);
+        const int s = (int)(blk % nst);
+        const long long et = blk / nst;
+        const int t = (int)(et % tiles), e = (int)(et / tiles);
+        const int r = q < 1024 ? 8 * (q >> 6) + (q & 7) : q - 1024;
+        const int row = half ? (r < 64 ? 64 * t + r : half + 64 * t + r - 64) : 128 * t + r;
+        uint8_t *dst = out + blk * kMxBlockBytes;
+        if (q < 1024) {
+            const int j = (q >> 3) & 7, piece = q & 63;
+            const int pos = (q & ~63) + 2 * (piece & 31) + (piece >> 5);   // pieces l and l + 32 side by side
+            *reinterpret_cast<uint2 *>(dst + 8 * pos) =
+                *reinterpret_cast<const uint2 *>(w + ((size_t)e * rows + row) * K2 + s * 64 + j * 8);
+        } else {
+            *reinterpret_cast<uint32_t *>(dst + 8192 + 4 * r) =
+                *reinterpret_cast<const uint32_t *>(sc + ((size_t)e * rows + row) * K32 + s * 4);
+        }
+    }
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ host
+
+size_t mx8_packed_size(int H, int I, int n_tot) {
+    return (size_t)n_tot * ((size_t)(I / 64) * (H / 128) + (size_t)(H / 128) * (I / 128)) * kMxBlockBytes;
+}
+
+static size_t mx8_dn_offset(int H, int I, int n_tot) {
+    return (size_t)n_tot * (I / 64) * (H / 128) * kMxBlockBytes;
+}
+
+cudaError_t launch_mx8_pack(const moe_mxfp4_bank_t &b, uint8_t *out, cudaStream_t stream) {
+    const int H = b.hidden, I = b.inter, n = b.num_experts + b.has_shared;
+    mx8_pack_kernel<<<4096, 256, 0, stream>>>(b.w13, b.s13, n, 2 * I, H, I / 64, I, out);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess)
+        return err;
+    mx8_pack_kernel<<<4096, 256, 0, stream>>>(b.w2, b.s2, n, H, I, H / 128, 0, out + mx8_dn_offset(H, I, n));
+    return cudaGetLastError();
+}
 
 bool mx8_shape_supported(int H, int I) { return H > 0 && I > 0 && H % 128 == 0 && I % 128 == 0; }
 
@@ -366,17 +445,15 @@ cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cud
     if (err != cudaSuccess)
         return err;
     MxGemmArgs g{};
-    g.w = b.w13;
-    g.wsc = b.s13;
+    g.blocks = p.packed_mx;
     g.aq = xq;
     g.asc = xs;
     g.passes = ws_at<Pass>(ws, L.passesw4);
     g.sorted_tok = ws_at<int32_t>(ws, L.sorted_tok);
     g.out = h32;
     g.hdr = hdr;
-    g.rows = 2 * I;
+    g.tiles = I / 64;
     g.K = H;
-    g.half = I;
     g.out_ld = I;
     g.n_tot = n_tot;
     g.act_rows = T;
@@ -388,15 +465,13 @@ cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cud
                           entries, I, hq, hs)) != cudaSuccess)
         return err;
     MxGemmArgs d = g;
-    d.w = b.w2;
-    d.wsc = b.s2;
+    d.blocks = p.packed_mx + mx8_dn_offset(H, I, n_tot);
     d.aq = hq;
     d.asc = hs;
     d.sorted_tok = nullptr;
     d.out = yent;
-    d.rows = H;
+    d.tiles = H / 128;
     d.K = I;
-    d.half = 0;
     d.out_ld = H;
     d.act_rows = entries;
     if ((err = launch_pdl(mx8_gemm_kernel<false>, dim3(H / 128, max_pass), dim3(kMxThreads), kMxSmem, stream, d)) !=

@@ -72,7 +72,9 @@ def lib() -> C.CDLL:
                     "moe_layer_forward_noalloc": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, p, p]),
                     "moe_layer_forward_next": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, p, p, s, p,
                                                    C.POINTER(_Bank), p]),
-                    "moe_layer_forward_mxfp8": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, p, p, s, p]),
+                    "moe_layer_forward_mxfp8": (i, [p, p, p, i, i, C.POINTER(_Bank), p, f, p, p, p, p, s, p]),
+                    "moe_packed_mx_bank_size": (s, [i, i, i, i]),
+                    "moe_pack_bank_mx": (i, [C.POINTER(_Bank), p, s, p]),
                     "moe_layer_forward_profiled": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, s, p, i, p]),
                     "moe_check_device_status": (i, [p, p]),
                     "moe_layer_launches": (i, [i, i, i, i, i, i]),
@@ -90,7 +92,7 @@ def lib() -> C.CDLL:
 
 
 def exported_symbols() -> list[str]:
-    return ["moe_workspace_size", "moe_workspace_offset", "moe_workspace_init", "moe_packed_bank_size", "moe_pack_bank", "moe_route_topk", "moe_group_tokens", "moe_expert_ffn_mxfp4",
+    return ["moe_workspace_size", "moe_workspace_offset", "moe_workspace_init", "moe_packed_bank_size", "moe_pack_bank", "moe_packed_mx_bank_size", "moe_pack_bank_mx", "moe_route_topk", "moe_group_tokens", "moe_expert_ffn_mxfp4",
             "moe_layer_forward", "moe_layer_forward_hostio", "moe_layer_forward_mxfp8", "moe_layer_forward_next",
             "moe_layer_forward_noalloc", "moe_layer_forward_profiled",
             "moe_layer_launches", "moe_read_phase_times", "moe_check_device_status", "moe_selftest_decode_e2m1", "moe_selftest_wait_timeout",
@@ -141,6 +143,7 @@ class MXFP4Bank:
     s13: torch.Tensor | None = None
     w2: torch.Tensor | None = None
     s2: torch.Tensor | None = None
+    packed_mx: torch.Tensor | None = None     # stage-ordered copy for moe_layer_forward_mxfp8
 
     def c_struct(self) -> _Bank:
         ptrs = []
@@ -159,6 +162,18 @@ class MXFP4Bank:
                                    _stream(stream)), "moe_pack_bank")
         return self
 
+    def pack_mx(self, stream=None) -> "MXFP4Bank":
+        """Fill ``packed_mx`` from the canonical arrays (moe_pack_bank_mx)."""
+        n = int(lib().moe_packed_mx_bank_size(self.hidden, self.inter, self.num_experts, self.has_shared))
+        if n == 0:
+            raise MoEError(MOE_ERR_UNSUPPORTED_SHAPE, "moe_packed_mx_bank_size")
+        if self.packed_mx is None or self.packed_mx.numel() < n:
+            self.packed_mx = torch.empty(n, dtype=torch.uint8, device=self.w13.device)
+        b = self.c_struct()
+        _check(lib().moe_pack_bank_mx(C.byref(b), _ptr(self.packed_mx, torch.uint8, "packed_mx"),
+                                      self.packed_mx.numel(), _stream(stream)), "moe_pack_bank_mx")
+        return self
+
     def drop_canonical(self) -> "MXFP4Bank":
         self.w13 = self.s13 = self.w2 = self.s2 = None
         return self
@@ -168,13 +183,15 @@ class MXFP4Bank:
 
     @staticmethod
     def from_host(arrays: dict, num_experts: int, has_shared: int, device="cuda",
-                  keep_canonical: bool = False) -> "MXFP4Bank":
+                  keep_canonical: bool = False, with_mx: bool = False) -> "MXFP4Bank":
         t = {k: torch.from_numpy(arrays[k]).to(device) for k in ("w13", "s13", "w2", "s2")}
         hidden = t["w2"].shape[1]
         inter = t["w13"].shape[1] // 2
         bank = MXFP4Bank(num_experts, has_shared, hidden, inter, **t)
         with torch.cuda.device(t["w13"].device):
             bank.pack()
+            if with_mx:
+                bank.pack_mx()
         if not keep_canonical:
             torch.cuda.current_stream(t["w13"].device).synchronize()
             bank.drop_canonical()
@@ -270,12 +287,12 @@ def moe_layer_forward_next(x, router_w, logit_bias, top_k, bank: MXFP4Bank, shar
 
 def moe_layer_forward_mxfp8(x, router_w, logit_bias, top_k, bank: MXFP4Bank, shared_weight, y, topk_ids_out=None,
                             topk_w_out=None, ws=None, stream=None):
-    """The MXFP8 live-activation-quantisation variant (needs the bank's canonical arrays)."""
+    """The MXFP8 live-activation-quantisation variant (needs ``bank.packed_mx``: from_host(with_mx=True))."""
     T = x.shape[0]
     b = bank.c_struct()
     _check(lib().moe_layer_forward_mxfp8(_ptr(x, torch.bfloat16, "x"), _ptr(router_w, torch.float32, "router_w"),
                                          _ptr(logit_bias, torch.float32, "logit_bias"), T, top_k, C.byref(b),
-                                         float(shared_weight), _ptr(y, torch.bfloat16, "y"),
+                                         _ptr(bank.packed_mx, torch.uint8, "packed_mx"), float(shared_weight), _ptr(y, torch.bfloat16, "y"),
                                          _ptr(topk_ids_out, torch.int32, "topk_ids_out"),
                                          _ptr(topk_w_out, torch.float32, "topk_w_out"), _ptr(ws, torch.uint8, "ws"),
                                          ws.numel(), _stream(stream)), "moe_layer_forward_mxfp8")

@@ -235,17 +235,42 @@ moe_status_t moe_layer_forward_next(const uint16_t *x, const float *router_w, co
  * from it by the activation quantisation (a few 1e-2 of max|y| at the
  * shapes tested), and it is compared against its own oracle mode.
  *
- * Reads the canonical bank arrays w13, s13, w2, s2 (non-NULL; w13 and w2
- * 16-byte aligned, s13 and s2 4-byte aligned); `packed` is not used.
- * H and I must be multiples of 128 (MOE_ERR_UNSUPPORTED_SHAPE).  Workspace:
+ * bank gives the dimensions only (its arrays are not read); the weights are
+ * read from packed_mx, the stage-ordered copy moe_pack_bank_mx writes
+ * (256-byte aligned).  H and I must be multiples of 128
+ * (MOE_ERR_UNSUPPORTED_SHAPE).  Workspace:
  * moe_workspace_size(T, ...) bytes, as for moe_layer_forward.  Seven
  * launches (two of routing, two quantisations, two GEMMs, the combine);
  * asynchronous on `stream`, graph-capturable.
  */
 moe_status_t moe_layer_forward_mxfp8(const uint16_t *x, const float *router_w, const float *logit_bias,
-                                     int T, int top_k, const moe_mxfp4_bank_t *bank, float shared_weight,
-                                     uint16_t *y, int32_t *topk_ids_out, float *topk_w_out, void *ws,
-                                     size_t ws_bytes, cudaStream_t stream);
+                                     int T, int top_k, const moe_mxfp4_bank_t *bank, const void *packed_mx,
+                                     float shared_weight, uint16_t *y, int32_t *topk_ids_out,
+                                     float *topk_w_out, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Bytes of the stage-ordered bank of the MXFP8 variant (0 when H or I is not
+ * a multiple of 128): the same codes and scales as the canonical arrays,
+ * reordered so that the block-scaled GEMMs read each pipeline stage of a
+ * 128-row tile as one contiguous block.  Per section (gate/up, then down),
+ * per expert, per 128-row tile (gate/up tile t: gate rows 64t..64t+63 then
+ * up rows I+64t..; down tile t: rows 128t..128t+127), per K stage of 128: an
+ * 8,704-byte block = the codes, then the scales [row][4 bytes].  The codes
+ * are 16 groups of 8 rows, each 64 eight-byte pieces (16 elements of one
+ * row): piece w = 8 * slot + row-in-group holds K elements 16 slot .. +15;
+ * a group stores pieces w and w + 32 side by side (piece w at position
+ * 2 (w mod 32) + w / 32).
+ */
+size_t moe_packed_mx_bank_size(int H, int I, int E, int has_shared);
+
+/*
+ * Fill packed_mx (moe_packed_mx_bank_size bytes, 256-byte aligned) from the
+ * bank's canonical arrays (w13, s13, w2, s2: non-NULL, w13 / w2 16-byte and
+ * s13 / s2 4-byte aligned).  One-time, load-time work; asynchronous on
+ * `stream`; the canonical arrays may be freed once it has completed.
+ */
+moe_status_t moe_pack_bank_mx(const moe_mxfp4_bank_t *bank, void *packed_mx, size_t packed_mx_bytes,
+                              cudaStream_t stream);
 
 /*
  * The whole layer without a caller-provided workspace.  The pages have no

@@ -97,6 +97,31 @@ def test_pack_argument_checks(L):
     assert L.moe_pack_bank(C.byref(bank()), p, n - 1, None) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
 
 
+def forward_mx(L, b, T=1, k=8, pmx=FAKE, x=FAKE, y=FAKE, ws=FAKE, ws_bytes=1 << 40):
+    return L.moe_layer_forward_mxfp8(C.c_void_p(x), C.c_void_p(FAKE), None, T, k, C.byref(b), C.c_void_p(pmx), 1.0,
+                                     C.c_void_p(y), None, None, C.c_void_p(ws), ws_bytes, None)
+
+
+def test_mxfp8_argument_checks(L):
+    # stage-ordered bank: the same bytes as the canonical arrays
+    n = moe.lib().moe_packed_mx_bank_size(5120, 1536, 160, 1)
+    assert n == 161 * 3 * 1536 * 5120 * 17 // 32
+    assert moe.lib().moe_packed_mx_bank_size(5120 + 64, 1536, 160, 1) == 0      # H % 128
+    assert moe.lib().moe_packed_mx_bank_size(5120, 1536 + 64, 160, 1) == 0      # I % 128
+    p = C.c_void_p(FAKE)
+    assert L.moe_pack_bank_mx(C.byref(bank(w2=0)), p, n, None) == moe.MOE_ERR_INVALID_ARG
+    assert L.moe_pack_bank_mx(C.byref(bank()), C.c_void_p(FAKE + 16), n, None) == moe.MOE_ERR_MISALIGNED
+    assert L.moe_pack_bank_mx(C.byref(bank()), p, n - 1, None) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+    assert L.moe_pack_bank_mx(C.byref(bank(H=5120 + 64)), p, n, None) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    assert forward_mx(L, bank(), pmx=0) == moe.MOE_ERR_INVALID_ARG
+    assert forward_mx(L, bank(), pmx=FAKE + 16) == moe.MOE_ERR_MISALIGNED
+    assert forward_mx(L, bank(H=5120 + 64)) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    assert forward_mx(L, bank(), x=0) == moe.MOE_ERR_INVALID_ARG
+    assert forward_mx(L, bank(), k=161) == moe.MOE_ERR_UNSUPPORTED_SHAPE
+    need = moe.moe_workspace_size(1, 5120, 1536, 160, 8, 1)
+    assert forward_mx(L, bank(), ws_bytes=need - 1) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+
+
 def test_other_entry_points_argument_checks(L):
     p = C.c_void_p(FAKE)
     assert L.moe_route_topk(p, p, None, 1, 5120, 160, 9, 1, 1.0, None, p, p, 1 << 30, None) == moe.MOE_ERR_INVALID_ARG

@@ -61,7 +61,7 @@ class MxProblem:
             "s13": rng.integers(118, 125, (n, 2 * I, H // 32), dtype=np.uint8),
             "w2": rng.integers(0, 256, (n, H, I // 2), dtype=np.uint8),
             "s2": rng.integers(118, 125, (n, H, I // 32), dtype=np.uint8)}
-        self.bank = moe.MXFP4Bank.from_host(self.bank_np, E, has_shared, keep_canonical=True)
+        self.bank = moe.MXFP4Bank.from_host(self.bank_np, E, has_shared, with_mx=True)
 
     def expert(self, e):
         return {kk: v[e] for kk, v in self.bank_np.items()}
@@ -179,3 +179,39 @@ def test_mxfp8_routing_matches_exact_entry_point():
                           p.bank, 1.0, y, ids, w, ws)
     np.testing.assert_array_equal(ids.cpu().numpy(), out["ids"])
     np.testing.assert_array_equal(w.cpu().numpy(), out["w"])
+
+
+def mx_layout_reference(bank_np, H, I):
+    """The stage-ordered bank as documented in moe_fp4.h, built with numpy."""
+    n = bank_np["w13"].shape[0]
+    out = []
+    for codes, scales, tiles, rows_of in (
+            (bank_np["w13"], bank_np["s13"], I // 64,
+             lambda t: np.concatenate([64 * t + np.arange(64), I + 64 * t + np.arange(64)])),
+            (bank_np["w2"], bank_np["s2"], H // 128, lambda t: 128 * t + np.arange(128))):
+        K = codes.shape[2] * 2
+        for e in range(n):
+            for t in range(tiles):
+                R = rows_of(t)
+                for s in range(K // 128):
+                    c = codes[e][R][:, 64 * s:64 * (s + 1)].reshape(16, 8, 8, 8)    # [group][row][slot][byte]
+                    img = c.transpose(0, 2, 1, 3).reshape(16, 2, 32, 8)              # pieces w = 8 slot + row
+                    out.append(img.transpose(0, 2, 1, 3).ravel())                    # w and w + 32 side by side
+                    out.append(scales[e][R][:, 4 * s:4 * s + 4].ravel())
+    return np.concatenate(out)
+
+
+def test_pack_mx_matches_documented_layout():
+    H, I, E = 384, 256, 2
+    rng = np.random.default_rng(11)
+    n = E + 1
+    bank_np = {"w13": rng.integers(0, 256, (n, 2 * I, H // 2), dtype=np.uint8),
+               "s13": rng.integers(0, 256, (n, 2 * I, H // 32), dtype=np.uint8),
+               "w2": rng.integers(0, 256, (n, H, I // 2), dtype=np.uint8),
+               "s2": rng.integers(0, 256, (n, H, I // 32), dtype=np.uint8)}
+    bank = moe.MXFP4Bank.from_host(bank_np, E, 1, with_mx=True)
+    torch.cuda.synchronize()
+    want = mx_layout_reference(bank_np, H, I)
+    got = bank.packed_mx.cpu().numpy()
+    assert got.size == want.size == moe.lib().moe_packed_mx_bank_size(H, I, E, 1)
+    np.testing.assert_array_equal(got, want)
