@@ -33,6 +33,12 @@ Extra JSON keys:
 --impl reference times the oracle (the only other implementation of this
 layer) on the same workload and prints the same line with "impl":
 "reference".
+
+--act mxfp8 runs the MXFP8 live-activation-quantisation variant
+(moe_layer_forward_mxfp8: x and h quantised to MXFP8, both projections as
+block-scaled tcgen05 MMAs) on the same workload and bytes; its roofline
+object is the gate/up GEMM, its e2e copies x from and y to pinned host memory
+around every call, and the reference arm runs the oracle's MXFP8 mode.
 """
 from __future__ import annotations
 
@@ -61,6 +67,8 @@ DEFAULT_CONFIG = "glm_t1"
 TRAFFIC_BYTES = {
     # profiles/fused_layer_glm_t1.md: 116,255,744 read + 3,048,960 written
     ("glm_t1", "fused_layer_kernel"): 119304704,
+    # profiles/mx8_gemm_glm_t1.md: 75,246,592 read + 1,009,408 written
+    ("glm_t1", "mx8_gemm_kernel<gate/up>"): 76256000,
 }
 
 
@@ -159,7 +167,7 @@ def job_value(world: int, bytes_per_call: float, per_call_s: float) -> float:
 
 # ---------------------------------------------------------------- reference
 
-def oracle_call_factory(cfg: inputs.MoEConfig):
+def oracle_call_factory(cfg: inputs.MoEConfig, act: str = "exact"):
     import oracle
     x = inputs.make_x(cfg)
     wr, bias = inputs.make_router(cfg)
@@ -170,14 +178,14 @@ def oracle_call_factory(cfg: inputs.MoEConfig):
 
     def call(tokens):
         r = oracle.route(x, wr, bias, cfg.top_k)
-        return oracle.moe_tokens(x, r["ids"], r["w"], lambda e: experts[e], tokens)
+        return oracle.moe_tokens(x, r["ids"], r["w"], lambda e: experts[e], tokens, act=act)
     return call, route
 
 
-def time_oracle(cfg, budget_s: float, max_calls: int | None = None):
+def time_oracle(cfg, budget_s: float, max_calls: int | None = None, act: str = "exact"):
     """Wall time of whole oracle layer calls on a bounded sample of tokens."""
     import oracle
-    call, route = oracle_call_factory(cfg)
+    call, route = oracle_call_factory(cfg, act)
     n_exp = len(set(int(v) for v in route["ids"].ravel()))
     # tokens per call: all of them when the whole call fits the budget, else a prefix
     t0 = time.perf_counter()
@@ -207,8 +215,8 @@ def run_reference(args, cfg):
         return 0
     budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        time_oracle(cfg, budget_s=0.0, max_calls=1)
-    res = [time_oracle(cfg, budget_s=budget, max_calls=1) for _ in range(args.steps)]
+        time_oracle(cfg, budget_s=0.0, max_calls=1, act=args.act)
+    res = [time_oracle(cfg, budget_s=budget, max_calls=1, act=args.act) for _ in range(args.steps)]
     per_call = statistics.median(r["per_call_s"] for r in res)
     b = touched_bytes(cfg, res[0]["n_experts"])
     val = b["total"] / per_call / 1e12
@@ -216,7 +224,7 @@ def run_reference(args, cfg):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_call * 1e3,
             "us_per_call": per_call * 1e6, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
-            "config": {"workload": describe(cfg), "name": cfg.name},
+            "config": {"workload": describe(cfg), "name": cfg.name, "activations": args.act},
             "cpu_baseline": {"value": val, "unit": "TB/s", "cores": res[0]["cores"], "kind": "oracle",
                              "sample": res[0]["sample"]},
             "e2e": {"value": val, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -249,7 +257,8 @@ def run_mine(args, cfg):
     x = inputs.make_x(cfg)
     wr, bias = inputs.make_router(cfg)
     bank_np = inputs.make_bank(cfg)
-    base = moe.MXFP4Bank.from_host(bank_np, cfg.E, cfg.has_shared, device=dev)
+    mx = args.act == "mxfp8"
+    base = moe.MXFP4Bank.from_host(bank_np, cfg.E, cfg.has_shared, device=dev, with_mx=mx)
     del bank_np
     xd = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
     wrd = torch.from_numpy(wr).to(dev)
@@ -258,7 +267,8 @@ def run_mine(args, cfg):
     y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
     ids = torch.empty((cfg.T, cfg.slots), dtype=torch.int32, device=dev)
     tw = torch.empty((cfg.T, cfg.slots), dtype=torch.float32, device=dev)
-    moe.moe_layer_forward(xd, wrd, bd, cfg.top_k, base, 1.0, y, ids, tw, ws)
+    layer = moe.moe_layer_forward_mxfp8 if mx else moe.moe_layer_forward
+    layer(xd, wrd, bd, cfg.top_k, base, 1.0, y, ids, tw, ws)
     st = moe.moe_check_device_status(ws)
     if st != 0:
         raise RuntimeError(moe.moe_status_string(st))
@@ -279,8 +289,7 @@ def run_mine(args, cfg):
             moe.moe_layer_forward_next(xd, routers[i % n_layers], bd, cfg.top_k, banks[i % n_layers], 1.0, y,
                                        ws=ws, next_router_w=routers[j], next_bank=banks[j], stream=s)
         else:
-            moe.moe_layer_forward(xd, routers[i % n_layers], bd, cfg.top_k, banks[i % n_layers], 1.0, y, ws=ws,
-                                  stream=s)
+            layer(xd, routers[i % n_layers], bd, cfg.top_k, banks[i % n_layers], 1.0, y, ws=ws, stream=s)
 
     # graph of one rotation over all layers
     with torch.cuda.stream(stream):
@@ -333,8 +342,13 @@ def run_mine(args, cfg):
     # them back to back (no host gaps inside the measured intervals).  When a
     # call is a single launch, events 1..4 all follow it: ev0 -> ev4 is the
     # kernel, and its phases come from the kernel's own timestamps.
-    launches = moe.moe_layer_launches(cfg.T, base, cfg.top_k)
-    kern = {"router": [], "topk_group": [], "gateup_hfin": [], "down_combine": []}
+    launches = 7 if mx else moe.moe_layer_launches(cfg.T, base, cfg.top_k)
+    if mx:
+        kern = {"route": [], "quant_x": [], "gateup_gemm": [], "quant_h_down_combine": []}
+        profiled = moe.moe_layer_forward_mxfp8_profiled
+    else:
+        kern = {"router": [], "topk_group": [], "gateup_hfin": [], "down_combine": []}
+        profiled = moe.moe_layer_forward_profiled
     whole = []
     n_prof = min(max(steps, n_layers), 400)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_prof)]
@@ -346,8 +360,8 @@ def run_mine(args, cfg):
     with torch.cuda.stream(stream):
         torch.cuda._sleep(int(2e9 * 60e-6 * n_prof))      # ~60 us of host time per queued step
         for i in range(n_prof):
-            moe.moe_layer_forward_profiled(xd, routers[i % n_layers], bd, cfg.top_k, banks[i % n_layers], 1.0,
-                                           y, ws, evs[i], stream=stream)
+            profiled(xd, routers[i % n_layers], bd, cfg.top_k, banks[i % n_layers], 1.0, y, ws, evs[i],
+                     stream=stream)
     stream.synchronize()
     for i in range(n_prof):
         for j, name in enumerate(kern):
@@ -376,8 +390,7 @@ def run_mine(args, cfg):
         for i, (e0, e1) in enumerate(ce):
             scrub.fill_(float(i))
             e0.record(stream)
-            moe.moe_layer_forward(xd, routers[i % n_layers], bd, cfg.top_k, banks[i % n_layers], 1.0, y, ws=ws,
-                                  stream=stream)
+            layer(xd, routers[i % n_layers], bd, cfg.top_k, banks[i % n_layers], 1.0, y, ws=ws, stream=stream)
             e1.record(stream)
     stream.synchronize()
     cold = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in ce)
@@ -389,21 +402,38 @@ def run_mine(args, cfg):
     # ---- end to end through host buffers
     xh = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
     yh = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16).pin_memory()
+    xs = torch.empty_like(xd)
+
+    def e2e_call(i):
+        if mx:
+            # pinned x -> device, the layer, y -> pinned host, all on `stream`,
+            # then wait for the copy back
+            with torch.cuda.stream(stream):
+                xs.copy_(xh, non_blocking=True)
+                layer(xs, routers[i % n_layers], bd, cfg.top_k, banks[i % n_layers], 1.0, y, ws=ws, stream=stream)
+                yh.copy_(y, non_blocking=True)
+            stream.synchronize()
+        else:
+            moe.moe_layer_forward_hostio(xh, routers[i % n_layers], bd, cfg.top_k, banks[i % n_layers], 1.0, yh,
+                                         ws, stream=stream)
     for i in range(3):
-        moe.moe_layer_forward_hostio(xh, routers[i % n_layers], bd, cfg.top_k, banks[i % n_layers], 1.0, yh, ws,
-                                     stream=stream)
+        e2e_call(i)
     n_e2e = min(steps, 2000)
     t0 = time.perf_counter()
     for i in range(n_e2e):
-        moe.moe_layer_forward_hostio(xh, routers[i % n_layers], bd, cfg.top_k, banks[i % n_layers], 1.0, yh, ws,
-                                     stream=stream)
+        e2e_call(i)
     e2e_per_call = max_over_ranks((time.perf_counter() - t0) / n_e2e, world, dev)
     if not torch.equal(yh.to(dev), y):
         raise RuntimeError("host-buffer entry point disagrees with the device entry point")
 
     peaks = read_peaks()
     peak = peaks.get("hbm_gbs")
-    if launches == 1:
+    if mx:
+        # the gate/up GEMM: its weights plus the MXFP8 codes and scales of x
+        roof_kernel = "mx8_gemm_kernel<gate/up> (tcgen05 kind::mxf8f6f4 block-scaled)"
+        roof_bytes = n_exp * 2 * cfg.I * cfg.H * (0.5 + 1.0 / 32) + cfg.T * cfg.H * (1 + 1.0 / 32)
+        roof_us = kern_us["gateup_gemm"]
+    elif launches == 1:
         # one launch per step: its average duration inside the timed graph
         # replay is the step time
         roof_kernel, roof_bytes = "fused_layer_kernel (the whole layer)", b["total"]
@@ -414,15 +444,18 @@ def run_mine(args, cfg):
     achieved = roof_bytes / (roof_us * 1e-6) / 1e9
     line = None
     if rank == 0:
-        cpu = time_oracle(cfg, budget_s=args.cpu_budget)
+        cpu = time_oracle(cfg, budget_s=args.cpu_budget, act=args.act)
         clocks = clk.summary()
         line = {
             "metric": METRIC, "value": job_value(world, b["total"], per_call), "unit": "TB/s", "n_gpus": world,
             "steps": steps, "warmup": args.warmup, "ms_per_step": per_call * 1e3, "us_per_call": per_call * 1e6,
             "pct_of_8TBs": 100 * b["total"] / per_call / 1e12 / PAGES_ROOFLINE_TBS,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "mxfp4 weights x f16 activations -> f32 accumulate, bf16 out", "data": "synthetic",
+            "dtype": ("mxfp4 weights x mxfp8 (e4m3 + e8m0/32) activations -> f32 accumulate (tcgen05 "
+                      "block-scaled), bf16 out" if mx else "mxfp4 weights x f16 activations -> f32 accumulate, bf16 out"),
+            "data": "synthetic",
             "config": {"workload": describe(cfg), "name": cfg.name, "T": cfg.T, "experts_touched": n_exp,
+                       "activations": args.act,
                        "bytes_per_call": b["total"], "router_bytes_not_counted": b["router"],
                        "l2": f"inputs larger than L2: steps rotate over {n_layers} weight copies "
                              f"({n_layers} x {b['total'] / 1e6:.1f} MB vs L2 {l2 / 1e6:.0f} MB)",
@@ -436,7 +469,8 @@ def run_mine(args, cfg):
                          "peak": peak if peak else 6800.0, "unit": "GB/s",
                          "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if peak else "fallback",
                          "frac": achieved / (peak if peak else 6800.0),
-                         "traffic": TRAFFIC_BYTES.get((cfg.name, roof_kernel.split()[0])),
+                         "traffic": TRAFFIC_BYTES.get((cfg.name, roof_kernel.split()[0])) if not mx else
+                         TRAFFIC_BYTES.get((cfg.name, "mx8_gemm_kernel<gate/up>")),
                          "algorithmic_bytes": roof_bytes},
             "cpu_baseline": {"value": cpu["tbs"], "unit": "TB/s", "cores": cpu["cores"], "kind": "oracle",
                              "sample": cpu["sample"]},
@@ -463,16 +497,18 @@ def run_profile_case(args, cfg):
     dev = torch.device("cuda", 0)
     x = inputs.make_x(cfg)
     wr, bias = inputs.make_router(cfg)
-    bank = moe.MXFP4Bank.from_host(inputs.make_bank(cfg), cfg.E, cfg.has_shared, device=dev)
+    mx = args.act == "mxfp8"
+    bank = moe.MXFP4Bank.from_host(inputs.make_bank(cfg), cfg.E, cfg.has_shared, device=dev, with_mx=mx)
     xd = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
     wrd = torch.from_numpy(wr).to(dev)
     bd = None if bias is None else torch.from_numpy(bias).to(dev)
     ws = moe.alloc_workspace(cfg.T, bank, cfg.top_k, device=dev)
     y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
+    layer = moe.moe_layer_forward_mxfp8 if mx else moe.moe_layer_forward
     for _ in range(args.profile_calls):
-        moe.moe_layer_forward(xd, wrd, bd, cfg.top_k, bank, 1.0, y, ws=ws)
+        layer(xd, wrd, bd, cfg.top_k, bank, 1.0, y, ws=ws)
     st = moe.moe_check_device_status(ws)
-    print(json.dumps({"profile_case": cfg.name, "calls": args.profile_calls, "status": st}))
+    print(json.dumps({"profile_case": cfg.name, "act": args.act, "calls": args.profile_calls, "status": st}))
     return 0 if st == 0 else 1
 
 
@@ -487,11 +523,15 @@ def main():
     ap.add_argument("--chain", action=argparse.BooleanOptionalAction, default=False,
                     help="time the calls as a chain of layers that prefetch the next layer's router and shared "
                          "expert (moe_layer_forward_next)")
+    ap.add_argument("--act", choices=["exact", "mxfp8"], default="exact",
+                    help="activations: exact (bf16 x, f16 hi/lo h) or the MXFP8 live-quantisation variant")
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="profiling mode: run this many plain layer calls on one weight copy and exit")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)     # never fewer than 3 untimed warm-up steps
     cfg = inputs.CONFIGS[args.config]
+    if args.chain and args.act != "exact":
+        ap.error("--chain applies to the exact-activation layer only")
     if args.profile_calls:
         return run_profile_case(args, cfg)
     if args.impl == "reference":

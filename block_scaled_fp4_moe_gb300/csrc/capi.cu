@@ -426,10 +426,17 @@ moe_status_t moe_pack_bank_mx(const moe_mxfp4_bank_t *bank, void *packed_mx, siz
     return from_cuda(launch_mx8_pack(*bank, static_cast<uint8_t *>(packed_mx), stream));
 }
 
-moe_status_t moe_layer_forward_mxfp8(const uint16_t *x, const float *router_w, const float *logit_bias, int T,
-                                     int top_k, const moe_mxfp4_bank_t *bank, const void *packed_mx,
-                                     float shared_weight, uint16_t *y, int32_t *topk_ids_out, float *topk_w_out,
-                                     void *ws, size_t ws_bytes, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Body of the MXFP8 entry points; ev (nullable): 5 events recorded before the
+// routing, after it, after the x quantisation, after the gate/up GEMM and at
+// the end.
+moe_status_t layer_forward_mxfp8(const uint16_t *x, const float *router_w, const float *logit_bias, int T,
+                                 int top_k, const moe_mxfp4_bank_t *bank, const void *packed_mx,
+                                 float shared_weight, uint16_t *y, int32_t *topk_ids_out, float *topk_w_out,
+                                 void *ws, size_t ws_bytes, cudaEvent_t *ev, cudaStream_t stream) {
     moe_status_t st = check_bank_dims(bank);
     if (st != MOE_OK)
         return st;
@@ -460,12 +467,43 @@ moe_status_t moe_layer_forward_mxfp8(const uint16_t *x, const float *router_w, c
     int32_t *ids = topk_ids_out ? topk_ids_out : ws_at<int32_t>(ws, L.topk_ids);
     float *w = topk_w_out ? topk_w_out : ws_at<float>(ws, L.topk_w);
     const GroupOut go = group_out_for(ws, L, H);
+    if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
     cudaError_t err = launch_route(x, router_w, logit_bias, T, H, E, top_k, S, shared_weight, ids, w, ws, L, true, go,
                                    stream);
     if (err != cudaSuccess)
         return MOE_ERR_CUDA;
+    if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
     const Mx8Problem pr{x, bank, static_cast<const uint8_t *>(packed_mx), w, y, T, top_k + S};
-    return from_cuda(launch_mx8_ffn(pr, ws, L, stream));
+    if ((err = launch_mx8_ffn(pr, ws, L, stream, ev ? ev + 2 : nullptr)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (ev && cudaEventRecord(ev[4], stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_layer_forward_mxfp8(const uint16_t *x, const float *router_w, const float *logit_bias, int T,
+                                     int top_k, const moe_mxfp4_bank_t *bank, const void *packed_mx,
+                                     float shared_weight, uint16_t *y, int32_t *topk_ids_out, float *topk_w_out,
+                                     void *ws, size_t ws_bytes, cudaStream_t stream) {
+    return layer_forward_mxfp8(x, router_w, logit_bias, T, top_k, bank, packed_mx, shared_weight, y, topk_ids_out,
+                               topk_w_out, ws, ws_bytes, nullptr, stream);
+}
+
+moe_status_t moe_layer_forward_mxfp8_profiled(const uint16_t *x, const float *router_w, const float *logit_bias,
+                                              int T, int top_k, const moe_mxfp4_bank_t *bank,
+                                              const void *packed_mx, float shared_weight, uint16_t *y, void *ws,
+                                              size_t ws_bytes, cudaEvent_t *events, int n_events,
+                                              cudaStream_t stream) {
+    if (!events || n_events < 5)
+        return MOE_ERR_INVALID_ARG;
+    return layer_forward_mxfp8(x, router_w, logit_bias, T, top_k, bank, packed_mx, shared_weight, y, nullptr,
+                               nullptr, ws, ws_bytes, events, stream);
 }
 
 moe_status_t moe_layer_forward_noalloc(const uint16_t *x, const float *router_w, const float *logit_bias, int T,

@@ -82,7 +82,9 @@ struct Mx8Problem {
 bool mx8_shape_supported(int H, int I);
 size_t mx8_packed_size(int H, int I, int n_tot);
 cudaError_t launch_mx8_pack(const moe_mxfp4_bank_t &b, uint8_t *out, cudaStream_t stream);
-cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cudaStream_t stream);
+// ev (nullable): two events, recorded after the x quantisation and after the gate/up GEMM.
+cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cudaStream_t stream,
+                           cudaEvent_t *ev = nullptr);
 
 // f16 copy of x with per-token power-of-two scaling (x16, xundo regions).
 cudaError_t launch_x16(const uint16_t *x, int T, int H, void *ws, const WsLayout &L, cudaStream_t stream);

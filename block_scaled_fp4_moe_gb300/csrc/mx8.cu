@@ -419,7 +419,7 @@ cudaError_t launch_mx8_pack(const moe_mxfp4_bank_t &b, uint8_t *out, cudaStream_
 
 bool mx8_shape_supported(int H, int I) { return H > 0 && I > 0 && H % 128 == 0 && I % 128 == 0; }
 
-cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cudaStream_t stream) {
+cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cudaStream_t stream, cudaEvent_t *ev) {
     const moe_mxfp4_bank_t &b = *p.bank;
     const int H = b.hidden, I = b.inter, T = p.T, kps = p.kps;
     const int entries = T * kps;
@@ -444,6 +444,8 @@ cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cud
                                  xq, xs);
     if (err != cudaSuccess)
         return err;
+    if (ev && (err = cudaEventRecord(ev[0], stream)) != cudaSuccess)
+        return err;
     MxGemmArgs g{};
     g.blocks = p.packed_mx;
     g.aq = xq;
@@ -460,6 +462,8 @@ cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cud
     g.entries = entries;
     if ((err = launch_pdl(mx8_gemm_kernel<true>, dim3(I / 64, max_pass), dim3(kMxThreads), kMxSmem, stream, g)) !=
         cudaSuccess)
+        return err;
+    if (ev && (err = cudaEventRecord(ev[1], stream)) != cudaSuccess)
         return err;
     if ((err = launch_pdl(mx8_quant_kernel<float>, dim3((hblocks + 7) / 8), dim3(256), 0, stream, (const float *)h32,
                           entries, I, hq, hs)) != cudaSuccess)

@@ -73,6 +73,8 @@ def lib() -> C.CDLL:
                     "moe_layer_forward_next": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, p, p, s, p,
                                                    C.POINTER(_Bank), p]),
                     "moe_layer_forward_mxfp8": (i, [p, p, p, i, i, C.POINTER(_Bank), p, f, p, p, p, p, s, p]),
+                    "moe_layer_forward_mxfp8_profiled": (i, [p, p, p, i, i, C.POINTER(_Bank), p, f, p, p, s, p, i,
+                                                             p]),
                     "moe_packed_mx_bank_size": (s, [i, i, i, i]),
                     "moe_pack_bank_mx": (i, [C.POINTER(_Bank), p, s, p]),
                     "moe_layer_forward_profiled": (i, [p, p, p, i, i, C.POINTER(_Bank), f, p, p, s, p, i, p]),
@@ -93,7 +95,8 @@ def lib() -> C.CDLL:
 
 def exported_symbols() -> list[str]:
     return ["moe_workspace_size", "moe_workspace_offset", "moe_workspace_init", "moe_packed_bank_size", "moe_pack_bank", "moe_packed_mx_bank_size", "moe_pack_bank_mx", "moe_route_topk", "moe_group_tokens", "moe_expert_ffn_mxfp4",
-            "moe_layer_forward", "moe_layer_forward_hostio", "moe_layer_forward_mxfp8", "moe_layer_forward_next",
+            "moe_layer_forward", "moe_layer_forward_hostio", "moe_layer_forward_mxfp8", "moe_layer_forward_mxfp8_profiled",
+            "moe_layer_forward_next",
             "moe_layer_forward_noalloc", "moe_layer_forward_profiled",
             "moe_layer_launches", "moe_read_phase_times", "moe_check_device_status", "moe_selftest_decode_e2m1", "moe_selftest_wait_timeout",
             "moe_status_string"]
@@ -179,7 +182,9 @@ class MXFP4Bank:
         return self
 
     def clone_packed(self) -> "MXFP4Bank":
-        return MXFP4Bank(self.num_experts, self.has_shared, self.hidden, self.inter, packed=self.packed.clone())
+        mx = None if self.packed_mx is None else self.packed_mx.clone()
+        return MXFP4Bank(self.num_experts, self.has_shared, self.hidden, self.inter, packed=self.packed.clone(),
+                         packed_mx=mx)
 
     @staticmethod
     def from_host(arrays: dict, num_experts: int, has_shared: int, device="cuda",
@@ -321,6 +326,20 @@ def moe_layer_forward_profiled(x, router_w, logit_bias, top_k, bank: MXFP4Bank, 
                                             float(shared_weight), _ptr(y, torch.bfloat16, "y"),
                                             _ptr(ws, torch.uint8, "ws"), ws.numel(), ev, 5, _stream(stream)),
            "moe_layer_forward_profiled")
+
+
+def moe_layer_forward_mxfp8_profiled(x, router_w, logit_bias, top_k, bank: MXFP4Bank, shared_weight, y, ws, events,
+                                     stream=None):
+    T = x.shape[0]
+    b = bank.c_struct()
+    ev = (C.c_void_p * 5)(*[e.cuda_event for e in events])
+    _check(lib().moe_layer_forward_mxfp8_profiled(_ptr(x, torch.bfloat16, "x"),
+                                                  _ptr(router_w, torch.float32, "router_w"),
+                                                  _ptr(logit_bias, torch.float32, "logit_bias"), T, top_k,
+                                                  C.byref(b), _ptr(bank.packed_mx, torch.uint8, "packed_mx"),
+                                                  float(shared_weight), _ptr(y, torch.bfloat16, "y"),
+                                                  _ptr(ws, torch.uint8, "ws"), ws.numel(), ev, 5, _stream(stream)),
+           "moe_layer_forward_mxfp8_profiled")
 
 
 def moe_layer_forward_hostio(x_host, router_w, logit_bias, top_k, bank: MXFP4Bank, shared_weight, y_host, ws,

@@ -261,6 +261,19 @@ moe_status_t moe_layer_forward_mxfp8(const uint16_t *x, const float *router_w, c
  * a group stores pieces w and w + 32 side by side (piece w at position
  * 2 (w mod 32) + w / 32).
  */
+/*
+ * Diagnostics: moe_layer_forward_mxfp8 with CUDA events recorded on `stream`
+ * between its steps: events[0] before the routing, [1] after it, [2] after
+ * the x quantisation, [3] after the gate/up GEMM, [4] at the end (n_events
+ * >= 5, else MOE_ERR_INVALID_ARG).  topk ids and weights are not returned.
+ */
+moe_status_t moe_layer_forward_mxfp8_profiled(const uint16_t *x, const float *router_w,
+                                              const float *logit_bias, int T, int top_k,
+                                              const moe_mxfp4_bank_t *bank, const void *packed_mx,
+                                              float shared_weight, uint16_t *y, void *ws,
+                                              size_t ws_bytes, cudaEvent_t *events, int n_events,
+                                              cudaStream_t stream);
+
 size_t moe_packed_mx_bank_size(int H, int I, int E, int has_shared);
 
 /*
