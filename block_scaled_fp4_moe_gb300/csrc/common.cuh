@@ -126,9 +126,10 @@ inline void fused_router_tiling(int H, int E, int *groups, int *chunks, int *row
 struct WsLayout {
     size_t route_part, topk_ids, topk_w, offsets, sorted_tok, sorted_slot, inv_pos, active, passes, passes4, passesw,
         passesw4, x16, xundo,
-        gpart, h16, hundo, ypart, counters, xstage, ystage, fz_rpart, fz_h32, fz_yent, mx_xq, mx_xs, mx_h32, mx_hq,
-        mx_hs, mx_y, total;
+        gpart, h16, hundo, ypart, counters, xstage, ystage, fz_rpart, fz_h32, fz_yent, mx_xq, mx_xs, mx_gu, mx_h32,
+        mx_hq, mx_hs, mx_y, total;
     int n_kc_gu, n_kc_dn;
+    int mx_kc_gu;          // MXFP8 variant: K chunks of the gate/up GEMM
 
     static WsLayout make(int T, int H, int I, int E, int k, int S) {
         WsLayout L{};
@@ -169,9 +170,29 @@ struct WsLayout {
             L.fz_h32 = take(entries * (size_t)I * sizeof(float));
             L.fz_yent = take(entries * (size_t)H * sizeof(float));
         }
-        // MXFP8 variant: quantised x and h, fp32 h and per-entry outputs
+        // MXFP8 variant: quantised x and h, the gate/up GEMM's K-chunk sums,
+        // fp32 h and per-entry outputs.  The gate/up GEMM splits K into 1, 2
+        // or 4 chunks (a function of the shapes only): the count whose CTAs
+        // (128-row tiles = active experts x I/64, times the chunks) fill the
+        // 3 x 152 CTA slots of its waves best; ties go to fewer chunks.
+        L.mx_kc_gu = 1;
+        if (H % 128 == 0 && I % 64 == 0) {
+            const long long tiles = active * (I / 64), slots = 3LL * kFusedGridTarget;
+            double best = 0.0;
+            for (int kc = 1; kc <= 4; kc *= 2) {
+                if ((H / 128) % kc)
+                    break;
+                const long long ctas = tiles * kc;
+                const double fill = (double)ctas / (double)(((ctas + slots - 1) / slots) * slots);
+                if (fill > best + 1e-9) {
+                    best = fill;
+                    L.mx_kc_gu = kc;
+                }
+            }
+        }
         L.mx_xq = take((size_t)T * H);
         L.mx_xs = take((size_t)T * (H / 32));
+        L.mx_gu = take((size_t)L.mx_kc_gu * entries * 2 * (size_t)I * sizeof(float));
         L.mx_h32 = take(entries * (size_t)I * sizeof(float));
         L.mx_hq = take(entries * (size_t)I);
         L.mx_hs = take(entries * (size_t)(I / 32));

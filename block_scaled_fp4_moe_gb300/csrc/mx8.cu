@@ -37,7 +37,7 @@
 // 16-byte chunk then holds two pieces whose slots are 32 apart, so the
 // 8-byte shared stores of a warp cover 32 consecutive slots.  Scale-factor
 // regions start on 32-column (A) and 16-column (B) boundaries of the CTA's
-// 256-column allocation (two CTAs per SM).
+// 128-column allocation (three CTAs per SM).
 #include <cuda_bf16.h>
 
 #include <atomic>
@@ -52,7 +52,7 @@ constexpr int kMxThreads = 128;
 constexpr int kMxN = 16;                       // MMA N: entries of one pass
 constexpr int kMxStageK = 128;                 // K elements per stage
 constexpr int kMxStages = 3;                   // shared-memory ring buffers
-constexpr int kMxRegStages = 6;                // stages of operands in flight in registers
+constexpr int kMxRegStages = 4;                // stages of operands in flight in registers
 constexpr int kMxLbo = 128;                    // bytes between core matrices adjacent in K
 constexpr int kMxSbo = 8 * 128;                // bytes between 8-row groups (8 K slots of 16 B)
 constexpr int kMxABytes = 128 * kMxStageK;     // 128 rows x 8 slots x 16 B
@@ -60,16 +60,16 @@ constexpr int kMxBBytes = kMxN * kMxStageK;    // 16 rows x 128 E4M3
 constexpr int kMxSfaBytes = 128 * 4;
 constexpr int kMxSfbBytes = kMxN * 4;
 constexpr int kMxStageBytes = kMxABytes + kMxBBytes + kMxSfaBytes + kMxSfbBytes;
-constexpr int kMxTmemCols = 256;               // D: columns 0..15; scale factors on aligned columns
+constexpr int kMxTmemCols = 128;               // D: columns 0..15; scale factors on aligned columns
 constexpr int kMxColSfa = 32;                  // SFA of buffer b: 4 columns at 32 + 32 b
-constexpr int kMxColSfb = 176;                 // SFB of buffer b: 1 column at 176 + 16 b
+constexpr int kMxColSfb = 48;                  // SFB of buffer b: 1 column at 48 + 32 b
+constexpr int kMxCtasPerSm = 3;                // 3 x 128 TMEM columns, 3 x 57 KB shared memory
 constexpr int kMxBlockBytes = 8192 + 512;      // one stage of a 128-row tile in the stage-ordered bank
 constexpr unsigned long long kMxWaitLimitNs = 200ull * 1000 * 1000;
 // at least 80 KB, so that no more than two CTAs (2 x 256 TMEM columns) share an SM
-constexpr size_t kMxSmemNeed = (size_t)kMxStages * kMxStageBytes + 64;
-constexpr size_t kMxSmem = kMxSmemNeed > 80 * 1024 ? kMxSmemNeed : 80 * 1024;
+constexpr size_t kMxSmem = (size_t)kMxStages * kMxStageBytes + 64;
 
-static_assert(kMxColSfa + 32 * (kMxStages - 1) + 4 <= kMxColSfb && kMxColSfb + 16 * kMxStages <= kMxTmemCols,
+static_assert(kMxColSfb + 32 * (kMxStages - 1) + 1 <= kMxTmemCols && kMxCtasPerSm * kMxTmemCols <= 512,
               "TMEM columns");
 static_assert((size_t)128 * 17 * 4 <= (size_t)kMxStageBytes, "epilogue buffer fits a stage");
 
@@ -122,11 +122,15 @@ struct MxGemmArgs {
     const uint8_t *asc;         // E8M0 scales [act_rows][K/32]
     const Pass *passes;         // passes of <= 16 entries
     const int32_t *sorted_tok;  // gate/up: entry -> activation row (token); down: null (row = entry)
-    float *out;                 // gate/up: h [entries][I]; down: Y [entries][H]
+    float *out;                 // [kc][entries][rows]: per K chunk, the sums of every weight row
+                                // (gate/up: g then u, 2I columns; down: Y, H columns)
     uint32_t *hdr;
     int tiles;                  // 128-row tiles per expert: I/64 (gate/up) or H/128 (down)
     int K;                      // H (gate/up) or I (down)
-    int out_ld;                 // I (gate/up) or H (down)
+    int half;                   // gate/up: I (up rows start there); down: 0
+    int out_ld;                 // 2I (gate/up) or H (down)
+    int kc;                     // K chunks (split K): blockIdx.x = tile * kc + chunk
+    size_t kstride;             // floats between the chunks' outputs
     int n_tot;                  // experts in the bank
     int act_rows;               // rows of aq: T (gate/up) or entries (down)
     int entries;                // T * (k + S)
@@ -135,7 +139,7 @@ struct MxGemmArgs {
 // ------------------------------------------------------------------ GEMM
 
 template <bool GATEUP>
-__global__ void __launch_bounds__(kMxThreads, 1) mx8_gemm_kernel(const __grid_constant__ MxGemmArgs a) {
+__global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(const __grid_constant__ MxGemmArgs a) {
     extern __shared__ __align__(1024) uint8_t mx_smem[];
     __shared__ uint32_t s_taddr;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -145,7 +149,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx8_gemm_kernel(const __grid_co
     if ((int)blockIdx.y >= n_pass)
         return;
     const Pass ps = a.passes[blockIdx.y];
-    const int tile = blockIdx.x;
+    const int tile = blockIdx.x / a.kc, chunk = blockIdx.x - tile * a.kc;
     // the pass and its activation rows must lie inside the buffers
     {
         int bad = ps.expert < 0 || ps.expert >= a.n_tot || ps.count < 1 || ps.count > kMxN || ps.begin < 0 ||
@@ -180,15 +184,16 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx8_gemm_kernel(const __grid_co
     // block, 16 bytes of its scales (tid < 32); B row tid / 8, 16-byte slot
     // tid % 8; SFB row tid (< 16)
     const int K32 = a.K / 32;
-    const int nst = a.K / kMxStageK;
-    const uint8_t *wblk = a.blocks + ((size_t)ps.expert * a.tiles + tile) * nst * kMxBlockBytes;
+    const int nst = a.K / kMxStageK / a.kc;          // stages of this chunk
+    const int s_first = chunk * nst;
+    const uint8_t *wblk = a.blocks + (((size_t)ps.expert * a.tiles + tile) * a.kc * nst + s_first) * kMxBlockBytes;
     auto arow = [&](int n) {
         const int e = ps.begin + min(n, ps.count - 1);
         return GATEUP ? a.sorted_tok[e] : e;
     };
     const int slot = tid & 7, r0 = tid >> 3;
-    const uint8_t *asrc = a.aq + (size_t)arow(r0) * a.K + slot * 16;
-    const uint8_t *sfb_src = a.asc + (size_t)arow(tid & 15) * K32;
+    const uint8_t *asrc = a.aq + (size_t)arow(r0) * a.K + (size_t)s_first * kMxStageK + slot * 16;
+    const uint8_t *sfb_src = a.asc + (size_t)arow(tid & 15) * K32 + s_first * 4;
     const uint32_t sbase = smem_addr(mx_smem);
 
     // every operand of a stage arrives through registers, kMxRegStages
@@ -258,7 +263,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx8_gemm_kernel(const __grid_co
         const uint8_t *st = mx_smem + (size_t)b * kMxStageBytes;
         const uint32_t *sfa = reinterpret_cast<const uint32_t *>(st + kMxABytes + kMxBBytes);
         const uint32_t *sfb = sfa + 128;
-        const uint32_t colA = (uint32_t)(kMxColSfa + 32 * b), colB = (uint32_t)(kMxColSfb + 16 * b);
+        const uint32_t colA = (uint32_t)(kMxColSfa + 32 * b), colB = (uint32_t)(kMxColSfb + 32 * b);
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(tmem + lane_base + colA),
                      "r"(sfa[lane]), "r"(sfa[lane + 32]), "r"(sfa[lane + 64]), "r"(sfa[lane + 96])
@@ -303,24 +308,16 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx8_gemm_kernel(const __grid_co
               "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
             : "r"(tmem + ((uint32_t)(warp * 32) << 16)));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-        const int r = tid;                  // MMA row = TMEM lane
-        if (GATEUP) {
-            // rows 0..63 hold g, 64..127 the matching u: pass u through shared memory
-            float *ub = reinterpret_cast<float *>(mx_smem);
-            if (r >= 64)
-                for (int n = 0; n < kMxN; ++n)
-                    ub[(r - 64) * 17 + n] = __uint_as_float(v[n]);
-            __syncthreads();
-            if (r < 64) {
-                for (int n = 0; n < ps.count; ++n) {
-                    const float g = __uint_as_float(v[n]), u = ub[r * 17 + n];
-                    a.out[(size_t)(ps.begin + n) * a.out_ld + tile * 64 + r] = g / (1.0f + expf(-g)) * u;
-                }
-            }
-        } else {
-            for (int n = 0; n < ps.count; ++n)
-                a.out[(size_t)(ps.begin + n) * a.out_ld + tile * 128 + r] = __uint_as_float(v[n]);
-        }
+        // MMA row r = TMEM lane = weight row of the tile: gate/up rows 0..63
+        // are gate rows 64 tile.., 64..127 the up rows; output column = that
+        // weight row's index
+        const int r = tid;
+        const int col = GATEUP ? (r < 64 ? tile * 64 + r : a.half + tile * 64 + r - 64) : tile * 128 + r;
+        float *dst = a.out + chunk * a.kstride + (size_t)ps.begin * a.out_ld + col;
+#pragma unroll
+        for (int n = 0; n < kMxN; ++n)
+            if (n < ps.count)
+                dst[(size_t)n * a.out_ld] = __uint_as_float(v[n]);
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -330,28 +327,12 @@ __global__ void __launch_bounds__(kMxThreads, 1) mx8_gemm_kernel(const __grid_co
 
 // ------------------------------------------------------------ quantisation
 
-__device__ __forceinline__ float load_act(const uint16_t *p) {
-    return __uint_as_float((uint32_t)*p << 16);   // bf16
-}
-__device__ __forceinline__ float load_act(const float *p) { return __ldcg(p); }
-
-// MXFP8 (OCP MX v1.0) of rows x cols values, one warp per block of 32: the
-// shared exponent is floor(log2(max |v|)) - 8 (E4M3's largest exponent),
-// kept in [-127, 127], -127 for an all-zero block; each element is v / 2^e
-// rounded to E4M3, ties to even, saturating at 448.  v / 2^e is exact in
-// fp32, so the codes are those of the exact quotient.
-template <typename In>
-__global__ void __launch_bounds__(256) mx8_quant_kernel(const In *__restrict__ in, int rows, int cols,
-                                                        uint8_t *__restrict__ codes, uint8_t *__restrict__ scales) {
-    pdl_wait();
-    pdl_trigger();
-    const int lane = threadIdx.x & 31;
-    const long long blk = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-    const int per_row = cols / 32;
-    if (blk >= (long long)rows * per_row)
-        return;
-    const size_t i = (size_t)blk * 32 + lane;
-    const float v = load_act(in + i);
+// MXFP8 (OCP MX v1.0) of one block of 32 values, one per lane: the shared
+// exponent is floor(log2(max |v|)) - 8 (E4M3's largest exponent), kept in
+// [-127, 127], -127 for an all-zero block; each element is v / 2^e rounded
+// to E4M3, ties to even, saturating at 448.  v / 2^e is exact in fp32, so the
+// codes are those of the exact quotient.  Lane 0 writes the scale byte.
+__device__ __forceinline__ void mx8_quant_block(float v, uint8_t *code, uint8_t *scale) {
     const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
     const int ef = (int)(amax >> 23);           // biased exponent of max |v| (0: zero or subnormal)
     int se = ef == 0 ? -127 : ef - 127 - 8;
@@ -359,9 +340,46 @@ __global__ void __launch_bounds__(256) mx8_quant_kernel(const In *__restrict__ i
     const float q = v * exp2i(-se);             // -se <= 127: a normal power of two
     uint16_t pair;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.0f), "f"(q));
-    codes[i] = (uint8_t)(pair & 0xFF);
-    if (lane == 0)
-        scales[blk] = (uint8_t)(se + 127);
+    *code = (uint8_t)(pair & 0xFF);
+    if ((threadIdx.x & 31) == 0)
+        *scale = (uint8_t)(se + 127);
+}
+
+// x (bf16 [T][H]) to MXFP8, one warp per block of 32.
+__global__ void __launch_bounds__(256) mx8_quant_kernel(const uint16_t *__restrict__ x, int rows, int cols,
+                                                        uint8_t *__restrict__ codes, uint8_t *__restrict__ scales) {
+    pdl_wait();
+    pdl_trigger();
+    const long long blk = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (blk >= (long long)rows * (cols / 32))
+        return;
+    const size_t i = (size_t)blk * 32 + (threadIdx.x & 31);
+    mx8_quant_block(__uint_as_float((uint32_t)x[i] << 16), codes + i, scales + blk);
+}
+
+// h = silu(g) * u from the gate/up GEMM's K-chunk sums (g and u each summed
+// over the chunks in chunk order), written in fp32 and as MXFP8; one warp per
+// block of 32 of an entry's h.
+__global__ void __launch_bounds__(256) mx8_hfin_kernel(const float *__restrict__ gu, int kc, size_t kstride,
+                                                       int entries, int I, float *__restrict__ h32,
+                                                       uint8_t *__restrict__ codes, uint8_t *__restrict__ scales) {
+    pdl_wait();
+    pdl_trigger();
+    const long long blk = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const int per = I / 32;
+    if (blk >= (long long)entries * per)
+        return;
+    const int e = (int)(blk / per), j = (int)(blk - (long long)e * per);
+    const int i = 32 * j + (threadIdx.x & 31);
+    const float *src = gu + (size_t)e * 2 * I + i;
+    float g = 0.0f, u = 0.0f;
+    for (int c = 0; c < kc; ++c) {
+        g += __ldcg(src + c * kstride);
+        u += __ldcg(src + c * kstride + I);
+    }
+    const float h = g / (1.0f + expf(-g)) * u;
+    h32[(size_t)e * I + i] = h;
+    mx8_quant_block(h, codes + (size_t)e * I + i, scales + blk);
 }
 
 // Stage-ordered copy of one section of the bank: one thread per 8-byte code
@@ -428,7 +446,7 @@ cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cud
     uint32_t *hdr = ws_at<uint32_t>(ws, 0);
     uint8_t *xq = ws_at<uint8_t>(ws, L.mx_xq), *xs = ws_at<uint8_t>(ws, L.mx_xs);
     uint8_t *hq = ws_at<uint8_t>(ws, L.mx_hq), *hs = ws_at<uint8_t>(ws, L.mx_hs);
-    float *h32 = ws_at<float>(ws, L.mx_h32), *yent = ws_at<float>(ws, L.mx_y);
+    float *h32 = ws_at<float>(ws, L.mx_h32), *yent = ws_at<float>(ws, L.mx_y), *gu = ws_at<float>(ws, L.mx_gu);
     static std::atomic<int> attr_set{0};
     if (!attr_set.load()) {
         cudaError_t err;
@@ -440,8 +458,7 @@ cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cud
         attr_set.store(1);
     }
     const int xblocks = T * (H / 32), hblocks = entries * (I / 32);
-    cudaError_t err = launch_pdl(mx8_quant_kernel<uint16_t>, dim3((xblocks + 7) / 8), dim3(256), 0, stream, p.x, T, H,
-                                 xq, xs);
+    cudaError_t err = launch_pdl(mx8_quant_kernel, dim3((xblocks + 7) / 8), dim3(256), 0, stream, p.x, T, H, xq, xs);
     if (err != cudaSuccess)
         return err;
     if (ev && (err = cudaEventRecord(ev[0], stream)) != cudaSuccess)
@@ -452,21 +469,24 @@ cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cud
     g.asc = xs;
     g.passes = ws_at<Pass>(ws, L.passesw4);
     g.sorted_tok = ws_at<int32_t>(ws, L.sorted_tok);
-    g.out = h32;
+    g.out = gu;
     g.hdr = hdr;
     g.tiles = I / 64;
     g.K = H;
-    g.out_ld = I;
+    g.half = I;
+    g.kc = L.mx_kc_gu;
+    g.kstride = (size_t)entries * 2 * I;
+    g.out_ld = 2 * I;
     g.n_tot = n_tot;
     g.act_rows = T;
     g.entries = entries;
-    if ((err = launch_pdl(mx8_gemm_kernel<true>, dim3(I / 64, max_pass), dim3(kMxThreads), kMxSmem, stream, g)) !=
-        cudaSuccess)
+    if ((err = launch_pdl(mx8_gemm_kernel<true>, dim3(I / 64 * g.kc, max_pass), dim3(kMxThreads), kMxSmem, stream,
+                          g)) != cudaSuccess)
         return err;
     if (ev && (err = cudaEventRecord(ev[1], stream)) != cudaSuccess)
         return err;
-    if ((err = launch_pdl(mx8_quant_kernel<float>, dim3((hblocks + 7) / 8), dim3(256), 0, stream, (const float *)h32,
-                          entries, I, hq, hs)) != cudaSuccess)
+    if ((err = launch_pdl(mx8_hfin_kernel, dim3((hblocks + 7) / 8), dim3(256), 0, stream, (const float *)gu, g.kc,
+                          g.kstride, entries, I, h32, hq, hs)) != cudaSuccess)
         return err;
     MxGemmArgs d = g;
     d.blocks = p.packed_mx + mx8_dn_offset(H, I, n_tot);
@@ -476,6 +496,9 @@ cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cud
     d.out = yent;
     d.tiles = H / 128;
     d.K = I;
+    d.half = 0;
+    d.kc = 1;
+    d.kstride = 0;
     d.out_ld = H;
     d.act_rows = entries;
     if ((err = launch_pdl(mx8_gemm_kernel<false>, dim3(H / 128, max_pass), dim3(kMxThreads), kMxSmem, stream, d)) !=
