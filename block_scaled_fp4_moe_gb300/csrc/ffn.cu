@@ -814,6 +814,20 @@ combine_kernel(const float *__restrict__ part, int n_kc, int n_entries, const in
         return;
     const size_t kstride = (size_t)n_entries * H;
     float s = 0.0f;
+    if (n_kc == 1) {                  // one partial per slot: all loads in flight at once
+        float v[kMaxSlots];
+#pragma unroll
+        for (int i = 0; i < kMaxSlots; ++i)
+            if (i < kps)
+                v[i] = part[(size_t)spos[i] * H + n];
+#pragma unroll
+        for (int i = 0; i < kMaxSlots; ++i)
+            if (i < kps)
+                s = fmaf(sw[i], v[i], s);
+        const __nv_bfloat16 b = __float2bfloat16_rn(s);
+        y[(size_t)t * H + n] = *reinterpret_cast<const uint16_t *>(&b);
+        return;
+    }
     for (int s0 = 0; s0 < kps; s0 += 4) {
         float v[4][kMaxKChunks];
 #pragma unroll

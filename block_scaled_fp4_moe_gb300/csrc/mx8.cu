@@ -16,9 +16,13 @@
 // outputs Y), combine (ffn.cu's combine_kernel).
 //
 // GEMM CTA: 128 weight rows x one pass of <= 16 entries (MMA M = 128,
-// N = 16), K in stages of 128 (four MMAs of K = 32).  Every operand of a
-// stage is loaded into registers kMxRegStages stages ahead and then stored
-// into a 3-buffer shared-memory ring in the canonical
+// N = 16), K in stages of 128 (four MMAs of K = 32), warp-specialised: four
+// producer warps load every operand of a stage into registers kMxRegStages
+// stages ahead, store it into a 3-buffer shared-memory ring, write its scale
+// factors into TMEM and arrive on the buffer's "full" mbarrier; a fifth warp
+// waits on it, issues the four MMAs and commits them to the buffer's "empty"
+// mbarrier, which the producers wait on before refilling the buffer.  The
+// shared operands use the
 // K-major no-swizzle layout: core matrices of 8 rows x 16 bytes, adjacent in
 // K 128 bytes apart, 8-row groups 1,024 bytes apart.  An E2M1 operand of
 // kind::mxf8f6f4 occupies a 16-byte slot per 16 elements with the 8 bytes of
@@ -48,30 +52,28 @@
 namespace moe {
 namespace {
 
-constexpr int kMxThreads = 128;
+constexpr int kMxProducers = 128;              // warps 0..3 load and stage the operands
+constexpr int kMxThreads = kMxProducers + 32;  // warp 4 issues the MMAs
 constexpr int kMxN = 16;                       // MMA N: entries of one pass
 constexpr int kMxStageK = 128;                 // K elements per stage
 constexpr int kMxStages = 3;                   // shared-memory ring buffers
-constexpr int kMxRegStages = 4;                // stages of operands in flight in registers
+constexpr int kMxRegStages = 3;                // stages of operands in flight in registers
 constexpr int kMxLbo = 128;                    // bytes between core matrices adjacent in K
 constexpr int kMxSbo = 8 * 128;                // bytes between 8-row groups (8 K slots of 16 B)
 constexpr int kMxABytes = 128 * kMxStageK;     // 128 rows x 8 slots x 16 B
 constexpr int kMxBBytes = kMxN * kMxStageK;    // 16 rows x 128 E4M3
-constexpr int kMxSfaBytes = 128 * 4;
-constexpr int kMxSfbBytes = kMxN * 4;
-constexpr int kMxStageBytes = kMxABytes + kMxBBytes + kMxSfaBytes + kMxSfbBytes;
+constexpr int kMxStageBytes = kMxABytes + kMxBBytes;
 constexpr int kMxTmemCols = 128;               // D: columns 0..15; scale factors on aligned columns
 constexpr int kMxColSfa = 32;                  // SFA of buffer b: 4 columns at 32 + 32 b
 constexpr int kMxColSfb = 48;                  // SFB of buffer b: 1 column at 48 + 32 b
-constexpr int kMxCtasPerSm = 3;                // 3 x 128 TMEM columns, 3 x 57 KB shared memory
+constexpr int kMxCtasPerSm = 3;                // 3 x 128 TMEM columns, 3 x 55 KB shared memory
 constexpr int kMxBlockBytes = 8192 + 512;      // one stage of a 128-row tile in the stage-ordered bank
 constexpr unsigned long long kMxWaitLimitNs = 200ull * 1000 * 1000;
 // at least 80 KB, so that no more than two CTAs (2 x 256 TMEM columns) share an SM
-constexpr size_t kMxSmem = (size_t)kMxStages * kMxStageBytes + 64;
+constexpr size_t kMxSmem = (size_t)kMxStages * kMxStageBytes + 2 * kMxStages * 8;   // buffers, full / empty barriers
 
 static_assert(kMxColSfb + 32 * (kMxStages - 1) + 1 <= kMxTmemCols && kMxCtasPerSm * kMxTmemCols <= 512,
               "TMEM columns");
-static_assert((size_t)128 * 17 * 4 <= (size_t)kMxStageBytes, "epilogue buffer fits a stage");
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -164,118 +166,125 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
             return;
         }
     }
-    uint64_t *mbar = reinterpret_cast<uint64_t *>(mx_smem + (size_t)kMxStages * kMxStageBytes);   // kMxStages barriers
+    // buffer b: full[b] completes when the 128 producers have staged a stage
+    // in it (shared operands, scale factors in TMEM); empty[b] when the MMAs
+    // reading it are done (tcgen05.commit)
+    uint64_t *full = reinterpret_cast<uint64_t *>(mx_smem + (size_t)kMxStages * kMxStageBytes);
+    uint64_t *empty = full + kMxStages;
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&s_taddr)),
                      "n"(kMxTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     if (tid == 0) {
-        for (int b = 0; b < kMxStages; ++b)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(mbar + b)));
+        for (int b = 0; b < kMxStages; ++b) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(full + b)), "r"(kMxProducers));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(empty + b)));
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = s_taddr;
-
-    // this thread's copies: 8-byte code pieces tid + 128 i of the stage's
-    // block, 16 bytes of its scales (tid < 32); B row tid / 8, 16-byte slot
-    // tid % 8; SFB row tid (< 16)
     const int K32 = a.K / 32;
     const int nst = a.K / kMxStageK / a.kc;          // stages of this chunk
     const int s_first = chunk * nst;
-    const uint8_t *wblk = a.blocks + (((size_t)ps.expert * a.tiles + tile) * a.kc * nst + s_first) * kMxBlockBytes;
-    auto arow = [&](int n) {
-        const int e = ps.begin + min(n, ps.count - 1);
-        return GATEUP ? a.sorted_tok[e] : e;
-    };
-    const int slot = tid & 7, r0 = tid >> 3;
-    const uint8_t *asrc = a.aq + (size_t)arow(r0) * a.K + (size_t)s_first * kMxStageK + slot * 16;
-    const uint8_t *sfb_src = a.asc + (size_t)arow(tid & 15) * K32 + s_first * 4;
     const uint32_t sbase = smem_addr(mx_smem);
-
-    // every operand of a stage arrives through registers, kMxRegStages
-    // stages ahead.  Weight codes: 16-byte chunk c = tid + 128 i (i < 4) of
-    // the block holds the pieces q0 = 64 (c / 32) + c % 32 and q0 + 32 of the
-    // shared-memory image (so each 8-byte store of a warp covers 32
-    // consecutive slots); weight scales: chunks of threads 0..31; activation
-    // codes: 16 bytes of row tid / 8, slot tid % 8; activation scales: 4 bytes
-    // of row tid (< 16).
-    const uint64_t pol = l2_evict_first_policy();
-    uint4 rq[kMxRegStages][4];
-    uint4 rsf[kMxRegStages];
-    uint4 rb[kMxRegStages];
-    uint32_t rsb[kMxRegStages];
-    auto load_stage = [&](int s, uint4(&q)[4], uint4 &sf, uint4 &bq, uint32_t &sb) {
-        const uint8_t *blk = wblk + (size_t)s * kMxBlockBytes;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            q[i] = ld_stream16(blk + 16 * (tid + kMxThreads * i), pol);
-        if (tid < 32)
-            sf = ld_stream16(blk + 8192 + 16 * tid, pol);
-        bq = __ldg(reinterpret_cast<const uint4 *>(asrc + (size_t)s * kMxStageK));
-        if (tid < kMxN)
-            sb = __ldg(reinterpret_cast<const uint32_t *>(sfb_src + s * 4));
-    };
-    auto store_stage = [&](int s, const uint4(&q)[4], const uint4 &sf, const uint4 &bq, uint32_t sb) {
-        uint8_t *st = mx_smem + (size_t)(s % kMxStages) * kMxStageBytes;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int c = tid + kMxThreads * i;
-            const int q0 = 64 * (c >> 5) + (c & 31);
-            *reinterpret_cast<uint2 *>(st + 16 * q0) = make_uint2(q[i].x, q[i].y);
-            *reinterpret_cast<uint2 *>(st + 16 * (q0 + 32)) = make_uint2(q[i].z, q[i].w);
-        }
-        if (tid < 32)
-            *reinterpret_cast<uint4 *>(st + kMxABytes + kMxBBytes + 16 * tid) = sf;
-        *reinterpret_cast<uint4 *>(st + kMxABytes + (r0 >> 3) * kMxSbo + slot * kMxLbo + (r0 & 7) * 16) = bq;
-        if (tid < kMxN)
-            *reinterpret_cast<uint32_t *>(st + kMxABytes + kMxBBytes + kMxSfaBytes + 4 * tid) = sb;
-    };
-
     bool ok = true;
-#pragma unroll
-    for (int k = 0; k < kMxRegStages; ++k)
-        if (k < nst)
-            load_stage(k, rq[k], rsf[k], rb[k], rsb[k]);
-    for (int s0 = 0; s0 < nst && ok; s0 += kMxRegStages) {
-#pragma unroll
-        for (int k = 0; k < kMxRegStages; ++k) {
-        const int s = s0 + k;
-        if (s >= nst)
-            break;
-        // shared buffer s % kMxStages was read by the MMAs of stage s - kMxStages
-        if (s >= kMxStages)
-            ok = ok && mbar_wait(smem_addr(mbar + (s - kMxStages) % kMxStages), ((s - kMxStages) / kMxStages) & 1);
-        if (ok)
-            store_stage(s, rq[k], rsf[k], rb[k], rsb[k]);
-        if (s + kMxRegStages < nst)
-            load_stage(s + kMxRegStages, rq[k], rsf[k], rb[k], rsb[k]);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        if (__syncthreads_or(!ok)) {
-            ok = false;
-            break;
-        }
-        // scale factors of stage s into this buffer's TMEM columns, every quarter
-        const int b = s % kMxStages;
-        const uint8_t *st = mx_smem + (size_t)b * kMxStageBytes;
-        const uint32_t *sfa = reinterpret_cast<const uint32_t *>(st + kMxABytes + kMxBBytes);
-        const uint32_t *sfb = sfa + 128;
-        const uint32_t colA = (uint32_t)(kMxColSfa + 32 * b), colB = (uint32_t)(kMxColSfb + 32 * b);
+
+    if (warp < kMxProducers / 32) {
+        // ---- producers.  Every operand of a stage is loaded into registers
+        // kMxRegStages stages ahead: weight codes as 16-byte chunks c = tid +
+        // 128 i (i < 4) of the block, holding the pieces q0 = 64 (c / 32) +
+        // c % 32 and q0 + 32 of the shared-memory image (each 8-byte store of
+        // a warp then covers 32 consecutive slots); the scale words of rows
+        // lane + 32 q (q < 4); 16 bytes of activation row tid / 8, slot tid %
+        // 8; the scale word of activation row lane % 16.  Each warp writes the
+        // scale factors into its own 32-lane quarter of TMEM.
+        const uint8_t *wblk =
+            a.blocks + (((size_t)ps.expert * a.tiles + tile) * a.kc * nst + s_first) * kMxBlockBytes;
+        auto arow = [&](int n) {
+            const int e = ps.begin + min(n, ps.count - 1);
+            return GATEUP ? a.sorted_tok[e] : e;
+        };
+        const int slot = tid & 7, r0 = tid >> 3;
+        const uint8_t *asrc = a.aq + (size_t)arow(r0) * a.K + (size_t)s_first * kMxStageK + slot * 16;
+        const uint8_t *sfb_src = a.asc + (size_t)arow(lane & 15) * K32 + s_first * 4;
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(tmem + lane_base + colA),
-                     "r"(sfa[lane]), "r"(sfa[lane + 32]), "r"(sfa[lane + 64]), "r"(sfa[lane + 96])
-                     : "memory");
-        asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(tmem + lane_base + colB),
-                     "r"(sfb[lane & 15])
-                     : "memory");
-        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-        __syncthreads();
-        if (tid == 0) {
+        const uint64_t pol = l2_evict_first_policy();
+        uint4 rq[kMxRegStages][4];
+        uint32_t rsa[kMxRegStages][4];
+        uint4 rb[kMxRegStages];
+        uint32_t rsb[kMxRegStages];
+        auto load_stage = [&](int s, uint4(&q)[4], uint32_t(&sa)[4], uint4 &bq, uint32_t &sb) {
+            const uint8_t *blk = wblk + (size_t)s * kMxBlockBytes;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                q[i] = ld_stream16(blk + 16 * (tid + kMxProducers * i), pol);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                sa[i] = __ldg(reinterpret_cast<const uint32_t *>(blk + 8192 + 4 * (lane + 32 * i)));
+            bq = __ldg(reinterpret_cast<const uint4 *>(asrc + (size_t)s * kMxStageK));
+            sb = __ldg(reinterpret_cast<const uint32_t *>(sfb_src + s * 4));
+        };
+#pragma unroll
+        for (int k = 0; k < kMxRegStages; ++k)
+            if (k < nst)
+                load_stage(k, rq[k], rsa[k], rb[k], rsb[k]);
+        for (int s0 = 0; s0 < nst && ok; s0 += kMxRegStages) {
+#pragma unroll
+            for (int k = 0; k < kMxRegStages; ++k) {
+                const int s = s0 + k;
+                if (s >= nst)
+                    break;
+                const int b = s % kMxStages;
+                // buffer b and its TMEM columns were read by the MMAs of stage s - kMxStages
+                if (s >= kMxStages &&
+                    !__all_sync(0xffffffffu, mbar_wait(smem_addr(empty + b), ((s - kMxStages) / kMxStages) & 1))) {
+                    ok = false;           // warp-uniform: the tcgen05 stores below are .sync.aligned
+                    break;
+                }
+                uint8_t *st = mx_smem + (size_t)b * kMxStageBytes;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int c = tid + kMxProducers * i;
+                    const int q0 = 64 * (c >> 5) + (c & 31);
+                    *reinterpret_cast<uint2 *>(st + 16 * q0) = make_uint2(rq[k][i].x, rq[k][i].y);
+                    *reinterpret_cast<uint2 *>(st + 16 * (q0 + 32)) = make_uint2(rq[k][i].z, rq[k][i].w);
+                }
+                *reinterpret_cast<uint4 *>(st + kMxABytes + (r0 >> 3) * kMxSbo + slot * kMxLbo + (r0 & 7) * 16) =
+                    rb[k];
+                const uint32_t colA = (uint32_t)(kMxColSfa + 32 * b), colB = (uint32_t)(kMxColSfb + 32 * b);
+                asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                 tmem + lane_base + colA),
+                             "r"(rsa[k][0]), "r"(rsa[k][1]), "r"(rsa[k][2]), "r"(rsa[k][3])
+                             : "memory");
+                asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(tmem + lane_base + colB),
+                             "r"(rsb[k])
+                             : "memory");
+                if (s + kMxRegStages < nst)
+                    load_stage(s + kMxRegStages, rq[k], rsa[k], rb[k], rsb[k]);
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(full + b)) : "memory");
+            }
+        }
+        // the last commit covers every MMA of the CTA
+        if (ok)
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(smem_addr(empty + (nst - 1) % kMxStages), ((nst - 1) / kMxStages) & 1));
+    } else if (lane == 0) {
+        // ---- the MMA issuer
+        for (int s = 0; s < nst; ++s) {
+            const int b = s % kMxStages;
+            if (!mbar_wait(smem_addr(full + b), (s / kMxStages) & 1)) {
+                ok = false;
+                break;
+            }
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t colA = (uint32_t)(kMxColSfa + 32 * b), colB = (uint32_t)(kMxColSfb + 32 * b);
             const uint32_t sa = sbase + (uint32_t)(b * kMxStageBytes), sb = sa + kMxABytes;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -288,19 +297,16 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
                     : "memory");
             }
             asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                             smem_addr(mbar + b))
+                             smem_addr(empty + b))
                          : "memory");
         }
-        }
     }
-    if (ok)
-        ok = mbar_wait(smem_addr(mbar + (nst - 1) % kMxStages), ((nst - 1) / kMxStages) & 1);
     ok = !__syncthreads_or(!ok);
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     if (!ok) {
         if (tid == 0)
             record_status(a.hdr, MOE_ERR_DEVICE_TIMEOUT);
-    } else {
+    } else if (warp < kMxProducers / 32) {
         uint32_t v[16];
         asm volatile(
             "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
