@@ -469,9 +469,21 @@ moe_status_t layer_forward_mxfp8(const uint16_t *x, const float *router_w, const
     const GroupOut go = group_out_for(ws, L, H);
     if (ev && cudaEventRecord(ev[0], stream) != cudaSuccess)
         return MOE_ERR_CUDA;
-    cudaError_t err = launch_route(x, router_w, logit_bias, T, H, E, top_k, S, shared_weight, ids, w, ws, L, true, go,
-                                   stream);
-    if (err != cudaSuccess)
+    // routing and grouping: for decode-sized T the routing phases of the
+    // single-launch kernel (one cooperative launch), else the two routing
+    // launches of the multi-launch path
+    cudaError_t err = cudaErrorCooperativeLaunchTooLarge;
+    if (T <= kFusedMaxTokens && fused_plan(T, H, I, E, top_k, S, sms).ok) {
+        FusedProblem fp{x, router_w, logit_bias, bank, shared_weight, nullptr, ids, w, T, top_k,
+                        nullptr, 0, nullptr, nullptr, 0, 0};
+        err = launch_fused(fp, ws, L, sms, stream, &go);
+        if (err != cudaSuccess && err != cudaErrorCooperativeLaunchTooLarge)
+            return MOE_ERR_CUDA;
+        (void)cudaGetLastError();
+    }
+    if (err != cudaSuccess &&
+        launch_route(x, router_w, logit_bias, T, H, E, top_k, S, shared_weight, ids, w, ws, L, true, go, stream) !=
+            cudaSuccess)
         return MOE_ERR_CUDA;
     if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess)
         return MOE_ERR_CUDA;

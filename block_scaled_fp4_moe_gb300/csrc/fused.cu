@@ -67,6 +67,8 @@ struct FusedArgs {
     int off_hundo, off_b;             // dynamic shared-memory offsets (bytes)
     const uint8_t *next_pf[3];        // next layer: router, shared gate/up, shared down (nullable)
     size_t next_pf_bytes[3];
+    Pass *x_passes;                   // routing only: the gate/up passes (one per active expert, <= 8 entries)
+    int32_t *x_sorted_tok, *x_inv_pos;   // routing only: sorted position -> token, entry -> sorted position
 };
 
 namespace {
@@ -1170,9 +1172,31 @@ __device__ void combine_share(const FusedArgs &a, const RouteState &rs) {
     }
 }
 
+// Routing only: CTA 0 writes the grouping every CTA derived (the passes of
+// one expert's entries, the sorted order and its inverse) for kernels that
+// run the expert projections themselves; 0 passes when the routing was
+// rejected.
+__device__ void route_export(const FusedArgs &a, const RouteState &rs, bool ok) {
+    const int n = a.T * (a.k + a.S);
+    if (ok) {
+        for (int i = threadIdx.x; i < n; i += NT) {
+            a.x_sorted_tok[i] = rs.sorted_tok[i];
+            a.x_inv_pos[i] = rs.inv_pos[i];
+        }
+        for (int p = threadIdx.x; p < rs.n_gu; p += NT)
+            a.x_passes[p] = rs.pgu[p];
+    }
+    if (threadIdx.x == 0) {
+        a.hdr[kHdrNumPassesW4] = ok ? (uint32_t)rs.n_gu : 0u;
+        a.hdr[kHdrNumPasses] = ok ? (uint32_t)rs.n_gu : 0u;
+    }
+}
+
 // ---------------------------------------------------------------- kernel
 
-template <bool FULL>
+// ROUTE_ONLY: phases R and T, then the grouping is exported (route_export)
+// and the CTAs leave; no expert weights are read.
+template <bool FULL, bool ROUTE_ONLY>
 __global__ void __launch_bounds__(NT, 1) fused_layer_kernel(const __grid_constant__ FusedArgs a) {
     uint8_t *smem = fz_smem;
     RouteState &rs = fz_rs;
@@ -1181,7 +1205,8 @@ __global__ void __launch_bounds__(NT, 1) fused_layer_kernel(const __grid_constan
     // read-only prefetches, then wait until the previous kernel on the stream
     // has completed (its outputs and the workspace are then ours); the next
     // kernel may be scheduled from here on
-    prefetch_shared_expert(a);
+    if constexpr (!ROUTE_ONLY)
+        prefetch_shared_expert(a);
     prefetch_router_tile(a);
     pdl_wait();
     pdl_trigger();
@@ -1193,13 +1218,17 @@ __global__ void __launch_bounds__(NT, 1) fused_layer_kernel(const __grid_constan
     phase_router(a, smem);                  // nothing else lives in shared memory yet
     stamp(a, 1);
     grid_arrive(a);
-    x_window_local(a, rs, reinterpret_cast<__half *>(smem));
+    if constexpr (!ROUTE_ONLY)
+        x_window_local(a, rs, reinterpret_cast<__half *>(smem));
     bool ok = grid_wait(a, (unsigned)G);
     stamp(a, 2);
     if (ok)
         ok = phase_route(a, rs, smem, smem + a.off_b);
     stamp(a, 3);
-    if (ok) {
+    if constexpr (ROUTE_ONLY) {
+        if (blockIdx.x == 0)
+            route_export(a, rs, ok);
+    } else if (ok) {
         // gate/up, then down: one copy of the streaming code runs both
 #pragma unroll 1
         for (int mode = kFfnGateUp; mode <= kFfnDown; ++mode) {
@@ -1316,7 +1345,7 @@ FusedPlan fused_plan(int T, int H, int I, int E, int k, int S, int grid) {
     return p;
 }
 
-template <bool FULL>
+template <bool FULL, bool ROUTE_ONLY>
 static cudaError_t launch_fused_t(const FusedArgs &args, int grid, size_t smem, cudaStream_t stream) {
     static std::atomic<int> set_bytes[64];
     int dev = 0;
@@ -1324,7 +1353,8 @@ static cudaError_t launch_fused_t(const FusedArgs &args, int grid, size_t smem, 
     if (err != cudaSuccess)
         return err;
     if (set_bytes[dev & 63].load() < (int)smem) {
-        err = cudaFuncSetAttribute(fused_layer_kernel<FULL>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        err = cudaFuncSetAttribute(fused_layer_kernel<FULL, ROUTE_ONLY>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)smem);
         if (err != cudaSuccess)
             return err;
         set_bytes[dev & 63].store((int)smem);
@@ -1341,10 +1371,11 @@ static cudaError_t launch_fused_t(const FusedArgs &args, int grid, size_t smem, 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, fused_layer_kernel<FULL>, args);
+    return cudaLaunchKernelEx(&cfg, fused_layer_kernel<FULL, ROUTE_ONLY>, args);
 }
 
-cudaError_t launch_fused(const FusedProblem &pr, void *ws, const WsLayout &L, int num_sms, cudaStream_t stream) {
+cudaError_t launch_fused(const FusedProblem &pr, void *ws, const WsLayout &L, int num_sms, cudaStream_t stream,
+                         const GroupOut *route_only) {
     const moe_mxfp4_bank_t &b = *pr.bank;
     const int H = b.hidden, I = b.inter, E = b.num_experts, S = b.has_shared;
     const FusedPlan plan = fused_plan(pr.T, H, I, E, pr.top_k, S, num_sms);
@@ -1355,8 +1386,8 @@ cudaError_t launch_fused(const FusedProblem &pr, void *ws, const WsLayout &L, in
     a.x = pr.x;
     a.wr = pr.router_w;
     a.bias = pr.bias;
-    a.gu = b.packed + PL.gu_offset;
-    a.dn = b.packed + PL.dn_offset;
+    a.gu = b.packed ? b.packed + PL.gu_offset : nullptr;     // routing only: no expert weights are read
+    a.dn = b.packed ? b.packed + PL.dn_offset : nullptr;
     a.y = pr.y;
     a.ids_out = pr.ids_out;
     a.w_out = pr.w_out;
@@ -1390,9 +1421,17 @@ cudaError_t launch_fused(const FusedProblem &pr, void *ws, const WsLayout &L, in
     a.next_pf_bytes[1] = pr.next_shared_gu_bytes;
     a.next_pf[2] = static_cast<const uint8_t *>(pr.next_shared_dn);
     a.next_pf_bytes[2] = pr.next_shared_dn_bytes;
+    if (route_only) {
+        a.x_passes = route_only->passesw4;
+        a.x_sorted_tok = route_only->sorted_tok;
+        a.x_inv_pos = route_only->inv_pos;
+        return launch_fused_t<false, true>(a, num_sms, plan.smem, stream);
+    }
+    if (!b.packed)
+        return cudaErrorInvalidValue;
     if (H % (64 * SB) == 0 && I % (64 * SB) == 0)
-        return launch_fused_t<true>(a, num_sms, plan.smem, stream);
-    return launch_fused_t<false>(a, num_sms, plan.smem, stream);
+        return launch_fused_t<true, false>(a, num_sms, plan.smem, stream);
+    return launch_fused_t<false, false>(a, num_sms, plan.smem, stream);
 }
 
 }  // namespace moe

@@ -116,7 +116,11 @@ struct FusedPlan {
     size_t off_hundo, off_b, smem;
 };
 FusedPlan fused_plan(int T, int H, int I, int E, int k, int S, int grid);
-cudaError_t launch_fused(const FusedProblem &p, void *ws, const WsLayout &L, int num_sms, cudaStream_t stream);
+// route_only (nullable): run only the routing phases and write the grouping
+// (passes of one expert's entries into route_only->passesw4, the sorted order
+// and its inverse, the pass count in the header) instead of the whole layer.
+cudaError_t launch_fused(const FusedProblem &p, void *ws, const WsLayout &L, int num_sms, cudaStream_t stream,
+                         const GroupOut *route_only = nullptr);
 cudaError_t launch_wait_selftest(uint32_t *hdr, cudaStream_t stream);
 
 // Byte offsets inside a repacked bank (pack.cu).
