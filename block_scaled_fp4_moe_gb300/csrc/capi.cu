@@ -475,7 +475,7 @@ moe_status_t layer_forward_mxfp8(const uint16_t *x, const float *router_w, const
     cudaError_t err = cudaErrorCooperativeLaunchTooLarge;
     if (T <= kFusedMaxTokens && fused_plan(T, H, I, E, top_k, S, sms).ok) {
         FusedProblem fp{x, router_w, logit_bias, bank, shared_weight, nullptr, ids, w, T, top_k,
-                        nullptr, 0, nullptr, nullptr, 0, 0};
+                        nullptr, 0, nullptr, nullptr, 0, 0, ws_at<uint8_t>(ws, L.mx_xq), ws_at<uint8_t>(ws, L.mx_xs)};
         err = launch_fused(fp, ws, L, sms, stream, &go);
         if (err != cudaSuccess && err != cudaErrorCooperativeLaunchTooLarge)
             return MOE_ERR_CUDA;
@@ -487,7 +487,7 @@ moe_status_t layer_forward_mxfp8(const uint16_t *x, const float *router_w, const
         return MOE_ERR_CUDA;
     if (ev && cudaEventRecord(ev[1], stream) != cudaSuccess)
         return MOE_ERR_CUDA;
-    const Mx8Problem pr{x, bank, static_cast<const uint8_t *>(packed_mx), w, y, T, top_k + S};
+    const Mx8Problem pr{x, bank, static_cast<const uint8_t *>(packed_mx), w, y, T, top_k + S, err == cudaSuccess};
     if ((err = launch_mx8_ffn(pr, ws, L, stream, ev ? ev + 2 : nullptr)) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (ev && cudaEventRecord(ev[4], stream) != cudaSuccess)

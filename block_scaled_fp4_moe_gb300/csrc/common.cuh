@@ -313,6 +313,25 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
 // 2^e as fp32 for |e| <= 126.
 __device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
 
+// MXFP8 (OCP MX v1.0) of one block of 32 values, one per lane: the shared
+// exponent is floor(log2(max |v|)) - 8 (E4M3's largest exponent), kept in
+// [-127, 127], -127 for an all-zero block; each element is v / 2^e rounded
+// to E4M3, ties to even, saturating at 448.  v / 2^e is exact in fp32, so the
+// codes are those of the exact quotient.  Lane 0 writes the scale byte.
+__device__ __forceinline__ void mxfp8_quant_block(float v, uint8_t *code, uint8_t *scale) {
+    const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
+    const int ef = (int)(amax >> 23);           // biased exponent of max |v| (0: zero or subnormal)
+    int se = ef == 0 ? -127 : ef - 127 - 8;
+    se = max(-127, min(127, se));
+    const float q = v * exp2i(-se);             // -se <= 127: a normal power of two
+    uint16_t pair;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.0f), "f"(q));
+    *code = (uint8_t)(pair & 0xFF);
+    if ((threadIdx.x & 31) == 0)
+        *scale = (uint8_t)(se + 127);
+}
+
+
 // Exponent shift that maps a maximum magnitude m into [2^14, 2^15), clamped
 // so that 2^shift stays a normal fp32.
 __device__ __forceinline__ int f16_shift_for_max(float m) {

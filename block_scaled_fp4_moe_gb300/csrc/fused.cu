@@ -69,6 +69,7 @@ struct FusedArgs {
     size_t next_pf_bytes[3];
     Pass *x_passes;                   // routing only: the gate/up passes (one per active expert, <= 8 entries)
     int32_t *x_sorted_tok, *x_inv_pos;   // routing only: sorted position -> token, entry -> sorted position
+    uint8_t *x_q, *x_qs;              // routing only, nullable: x as MXFP8 codes [T][H] and scales [T][H/32]
 };
 
 namespace {
@@ -1218,8 +1219,16 @@ __global__ void __launch_bounds__(NT, 1) fused_layer_kernel(const __grid_constan
     phase_router(a, smem);                  // nothing else lives in shared memory yet
     stamp(a, 1);
     grid_arrive(a);
-    if constexpr (!ROUTE_ONLY)
+    if constexpr (!ROUTE_ONLY) {
         x_window_local(a, rs, reinterpret_cast<__half *>(smem));
+    } else if (a.x_q) {
+        // while the routing waits: x to MXFP8, one warp per block of 32
+        const int nblk = a.T * (a.H / 32);
+        for (int b = blockIdx.x * NW + (threadIdx.x >> 5); b < nblk; b += G * NW) {
+            const size_t i = (size_t)b * 32 + (threadIdx.x & 31);
+            mxfp8_quant_block(__uint_as_float((uint32_t)a.x[i] << 16), a.x_q + i, a.x_qs + b);
+        }
+    }
     bool ok = grid_wait(a, (unsigned)G);
     stamp(a, 2);
     if (ok)
@@ -1425,6 +1434,8 @@ cudaError_t launch_fused(const FusedProblem &pr, void *ws, const WsLayout &L, in
         a.x_passes = route_only->passesw4;
         a.x_sorted_tok = route_only->sorted_tok;
         a.x_inv_pos = route_only->inv_pos;
+        a.x_q = pr.mx_xq;
+        a.x_qs = pr.mx_xs;
         return launch_fused_t<false, true>(a, num_sms, plan.smem, stream);
     }
     if (!b.packed)

@@ -78,6 +78,7 @@ struct Mx8Problem {
     const float *topk_w;     // [T, kps]
     uint16_t *y;             // [T, H] bf16
     int T, kps;
+    bool x_quantised;        // x's MXFP8 codes are already in the workspace
 };
 bool mx8_shape_supported(int H, int I);
 size_t mx8_packed_size(int H, int I, int n_tot);
@@ -105,6 +106,8 @@ struct FusedProblem {
     size_t next_router_bytes;
     const void *next_shared_gu, *next_shared_dn;
     size_t next_shared_gu_bytes, next_shared_dn_bytes;
+    // routing only (launch_fused with route_only), nullable: x as MXFP8
+    uint8_t *mx_xq = nullptr, *mx_xs = nullptr;
 };
 
 // Shared-memory plan of the single-launch kernel; ok = the shape fits.

@@ -333,24 +333,6 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
 
 // ------------------------------------------------------------ quantisation
 
-// MXFP8 (OCP MX v1.0) of one block of 32 values, one per lane: the shared
-// exponent is floor(log2(max |v|)) - 8 (E4M3's largest exponent), kept in
-// [-127, 127], -127 for an all-zero block; each element is v / 2^e rounded
-// to E4M3, ties to even, saturating at 448.  v / 2^e is exact in fp32, so the
-// codes are those of the exact quotient.  Lane 0 writes the scale byte.
-__device__ __forceinline__ void mx8_quant_block(float v, uint8_t *code, uint8_t *scale) {
-    const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
-    const int ef = (int)(amax >> 23);           // biased exponent of max |v| (0: zero or subnormal)
-    int se = ef == 0 ? -127 : ef - 127 - 8;
-    se = max(-127, min(127, se));
-    const float q = v * exp2i(-se);             // -se <= 127: a normal power of two
-    uint16_t pair;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(pair) : "f"(0.0f), "f"(q));
-    *code = (uint8_t)(pair & 0xFF);
-    if ((threadIdx.x & 31) == 0)
-        *scale = (uint8_t)(se + 127);
-}
-
 // x (bf16 [T][H]) to MXFP8, one warp per block of 32.
 __global__ void __launch_bounds__(256) mx8_quant_kernel(const uint16_t *__restrict__ x, int rows, int cols,
                                                         uint8_t *__restrict__ codes, uint8_t *__restrict__ scales) {
@@ -360,7 +342,7 @@ __global__ void __launch_bounds__(256) mx8_quant_kernel(const uint16_t *__restri
     if (blk >= (long long)rows * (cols / 32))
         return;
     const size_t i = (size_t)blk * 32 + (threadIdx.x & 31);
-    mx8_quant_block(__uint_as_float((uint32_t)x[i] << 16), codes + i, scales + blk);
+    mxfp8_quant_block(__uint_as_float((uint32_t)x[i] << 16), codes + i, scales + blk);
 }
 
 // h = silu(g) * u from the gate/up GEMM's K-chunk sums (g and u each summed
@@ -385,7 +367,7 @@ __global__ void __launch_bounds__(256) mx8_hfin_kernel(const float *__restrict__
     }
     const float h = g / (1.0f + expf(-g)) * u;
     h32[(size_t)e * I + i] = h;
-    mx8_quant_block(h, codes + (size_t)e * I + i, scales + blk);
+    mxfp8_quant_block(h, codes + (size_t)e * I + i, scales + blk);
 }
 
 // Stage-ordered copy of one section of the bank: one thread per 8-byte code
@@ -464,8 +446,10 @@ cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cud
         attr_set.store(1);
     }
     const int xblocks = T * (H / 32), hblocks = entries * (I / 32);
-    cudaError_t err = launch_pdl(mx8_quant_kernel, dim3((xblocks + 7) / 8), dim3(256), 0, stream, p.x, T, H, xq, xs);
-    if (err != cudaSuccess)
+    cudaError_t err = cudaSuccess;
+    if (!p.x_quantised &&
+        (err = launch_pdl(mx8_quant_kernel, dim3((xblocks + 7) / 8), dim3(256), 0, stream, p.x, T, H, xq, xs)) !=
+            cudaSuccess)
         return err;
     if (ev && (err = cudaEventRecord(ev[0], stream)) != cudaSuccess)
         return err;
