@@ -342,7 +342,12 @@ def run_mine(args, cfg):
     # them back to back (no host gaps inside the measured intervals).  When a
     # call is a single launch, events 1..4 all follow it: ev0 -> ev4 is the
     # kernel, and its phases come from the kernel's own timestamps.
-    launches = 7 if mx else moe.moe_layer_launches(cfg.T, base, cfg.top_k)
+    launches = moe.moe_layer_launches(cfg.T, base, cfg.top_k)
+    if mx:
+        # routing (+ x quantisation) by the single-launch kernel's routing phases
+        # when the layer would be one launch, else two routing launches and the
+        # x quantisation; then gate/up GEMM, h finalise, down GEMM, combine
+        launches = 5 if launches == 1 else 7
     if mx:
         kern = {"route": [], "quant_x": [], "gateup_gemm": [], "quant_h_down_combine": []}
         profiled = moe.moe_layer_forward_mxfp8_profiled

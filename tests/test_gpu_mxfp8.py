@@ -215,3 +215,35 @@ def test_pack_mx_matches_documented_layout():
     got = bank.packed_mx.cpu().numpy()
     assert got.size == want.size == moe.lib().moe_packed_mx_bank_size(H, I, E, 1)
     np.testing.assert_array_equal(got, want)
+
+
+def test_mxfp8_zero_tokens_is_a_noop():
+    p = MxProblem(T=1, H=1024, E=16, k=4, I=512, seed=3)
+    y = torch.empty((0, p.H), dtype=torch.bfloat16, device="cuda")
+    x = torch.empty((0, p.H), dtype=torch.bfloat16, device="cuda")
+    ws = torch.zeros(moe.moe_workspace_size(0, p.H, p.I, p.E, p.k, 1) + 256, dtype=torch.uint8, device="cuda")
+    moe.moe_layer_forward_mxfp8(x, torch.from_numpy(p.wr).cuda(), torch.from_numpy(p.bias).cuda(), p.k, p.bank,
+                                1.0, y, ws=ws)
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("name", ["1t_t1", "glm_verify_t4"])
+def test_mxfp8_layer_full_size(name):
+    """Full-size shapes: every stage checked on sampled tokens (1T: split K
+    in four chunks; GLM T = 4: one chunk, experts shared by tokens)."""
+    cfg = inputs.CONFIGS[name]
+    wr, bias = inputs.make_router(cfg)
+    p = MxProblem(cfg.T, cfg.H, cfg.E, cfg.top_k, cfg.I, cfg.has_shared, bank_np=inputs.make_bank(cfg),
+                  x=inputs.make_x(cfg), wr=wr, bias=bias)
+    out = p.forward()
+    check_mx(p, out, np.array([0, cfg.T - 1]) if cfg.T > 1 else np.arange(1), name)
+    del p
+    torch.cuda.empty_cache()
+
+
+def test_mxfp8_is_deterministic_across_calls():
+    p = MxProblem(T=6, H=1024, E=16, k=4, I=512, seed=8)
+    a = p.forward()
+    b = p.forward()
+    np.testing.assert_array_equal(a["y"], b["y"])
+    np.testing.assert_array_equal(a["hq"], b["hq"])
