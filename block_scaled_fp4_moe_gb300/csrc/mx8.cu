@@ -54,15 +54,12 @@ namespace {
 
 constexpr int kMxProducers = 128;              // warps 0..3 load and stage the operands
 constexpr int kMxThreads = kMxProducers + 32;  // warp 4 issues the MMAs
-constexpr int kMxN = 16;                       // MMA N: entries of one pass
 constexpr int kMxStageK = 128;                 // K elements per stage
 constexpr int kMxStages = 3;                   // shared-memory ring buffers
 constexpr int kMxRegStages = 3;                // stages of operands in flight in registers
 constexpr int kMxLbo = 128;                    // bytes between core matrices adjacent in K
 constexpr int kMxSbo = 8 * 128;                // bytes between 8-row groups (8 K slots of 16 B)
 constexpr int kMxABytes = 128 * kMxStageK;     // 128 rows x 8 slots x 16 B
-constexpr int kMxBBytes = kMxN * kMxStageK;    // 16 rows x 128 E4M3
-constexpr int kMxStageBytes = kMxABytes + kMxBBytes;
 constexpr int kMxTmemCols = 128;               // D: columns 0..15; scale factors on aligned columns
 constexpr int kMxColSfa = 32;                  // SFA of buffer b: 4 columns at 32 + 32 b
 constexpr int kMxColSfb = 48;                  // SFB of buffer b: 1 column at 48 + 32 b
@@ -70,7 +67,15 @@ constexpr int kMxCtasPerSm = 3;                // 3 x 128 TMEM columns, 3 x 55 K
 constexpr int kMxBlockBytes = 8192 + 512;      // one stage of a 128-row tile in the stage-ordered bank
 constexpr unsigned long long kMxWaitLimitNs = 200ull * 1000 * 1000;
 // at least 80 KB, so that no more than two CTAs (2 x 256 TMEM columns) share an SM
-constexpr size_t kMxSmem = (size_t)kMxStages * kMxStageBytes + 2 * kMxStages * 8;   // buffers, full / empty barriers
+// Per MMA width N (entries of one pass: 16, or 32 for the wide passes of
+// the multi-launch grouping): the B tile, a ring stage and the shared memory.
+template <int NN>
+struct MxTile {
+    static_assert(NN == 16 || NN == 32, "N");
+    static constexpr int kB = NN * kMxStageK;                 // NN rows x 128 E4M3
+    static constexpr int kStage = kMxABytes + kB;
+    static constexpr size_t kSmem = (size_t)kMxStages * kStage + 2 * kMxStages * 8;   // buffers, full / empty barriers
+};
 
 static_assert(kMxColSfb + 32 * (kMxStages - 1) + 1 <= kMxTmemCols && kMxCtasPerSm * kMxTmemCols <= 512,
               "TMEM columns");
@@ -91,8 +96,9 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
 // B E4M3 (0), both K-major, N >> 3 at bit 17, UE8M0 scales (bit 23),
 // M >> 4 at bit 24; scale-factor ids (byte of the TMEM cell) of B at bits
 // 4-5 and of A at bits 29-30.
+template <int NN>
 __host__ __device__ constexpr uint32_t mx_idesc(int sf_id) {
-    return ((uint32_t)(sf_id & 3) << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(kMxN >> 3) << 17) | (1u << 23) |
+    return ((uint32_t)(sf_id & 3) << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(NN >> 3) << 17) | (1u << 23) |
            ((uint32_t)(128 >> 4) << 24) | ((uint32_t)(sf_id & 3) << 29);
 }
 
@@ -122,7 +128,8 @@ struct MxGemmArgs {
     const uint8_t *blocks;      // section of the stage-ordered bank: [n_tot][tiles][K/128] blocks
     const uint8_t *aq;          // E4M3 activations [act_rows][K]
     const uint8_t *asc;         // E8M0 scales [act_rows][K/32]
-    const Pass *passes;         // passes of <= 16 entries
+    const Pass *passes;         // passes of <= N entries
+    int npass_word;             // header word holding the number of passes
     const int32_t *sorted_tok;  // gate/up: entry -> activation row (token); down: null (row = entry)
     float *out;                 // [kc][entries][rows]: per K chunk, the sums of every weight row
                                 // (gate/up: g then u, 2I columns; down: Y, H columns)
@@ -140,21 +147,22 @@ struct MxGemmArgs {
 
 // ------------------------------------------------------------------ GEMM
 
-template <bool GATEUP>
+template <bool GATEUP, int NN>
 __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(const __grid_constant__ MxGemmArgs a) {
+    using Tile = MxTile<NN>;
     extern __shared__ __align__(1024) uint8_t mx_smem[];
     __shared__ uint32_t s_taddr;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_wait();
     pdl_trigger();
-    const int n_pass = (int)*reinterpret_cast<const volatile uint32_t *>(a.hdr + kHdrNumPassesW4);
+    const int n_pass = (int)*reinterpret_cast<const volatile uint32_t *>(a.hdr + a.npass_word);
     if ((int)blockIdx.y >= n_pass)
         return;
     const Pass ps = a.passes[blockIdx.y];
     const int tile = blockIdx.x / a.kc, chunk = blockIdx.x - tile * a.kc;
     // the pass and its activation rows must lie inside the buffers
     {
-        int bad = ps.expert < 0 || ps.expert >= a.n_tot || ps.count < 1 || ps.count > kMxN || ps.begin < 0 ||
+        int bad = ps.expert < 0 || ps.expert >= a.n_tot || ps.count < 1 || ps.count > NN || ps.begin < 0 ||
                   ps.begin + ps.count > a.entries;
         if (!bad && tid < ps.count) {
             const int row = GATEUP ? a.sorted_tok[ps.begin + tid] : ps.begin + tid;
@@ -169,7 +177,7 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
     // buffer b: full[b] completes when the 128 producers have staged a stage
     // in it (shared operands, scale factors in TMEM); empty[b] when the MMAs
     // reading it are done (tcgen05.commit)
-    uint64_t *full = reinterpret_cast<uint64_t *>(mx_smem + (size_t)kMxStages * kMxStageBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(mx_smem + (size_t)kMxStages * Tile::kStage);
     uint64_t *empty = full + kMxStages;
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&s_taddr)),
@@ -199,9 +207,10 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
         // 128 i (i < 4) of the block, holding the pieces q0 = 64 (c / 32) +
         // c % 32 and q0 + 32 of the shared-memory image (each 8-byte store of
         // a warp then covers 32 consecutive slots); the scale words of rows
-        // lane + 32 q (q < 4); 16 bytes of activation row tid / 8, slot tid %
-        // 8; the scale word of activation row lane % 16.  Each warp writes the
-        // scale factors into its own 32-lane quarter of TMEM.
+        // lane + 32 q (q < 4); 16 bytes of activation rows tid / 8 + 16 j
+        // (j < N / 16), slot tid % 8; the scale word of activation row
+        // lane % N.  Each warp writes the scale factors into its own 32-lane
+        // quarter of TMEM.
         const uint8_t *wblk =
             a.blocks + (((size_t)ps.expert * a.tiles + tile) * a.kc * nst + s_first) * kMxBlockBytes;
         auto arow = [&](int n) {
@@ -209,15 +218,19 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
             return GATEUP ? a.sorted_tok[e] : e;
         };
         const int slot = tid & 7, r0 = tid >> 3;
-        const uint8_t *asrc = a.aq + (size_t)arow(r0) * a.K + (size_t)s_first * kMxStageK + slot * 16;
-        const uint8_t *sfb_src = a.asc + (size_t)arow(lane & 15) * K32 + s_first * 4;
+        constexpr int NB = NN / 16;                  // activation chunks per thread
+        const uint8_t *asrc[NB];
+#pragma unroll
+        for (int j = 0; j < NB; ++j)
+            asrc[j] = a.aq + (size_t)arow(r0 + 16 * j) * a.K + (size_t)s_first * kMxStageK + slot * 16;
+        const uint8_t *sfb_src = a.asc + (size_t)arow(lane % NN) * K32 + s_first * 4;
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const uint64_t pol = l2_evict_first_policy();
         uint4 rq[kMxRegStages][4];
         uint32_t rsa[kMxRegStages][4];
-        uint4 rb[kMxRegStages];
+        uint4 rb[kMxRegStages][NB];
         uint32_t rsb[kMxRegStages];
-        auto load_stage = [&](int s, uint4(&q)[4], uint32_t(&sa)[4], uint4 &bq, uint32_t &sb) {
+        auto load_stage = [&](int s, uint4(&q)[4], uint32_t(&sa)[4], uint4(&bq)[NB], uint32_t &sb) {
             const uint8_t *blk = wblk + (size_t)s * kMxBlockBytes;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -225,7 +238,9 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
 #pragma unroll
             for (int i = 0; i < 4; ++i)
                 sa[i] = __ldg(reinterpret_cast<const uint32_t *>(blk + 8192 + 4 * (lane + 32 * i)));
-            bq = __ldg(reinterpret_cast<const uint4 *>(asrc + (size_t)s * kMxStageK));
+#pragma unroll
+            for (int j = 0; j < NB; ++j)
+                bq[j] = __ldg(reinterpret_cast<const uint4 *>(asrc[j] + (size_t)s * kMxStageK));
             sb = __ldg(reinterpret_cast<const uint32_t *>(sfb_src + s * 4));
         };
 #pragma unroll
@@ -245,7 +260,7 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
                     ok = false;           // warp-uniform: the tcgen05 stores below are .sync.aligned
                     break;
                 }
-                uint8_t *st = mx_smem + (size_t)b * kMxStageBytes;
+                uint8_t *st = mx_smem + (size_t)b * Tile::kStage;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int c = tid + kMxProducers * i;
@@ -253,8 +268,12 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
                     *reinterpret_cast<uint2 *>(st + 16 * q0) = make_uint2(rq[k][i].x, rq[k][i].y);
                     *reinterpret_cast<uint2 *>(st + 16 * (q0 + 32)) = make_uint2(rq[k][i].z, rq[k][i].w);
                 }
-                *reinterpret_cast<uint4 *>(st + kMxABytes + (r0 >> 3) * kMxSbo + slot * kMxLbo + (r0 & 7) * 16) =
-                    rb[k];
+#pragma unroll
+                for (int j = 0; j < NB; ++j) {
+                    const int r = r0 + 16 * j;
+                    *reinterpret_cast<uint4 *>(st + kMxABytes + (r >> 3) * kMxSbo + slot * kMxLbo + (r & 7) * 16) =
+                        rb[k][j];
+                }
                 const uint32_t colA = (uint32_t)(kMxColSfa + 32 * b), colB = (uint32_t)(kMxColSfb + 32 * b);
                 asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
                                  tmem + lane_base + colA),
@@ -285,7 +304,7 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
             }
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const uint32_t colA = (uint32_t)(kMxColSfa + 32 * b), colB = (uint32_t)(kMxColSfb + 32 * b);
-            const uint32_t sa = sbase + (uint32_t)(b * kMxStageBytes), sb = sa + kMxABytes;
+            const uint32_t sa = sbase + (uint32_t)(b * Tile::kStage), sb = sa + kMxABytes;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint64_t ad = smem_desc(sa + j * 2 * kMxLbo), bd = smem_desc(sb + j * 2 * kMxLbo);
@@ -293,7 +312,7 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
                 asm volatile(
                     "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
                     "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n}\n"
-                    ::"r"(tmem), "l"(ad), "l"(bd), "r"(mx_idesc(j)), "r"(acc), "r"(tmem + colA), "r"(tmem + colB)
+                    ::"r"(tmem), "l"(ad), "l"(bd), "r"(mx_idesc<NN>(j)), "r"(acc), "r"(tmem + colA), "r"(tmem + colB)
                     : "memory");
             }
             asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -307,12 +326,16 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
         if (tid == 0)
             record_status(a.hdr, MOE_ERR_DEVICE_TIMEOUT);
     } else if (warp < kMxProducers / 32) {
-        uint32_t v[16];
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-            : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-              "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-            : "r"(tmem + ((uint32_t)(warp * 32) << 16)));
+        uint32_t v[NN];
+#pragma unroll
+        for (int c0 = 0; c0 < NN; c0 += 16)
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+                "[%16];"
+                : "=r"(v[c0]), "=r"(v[c0 + 1]), "=r"(v[c0 + 2]), "=r"(v[c0 + 3]), "=r"(v[c0 + 4]), "=r"(v[c0 + 5]),
+                  "=r"(v[c0 + 6]), "=r"(v[c0 + 7]), "=r"(v[c0 + 8]), "=r"(v[c0 + 9]), "=r"(v[c0 + 10]),
+                  "=r"(v[c0 + 11]), "=r"(v[c0 + 12]), "=r"(v[c0 + 13]), "=r"(v[c0 + 14]), "=r"(v[c0 + 15])
+                : "r"(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         // MMA row r = TMEM lane = weight row of the tile: gate/up rows 0..63
         // are gate rows 64 tile.., 64..127 the up rows; output column = that
@@ -321,7 +344,7 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
         const int col = GATEUP ? (r < 64 ? tile * 64 + r : a.half + tile * 64 + r - 64) : tile * 128 + r;
         float *dst = a.out + chunk * a.kstride + (size_t)ps.begin * a.out_ld + col;
 #pragma unroll
-        for (int n = 0; n < kMxN; ++n)
+        for (int n = 0; n < NN; ++n)
             if (n < ps.count)
                 dst[(size_t)n * a.out_ld] = __uint_as_float(v[n]);
     }
@@ -425,39 +448,34 @@ cudaError_t launch_mx8_pack(const moe_mxfp4_bank_t &b, uint8_t *out, cudaStream_
 
 bool mx8_shape_supported(int H, int I) { return H > 0 && I > 0 && H % 128 == 0 && I % 128 == 0; }
 
-cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cudaStream_t stream, cudaEvent_t *ev) {
+// The two GEMMs with MMA width NN around the h finalisation, then the combine.
+template <int NN>
+static cudaError_t launch_gemms(const Mx8Problem &p, void *ws, const WsLayout &L, cudaStream_t stream,
+                                cudaEvent_t *ev, const Pass *passes, int npass_word, int max_pass) {
     const moe_mxfp4_bank_t &b = *p.bank;
     const int H = b.hidden, I = b.inter, T = p.T, kps = p.kps;
     const int entries = T * kps;
     const int n_tot = b.num_experts + b.has_shared;
-    const int max_pass = max_passes(T, kps, n_tot, kWidePassEntries);
-    uint32_t *hdr = ws_at<uint32_t>(ws, 0);
-    uint8_t *xq = ws_at<uint8_t>(ws, L.mx_xq), *xs = ws_at<uint8_t>(ws, L.mx_xs);
-    uint8_t *hq = ws_at<uint8_t>(ws, L.mx_hq), *hs = ws_at<uint8_t>(ws, L.mx_hs);
-    float *h32 = ws_at<float>(ws, L.mx_h32), *yent = ws_at<float>(ws, L.mx_y), *gu = ws_at<float>(ws, L.mx_gu);
+    constexpr size_t smem = MxTile<NN>::kSmem;
     static std::atomic<int> attr_set{0};
+    cudaError_t err;
     if (!attr_set.load()) {
-        cudaError_t err;
-        if ((err = cudaFuncSetAttribute(mx8_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kMxSmem)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(mx8_gemm_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kMxSmem)) != cudaSuccess)
+        if ((err = cudaFuncSetAttribute(mx8_gemm_kernel<true, NN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)smem)) != cudaSuccess ||
+            (err = cudaFuncSetAttribute(mx8_gemm_kernel<false, NN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)smem)) != cudaSuccess)
             return err;
         attr_set.store(1);
     }
-    const int xblocks = T * (H / 32), hblocks = entries * (I / 32);
-    cudaError_t err = cudaSuccess;
-    if (!p.x_quantised &&
-        (err = launch_pdl(mx8_quant_kernel, dim3((xblocks + 7) / 8), dim3(256), 0, stream, p.x, T, H, xq, xs)) !=
-            cudaSuccess)
-        return err;
-    if (ev && (err = cudaEventRecord(ev[0], stream)) != cudaSuccess)
-        return err;
+    uint32_t *hdr = ws_at<uint32_t>(ws, 0);
+    uint8_t *hq = ws_at<uint8_t>(ws, L.mx_hq), *hs = ws_at<uint8_t>(ws, L.mx_hs);
+    float *h32 = ws_at<float>(ws, L.mx_h32), *yent = ws_at<float>(ws, L.mx_y), *gu = ws_at<float>(ws, L.mx_gu);
     MxGemmArgs g{};
     g.blocks = p.packed_mx;
-    g.aq = xq;
-    g.asc = xs;
-    g.passes = ws_at<Pass>(ws, L.passesw4);
+    g.aq = ws_at<uint8_t>(ws, L.mx_xq);
+    g.asc = ws_at<uint8_t>(ws, L.mx_xs);
+    g.passes = passes;
+    g.npass_word = npass_word;
     g.sorted_tok = ws_at<int32_t>(ws, L.sorted_tok);
     g.out = gu;
     g.hdr = hdr;
@@ -470,11 +488,12 @@ cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cud
     g.n_tot = n_tot;
     g.act_rows = T;
     g.entries = entries;
-    if ((err = launch_pdl(mx8_gemm_kernel<true>, dim3(I / 64 * g.kc, max_pass), dim3(kMxThreads), kMxSmem, stream,
+    if ((err = launch_pdl(mx8_gemm_kernel<true, NN>, dim3(I / 64 * g.kc, max_pass), dim3(kMxThreads), smem, stream,
                           g)) != cudaSuccess)
         return err;
     if (ev && (err = cudaEventRecord(ev[1], stream)) != cudaSuccess)
         return err;
+    const int hblocks = entries * (I / 32);
     if ((err = launch_pdl(mx8_hfin_kernel, dim3((hblocks + 7) / 8), dim3(256), 0, stream, (const float *)gu, g.kc,
                           g.kstride, entries, I, h32, hq, hs)) != cudaSuccess)
         return err;
@@ -491,10 +510,34 @@ cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cud
     d.kstride = 0;
     d.out_ld = H;
     d.act_rows = entries;
-    if ((err = launch_pdl(mx8_gemm_kernel<false>, dim3(H / 128, max_pass), dim3(kMxThreads), kMxSmem, stream, d)) !=
+    if ((err = launch_pdl(mx8_gemm_kernel<false, NN>, dim3(H / 128, max_pass), dim3(kMxThreads), smem, stream, d)) !=
         cudaSuccess)
         return err;
     return launch_combine(yent, entries, ws_at<int32_t>(ws, L.inv_pos), p.topk_w, T, kps, H, p.y, hdr, stream);
+}
+
+cudaError_t launch_mx8_ffn(const Mx8Problem &p, void *ws, const WsLayout &L, cudaStream_t stream, cudaEvent_t *ev) {
+    const moe_mxfp4_bank_t &b = *p.bank;
+    const int H = b.hidden, T = p.T, kps = p.kps;
+    const int n_tot = b.num_experts + b.has_shared;
+    cudaError_t err = cudaSuccess;
+    if (!p.x_quantised &&
+        (err = launch_pdl(mx8_quant_kernel, dim3((T * (H / 32) + 7) / 8), dim3(256), 0, stream, p.x, T, H,
+                          ws_at<uint8_t>(ws, L.mx_xq), ws_at<uint8_t>(ws, L.mx_xs))) != cudaSuccess)
+        return err;
+    if (ev && (err = cudaEventRecord(ev[0], stream)) != cudaSuccess)
+        return err;
+    // routing by the single-launch kernel's phases (which also quantised x)
+    // exports passes of one expert's <= 8 entries; the multi-launch grouping
+    // also writes passes of <= 32, which the wider MMA (N = 32) reads for
+    // T > 128, where experts with many tokens re-read their weights half as
+    // often (measured: Zipf T = 256 798 -> 764 us; at T = 64 the fewer,
+    // heavier CTAs cost more than that: 355 -> 388 us)
+    if (p.x_quantised || T <= 128)
+        return launch_gemms<16>(p, ws, L, stream, ev, ws_at<Pass>(ws, L.passesw4), kHdrNumPassesW4,
+                                max_passes(T, kps, n_tot, kWidePassEntries));
+    return launch_gemms<32>(p, ws, L, stream, ev, ws_at<Pass>(ws, L.passesw), kHdrNumPassesW,
+                            max_passes(T, kps, n_tot, kWidePassTokens));
 }
 
 }  // namespace moe

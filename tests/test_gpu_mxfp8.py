@@ -100,6 +100,13 @@ def check_mx(p: MxProblem, out, tokens, label):
     ref = oracle.moe_tokens(p.x, r["ids"], r["w"], p.expert, tokens, want_h=True, act="mxfp8")
     xd = bf16_to_f64(p.x)
     H, I = p.H, p.I
+    decoded = {}
+
+    def dense_of(e):
+        if e not in decoded:
+            ex = p.expert(e)
+            decoded[e] = (dense(ex["w13"], ex["s13"]), dense(ex["w2"], ex["s2"]))
+        return decoded[e]
     for i, t in enumerate(tokens):
         codes, scales, xq = oracle.mxfp8_quantize(xd[t])
         np.testing.assert_array_equal(out["xq"][t], codes, err_msg=f"{label} x codes t={t}")
@@ -109,8 +116,7 @@ def check_mx(p: MxProblem, out, tokens, label):
         for s in range(p.kps):
             e = int(out["ids"][t, s])
             pos = int(out["inv_pos"][t, s])
-            ex = p.expert(e)
-            W13 = dense(ex["w13"], ex["s13"])
+            W13, W2 = dense_of(e)
             G, U = W13[:I] @ xq, W13[I:] @ xq
             Sg, Su = np.abs(W13[:I]) @ np.abs(xq), np.abs(W13[I:]) @ np.abs(xq)
             hk = out["h"][pos].astype(np.float64)
@@ -123,7 +129,6 @@ def check_mx(p: MxProblem, out, tokens, label):
             c2, s2, hdq = oracle.mxfp8_quantize(hk)
             np.testing.assert_array_equal(out["hq"][pos], c2, err_msg=f"{label} h codes t={t} s={s}")
             np.testing.assert_array_equal(out["hs"][pos], s2, err_msg=f"{label} h scales t={t} s={s}")
-            W2 = dense(ex["w2"], ex["s2"])
             Yd = W2 @ hdq
             Yb = I * 2.0 ** -24 * (np.abs(W2) @ np.abs(hdq)) + 1e-30
             Yk = out["Y"][pos].astype(np.float64)
@@ -147,6 +152,7 @@ SMALL = [
     dict(T=40, H=1024, E=6, k=3, I=512),           # experts hold up to 40 tokens: several passes of 16
     dict(T=5, H=2048, E=24, k=6, I=1024, has_shared=0),
     dict(T=2, H=768, E=8, k=2, I=384),             # K of 3 and 6 stages
+    dict(T=160, H=1024, E=4, k=2, I=512),          # T > 128: MMA N = 32, passes of up to 32 entries
 ]
 
 
