@@ -29,6 +29,10 @@
 //  C  every CTA combines an equal share of the outputs:
 //     y = bf16(sum over slots in order of w * Y).
 //
+// A second instantiation (ROUTE_ONLY) runs phases R and T alone and writes the
+// grouping to the workspace: the MXFP8 variant (mx8.cu) routes with it for
+// T <= 8 and runs the expert projections itself.
+//
 // Waits spin on a counter in the workspace with a time limit; a wait that runs
 // out records MOE_ERR_DEVICE_TIMEOUT and every CTA leaves without writing y.
 // The cooperative launch guarantees that all CTAs are resident, so a wait can

@@ -8,15 +8,18 @@
 // conversion -- and both projections run as block-scaled tensor-core MMAs,
 // `tcgen05.mma.kind::mxf8f6f4.block_scale`: A = MXFP4 weights read as E2M1 by
 // the tensor core, B = the MXFP8 activations, both block scales applied by the
-// hardware, fp32 accumulators in TMEM.  The weights are read from the
-// canonical bank arrays (w13, s13, w2, s2); no decode instruction runs.
+// hardware, fp32 accumulators in TMEM.  The weights are read from a
+// stage-ordered copy of the bank (below); no decode instruction runs.
 //
-// Launches: routing + grouping (route.cu), x quantisation, gate/up GEMM
-// (writes h = silu(g) * u in fp32), h quantisation, down GEMM (per-entry
-// outputs Y), combine (ffn.cu's combine_kernel).
+// Launches: routing + grouping and the x quantisation (for T <= 8 the
+// routing phases of the single-launch kernel, which quantise x while they
+// wait; else route.cu's two launches and mx8_quant_kernel), the gate/up GEMM
+// (the g and u sums of each K chunk), mx8_hfin_kernel (h = silu(g) * u in
+// fp32, quantised), the down GEMM (per-entry outputs Y), the combine
+// (ffn.cu's combine_kernel).
 //
-// GEMM CTA: 128 weight rows x one pass of <= 16 entries (MMA M = 128,
-// N = 16), K in stages of 128 (four MMAs of K = 32), warp-specialised: four
+// GEMM CTA: 128 weight rows x one pass of <= N entries (MMA M = 128, N = 16,
+// or 32 for T > 128), K in stages of 128 (four MMAs of K = 32), warp-specialised: four
 // producer warps load every operand of a stage into registers kMxRegStages
 // stages ahead, store it into a 3-buffer shared-memory ring, write its scale
 // factors into TMEM and arrive on the buffer's "full" mbarrier; a fifth warp
@@ -60,13 +63,12 @@ constexpr int kMxRegStages = 3;                // stages of operands in flight i
 constexpr int kMxLbo = 128;                    // bytes between core matrices adjacent in K
 constexpr int kMxSbo = 8 * 128;                // bytes between 8-row groups (8 K slots of 16 B)
 constexpr int kMxABytes = 128 * kMxStageK;     // 128 rows x 8 slots x 16 B
-constexpr int kMxTmemCols = 128;               // D: columns 0..15; scale factors on aligned columns
+constexpr int kMxTmemCols = 128;               // D: columns 0..N-1; scale factors on aligned columns
 constexpr int kMxColSfa = 32;                  // SFA of buffer b: 4 columns at 32 + 32 b
 constexpr int kMxColSfb = 48;                  // SFB of buffer b: 1 column at 48 + 32 b
-constexpr int kMxCtasPerSm = 3;                // 3 x 128 TMEM columns, 3 x 55 KB shared memory
+constexpr int kMxCtasPerSm = 3;                // 3 x 128 TMEM columns, 3 x 55 (N = 16) or 61 KB shared memory
 constexpr int kMxBlockBytes = 8192 + 512;      // one stage of a 128-row tile in the stage-ordered bank
 constexpr unsigned long long kMxWaitLimitNs = 200ull * 1000 * 1000;
-// at least 80 KB, so that no more than two CTAs (2 x 256 TMEM columns) share an SM
 // Per MMA width N (entries of one pass: 16, or 32 for the wide passes of
 // the multi-launch grouping): the B tile, a ring stage and the shared memory.
 template <int NN>
@@ -77,8 +79,9 @@ struct MxTile {
     static constexpr size_t kSmem = (size_t)kMxStages * kStage + 2 * kMxStages * 8;   // buffers, full / empty barriers
 };
 
-static_assert(kMxColSfb + 32 * (kMxStages - 1) + 1 <= kMxTmemCols && kMxCtasPerSm * kMxTmemCols <= 512,
-              "TMEM columns");
+static_assert(kMxColSfb + 32 * (kMxStages - 1) + 1 <= kMxTmemCols && kMxCtasPerSm * kMxTmemCols <= 512 &&
+                  32 <= kMxColSfa,
+              "TMEM columns: D (up to 32 columns) below the scale factors");
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
