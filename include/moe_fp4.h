@@ -239,9 +239,11 @@ moe_status_t moe_layer_forward_next(const uint16_t *x, const float *router_w, co
  * read from packed_mx, the stage-ordered copy moe_pack_bank_mx writes
  * (256-byte aligned).  H and I must be multiples of 128
  * (MOE_ERR_UNSUPPORTED_SHAPE).  Workspace:
- * moe_workspace_size(T, ...) bytes, as for moe_layer_forward.  Seven
- * launches (two of routing, two quantisations, two GEMMs, the combine);
- * asynchronous on `stream`, graph-capturable.
+ * moe_workspace_size(T, ...) bytes, as for moe_layer_forward.  Five
+ * launches for T <= 8 (the routing phases of the single-launch kernel, which
+ * also quantise x; the gate/up GEMM; the h finalisation and quantisation;
+ * the down GEMM; the combine), seven above (two routing launches and a
+ * separate x quantisation); asynchronous on `stream`, graph-capturable.
  */
 moe_status_t moe_layer_forward_mxfp8(const uint16_t *x, const float *router_w, const float *logit_bias,
                                      int T, int top_k, const moe_mxfp4_bank_t *bank, const void *packed_mx,

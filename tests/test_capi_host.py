@@ -120,6 +120,10 @@ def test_mxfp8_argument_checks(L):
     assert forward_mx(L, bank(), k=161) == moe.MOE_ERR_UNSUPPORTED_SHAPE
     need = moe.moe_workspace_size(1, 5120, 1536, 160, 8, 1)
     assert forward_mx(L, bank(), ws_bytes=need - 1) == moe.MOE_ERR_WORKSPACE_TOO_SMALL
+    ev = (C.c_void_p * 5)()
+    assert L.moe_layer_forward_mxfp8_profiled(C.c_void_p(FAKE), C.c_void_p(FAKE), None, 1, 8, C.byref(bank()), p,
+                                              1.0, C.c_void_p(FAKE), C.c_void_p(FAKE), 1 << 40, ev, 4,
+                                              None) == moe.MOE_ERR_INVALID_ARG      # fewer than 5 events
 
 
 def test_other_entry_points_argument_checks(L):
