@@ -177,6 +177,59 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
             return;
         }
     }
+    const int K32 = a.K / 32;
+    const int nst = a.K / kMxStageK / a.kc;          // stages of this chunk
+    const int s_first = chunk * nst;
+    const uint32_t sbase = smem_addr(mx_smem);
+    // ---- producers.  Every operand of a stage is loaded into registers
+    // kMxRegStages stages ahead: weight codes as 16-byte chunks c = tid +
+    // 128 i (i < 4) of the block, holding the pieces q0 = 64 (c / 32) +
+    // c % 32 and q0 + 32 of the shared-memory image (each 8-byte store of
+    // a warp then covers 32 consecutive slots); the scale words of rows
+    // lane + 32 q (q < 4); 16 bytes of activation rows tid / 8 + 16 j
+    // (j < N / 16), slot tid % 8; the scale word of activation row
+    // lane % N.  Each warp writes the scale factors into its own 32-lane
+    // quarter of TMEM.
+    const uint8_t *wblk =
+        a.blocks + (((size_t)ps.expert * a.tiles + tile) * a.kc * nst + s_first) * kMxBlockBytes;
+    auto arow = [&](int n) {
+        const int e = ps.begin + min(n, ps.count - 1);
+        return GATEUP ? a.sorted_tok[e] : e;
+    };
+    const int slot = tid & 7, r0 = tid >> 3;
+    constexpr int NB = NN / 16;                  // activation chunks per thread
+    const uint8_t *asrc[NB];
+#pragma unroll
+    for (int j = 0; j < NB; ++j)
+        asrc[j] = a.aq + (size_t)arow(r0 + 16 * j) * a.K + (size_t)s_first * kMxStageK + slot * 16;
+    const uint8_t *sfb_src = a.asc + (size_t)arow(lane % NN) * K32 + s_first * 4;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint64_t pol = l2_evict_first_policy();
+    uint4 rq[kMxRegStages][4];
+    uint32_t rsa[kMxRegStages][4];
+    uint4 rb[kMxRegStages][NB];
+    uint32_t rsb[kMxRegStages];
+    auto load_stage = [&](int s, uint4(&q)[4], uint32_t(&sa)[4], uint4(&bq)[NB], uint32_t &sb) {
+        const uint8_t *blk = wblk + (size_t)s * kMxBlockBytes;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            q[i] = ld_stream16(blk + 16 * (tid + kMxProducers * i), pol);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            sa[i] = __ldg(reinterpret_cast<const uint32_t *>(blk + 8192 + 4 * (lane + 32 * i)));
+#pragma unroll
+        for (int j = 0; j < NB; ++j)
+            bq[j] = __ldg(reinterpret_cast<const uint4 *>(asrc[j] + (size_t)s * kMxStageK));
+        sb = __ldg(reinterpret_cast<const uint32_t *>(sfb_src + s * 4));
+    };
+    // the first stages' loads go out before the TMEM allocation and barrier
+    // set-up, whose latency they hide (they need only the pass)
+    if (warp < kMxProducers / 32) {
+#pragma unroll
+        for (int k = 0; k < kMxRegStages; ++k)
+            if (k < nst)
+                load_stage(k, rq[k], rsa[k], rb[k], rsb[k]);
+    }
     // buffer b: full[b] completes when the 128 producers have staged a stage
     // in it (shared operands, scale factors in TMEM); empty[b] when the MMAs
     // reading it are done (tcgen05.commit)
@@ -198,58 +251,9 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = s_taddr;
-    const int K32 = a.K / 32;
-    const int nst = a.K / kMxStageK / a.kc;          // stages of this chunk
-    const int s_first = chunk * nst;
-    const uint32_t sbase = smem_addr(mx_smem);
     bool ok = true;
 
     if (warp < kMxProducers / 32) {
-        // ---- producers.  Every operand of a stage is loaded into registers
-        // kMxRegStages stages ahead: weight codes as 16-byte chunks c = tid +
-        // 128 i (i < 4) of the block, holding the pieces q0 = 64 (c / 32) +
-        // c % 32 and q0 + 32 of the shared-memory image (each 8-byte store of
-        // a warp then covers 32 consecutive slots); the scale words of rows
-        // lane + 32 q (q < 4); 16 bytes of activation rows tid / 8 + 16 j
-        // (j < N / 16), slot tid % 8; the scale word of activation row
-        // lane % N.  Each warp writes the scale factors into its own 32-lane
-        // quarter of TMEM.
-        const uint8_t *wblk =
-            a.blocks + (((size_t)ps.expert * a.tiles + tile) * a.kc * nst + s_first) * kMxBlockBytes;
-        auto arow = [&](int n) {
-            const int e = ps.begin + min(n, ps.count - 1);
-            return GATEUP ? a.sorted_tok[e] : e;
-        };
-        const int slot = tid & 7, r0 = tid >> 3;
-        constexpr int NB = NN / 16;                  // activation chunks per thread
-        const uint8_t *asrc[NB];
-#pragma unroll
-        for (int j = 0; j < NB; ++j)
-            asrc[j] = a.aq + (size_t)arow(r0 + 16 * j) * a.K + (size_t)s_first * kMxStageK + slot * 16;
-        const uint8_t *sfb_src = a.asc + (size_t)arow(lane % NN) * K32 + s_first * 4;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        const uint64_t pol = l2_evict_first_policy();
-        uint4 rq[kMxRegStages][4];
-        uint32_t rsa[kMxRegStages][4];
-        uint4 rb[kMxRegStages][NB];
-        uint32_t rsb[kMxRegStages];
-        auto load_stage = [&](int s, uint4(&q)[4], uint32_t(&sa)[4], uint4(&bq)[NB], uint32_t &sb) {
-            const uint8_t *blk = wblk + (size_t)s * kMxBlockBytes;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                q[i] = ld_stream16(blk + 16 * (tid + kMxProducers * i), pol);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                sa[i] = __ldg(reinterpret_cast<const uint32_t *>(blk + 8192 + 4 * (lane + 32 * i)));
-#pragma unroll
-            for (int j = 0; j < NB; ++j)
-                bq[j] = __ldg(reinterpret_cast<const uint4 *>(asrc[j] + (size_t)s * kMxStageK));
-            sb = __ldg(reinterpret_cast<const uint32_t *>(sfb_src + s * 4));
-        };
-#pragma unroll
-        for (int k = 0; k < kMxRegStages; ++k)
-            if (k < nst)
-                load_stage(k, rq[k], rsa[k], rb[k], rsb[k]);
         for (int s0 = 0; s0 < nst && ok; s0 += kMxRegStages) {
 #pragma unroll
             for (int k = 0; k < kMxRegStages; ++k) {
