@@ -315,6 +315,42 @@ def test_linearity_over_slots():
                                        atol=1e-12 * np.abs(out["y_slots"][t, s]).max())
 
 
+# ------------------------------------------------- near-tie diagnostic
+
+@pytest.mark.parametrize("T,H,E,k,bias", [(64, 96, 24, 4, True), (48, 64, 9, 3, False), (16, 32, 6, 6, True)])
+def test_near_tie_diagnostic_against_numpy(T, H, E, k, bias):
+    """The margin that makes bit-exact routing a fair demand: abs_sum is the
+    dense |x|.|Wr| product and gap the smallest difference between
+    neighbours among each token's k+1 largest logits (all k when k = E),
+    both recomputed with numpy from the inputs alone.  The cases are chosen
+    so that the last pair (ranks k, k+1) decides the minimum for some
+    tokens and an earlier pair for others, so a range cut short by one or
+    an unsigned magnitude sum both fail."""
+    x, wr, b, _ = random_layer(T=T, H=H, E=E, k=k, I=32, bias=bias, seed=5 + E)
+    r = oracle.route(x, wr, b, k)
+    xf = inputs.bf16_bits_to_f32(x).astype(np.float64)
+    w64 = wr.astype(np.float64)
+    abs_np = np.abs(xf) @ np.abs(w64)
+    np.testing.assert_allclose(r["abs_sum"], abs_np, rtol=1e-13, atol=0)
+    logits = xf @ w64 + (0.0 if b is None else b.astype(np.float64))
+    nsel = k + 1 if k < E else k
+    order = np.lexsort((np.broadcast_to(np.arange(E), logits.shape), -logits), axis=-1)[:, :nsel]
+    top = np.take_along_axis(logits, order, axis=1)
+    diffs = top[:, :-1] - top[:, 1:]
+    gap_np = diffs.min(axis=1)
+    tol = 1e-12 * abs_np.max(axis=1)
+    assert np.all(np.abs(r["gap"] - gap_np) <= tol), (r["gap"], gap_np)
+    np.testing.assert_allclose(r["rel_gap"], r["gap"] / r["abs_sum"].max(axis=1), rtol=1e-15)
+    if k < E:
+        # discriminating: the (k, k+1) pair is the minimum for some token, and
+        # not for every token
+        last_decides = diffs[:, -1] < diffs[:, :-1].min(axis=1) if k > 1 else np.ones(T, bool)
+        assert last_decides.any() and (k == 1 or not last_decides.all())
+    # without the bias, the magnitude sum bounds |logit| (an unsigned sum would not)
+    if b is None:
+        assert np.all(np.abs(r["logits"]) <= r["abs_sum"] * (1 + 1e-12))
+
+
 # ---------------------------------------------------- workloads are well posed
 
 @pytest.mark.parametrize("name", list(inputs.CONFIGS))
