@@ -195,8 +195,10 @@ std::mutex g_static_mu;
 
 // Device address of the static scratch on the current device.  The first call
 // on a device looks it up (the host-side name of the array is not a device
-// address) and clears its header on `stream`.
-moe_status_t static_scratch(void **out, cudaStream_t stream) {
+// address) and keeps it for the life of the process.  The array needs no
+// clearing: a __device__ array without an initialiser is zero-filled when the
+// module loads, and every call leaves the header's counters at zero again.
+moe_status_t static_scratch(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return MOE_ERR_CUDA;
@@ -209,8 +211,6 @@ moe_status_t static_scratch(void **out, cudaStream_t stream) {
         if (!p) {
             void *ptr = nullptr;
             if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr)
-                return MOE_ERR_CUDA;
-            if (cudaMemsetAsync(ptr, 0, kHeaderBytes, stream) != cudaSuccess)
                 return MOE_ERR_CUDA;
             p = reinterpret_cast<uintptr_t>(ptr);
             g_static_addr[dev].store(p, std::memory_order_release);
@@ -232,7 +232,9 @@ size_t moe_workspace_offset(int T, int H, int I, int E, int top_k, int has_share
         const char *name;
         size_t off;
     } regions[] = {{"topk_ids", L.topk_ids}, {"topk_w", L.topk_w}, {"inv_pos", L.inv_pos},
-                   {"sorted_tok", L.sorted_tok}, {"mx_xq", L.mx_xq}, {"mx_xs", L.mx_xs},
+                   {"sorted_tok", L.sorted_tok}, {"sorted_slot", L.sorted_slot}, {"offsets", L.offsets},
+                   {"active", L.active}, {"num_active", kHdrNumActive * sizeof(uint32_t)},
+                   {"mx_xq", L.mx_xq}, {"mx_xs", L.mx_xs},
                    {"mx_h32", L.mx_h32}, {"mx_hq", L.mx_hq}, {"mx_hs", L.mx_hs}, {"mx_y", L.mx_y}};
     for (const auto &r : regions)
         if (std::strcmp(r.name, region) == 0)
@@ -534,7 +536,7 @@ moe_status_t moe_layer_forward_noalloc(const uint16_t *x, const float *router_w,
     if (!x || !router_w || !y)
         return MOE_ERR_INVALID_ARG;
     void *ws = nullptr;
-    if ((st = static_scratch(&ws, stream)) != MOE_OK)
+    if ((st = static_scratch(&ws)) != MOE_OK)
         return st;
     return layer_forward(x, router_w, logit_bias, T, top_k, bank, shared_weight, y, topk_ids_out, topk_w_out, ws,
                          kStaticScratchBytes, nullptr, stream);

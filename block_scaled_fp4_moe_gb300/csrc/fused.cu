@@ -72,7 +72,10 @@ struct FusedArgs {
     const uint8_t *next_pf[3];        // next layer: router, shared gate/up, shared down (nullable)
     size_t next_pf_bytes[3];
     Pass *x_passes;                   // routing only: the gate/up passes (one per active expert, <= 8 entries)
-    int32_t *x_sorted_tok, *x_inv_pos;   // routing only: sorted position -> token, entry -> sorted position
+    // the grouping every CTA derived, written by CTA 0 (the layout of the
+    // multi-launch grouping): sorted position -> token and slot, entry ->
+    // sorted position, per-expert offsets [n_tot + 1], active experts
+    int32_t *x_sorted_tok, *x_sorted_slot, *x_inv_pos, *x_offsets, *x_active;
     uint8_t *x_q, *x_qs;              // routing only, nullable: x as MXFP8 codes [T][H] and scales [T][H/32]
 };
 
@@ -1177,23 +1180,46 @@ __device__ void combine_share(const FusedArgs &a, const RouteState &rs) {
     }
 }
 
-// Routing only: CTA 0 writes the grouping every CTA derived (the passes of
-// one expert's entries, the sorted order and its inverse) for kernels that
-// run the expert projections themselves; 0 passes when the routing was
-// rejected.
-__device__ void route_export(const FusedArgs &a, const RouteState &rs, bool ok) {
-    const int n = a.T * (a.k + a.S);
+// CTA 0 writes the grouping every CTA derived: the sorted order (token and
+// slot of each sorted position) and its inverse, the per-expert offsets
+// (exclusive prefix of the counts, n_tot + 1 values), the active experts in
+// ascending order and their count (header), and for the routing-only
+// instantiation the passes of one expert's entries.  0 passes and 0 active
+// experts when the routing was rejected.
+__device__ void route_export(const FusedArgs &a, const RouteState &rs, bool ok, bool with_passes) {
+    const int kps = a.k + a.S, n = a.T * kps, n_tot = a.E + a.S;
     if (ok) {
         for (int i = threadIdx.x; i < n; i += NT) {
+            const int ent = rs.sorted_ent[i];
             a.x_sorted_tok[i] = rs.sorted_tok[i];
+            a.x_sorted_slot[i] = ent - (ent / kps) * kps;
             a.x_inv_pos[i] = rs.inv_pos[i];
         }
-        for (int p = threadIdx.x; p < rs.n_gu; p += NT)
-            a.x_passes[p] = rs.pgu[p];
+        for (int p = threadIdx.x; p < rs.n_gu; p += NT) {
+            a.x_active[p] = rs.pgu[p].expert;
+            if (with_passes)
+                a.x_passes[p] = rs.pgu[p];
+        }
+        // offsets[e]: the first sorted position whose expert is >= e, i.e. the
+        // begin of the first pass (ascending experts) with expert >= e
+        for (int e = threadIdx.x; e <= n_tot; e += NT) {
+            int lo = 0, hi = rs.n_gu;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (rs.pgu[mid].expert < e)
+                    lo = mid + 1;
+                else
+                    hi = mid;
+            }
+            a.x_offsets[e] = lo < rs.n_gu ? rs.pgu[lo].begin : n;
+        }
     }
     if (threadIdx.x == 0) {
-        a.hdr[kHdrNumPassesW4] = ok ? (uint32_t)rs.n_gu : 0u;
-        a.hdr[kHdrNumPasses] = ok ? (uint32_t)rs.n_gu : 0u;
+        a.hdr[kHdrNumActive] = ok ? (uint32_t)rs.n_gu : 0u;
+        if (with_passes) {
+            a.hdr[kHdrNumPassesW4] = ok ? (uint32_t)rs.n_gu : 0u;
+            a.hdr[kHdrNumPasses] = ok ? (uint32_t)rs.n_gu : 0u;
+        }
     }
 }
 
@@ -1240,7 +1266,7 @@ __global__ void __launch_bounds__(NT, 1) fused_layer_kernel(const __grid_constan
     stamp(a, 3);
     if constexpr (ROUTE_ONLY) {
         if (blockIdx.x == 0)
-            route_export(a, rs, ok);
+            route_export(a, rs, ok, true);
     } else if (ok) {
         // gate/up, then down: one copy of the streaming code runs both
 #pragma unroll 1
@@ -1248,6 +1274,8 @@ __global__ void __launch_bounds__(NT, 1) fused_layer_kernel(const __grid_constan
             if (mode == kFfnDown) {
                 stamp(a, 4);
                 grid_arrive(a);
+                if (blockIdx.x == 0)        // while CTA 0 waits for the other CTAs' h
+                    route_export(a, rs, true, false);
             }
             if (!stream_phase<FULL>(&a, mode)) {
                 ok = false;
@@ -1434,10 +1462,13 @@ cudaError_t launch_fused(const FusedProblem &pr, void *ws, const WsLayout &L, in
     a.next_pf_bytes[1] = pr.next_shared_gu_bytes;
     a.next_pf[2] = static_cast<const uint8_t *>(pr.next_shared_dn);
     a.next_pf_bytes[2] = pr.next_shared_dn_bytes;
+    a.x_sorted_tok = ws_at<int32_t>(ws, L.sorted_tok);
+    a.x_sorted_slot = ws_at<int32_t>(ws, L.sorted_slot);
+    a.x_inv_pos = ws_at<int32_t>(ws, L.inv_pos);
+    a.x_offsets = ws_at<int32_t>(ws, L.offsets);
+    a.x_active = ws_at<int32_t>(ws, L.active);
     if (route_only) {
         a.x_passes = route_only->passesw4;
-        a.x_sorted_tok = route_only->sorted_tok;
-        a.x_inv_pos = route_only->inv_pos;
         a.x_q = pr.mx_xq;
         a.x_qs = pr.mx_xs;
         return launch_fused_t<false, true>(a, num_sms, plan.smem, stream);

@@ -303,6 +303,7 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
                             mbar_wait(smem_addr(empty + (nst - 1) % kMxStages), ((nst - 1) / kMxStages) & 1));
     } else if (lane == 0) {
         // ---- the MMA issuer
+        int committed = -1;                  // last stage whose MMAs were committed
         for (int s = 0; s < nst; ++s) {
             const int b = s % kMxStages;
             if (!mbar_wait(smem_addr(full + b), (s / kMxStages) & 1)) {
@@ -325,7 +326,13 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
             asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                              smem_addr(empty + b))
                          : "memory");
+            committed = s;
         }
+        // a wait gave up: the MMAs already issued may still read shared
+        // memory and TMEM; wait (bounded) for the last commit, which tracks
+        // all of them, before the CTA frees its TMEM and leaves
+        if (!ok && committed >= 0)
+            mbar_wait(smem_addr(empty + committed % kMxStages), (committed / kMxStages) & 1);
     }
     ok = !__syncthreads_or(!ok);
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");

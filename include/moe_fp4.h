@@ -134,8 +134,13 @@ size_t moe_workspace_size(int T, int H, int I, int E, int top_k, int has_shared)
 
 /*
  * Diagnostics: byte offset inside the workspace of a named region of the
- * T-token layout ("topk_ids", "topk_w", "inv_pos", "sorted_tok", and the
- * MXFP8 variant's "mx_xq" [T][H] E4M3 codes of x, "mx_xs" [T][H/32] their
+ * T-token layout.  After moe_layer_forward (either launch form) the
+ * grouping of a3 lies there, as moe_group_tokens returns it: "offsets"
+ * int32 [E+S+1], "sorted_tok" / "sorted_slot" int32 [T*(k+S)], "active"
+ * int32 [E+S] (the first num_active entries), "num_active" one uint32, and
+ * "inv_pos" int32 [T*(k+S)] (entry t*(k+S)+s -> its sorted position).
+ * Also "topk_ids", "topk_w" (when the call was not given output arrays) and
+ * the MXFP8 variant's "mx_xq" [T][H] E4M3 codes of x, "mx_xs" [T][H/32] their
  * E8M0 scales, "mx_h32" [T*(k+S)][I] fp32 h, "mx_hq" / "mx_hs" its MXFP8
  * codes and scales, "mx_y" [T*(k+S)][H] fp32 per-entry outputs; entry rows in
  * grouped order).  (size_t)-1 for an unknown name or invalid sizes.
@@ -297,12 +302,19 @@ moe_status_t moe_pack_bank_mx(const moe_mxfp4_bank_t *bank, void *packed_mx, siz
  * whose workspace (moe_workspace_size) exceeds it are rejected with
  * MOE_ERR_WORKSPACE_TOO_SMALL.  The call allocates nothing (no cudaMalloc or
  * cudaFree).  The first call on a device looks up the array's device address
- * and clears its header; make that first call before any stream capture.
- * All calls on a device share the array and it keeps the last call's
- * contents: calls that overlap on the GPU (other streams, other host threads)
- * race and must be serialised by the caller.  Arguments and outputs as in
- * moe_layer_forward.  A device-side routing error leaves y untouched; it is
- * recorded in the array's status word, which this call does not report.
+ * (cudaGetSymbolAddress) and keeps it for the life of the process; make that
+ * first call before any stream capture, and do not use this entry point
+ * across a cudaDeviceReset or from a context other than the device's primary
+ * context (the kept address would be stale there).  The array needs no
+ * clearing: it is zero-filled when the library's device code loads, and
+ * every call leaves its counters at zero.  All calls on a device share the
+ * array and it keeps the last call's contents: calls that overlap on the GPU
+ * (other streams, other host threads) race and must be serialised by the
+ * caller.  Arguments and outputs as in moe_layer_forward.  A device-side
+ * routing error leaves y untouched; it is recorded in the array's status
+ * word, which no call can read or clear (the first such error stays latched
+ * for the life of the process): callers that need device-side error reports
+ * use moe_layer_forward with a workspace of their own.
  */
 moe_status_t moe_layer_forward_noalloc(const uint16_t *x, const float *router_w, const float *logit_bias,
                                        int T, int top_k, const moe_mxfp4_bank_t *bank,

@@ -58,11 +58,37 @@ class Problem:
         assert st == 0, moe.moe_status_string(st)
         return {"y": host_bits(y), "ids": ids.cpu().numpy(), "w": w.cpu().numpy(), "ws": ws}
 
+    def grouping(self, ws):
+        """The grouping the layer call left in its workspace (a3), in the form
+        oracle.group returns."""
+        kps, n_tot = self.kps, self.E + self.has_shared
+        host = ws.cpu().numpy()
+
+        def region(name, count):
+            off = moe.moe_workspace_offset(self.T, self.H, self.bank.inter, self.E, self.top_k, self.has_shared, name)
+            return host[off: off + 4 * count].view(np.int32).copy()
+        na = int(region("num_active", 1)[0])
+        n = self.T * kps
+        return {"offsets": region("offsets", n_tot + 1), "sorted_tok": region("sorted_tok", n),
+                "sorted_slot": region("sorted_slot", n), "active": region("active", n_tot)[:na],
+                "num_active": na, "inv_pos": region("inv_pos", n)}
+
     def oracle_route(self):
         return oracle.route(self.x, self.wr, self.bias, self.top_k, self.has_shared, self.shared_weight)
 
     def oracle_tokens(self, route, tokens):
         return oracle.moe_tokens(self.x, route["ids"], route["w"], self.expert, tokens)
+
+
+def check_grouping(got: dict, ids: np.ndarray, n_tot: int, label: str = "") -> None:
+    """Bit-exact grouping against the oracle's, and the inverse permutation."""
+    g = oracle.group(ids, n_tot)
+    for key in ("offsets", "sorted_tok", "sorted_slot", "active"):
+        np.testing.assert_array_equal(got[key], g[key], err_msg=f"{label}: {key}")
+    assert got["num_active"] == g["num_active"], label
+    kps = ids.shape[1]
+    entry = g["sorted_tok"] * kps + g["sorted_slot"]          # sorted position -> entry
+    np.testing.assert_array_equal(got["inv_pos"][entry], np.arange(entry.size), err_msg=f"{label}: inv_pos")
 
 
 def check_output(y_bits: np.ndarray, ref: np.ndarray, label: str = "") -> dict:

@@ -3,8 +3,9 @@
 Routing and grouping must match exactly; the bf16 layer output must meet
 max|err| <= 2e-2 max|ref| and mean|err|/mean|ref| <= 5e-3, and the tighter
 bound derived from the kernels' arithmetic (see gpu_support.check_output).
-Small shapes are compared element by element on every token; the full-size
-workloads compare routing on every token and outputs on sampled tokens.
+Every shape, small or full size, is compared element by element on every
+token; the grouping the call leaves in its workspace is compared with the
+oracle's bit for bit.
 """
 import zlib
 
@@ -14,7 +15,7 @@ import torch
 
 import oracle
 from block_scaled_fp4_moe_gb300 import _build, inputs, moe
-from gpu_support import Problem, check_output, dev_bf16, host_bits
+from gpu_support import Problem, check_grouping, check_output, dev_bf16, host_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -43,6 +44,7 @@ def compare_all(p: Problem, label: str):
     out = p.forward()
     r = p.oracle_route()
     np.testing.assert_array_equal(out["ids"], r["ids"], err_msg=label)
+    check_grouping(p.grouping(out["ws"]), r["ids"], p.E + p.has_shared, label)
     np.testing.assert_allclose(out["w"], r["w"], rtol=2e-6, atol=1e-7, err_msg=label)
     ref = p.oracle_tokens(r, np.arange(p.T))["y"]
     return check_output(out["y"], ref, label)
@@ -207,6 +209,25 @@ def test_layer_exact_logit_ties_go_to_the_lower_index(T):
     compare_all(p, f"ties T={T}")
 
 
+@pytest.mark.parametrize("T,E,k", [(1, 16, 4), (3, 6, 3), (4, 5, 4), (6, 6, 4), (8, 6, 3), (8, 64, 6), (8, 40, 31)])
+def test_layer_grouping_is_the_oracles(T, E, k):
+    """The single-launch kernel (T <= 8) groups the entries in shared memory
+    on every CTA; CTA 0 leaves that grouping in the workspace.  It must be the
+    oracle's bit for bit: few experts make tokens share them (repeated
+    experts, groups of several entries), and T * (k + 1) runs from below 32
+    entries (the one-warp grouping) to above 32 (the multi-warp one)."""
+    p = random_problem(T=T, H=1024, E=E, k=k, I=512, seed=60 + T + E)
+    assert moe.moe_layer_launches(T, p.bank, k) == 1
+    out = p.forward()
+    r = p.oracle_route()
+    np.testing.assert_array_equal(out["ids"], r["ids"])
+    got = p.grouping(out["ws"])
+    check_grouping(got, r["ids"], E + 1, f"T={T} E={E} k={k}")
+    if T > 1:
+        assert got["num_active"] < T * (k + 1)          # some expert holds several entries
+    check_output(out["y"], p.oracle_tokens(r, np.arange(T))["y"], f"grouping case T={T}")
+
+
 def test_layer_tiny_workload_against_fixture():
     cfg = inputs.CONFIGS["tiny"]
     p = Problem.from_config(cfg)
@@ -234,9 +255,13 @@ def test_layer_is_deterministic_and_entry_points_agree():
 
 @pytest.mark.parametrize("T", [1, 4, 13])
 def test_chained_layer_hint_changes_nothing(T):
+    """moe_layer_forward_next against the oracle, and bit-identical to the
+    unchained call (the hint only moves the next layer's bytes into L2)."""
     p = random_problem(T=T, H=1024, E=16, k=4, I=512, seed=40 + T)
     q = random_problem(T=T, H=1024, E=16, k=4, I=512, seed=90 + T)    # the layer that runs next
     a = p.forward()
+    r = p.oracle_route()
+    ref = p.oracle_tokens(r, np.arange(T))["y"]
     for nr, nb in ((q.wrd, q.bank), (None, q.bank), (q.wrd, None), (None, None)):
         ws = p.workspace()
         y = torch.full((p.T, p.H), float("nan"), dtype=torch.bfloat16, device="cuda")
@@ -245,6 +270,8 @@ def test_chained_layer_hint_changes_nothing(T):
         moe.moe_layer_forward_next(p.xd, p.wrd, p.bd, p.top_k, p.bank, p.shared_weight, y, ids, w, ws,
                                    next_router_w=nr, next_bank=nb)
         assert moe.moe_check_device_status(ws) == 0
+        np.testing.assert_array_equal(ids.cpu().numpy(), r["ids"])
+        check_output(host_bits(y), ref, f"chained T={T}")
         np.testing.assert_array_equal(host_bits(y), a["y"])
         np.testing.assert_array_equal(ids.cpu().numpy(), a["ids"])
         np.testing.assert_array_equal(w.cpu().numpy(), a["w"])
@@ -277,9 +304,8 @@ def test_bad_routing_is_reported_and_leaves_outputs_untouched():
 
 # ------------------------------------------------------ full-size workloads
 
-SAMPLED = {"glm_t1": [0], "glm_verify_t4": [0, 1, 2, 3], "glm_verify_t16": [0, 9, 15],
-           "glm_zipf_t64": [0, 40, 63], "glm_zipf_t256": [0, 128, 255],
-           "1t_t1": [0], "1t_t4": [0, 3], "1t_t8": [0, 6]}
+# every token of every full-size workload is compared with the oracle
+FULL = ["glm_t1", "glm_verify_t4", "glm_verify_t16", "glm_zipf_t64", "glm_zipf_t256", "1t_t1", "1t_t4", "1t_t8"]
 
 
 @pytest.fixture(scope="module")
@@ -296,19 +322,19 @@ def banks():
     return get
 
 
-@pytest.mark.parametrize("name", list(SAMPLED))
+@pytest.mark.parametrize("name", FULL)
 def test_layer_full_size(name, banks):
+    """Full-size workloads in the launch form the benchmark times: routing
+    and grouping bit-exact, every token's output within the tolerance."""
     cfg = inputs.CONFIGS[name]
     p = Problem.from_config(cfg, banks(cfg))
     out = p.forward()
     r = p.oracle_route()
     np.testing.assert_array_equal(out["ids"], r["ids"])
     np.testing.assert_allclose(out["w"], r["w"], rtol=2e-6, atol=1e-7)
-    tok = np.array(SAMPLED[name], dtype=np.int32)
-    ref = p.oracle_tokens(r, tok)["y"]
-    check_output(out["y"][tok], ref, name)
-    yall = inputs.bf16_bits_to_f32(out["y"])
-    assert np.all(np.isfinite(yall))
+    check_grouping(p.grouping(out["ws"]), r["ids"], cfg.E + cfg.has_shared, name)
+    ref = p.oracle_tokens(r, np.arange(cfg.T, dtype=np.int32))["y"]
+    check_output(out["y"], ref, name)
     del p
     torch.cuda.empty_cache()
 
