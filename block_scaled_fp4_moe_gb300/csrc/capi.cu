@@ -234,6 +234,8 @@ size_t moe_workspace_offset(int T, int H, int I, int E, int top_k, int has_share
     } regions[] = {{"topk_ids", L.topk_ids}, {"topk_w", L.topk_w}, {"inv_pos", L.inv_pos},
                    {"sorted_tok", L.sorted_tok}, {"sorted_slot", L.sorted_slot}, {"offsets", L.offsets},
                    {"active", L.active}, {"num_active", kHdrNumActive * sizeof(uint32_t)},
+                   {"h", T <= kFusedMaxTokens ? L.fz_h32 : (size_t)-1},
+                   {"y_entries", T <= kFusedMaxTokens ? L.fz_yent : (size_t)-1},
                    {"mx_xq", L.mx_xq}, {"mx_xs", L.mx_xs},
                    {"mx_h32", L.mx_h32}, {"mx_hq", L.mx_hq}, {"mx_hs", L.mx_hs}, {"mx_y", L.mx_y}};
     for (const auto &r : regions)

@@ -211,6 +211,24 @@ __device__ __forceinline__ void record_status(uint32_t *hdr, uint32_t code) {
     atomicCAS(hdr + kHdrStatus, 0u, code);
 }
 
+// Debug build (-DMOE_DEBUG_BOUNDS, libmoe_fp4_debug.so): range checks on the
+// accesses whose indices are computed from routing data -- sorted positions,
+// window rows, output rows.  A failed check records MOE_ERR_DEVICE_ASSERT in
+// the status word and the access is skipped, so no kernel reads or writes
+// outside its buffers and none traps.  In the normal build the checks are
+// the constant true.
+#ifdef MOE_DEBUG_BOUNDS
+__device__ __forceinline__ bool dbg_in_range(long long i, long long n, const uint32_t *hdr) {
+    if (i >= 0 && i < n)
+        return true;
+    record_status(const_cast<uint32_t *>(hdr), MOE_ERR_DEVICE_ASSERT);
+    return false;
+}
+#define MOE_DBG_IN_RANGE(i, n, hdr) (::moe::dbg_in_range((long long)(i), (long long)(n), (hdr)))
+#else
+#define MOE_DBG_IN_RANGE(i, n, hdr) true
+#endif
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -249,16 +267,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
-}
-
-// Bulk async copy global -> shared (this CTA), completion counted in bytes on
-// `bar`.  dst, src 16-byte aligned; bytes a multiple of 16.
-__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
-                                         uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
-        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
 }
 
 // L2 policy for data read exactly once (streamed expert weights).

@@ -121,7 +121,8 @@ __device__ __noinline__ void write_partials(const FfnArgs *a, float a0, float a1
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int n = 2 * c + h;
-            if (n < count) {
+            if (n < count && MOE_DBG_IN_RANGE(begin + n, a->n_entries, a->hdr) &&
+                MOE_DBG_IN_RANGE(j0, a->out_len, a->hdr)) {
                 float *dst = a->part + ((size_t)kc * a->n_entries + begin + n) * 2 * a->out_len + j0;
                 dst[0] = acc[h];                 // gate row j0
                 dst[a->out_len] = acc[2 + h];    // up row j0
@@ -136,7 +137,8 @@ __device__ __noinline__ void write_partials(const FfnArgs *a, float a0, float a1
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int n = 2 * c + h;
-                if (n < count) {
+                if (n < count && MOE_DBG_IN_RANGE(begin + n, a->n_entries, a->hdr) &&
+                    MOE_DBG_IN_RANGE(rb * 16 + g + 8, a->out_len, a->hdr)) {
                     const int e = begin + n;
                     const float u = a->bundo[e];
                     float *dst = a->part + ((size_t)kc * a->n_entries + e) * a->out_len + rb * 16;
@@ -402,6 +404,7 @@ struct TiledArgs {
     float *part;                 // gate/up: [entries][2][I]; down: [entries][H]
     int out_len;                 // I (gate/up) or H (down)
     const float *bundo;          // down: per-entry factor that undoes the h scaling
+    int n_entries;               // T * (k + S) (range checks of the debug build)
 };
 
 // The sums of row block u of pass ps are complete: gate/up writes the gate
@@ -417,7 +420,8 @@ __device__ __forceinline__ void tiled_epilogue(const TiledArgs &a, const Pass &p
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int n = 8 * cg + 2 * c + h;
-                if (cg < ncg && n < ps.count) {
+                if (cg < ncg && n < ps.count && MOE_DBG_IN_RANGE(ps.begin + n, a.n_entries, a.hdr) &&
+                    MOE_DBG_IN_RANGE(8 * u + g, a.out_len, a.hdr)) {
                     float *dst = a.part + (size_t)(ps.begin + n) * 2 * a.out_len + 8 * u + g;
                     dst[0] = acc[cg][h];                      // gate row
                     dst[a.out_len] = acc[cg][2 + h];          // up row
@@ -436,7 +440,8 @@ __device__ __forceinline__ void tiled_epilogue(const TiledArgs &a, const Pass &p
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
                         const int n = 4 * cg + 2 * c + h;
-                        if (n < ps.count) {
+                        if (n < ps.count && MOE_DBG_IN_RANGE(ps.begin + n, a.n_entries, a.hdr) &&
+                            MOE_DBG_IN_RANGE(16 * u + g + 8, a.out_len, a.hdr)) {
                             const int e = ps.begin + n;
                             const float un = a.bundo[e];
                             float *dst = a.part + (size_t)e * a.out_len + 16 * u;
@@ -947,6 +952,7 @@ static cudaError_t launch_ffn_tiled(const FfnProblem &pr, void *ws, const WsLayo
     g.hdr = hdr;
     g.part = ws_at<float>(ws, L.gpart);
     g.out_len = I;
+    g.n_entries = entries;
     const size_t gsm = kfull_smem(H, kWidePassEntries);
     if (gsm <= 200 * 1024) {                // 16 tokens' x rows over all of H fit: whole-K items
         g.passes = ws_at<Pass>(ws, L.passesw4);
@@ -990,6 +996,7 @@ static cudaError_t launch_ffn_tiled(const FfnProblem &pr, void *ws, const WsLayo
     d.hdr = hdr;
     d.part = ws_at<float>(ws, L.ypart);
     d.out_len = H;
+    d.n_entries = entries;
     d.bundo = ws_at<float>(ws, L.hundo);
     const size_t ksm = kfull_smem(I, kTileCols);
     if (ksm <= 200 * 1024) {                // the pass's h rows over all of I fit: whole-K items

@@ -877,6 +877,8 @@ struct Phase {
     int win_row;
     int e_lo;                // down: first entry of the window
     const float *hundo;      // down: per window entry, undoes the h scaling
+    int win_rows;            // rows the window holds (range checks of the debug build)
+    const uint32_t *hdr;
 };
 
 template <bool FULL>
@@ -939,8 +941,10 @@ __device__ __forceinline__ const __half *unit_bptr(int mode, const Phase &ph, co
                                                    const UnitCursor &c, int lane) {
     const Pass ps = ph.passes[c.P];
     const int g = lane >> 2, cc = lane & 3;
-    const int row = mode == kFfnGateUp ? rs.sorted_tok[ps.begin + min(g, ps.count - 1)]
-                                       : 2 * (ps.begin + min(g & 3, ps.count - 1) - ph.e_lo) + (g >> 2);
+    int row = mode == kFfnGateUp ? rs.sorted_tok[ps.begin + min(g, ps.count - 1)]
+                                 : 2 * (ps.begin + min(g & 3, ps.count - 1) - ph.e_lo) + (g >> 2);
+    if (!MOE_DBG_IN_RANGE(row, ph.win_rows, ph.hdr))
+        row = 0;
     return ph.win + (size_t)row * ph.win_row + 8 * cc;
 }
 
@@ -951,12 +955,14 @@ __device__ __forceinline__ void finish_unit(int mode, const FusedArgs *a, const 
                                          float a3) {
     const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
     const Pass ps = passes[P];
+    const int entries = a->T * (a->k + a->S);
     if (mode == kFfnGateUp) {
         const float acc[4] = {a0, a1, a2, a3};
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int n = 2 * c + h;
-            if (n < ps.count) {
+            if (n < ps.count && MOE_DBG_IN_RANGE(ps.begin + n, entries, a->hdr) &&
+                MOE_DBG_IN_RANGE(8 * rb + g, a->I, a->hdr)) {
                 const float xu = rs->xundo[rs->sorted_tok[ps.begin + n]];
                 const float G = acc[h] * xu, U = acc[2 + h] * xu;
                 a->h32[(size_t)(ps.begin + n) * a->I + 8 * rb + g] = G / (1.0f + expf(-G)) * U;
@@ -971,7 +977,9 @@ __device__ __forceinline__ void finish_unit(int mode, const FusedArgs *a, const 
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int n = 2 * c + h;
-                if (n < ps.count) {
+                if (n < ps.count && MOE_DBG_IN_RANGE(ps.begin + n, entries, a->hdr) &&
+                    MOE_DBG_IN_RANGE(ps.begin + n - e_lo, a->win_entries, a->hdr) &&
+                    MOE_DBG_IN_RANGE(16 * rb + g + 8, a->H, a->hdr)) {
                     const int e = ps.begin + n;
                     const float u = hundo[e - e_lo];
                     float *dst = a->yent + (size_t)e * a->H + 16 * rb;
@@ -1048,6 +1056,8 @@ __device__ __forceinline__ bool stream_phase(const FusedArgs *ap, int mode) {
     ph.win_row = down ? a.hwin_row : a.xwin_row;
     ph.e_lo = 0;
     ph.hundo = hundo;
+    ph.win_rows = down ? 2 * a.win_entries : a.T;
+    ph.hdr = a.hdr;
     const long long U = (long long)(down ? rs.n_dn : rs.n_gu) * ph.upe;
     const long long u0 = (long long)blockIdx.x * U / G, u1 = (long long)(blockIdx.x + 1) * U / G;
     const long long Bc = (u1 - u0) * ph.nb;
@@ -1169,7 +1179,9 @@ __device__ void combine_share(const FusedArgs &a, const RouteState &rs) {
 #pragma unroll
         for (int s = 0; s < kMaxSlots; ++s)
             if (s < kps)
-                v[s] = __ldcg(a.yent + (size_t)rs.inv_pos[t * kps + s] * a.H + hcol);
+                v[s] = MOE_DBG_IN_RANGE(rs.inv_pos[t * kps + s], a.T * kps, a.hdr)
+                           ? __ldcg(a.yent + (size_t)rs.inv_pos[t * kps + s] * a.H + hcol)
+                           : 0.0f;
         float acc = 0.0f;
 #pragma unroll
         for (int s = 0; s < kMaxSlots; ++s)

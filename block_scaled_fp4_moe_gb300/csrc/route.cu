@@ -215,10 +215,12 @@ __device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const
             const unsigned same = __match_any_sync(0xffffffffu, e);
             if (i < n) {
                 const int pos = cursor[e] + __popc(same & ((1u << lane) - 1u));
-                o.sorted_tok[pos] = i / kps;
-                o.sorted_slot[pos] = i % kps;
-                if (o.inv_pos)
-                    o.inv_pos[i] = pos;
+                if (MOE_DBG_IN_RANGE(pos, n, hdr)) {
+                    o.sorted_tok[pos] = i / kps;
+                    o.sorted_slot[pos] = i % kps;
+                    if (o.inv_pos)
+                        o.inv_pos[i] = pos;
+                }
             }
             __syncwarp();
             if (i < n && lane == 31 - __clz(same))

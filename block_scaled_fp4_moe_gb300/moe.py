@@ -7,6 +7,7 @@ library is not built or cannot be loaded, every call raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes as C
 import dataclasses
 import os
@@ -39,24 +40,39 @@ class _Bank(C.Structure):
                 ("hidden", C.c_int32), ("inter", C.c_int32)]
 
 
-_lib = None
+_libs: dict[bool, C.CDLL] = {}
 _lock = threading.Lock()
+_debug = False
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    return _build.DEBUG_LIB_PATH if _debug else _build.LIB_PATH
+
+
+@contextlib.contextmanager
+def debug_bounds():
+    """Route the calls below to libmoe_fp4_debug.so, the build with device-side
+    range checks (MOE_DEBUG_BOUNDS), for the duration of the block."""
+    global _debug
+    old, _debug = _debug, True
+    try:
+        yield lib()
+    finally:
+        _debug = old
 
 
 def lib() -> C.CDLL:
-    """The loaded CUDA library; raises if it has not been built."""
-    global _lib
-    if _lib is None:
+    """The loaded CUDA library (the debug build inside debug_bounds()); raises
+    if it has not been built."""
+    debug = _debug
+    if debug not in _libs:
         with _lock:
-            if _lib is None:
-                if not os.path.exists(_build.LIB_PATH):
-                    raise RuntimeError(f"CUDA library {_build.LIB_PATH} is missing: run __graft_entry__.build() "
+            if debug not in _libs:
+                path = _build.DEBUG_LIB_PATH if debug else _build.LIB_PATH
+                if not os.path.exists(path):
+                    raise RuntimeError(f"CUDA library {path} is missing: run __graft_entry__.build() "
                                        "(or python -m block_scaled_fp4_moe_gb300._build)")
-                L = C.CDLL(_build.LIB_PATH)
+                L = C.CDLL(path)
                 p, i, f, s = C.c_void_p, C.c_int, C.c_float, C.c_size_t
                 sig = {
                     "moe_workspace_size": (s, [i, i, i, i, i, i]),
@@ -89,8 +105,8 @@ def lib() -> C.CDLL:
                     fn = getattr(L, name)
                     fn.restype = res
                     fn.argtypes = args
-                _lib = L
-    return _lib
+                _libs[debug] = L
+    return _libs[debug]
 
 
 def exported_symbols() -> list[str]:

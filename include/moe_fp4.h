@@ -127,7 +127,9 @@ moe_status_t moe_pack_bank(const moe_mxfp4_bank_t *bank, void *packed, size_t pa
                            cudaStream_t stream);
 
 /* Bytes of device workspace the calls below need for these sizes (a caller
- * may pass a larger one).  The workspace carries no state between calls
+ * may pass a larger one).  The pages describe no such buffer: it holds the
+ * intermediate results of a1..a6 (router partials, the grouping of a3, h and
+ * the per-entry outputs of a4/a5) so that the library allocates nothing.  The workspace carries no state between calls
  * except its header: the device status word and the counters of the
  * single-launch layer kernel, which every completed call leaves at zero. */
 size_t moe_workspace_size(int T, int H, int I, int E, int top_k, int has_shared);
@@ -139,8 +141,11 @@ size_t moe_workspace_size(int T, int H, int I, int E, int top_k, int has_shared)
  * int32 [E+S+1], "sorted_tok" / "sorted_slot" int32 [T*(k+S)], "active"
  * int32 [E+S] (the first num_active entries), "num_active" one uint32, and
  * "inv_pos" int32 [T*(k+S)] (entry t*(k+S)+s -> its sorted position).
- * Also "topk_ids", "topk_w" (when the call was not given output arrays) and
- * the MXFP8 variant's "mx_xq" [T][H] E4M3 codes of x, "mx_xs" [T][H/32] their
+ * When moe_layer_forward ran as one launch (T <= 8): "h" fp32 [T*(k+S)][I]
+ * (silu(gate) * up of each entry) and "y_entries" fp32 [T*(k+S)][H] (each
+ * entry's down projection, before the weighted combine), rows in sorted
+ * order.  Also "topk_ids", "topk_w" (when the call was not given output
+ * arrays) and the MXFP8 variant's "mx_xq" [T][H] E4M3 codes of x, "mx_xs" [T][H/32] their
  * E8M0 scales, "mx_h32" [T*(k+S)][I] fp32 h, "mx_hq" / "mx_hs" its MXFP8
  * codes and scales, "mx_y" [T*(k+S)][H] fp32 per-entry outputs; entry rows in
  * grouped order).  (size_t)-1 for an unknown name or invalid sizes.
@@ -170,7 +175,10 @@ moe_status_t moe_route_topk(const uint16_t *x, const float *router_w, const floa
                             cudaStream_t stream);
 
 /*
- * a3: token-to-expert grouping of caller-supplied topk_ids [T, k_plus_s].
+ * a3: token-to-expert grouping of caller-supplied topk_ids [T, k_plus_s] --
+ * the step that turns "top-9 of 161 with the shared expert always 9th" into
+ * per-expert batches ("Optimizing GLM4-MoE for production", section 1
+ * "Shared experts fusion").
  * Outputs (device): expert_offsets [n_experts_total+1] (exclusive prefix of
  * per-expert counts), sorted_tok and sorted_slot [T*k_plus_s] (pairs sorted
  * by expert, then token, then slot), active_experts [n_experts_total]
@@ -185,7 +193,11 @@ moe_status_t moe_group_tokens(const int32_t *topk_ids, int T, int k_plus_s, int 
 
 /*
  * a3..a6 for a given routing: grouping, gate/up + SiLU*up, down and the
- * weighted combine.  topk_ids / topk_w [T, top_k + bank->has_shared] (device;
+ * weighted combine -- each token's experts (the shared one included, with
+ * the same tensor shapes) evaluated on MXFP4 weights and their outputs
+ * weighted and summed ("Optimizing GLM4-MoE for production", section 1;
+ * MXFP4 blocks of 32 with one shared exponent: the 1T-model article,
+ * section 2).  topk_ids / topk_w [T, top_k + bank->has_shared] (device;
  * the shared slot, if any, must name expert E).  bank: host pointer to the
  * descriptor (its arrays are device memory).  y [T,H] bf16 (device).
  */

@@ -112,3 +112,16 @@ def check_output(y_bits: np.ndarray, ref: np.ndarray, label: str = "") -> dict:
     bad = err > bound
     assert not bad.any(), (label, stats, int(bad.sum()), float((err / bound).max()))
     return stats
+
+
+def random_problem(T, H, E, k, I, has_shared=1, seed=0, bias=True, shared_weight=1.0):
+    rng = np.random.default_rng(seed)
+    x = inputs.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    wr = (0.02 * rng.standard_normal((H, E))).astype(np.float32)
+    b = (0.05 * rng.standard_normal(E)).astype(np.float32) if bias else None
+    n = E + has_shared
+    bank = {"w13": rng.integers(0, 256, (n, 2 * I, H // 2), dtype=np.uint8),
+            "s13": rng.integers(118, 125, (n, 2 * I, H // 32), dtype=np.uint8),
+            "w2": rng.integers(0, 256, (n, H, I // 2), dtype=np.uint8),
+            "s2": rng.integers(118, 125, (n, H, I // 32), dtype=np.uint8)}
+    return Problem(x, wr, b, bank, E, k, has_shared, shared_weight)

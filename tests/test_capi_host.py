@@ -145,7 +145,22 @@ def test_other_entry_points_argument_checks(L):
 
 
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):
-    monkeypatch.setattr(moe, "_lib", None)
+    monkeypatch.setattr(moe, "_libs", {})
     monkeypatch.setattr(_build, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_build, "DEBUG_LIB_PATH", str(tmp_path / "missing_debug.so"))
     with pytest.raises(RuntimeError, match="missing"):
         moe.lib()
+    with pytest.raises(RuntimeError, match="missing"):
+        with moe.debug_bounds():
+            pass
+
+
+def test_debug_build_exports_the_same_symbols():
+    """libmoe_fp4_debug.so (range checks on) has the same C ABI."""
+    _build.build(debug=True)
+    with moe.debug_bounds() as L:
+        assert moe.library_path() == _build.DEBUG_LIB_PATH
+        for name in moe.exported_symbols():
+            assert hasattr(L, name), name
+        assert L.moe_status_string(moe.MOE_ERR_DEVICE_ASSERT) == b"device-side input check failed"
+    assert moe.library_path() == _build.LIB_PATH

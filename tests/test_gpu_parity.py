@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from block_scaled_fp4_moe_gb300 import _build, inputs, moe
-from gpu_support import Problem, check_grouping, check_output, dev_bf16, host_bits
+from gpu_support import Problem, check_grouping, check_output, dev_bf16, host_bits, random_problem
 
 pytestmark = pytest.mark.gpu
 
@@ -25,19 +25,6 @@ def built():
     _build.build()
     moe.lib()
     torch.cuda.init()
-
-
-def random_problem(T, H, E, k, I, has_shared=1, seed=0, bias=True, shared_weight=1.0):
-    rng = np.random.default_rng(seed)
-    x = inputs.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
-    wr = (0.02 * rng.standard_normal((H, E))).astype(np.float32)
-    b = (0.05 * rng.standard_normal(E)).astype(np.float32) if bias else None
-    n = E + has_shared
-    bank = {"w13": rng.integers(0, 256, (n, 2 * I, H // 2), dtype=np.uint8),
-            "s13": rng.integers(118, 125, (n, 2 * I, H // 32), dtype=np.uint8),
-            "w2": rng.integers(0, 256, (n, H, I // 2), dtype=np.uint8),
-            "s2": rng.integers(118, 125, (n, H, I // 32), dtype=np.uint8)}
-    return Problem(x, wr, b, bank, E, k, has_shared, shared_weight)
 
 
 def compare_all(p: Problem, label: str):
@@ -251,6 +238,55 @@ def test_layer_is_deterministic_and_entry_points_agree():
     yh = torch.empty((p.T, p.H), dtype=torch.bfloat16).pin_memory()
     moe.moe_layer_forward_hostio(xh, p.wrd, p.bd, p.top_k, p.bank, 1.0, yh, ws)
     np.testing.assert_array_equal(yh.view(torch.int16).numpy().view(np.uint16), a["y"])
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 5, 6, 7, 8])
+def test_single_launch_stages_against_the_oracle(T):
+    """The single-launch kernel's intermediate results, entry by entry: h =
+    silu(gate) * up (fp32) and each entry's down projection, against the
+    oracle's, three calls in a row.  At H = 2048 a row block's steps are split
+    across warps, whose partial sums meet in shared memory between the
+    shared expert's gate/up units, the routed ones and the down units."""
+    p = random_problem(T=T, H=2048, E=24, k=4, I=1024, seed=80 + T)
+    assert moe.moe_layer_launches(T, p.bank, p.top_k) == 1
+    r = p.oracle_route()
+    ref = oracle.moe_tokens(p.x, r["ids"], r["w"], p.expert, np.arange(T), want_h=True, want_slots=True)
+    g = oracle.group(r["ids"], p.E + 1)
+    n, I, H = T * p.kps, p.bank.inter, p.H
+    ws = p.workspace()
+    for call in range(3):
+        out = p.forward(ws)
+        np.testing.assert_array_equal(out["ids"], r["ids"])
+        host = ws.cpu().numpy()
+
+        def region(name, cols):
+            off = moe.moe_workspace_offset(T, H, I, p.E, p.top_k, 1, name)
+            return host[off: off + 4 * n * cols].view(np.float32).reshape(n, cols).astype(np.float64)
+        h, ye = region("h", I), region("y_entries", H)
+        for pos in range(n):
+            t, sl = g["sorted_tok"][pos], g["sorted_slot"][pos]
+            hr, yr = ref["h"][t, sl], ref["y_slots"][t, sl]
+            assert np.abs(h[pos] - hr).max() <= 1e-5 * np.abs(hr).max(), (call, pos, t, sl)
+            assert np.abs(ye[pos] - yr).max() <= 1e-5 * np.abs(yr).max(), (call, pos, t, sl)
+        check_output(out["y"], ref["y"], f"stages T={T} call {call}")
+
+
+@pytest.mark.parametrize("T,H,E,k,I", [(6, 512, 1024, 8, 256), (8, 1024, 160, 8, 512), (1, 1024, 16, 4, 512)])
+def test_single_launch_calls_in_a_row_on_one_workspace(T, H, E, k, I):
+    """Calls on one workspace leave its counters and router tickets ready for
+    the next: five calls in a row give the oracle's routing and bit-identical
+    outputs (E = 1024 and T = 8 take the ticketed router sums)."""
+    p = random_problem(T=T, H=H, E=E, k=k, I=I, seed=70 + T)
+    assert moe.moe_layer_launches(T, p.bank, k) == 1
+    ws = p.workspace()
+    first = p.forward(ws)
+    r = p.oracle_route()
+    np.testing.assert_array_equal(first["ids"], r["ids"])
+    check_output(first["y"], p.oracle_tokens(r, np.arange(T))["y"], f"repeat T={T} E={E}")
+    for _ in range(4):
+        again = p.forward(ws)
+        np.testing.assert_array_equal(again["ids"], first["ids"])
+        np.testing.assert_array_equal(again["y"], first["y"])
 
 
 @pytest.mark.parametrize("T", [1, 4, 13])
