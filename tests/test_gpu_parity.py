@@ -160,6 +160,8 @@ SMALL = [
     dict(T=80, H=1024, E=4, k=2, I=512),           # several wide passes per expert (tiled kernels)
     dict(T=33, H=1536, E=12, k=3, I=1024, has_shared=0),   # tiled kernels without a shared expert
     dict(T=9, H=1024, E=16, k=8, I=512),           # first T of the multi-launch path
+    dict(T=16, H=1024, E=16, k=8, I=512),          # the speculative-verify block size
+    dict(T=16, H=1024, E=40, k=8, I=512, has_shared=0),
     dict(T=5, H=1024, E=16, k=4, I=512, has_shared=0),
     dict(T=9, H=320, E=5, k=5, I=192),             # block-mode scales, k == E
     dict(T=2, H=2048, E=4, k=2, I=2048),
@@ -396,6 +398,7 @@ def test_launch_count_and_phase_times():
     assert moe.moe_layer_launches(1, p.bank, p.top_k) == 1
     assert moe.moe_layer_launches(8, p.bank, p.top_k) == 1
     assert moe.moe_layer_launches(9, p.bank, p.top_k) == 6
+    assert moe.moe_layer_launches(16, p.bank, p.top_k) == 6
     assert moe.moe_layer_launches(0, p.bank, p.top_k) == 0
     out = p.forward()
     ph = moe.moe_read_phase_times(out["ws"])
