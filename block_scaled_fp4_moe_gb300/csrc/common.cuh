@@ -125,7 +125,7 @@ inline void fused_router_tiling(int H, int E, int *groups, int *chunks, int *row
 // Offsets (bytes) of the workspace regions for one problem size.
 struct WsLayout {
     size_t route_part, topk_ids, topk_w, offsets, sorted_tok, sorted_slot, inv_pos, active, passes, passes4, passesw,
-        passesw4, x16, xundo,
+        passesw4, x16, xundo, xs16,
         gpart, h16, hundo, ypart, counters, xstage, ystage, fz_rpart, fz_h32, fz_yent, mx_xq, mx_xs, mx_gu, mx_h32,
         mx_hq, mx_hs, mx_y, total;
     int n_kc_gu, n_kc_dn;
@@ -156,6 +156,7 @@ struct WsLayout {
         L.passesw4 = take((size_t)max_passes(T, kps, n_tot, kWidePassEntries) * sizeof(Pass));
         L.x16 = take((size_t)T * H * 2);
         L.xundo = take((size_t)T * sizeof(float));
+        L.xs16 = T > kFusedMaxTokens ? take(entries * H * 2) : 0;   // x per sorted entry (tensor-memory kernels)
         L.gpart = take((size_t)L.n_kc_gu * entries * 2 * I * sizeof(float));
         L.h16 = take(entries * 2 * (size_t)I * 2);
         L.hundo = take(entries * sizeof(float));

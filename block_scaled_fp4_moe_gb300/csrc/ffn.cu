@@ -24,6 +24,10 @@
 //    maps its largest magnitude into [2^14, 2^15) (exact for every bf16 value
 //    within 2^28 of the maximum), h is split into hi + lo f16 terms after the
 //    same kind of scaling; scales are undone in fp32.
+//
+// From T = 9 on (and H, I multiples of 512) the gate/up and down projections
+// run instead on the tensor-memory kernels of tc.cu; the kernels here cover
+// the single-launch kernel's shapes that do not fit it and the other shapes.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -371,351 +375,8 @@ __global__ void __launch_bounds__(NW * 32, 1) ffn_kernel(const __grid_constant__
     }
 }
 
-// ------------------------------------------------------ tiled (large T)
-//
-// When experts hold many tokens, streaming a pass of 8 tokens at a time
-// re-reads an expert's weights once per pass and, past a few tokens, reads the
-// B operand from L2 with a long latency chain.  The tiled kernels take wide
-// passes (gate/up: up to 32 tokens, down: up to 16 entries as hi + lo
-// columns) so that every decoded weight tile feeds four MMA column groups,
-// and stage the B operand of the pass in shared memory one K-chunk (8 steps,
-// 512 elements) at a time, double-buffered with cp.async.  A work item is a
-// pass and a group of 12 row blocks (one per warp), streamed over the whole K
-// with the register batches of the other kernels; the item writes its sums
-// once (K-chunk count 1 in the partial layouts of hfin and combine).
-
-constexpr int kTileWarps = 12;
-constexpr int kTiledMinTokens = 9;               // T from which the tiled kernels run
-constexpr int kTileCols = 32;                    // B columns: 4 MMA column groups
-constexpr int kTileRow = 8 * 64 + 32;            // B tile row stride in halves: 1088 B, rows g and g+1 on disjoint bank quads
-constexpr size_t kTileSmem = (size_t)2 * kTileCols * kTileRow * sizeof(__half);
-
-struct TiledArgs {
-    const uint8_t *packed;       // section of the repacked bank
-    size_t unit_bytes;           // steps * 544
-    int upe;                     // row blocks per expert
-    int steps;                   // K / 64 (a multiple of 8)
-    const __half *b16;           // gate/up: x16 [T][H]; down: h16 [entries][2][I]
-    int b_row;                   // B row length (H or I)
-    const Pass *passes;          // wide passes
-    int passes_word;             // header word holding their number
-    const int32_t *sorted_tok;
-    const uint32_t *hdr;
-    float *part;                 // gate/up: [entries][2][I]; down: [entries][H]
-    int out_len;                 // I (gate/up) or H (down)
-    const float *bundo;          // down: per-entry factor that undoes the h scaling
-    int n_entries;               // T * (k + S) (range checks of the debug build)
-};
-
-// The sums of row block u of pass ps are complete: gate/up writes the gate
-// and up sums of its real tokens; down adds each lo column to its hi column,
-// undoes the entry's h scaling and writes the entries' outputs.
-template <int MODE>
-__device__ __forceinline__ void tiled_epilogue(const TiledArgs &a, const Pass &ps, int ncg, int u,
-                                               const float (&acc)[4][4]) {
-    const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-    if (MODE == kFfnGateUp) {
-#pragma unroll
-        for (int cg = 0; cg < 4; ++cg) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const int n = 8 * cg + 2 * c + h;
-                if (cg < ncg && n < ps.count && MOE_DBG_IN_RANGE(ps.begin + n, a.n_entries, a.hdr) &&
-                    MOE_DBG_IN_RANGE(8 * u + g, a.out_len, a.hdr)) {
-                    float *dst = a.part + (size_t)(ps.begin + n) * 2 * a.out_len + 8 * u + g;
-                    dst[0] = acc[cg][h];                      // gate row
-                    dst[a.out_len] = acc[cg][2 + h];          // up row
-                }
-            }
-        }
-    } else {
-#pragma unroll
-        for (int cg = 0; cg < 4; ++cg) {
-            if (cg < ncg) {
-                float y[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)                  // add the lo column to the hi column
-                    y[i] = acc[cg][i] + __shfl_xor_sync(0xffffffffu, acc[cg][i], 2);
-                if (c < 2) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int n = 4 * cg + 2 * c + h;
-                        if (n < ps.count && MOE_DBG_IN_RANGE(ps.begin + n, a.n_entries, a.hdr) &&
-                            MOE_DBG_IN_RANGE(16 * u + g + 8, a.out_len, a.hdr)) {
-                            const int e = ps.begin + n;
-                            const float un = a.bundo[e];
-                            float *dst = a.part + (size_t)e * a.out_len + 16 * u;
-                            dst[g] = y[h] * un;
-                            dst[g + 8] = y[2 + h] * un;
-                        }
-                    }
-                }
-            }
-        }
-    }
-}
-
-template <int MODE>
-__global__ void __launch_bounds__(kTileWarps * 32, 1) ffn_tiled_kernel(const __grid_constant__ TiledArgs a) {
-    extern __shared__ __align__(16) uint8_t tsm[];
-    __half *tile = reinterpret_cast<__half *>(tsm);            // [2][kTileCols][kTileRow]
-    __shared__ int brow[kTileCols];                            // element offset of each column's B row
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, c = lane & 3;
-    pdl_wait();
-    pdl_trigger();
-    const int n_passes = *reinterpret_cast<const volatile int *>(a.hdr + a.passes_word);
-    const int n_rg = (a.upe + kTileWarps - 1) / kTileWarps;
-    const long long n_items = (long long)n_passes * n_rg;
-    const int nkc = a.steps / 8;
-    const uint64_t pol = l2_evict_first_policy();
-    for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const int P = (int)(item / n_rg), rg = (int)(item - (long long)P * n_rg);
-        const Pass ps = a.passes[P];
-        // column groups of 8 in use: gate/up 8 tokens each, down 4 entries (hi, lo) each
-        const int ncg = MODE == kFfnGateUp ? (ps.count + 7) >> 3 : (ps.count + 3) >> 2;
-        __syncthreads();                                       // the previous item is done with brow and tile
-        if (threadIdx.x < kTileCols) {
-            const int col = threadIdx.x;
-            int row;
-            if (MODE == kFfnGateUp) {
-                row = a.sorted_tok[ps.begin + (col < ps.count ? col : 0)];
-            } else {
-                const int j = 4 * (col >> 3) + (col & 3);
-                row = 2 * (ps.begin + (j < ps.count ? j : 0)) + ((col >> 2) & 1);
-            }
-            brow[col] = row * a.b_row;
-        }
-        __syncthreads();
-        const int u = rg * kTileWarps + warp;
-        const bool active = u < a.upe;
-        const uint8_t *wp = a.packed + ((size_t)ps.expert * a.upe + (active ? u : 0)) * a.unit_bytes;
-        const int rows = 8 * ncg;
-        auto fill = [&](int kc) {
-            __half *dst = tile + (kc & 1) * (kTileCols * kTileRow);
-            for (int i = threadIdx.x; i < rows * 64; i += blockDim.x) {
-                const int r = i >> 6, k8 = i & 63;
-                cp_async16(dst + r * kTileRow + k8 * 8, a.b16 + brow[r] + kc * 512 + k8 * 8);
-            }
-            cp_async_commit();
-        };
-        uint4 q[2][8];
-        uint32_t s[2][8];
-        auto load = [&](int kc, uint4 (&qq)[8], uint32_t (&ss)[8]) {
-            if (!active)
-                return;
-            const uint8_t *p = wp + (size_t)kc * 8 * kStepBytes;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                qq[j] = ld_stream16(p + j * kStepBytes + lane * 16, pol);
-                ss[j] = ld_stream4(p + j * kStepBytes + 512 + g * 4, pol);
-            }
-        };
-        float acc[4][4];
-#pragma unroll
-        for (int cg = 0; cg < 4; ++cg)
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                acc[cg][i] = 0.0f;
-        auto compute = [&](const uint4 (&qq)[8], const uint32_t (&ss)[8], int kc) {
-            if (!active)
-                return;
-            const __half *tb = tile + (kc & 1) * (kTileCols * kTileRow) + g * kTileRow + 8 * c;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                uint32_t pa0[4], qa0[4], pa1[4], qa1[4];
-                decode_e2m1x8(qq[j].x, pa0);           // block 2q: rows g, g+8
-                decode_e2m1x8(qq[j].y, qa0);
-                decode_e2m1x8(qq[j].z, pa1);           // block 2q+1
-                decode_e2m1x8(qq[j].w, qa1);
-                float sg0, sg1, sh0, sh1;
-                e8m0x4_to_f32(ss[j], sg0, sg1, sh0, sh1);
-                const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                for (int cg = 0; cg < 4; ++cg) {
-                    if (cg < ncg) {
-                        const __half *bp = tb + cg * 8 * kTileRow + 64 * j;
-                        const uint4 b0 = *reinterpret_cast<const uint4 *>(bp);
-                        const uint4 b1 = *reinterpret_cast<const uint4 *>(bp + 32);
-                        float d[4], e[4];
-                        mma_m16n8k16_f16(d, pa0[0], qa0[0], pa0[1], qa0[1], b0.x, b0.y, zero);
-                        mma_m16n8k16_f16(d, pa0[2], qa0[2], pa0[3], qa0[3], b0.z, b0.w, d);
-                        mma_m16n8k16_f16(e, pa1[0], qa1[0], pa1[1], qa1[1], b1.x, b1.y, zero);
-                        mma_m16n8k16_f16(e, pa1[2], qa1[2], pa1[3], qa1[3], b1.z, b1.w, e);
-                        acc[cg][0] = fmaf(d[0], sg0, fmaf(e[0], sg1, acc[cg][0]));
-                        acc[cg][1] = fmaf(d[1], sg0, fmaf(e[1], sg1, acc[cg][1]));
-                        acc[cg][2] = fmaf(d[2], sh0, fmaf(e[2], sh1, acc[cg][2]));
-                        acc[cg][3] = fmaf(d[3], sh0, fmaf(e[3], sh1, acc[cg][3]));
-                    }
-                }
-            }
-        };
-        fill(0);
-        load(0, q[0], s[0]);
-        for (int kc = 0; kc < nkc; kc += 2) {
-            if (kc + 1 < nkc) {
-                fill(kc + 1);
-                load(kc + 1, q[1], s[1]);
-                cp_async_wait<1>();
-            } else {
-                cp_async_wait<0>();
-            }
-            __syncthreads();
-            compute(q[0], s[0], kc);
-            __syncthreads();                                   // buffer kc & 1 is refilled two chunks on
-            if (kc + 1 >= nkc)
-                break;
-            if (kc + 2 < nkc) {
-                fill(kc + 2);
-                load(kc + 2, q[0], s[0]);
-                cp_async_wait<1>();
-            } else {
-                cp_async_wait<0>();
-            }
-            __syncthreads();
-            compute(q[1], s[1], kc + 1);
-            __syncthreads();
-        }
-        if (!active)
-            continue;
-        tiled_epilogue<MODE>(a, ps, ncg, u, acc);
-    }
-}
-
-// Whole-K variant (the down projection, K = I): the pass's B rows over all of
-// K fit in shared memory, so they are copied once per item and every warp
-// streams several row blocks back to back (a ring of two register batches
-// running across row blocks), with no barrier inside the stream.  An item is
-// a pass and up to kKfUnitsPerWarp row blocks per warp.
-constexpr int kKfUnitsPerWarp = 4;
-
-inline size_t kfull_smem(int K, int cols) { return (size_t)cols * (K + 32) * sizeof(__half); }
-
-template <int MODE>
-__global__ void __launch_bounds__(kTileWarps * 32, 1) ffn_tiled_kfull_kernel(const __grid_constant__ TiledArgs a) {
-    extern __shared__ __align__(16) uint8_t tsm[];
-    __half *win = reinterpret_cast<__half *>(tsm);             // [kTileCols][K + 32]
-    __shared__ int brow[kTileCols];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int g = lane >> 2, c = lane & 3;
-    pdl_wait();
-    pdl_trigger();
-    const int K = a.b_row, wrow = K + 32;
-    const int n_passes = *reinterpret_cast<const volatile int *>(a.hdr + a.passes_word);
-    // row blocks per warp and item: up to kKfUnitsPerWarp, fewer when there
-    // are too few items to give every CTA about two
-    const int rg1 = (a.upe + kTileWarps - 1) / kTileWarps;
-    const int upw = max(1, min(kKfUnitsPerWarp, (int)((long long)n_passes * rg1 / (2 * gridDim.x))));
-    const int rgu = upw * kTileWarps;
-    const int n_rg = (a.upe + rgu - 1) / rgu;
-    const long long n_items = (long long)n_passes * n_rg;
-    const int nkc = a.steps / 8;
-    const uint64_t pol = l2_evict_first_policy();
-    for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const int P = (int)(item / n_rg), rg = (int)(item - (long long)P * n_rg);
-        const Pass ps = a.passes[P];
-        const int ncg = MODE == kFfnGateUp ? (ps.count + 7) >> 3 : (ps.count + 3) >> 2;
-        __syncthreads();
-        if (threadIdx.x < kTileCols) {
-            const int col = threadIdx.x;
-            int row;
-            if (MODE == kFfnGateUp) {
-                row = a.sorted_tok[ps.begin + (col < ps.count ? col : 0)];
-            } else {
-                const int j = 4 * (col >> 3) + (col & 3);
-                row = 2 * (ps.begin + (j < ps.count ? j : 0)) + ((col >> 2) & 1);
-            }
-            brow[col] = row * K;
-        }
-        __syncthreads();
-        // this warp's row blocks: rg * rgu + warp + kTileWarps * j
-        int nu = 0;
-        while (nu < upw && rg * rgu + warp + kTileWarps * nu < a.upe)
-            ++nu;
-        const int nbat = nu * nkc;
-        const uint8_t *ebase = a.packed + (size_t)ps.expert * a.upe * a.unit_bytes;
-        auto load = [&](int b, uint4 (&qq)[8], uint32_t (&ss)[8]) {
-            const int j = b / nkc, kc = b - j * nkc;
-            const int u = rg * rgu + warp + kTileWarps * j;
-            const uint8_t *p = ebase + (size_t)u * a.unit_bytes + (size_t)kc * 8 * kStepBytes;
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                qq[s] = ld_stream16(p + s * kStepBytes + lane * 16, pol);
-                ss[s] = ld_stream4(p + s * kStepBytes + 512 + g * 4, pol);
-            }
-        };
-        uint4 q[2][8];
-        uint32_t s[2][8];
-        if (nbat > 0)
-            load(0, q[0], s[0]);              // weights first, then the window copy
-        const int rows = 8 * ncg;
-        for (int i = threadIdx.x; i < rows * (K / 8); i += blockDim.x) {
-            const int r = i / (K / 8), k8 = i - r * (K / 8);
-            cp_async16(win + r * wrow + k8 * 8, a.b16 + brow[r] + k8 * 8);
-        }
-        cp_async_commit();
-        cp_async_wait<0>();
-        __syncthreads();
-        float acc[4][4];
-#pragma unroll
-        for (int cg = 0; cg < 4; ++cg)
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                acc[cg][i] = 0.0f;
-        const __half *wb = win + g * wrow + 8 * c;
-        auto compute = [&](const uint4 (&qq)[8], const uint32_t (&ss)[8], int b) {
-            const int j = b / nkc, kc = b - j * nkc;
-            const __half *tb = wb + kc * 512;
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                uint32_t pa0[4], qa0[4], pa1[4], qa1[4];
-                decode_e2m1x8(qq[t].x, pa0);
-                decode_e2m1x8(qq[t].y, qa0);
-                decode_e2m1x8(qq[t].z, pa1);
-                decode_e2m1x8(qq[t].w, qa1);
-                float sg0, sg1, sh0, sh1;
-                e8m0x4_to_f32(ss[t], sg0, sg1, sh0, sh1);
-                const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                for (int cg = 0; cg < 4; ++cg) {
-                    if (cg < ncg) {
-                        const __half *bp = tb + cg * 8 * wrow + 64 * t;
-                        const uint4 b0 = *reinterpret_cast<const uint4 *>(bp);
-                        const uint4 b1 = *reinterpret_cast<const uint4 *>(bp + 32);
-                        float d[4], e[4];
-                        mma_m16n8k16_f16(d, pa0[0], qa0[0], pa0[1], qa0[1], b0.x, b0.y, zero);
-                        mma_m16n8k16_f16(d, pa0[2], qa0[2], pa0[3], qa0[3], b0.z, b0.w, d);
-                        mma_m16n8k16_f16(e, pa1[0], qa1[0], pa1[1], qa1[1], b1.x, b1.y, zero);
-                        mma_m16n8k16_f16(e, pa1[2], qa1[2], pa1[3], qa1[3], b1.z, b1.w, e);
-                        acc[cg][0] = fmaf(d[0], sg0, fmaf(e[0], sg1, acc[cg][0]));
-                        acc[cg][1] = fmaf(d[1], sg0, fmaf(e[1], sg1, acc[cg][1]));
-                        acc[cg][2] = fmaf(d[2], sh0, fmaf(e[2], sh1, acc[cg][2]));
-                        acc[cg][3] = fmaf(d[3], sh0, fmaf(e[3], sh1, acc[cg][3]));
-                    }
-                }
-            }
-            if (kc == nkc - 1) {              // the row block is complete
-                const int u = rg * rgu + warp + kTileWarps * j;
-                tiled_epilogue<MODE>(a, ps, ncg, u, acc);
-#pragma unroll
-                for (int cg = 0; cg < 4; ++cg)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        acc[cg][i] = 0.0f;
-            }
-        };
-        for (int b = 0; b < nbat; b += 2) {
-            if (b + 1 < nbat)
-                load(b + 1, q[1], s[1]);
-            compute(q[0], s[0], b);
-            if (b + 1 >= nbat)
-                break;
-            if (b + 2 < nbat)
-                load(b + 2, q[0], s[0]);
-            compute(q[1], s[1], b + 1);
-        }
-    }
-}
+// T from which the expert FFN runs on the tensor-memory kernels (tc.cu).
+constexpr int kTiledMinTokens = 9;
 
 // --------------------------------------------------------- finalize + combine
 
@@ -725,7 +386,7 @@ __global__ void __launch_bounds__(kTileWarps * 32, 1) ffn_tiled_kfull_kernel(con
 __global__ void __launch_bounds__(512)
 hfin_kernel(const float *__restrict__ part, int n_kc, int n_entries, int I, const int32_t *__restrict__ sorted_tok,
             const float *__restrict__ xundo, __half *__restrict__ h16, float *__restrict__ hundo,
-            const uint32_t *__restrict__ hdr) {
+            const uint32_t *__restrict__ hdr, int tc_order) {
     extern __shared__ float hbuf[];   // [I]
     __shared__ float wmax[16];
     const int r = blockIdx.x;
@@ -784,8 +445,12 @@ hfin_kernel(const float *__restrict__ part, int n_kc, int n_entries, int I, cons
     for (int j = threadIdx.x; j < I; j += blockDim.x) {
         const float v = hbuf[j] * sc;
         const __half a = __float2half_rn(v);
-        hi[j] = a;
-        lo[j] = __float2half_rn(v - __half2float(a));
+        // tensor-memory K order: element k of a 64-element step at position
+        // (k & 0x23) | (bit 2 of k at bit 4) | (bits 3-4 of k at bits 2-3)
+        const int k = j & 63;
+        const int pos = tc_order ? (j & ~63) | (k & 0x23) | (((k >> 2) & 1) << 4) | (((k >> 3) & 3) << 2) : j;
+        hi[pos] = a;
+        lo[pos] = __float2half_rn(v - __half2float(a));
     }
     if (threadIdx.x == 0)
         hundo[r] = exp2i(-sh);
@@ -920,105 +585,6 @@ static cudaError_t launch_mode(FfnArgs &a, int grid, int cache_passes, int windo
     return launch_aligned<MODE, false>(a, grid, cache_bytes, stream);
 }
 
-// Large T: tiled gate/up, h finalize, tiled down, combine (K-chunk count 1).
-static cudaError_t launch_ffn_tiled(const FfnProblem &pr, void *ws, const WsLayout &L, int num_sms,
-                                   cudaStream_t stream, cudaEvent_t ev_after_gateup) {
-    const moe_mxfp4_bank_t &b = *pr.bank;
-    const int H = b.hidden, I = b.inter, T = pr.T, kps = pr.kps;
-    const int n_tot = b.num_experts + b.has_shared;
-    const int entries = T * kps;
-    const PackedLayout PL = packed_layout(H, I, n_tot);
-    uint32_t *hdr = ws_at<uint32_t>(ws, 0);
-    static std::atomic<int> attr_set{0};
-    cudaError_t err;
-    if (!attr_set.load()) {
-        if ((err = cudaFuncSetAttribute(ffn_tiled_kernel<kFfnGateUp>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kTileSmem)) != cudaSuccess ||
-            (err = cudaFuncSetAttribute(ffn_tiled_kernel<kFfnDown>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kTileSmem)) != cudaSuccess)
-            return err;
-        attr_set.store(1);
-    }
-    TiledArgs g{};
-    g.packed = b.packed + PL.gu_offset;
-    g.unit_bytes = PL.gu_unit_bytes;
-    g.upe = PL.gu_units_per_expert;
-    g.steps = H / 64;
-    g.b16 = ws_at<__half>(ws, L.x16);
-    g.b_row = H;
-    g.passes = ws_at<Pass>(ws, L.passesw);
-    g.passes_word = kHdrNumPassesW;
-    g.sorted_tok = ws_at<int32_t>(ws, L.sorted_tok);
-    g.hdr = hdr;
-    g.part = ws_at<float>(ws, L.gpart);
-    g.out_len = I;
-    g.n_entries = entries;
-    const size_t gsm = kfull_smem(H, kWidePassEntries);
-    if (gsm <= 200 * 1024) {                // 16 tokens' x rows over all of H fit: whole-K items
-        g.passes = ws_at<Pass>(ws, L.passesw4);
-        g.passes_word = kHdrNumPassesW4;
-        static std::atomic<int> gset{0};
-        if (gset.load() < (int)gsm) {
-            if ((err = cudaFuncSetAttribute(ffn_tiled_kfull_kernel<kFfnGateUp>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsm)) != cudaSuccess)
-                return err;
-            gset.store((int)gsm);
-        }
-        err = launch_pdl(ffn_tiled_kfull_kernel<kFfnGateUp>, dim3(num_sms), dim3(kTileWarps * 32), gsm, stream, g);
-    } else {
-        err = launch_pdl(ffn_tiled_kernel<kFfnGateUp>, dim3(num_sms), dim3(kTileWarps * 32), kTileSmem, stream, g);
-    }
-    if (err != cudaSuccess)
-        return err;
-    const size_t hsmem = (size_t)I * sizeof(float);
-    if (hsmem > 48 * 1024 &&
-        (err = cudaFuncSetAttribute(hfin_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsmem)) !=
-            cudaSuccess)
-        return err;
-    err = launch_pdl(hfin_kernel, dim3(entries), dim3(512), hsmem, stream, (const float *)ws_at<float>(ws, L.gpart),
-                     1, entries, I, (const int32_t *)ws_at<int32_t>(ws, L.sorted_tok),
-                     (const float *)ws_at<float>(ws, L.xundo), ws_at<__half>(ws, L.h16), ws_at<float>(ws, L.hundo),
-                     (const uint32_t *)hdr);
-    if (err != cudaSuccess)
-        return err;
-    if (ev_after_gateup && (err = cudaEventRecord(ev_after_gateup, stream)) != cudaSuccess)
-        return err;
-    TiledArgs d{};
-    d.packed = b.packed + PL.dn_offset;
-    d.unit_bytes = PL.dn_unit_bytes;
-    d.upe = PL.dn_units_per_expert;
-    d.steps = I / 64;
-    d.b16 = ws_at<__half>(ws, L.h16);
-    d.b_row = I;
-    d.passes = ws_at<Pass>(ws, L.passesw4);
-    d.passes_word = kHdrNumPassesW4;
-    d.sorted_tok = g.sorted_tok;
-    d.hdr = hdr;
-    d.part = ws_at<float>(ws, L.ypart);
-    d.out_len = H;
-    d.n_entries = entries;
-    d.bundo = ws_at<float>(ws, L.hundo);
-    const size_t ksm = kfull_smem(I, kTileCols);
-    if (ksm <= 200 * 1024) {                // the pass's h rows over all of I fit: whole-K items
-        static std::atomic<int> kset{0};
-        if (kset.load() < (int)ksm) {
-            if ((err = cudaFuncSetAttribute(ffn_tiled_kfull_kernel<kFfnDown>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ksm)) != cudaSuccess)
-                return err;
-            kset.store((int)ksm);
-        }
-        err = launch_pdl(ffn_tiled_kfull_kernel<kFfnDown>, dim3(num_sms), dim3(kTileWarps * 32), ksm, stream, d);
-    } else {
-        err = launch_pdl(ffn_tiled_kernel<kFfnDown>, dim3(num_sms), dim3(kTileWarps * 32), kTileSmem, stream, d);
-    }
-    if (err != cudaSuccess)
-        return err;
-    return launch_pdl(combine_kernel, dim3(T * ((H + 255) / 256)), dim3(256), 0, stream,
-                      (const float *)ws_at<float>(ws, L.ypart), 1, entries,
-                      (const int32_t *)ws_at<int32_t>(ws, L.inv_pos), pr.topk_w, T, kps, H, pr.y,
-                      (const uint32_t *)hdr);
-}
-
 cudaError_t launch_ffn(const FfnProblem &pr, void *ws, const WsLayout &L, int num_sms, cudaStream_t stream,
                        cudaEvent_t ev_after_gateup) {
     const moe_mxfp4_bank_t &b = *pr.bank;
@@ -1027,8 +593,8 @@ cudaError_t launch_ffn(const FfnProblem &pr, void *ws, const WsLayout &L, int nu
     const int entries = T * kps;
     const PackedLayout PL = packed_layout(H, I, n_tot);
     uint32_t *hdr = ws_at<uint32_t>(ws, 0);
-    if (T >= kTiledMinTokens && H % 512 == 0 && I % 512 == 0)
-        return launch_ffn_tiled(pr, ws, L, num_sms, stream, ev_after_gateup);
+    if (T >= kTiledMinTokens && tc_shape_supported(H, I) && L.xs16 != 0)
+        return launch_ffn_tc(pr, ws, L, num_sms, stream, ev_after_gateup);
     // passes a CTA can touch: its share of all passes plus both boundary passes
     const int cache_passes = max_passes(T, kps, n_tot) / num_sms + 3;
     const int cache_passes4 = max_passes(T, kps, n_tot, kPassEntries) / num_sms + 3;
@@ -1061,7 +627,7 @@ cudaError_t launch_ffn(const FfnProblem &pr, void *ws, const WsLayout &L, int nu
     err = launch_pdl(hfin_kernel, dim3(entries), dim3(512), hsmem, stream, (const float *)ws_at<float>(ws, L.gpart),
                      L.n_kc_gu, entries, I, (const int32_t *)ws_at<int32_t>(ws, L.sorted_tok),
                      (const float *)ws_at<float>(ws, L.xundo), ws_at<__half>(ws, L.h16), ws_at<float>(ws, L.hundo),
-                     (const uint32_t *)hdr);
+                     (const uint32_t *)hdr, 0);
     if (err != cudaSuccess)
         return err;
     if (ev_after_gateup &&
@@ -1100,6 +666,19 @@ cudaError_t launch_combine(const float *yent, int entries, const int32_t *inv_po
                            int H, uint16_t *y, const uint32_t *hdr, cudaStream_t stream) {
     return launch_pdl(combine_kernel, dim3(T * ((H + 255) / 256)), dim3(256), 0, stream, yent, 1, entries, inv_pos,
                       topk_w, T, kps, H, y, hdr);
+}
+
+cudaError_t launch_hfin(void *ws, const WsLayout &L, int entries, int I, bool tc_order, cudaStream_t stream) {
+    const size_t hsmem = (size_t)I * sizeof(float);
+    cudaError_t err;
+    if (hsmem > 48 * 1024 &&
+        (err = cudaFuncSetAttribute(hfin_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsmem)) !=
+            cudaSuccess)
+        return err;
+    return launch_pdl(hfin_kernel, dim3(entries), dim3(512), hsmem, stream, (const float *)ws_at<float>(ws, L.gpart),
+                      1, entries, I, (const int32_t *)ws_at<int32_t>(ws, L.sorted_tok),
+                      (const float *)ws_at<float>(ws, L.xundo), ws_at<__half>(ws, L.h16), ws_at<float>(ws, L.hundo),
+                      (const uint32_t *)ws_at<uint32_t>(ws, 0), tc_order ? 1 : 0);
 }
 
 cudaError_t launch_x16(const uint16_t *x, int T, int H, void *ws, const WsLayout &L, cudaStream_t stream) {

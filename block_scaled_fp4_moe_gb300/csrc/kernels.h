@@ -128,7 +128,7 @@ cudaError_t launch_wait_selftest(uint32_t *hdr, cudaStream_t stream);
 
 // Byte offsets inside a repacked bank (pack.cu).
 struct PackedLayout {
-    size_t gu_unit_bytes, dn_unit_bytes, gu_offset, dn_offset, total;
+    size_t gu_unit_bytes, dn_unit_bytes, gu_offset, dn_offset, gu_rowexp, dn_rowexp, total;
     int gu_units_per_expert, dn_units_per_expert;
 };
 PackedLayout packed_layout(int H, int I, int n_experts_total);
@@ -138,5 +138,18 @@ cudaError_t launch_selftest_decode(const uint8_t *codes, uint16_t *out, int n, c
 
 // Shape rules shared by validation and the kernels' staging choices.
 bool ffn_shape_supported(int H, int I);
+
+// Tensor-memory expert FFN for T > 8 (tc.cu): H and I multiples of 512.
+bool tc_shape_supported(int H, int I);
+// Exponent base per weight row into the packed bank's two row sections.
+cudaError_t launch_rowexp(const moe_mxfp4_bank_t &b, uint8_t *packed, cudaStream_t stream);
+// x gathered per sorted entry, the tensor-core gate/up, h finalisation, the
+// tensor-core down and the combine.  Grouping results (passes of <= 32
+// tokens and <= 16 entries) and x16 must already be in the workspace.
+cudaError_t launch_ffn_tc(const FfnProblem &p, void *ws, const WsLayout &L, int num_sms, cudaStream_t stream,
+                          cudaEvent_t ev_after_gateup);
+// h = silu(g) u from the gate/up sums (one K chunk) into h16 (hi, lo) and
+// hundo; tc_order: each 64-element step of h16 in the tensor-memory K order.
+cudaError_t launch_hfin(void *ws, const WsLayout &L, int entries, int I, bool tc_order, cudaStream_t stream);
 
 }  // namespace moe

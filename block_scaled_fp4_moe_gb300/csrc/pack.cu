@@ -6,6 +6,11 @@
 // delivers the mma.sync A-fragments of a 16-row x 64-element tile and one
 // 4-byte load per lane its block exponents.  Layout (see packed_layout()):
 //
+// followed by two small sections (not a permutation of the canonical bytes)
+// that the tensor-memory kernels read: one exponent base per weight row, in
+// the unit-row order of each section (gate/up [E+S][2I], down [E+S][H]),
+// each at a 256-byte aligned offset (launch_rowexp in tc.cu).
+//
 //   section gate/up: for expert e, for row block rb < I/8 (MMA rows 0..7 =
 //     gate rows 8rb..8rb+7, MMA rows 8..15 = up rows I+8rb..I+8rb+7):
 //   section down:    for expert e, for row block rb < H/16 (MMA rows 0..15 =
@@ -74,7 +79,9 @@ PackedLayout packed_layout(int H, int I, int n_experts_total) {
     p.dn_units_per_expert = H / 16;
     p.gu_offset = 0;
     p.dn_offset = align_up(p.gu_unit_bytes * p.gu_units_per_expert * n_experts_total, 256);
-    p.total = align_up(p.dn_offset + p.dn_unit_bytes * p.dn_units_per_expert * n_experts_total, 256);
+    p.gu_rowexp = align_up(p.dn_offset + p.dn_unit_bytes * p.dn_units_per_expert * n_experts_total, 256);
+    p.dn_rowexp = align_up(p.gu_rowexp + (size_t)n_experts_total * 2 * I, 256);
+    p.total = align_up(p.dn_rowexp + (size_t)n_experts_total * H, 256);
     return p;
 }
 
@@ -89,7 +96,9 @@ cudaError_t launch_pack(const moe_mxfp4_bank_t &b, uint8_t *out, cudaStream_t st
         return err;
     pack_kernel<<<blocks, threads, 0, stream>>>(b.w2, b.s2, n, b.hidden, b.inter, b.hidden / 16, 16, 0,
                                                 out + L.dn_offset);
-    return cudaGetLastError();
+    if ((err = cudaGetLastError()) != cudaSuccess)
+        return err;
+    return launch_rowexp(b, out, stream);
 }
 
 }  // namespace moe

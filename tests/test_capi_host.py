@@ -86,9 +86,11 @@ def test_pack_argument_checks(L):
     p = C.c_void_p(FAKE)
     assert moe.moe_packed_bank_size(5120, 1536, 160, 1) == moe.moe_packed_bank_size(5120, 1536, 160, 1)
     n = moe.moe_packed_bank_size(5120, 1536, 160, 1)
-    # same bytes as the canonical arrays (a permutation), up to section alignment
+    # the canonical bytes (a permutation) and one exponent base per weight row
+    # (2I gate/up rows and H down rows per expert), up to section alignment
     canon = 161 * (2 * 1536 * 5120 // 2 + 2 * 1536 * 5120 // 32 + 5120 * 1536 // 2 + 5120 * 1536 // 32)
-    assert canon <= n < canon + 512
+    rowexp = 161 * (2 * 1536 + 5120)
+    assert canon + rowexp <= n < canon + rowexp + 1024
     assert moe.moe_packed_bank_size(5000, 1536, 160, 1) == 0
     assert L.moe_pack_bank(C.byref(bank(w13=0)), p, n, None) == moe.MOE_ERR_INVALID_ARG
     assert L.moe_pack_bank(C.byref(bank()), None, n, None) == moe.MOE_ERR_INVALID_ARG

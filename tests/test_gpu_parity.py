@@ -104,6 +104,19 @@ def test_pack_bank_matches_documented_layout():
     canon = np.concatenate([a.ravel() for a in arrs.values()])
     np.testing.assert_array_equal(np.bincount(canon, minlength=256),
                                   np.bincount(np.concatenate([gu, dn]), minlength=256))
+    # then one exponent base per weight row in unit-row order: 255 where the
+    # row holds the NaN exponent, else max(largest exponent - 28, 0)
+    def bases(scales, rows):
+        s = scales[:, rows, :].astype(np.int64)
+        b = np.maximum(s.max(axis=2) - 28, 0)
+        b[(s == 255).any(axis=2)] = 255
+        return b.astype(np.uint8).ravel()
+    gu_rows = [8 * rb + m if m < 8 else I + 8 * rb + m - 8 for rb in range(I // 8) for m in range(16)]
+    gu_off = (dn_off + len(dn) + 255) // 256 * 256
+    dn_off2 = (gu_off + n * 2 * I + 255) // 256 * 256
+    np.testing.assert_array_equal(got[gu_off:gu_off + n * 2 * I], bases(arrs["s13"], gu_rows))
+    np.testing.assert_array_equal(got[dn_off2:dn_off2 + n * H], bases(arrs["s2"], list(range(H))))
+    assert (got[gu_off:gu_off + n * 2 * I] == 255).any()        # the NaN marker is exercised
 
 
 def test_group_tokens_matches_oracle():
