@@ -25,19 +25,22 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) { return __uint_
 
 // ------------------------------------------------------------ router GEMV
 
-// Grid (ceil(E/32), ceil(H/512), ceil(T/8)); CTA (bx, by, bz) owns experts
+// Grid (ceil(E/32), ceil(H/512), ceil(T/TOK)); CTA (bx, by, bz) owns experts
 // [32bx, 32bx+32) (one per lane), router rows [512by, 512by+512) (64 per
 // warp, summed in four interleaved Dot2 chains for instruction-level
-// parallelism) and tokens [8bz, 8bz+8), and writes the partial pairs
-// part[by][t][e].  The router weights do
-// not depend on earlier kernels, so they are loaded before the wait on the
-// preceding grid.
+// parallelism) and tokens [TOK bz, TOK bz + TOK), and writes the partial pairs
+// part[by][t][e].  TOK (2, 4 or 8) only spreads the tokens over more CTAs at
+// small T: each token's sums are the same for every TOK.  The router weights
+// do not depend on earlier kernels, so they are loaded before the wait on
+// the preceding grid.
+template <int TOK>
 __global__ void __launch_bounds__(kRouteThreads)
 route_partial_kernel(const uint16_t *__restrict__ x, const float *__restrict__ wr, int T, int H, int E,
                      float2 *__restrict__ part, uint32_t *__restrict__ hdr) {
     constexpr int kWarps = kRouteThreads / 32;
     constexpr int kRowsPerWarp = kRouteRows / kWarps;
-    constexpr int kTok = 8;
+    constexpr int kTok = TOK;
+    static_assert(kTok <= kWarps, "one warp per token of the chunk");
     __shared__ float xs[kTok][kRouteRows];
     __shared__ float2 red[kWarps][kTok][32];
 
@@ -110,31 +113,51 @@ route_partial_kernel(const uint16_t *__restrict__ x, const float *__restrict__ w
 
 // ------------------------------------------------------------------ grouping
 
-// Grouping of ids [T*kps] (entry i = t*kps + s) by one CTA of kGroupThreads:
-// per-expert counts, exclusive offsets, the stable scatter of entries sorted
-// by (expert, entry), the ascending list of active experts, the passes (runs
-// of up to kPassTokens entries of one expert) and the reset of the down-kernel
-// row-block counters.
+// Grouping of ids [T*kps] (entry i = t*kps + s) by one CTA of kGroupThreads
+// (8 warps): per-expert counts, exclusive offsets, the stable scatter of
+// entries sorted by (expert, entry), the ascending list of active experts, the
+// pass lists (runs of up to kPassTokens, kPassEntries, kWidePassTokens and
+// kWidePassEntries entries of one expert) and the reset of the down-kernel
+// row-block counters.  A counting sort done by the whole CTA: the entries are
+// cut into 8 contiguous segments, one per warp; each warp counts its segment
+// per expert; one block-wide scan gives the offsets, the active list and the
+// four pass lists; a warp's cursor for expert e starts at the offset of e plus
+// the counts of e in the earlier segments, so the warps scatter their
+// segments concurrently and the order stays the entry order.  Past
+// kGroupParExperts experts the per-warp counts do not fit and one warp
+// scatters all entries in order.
+constexpr int kGroupParExperts = 512;
+
 __device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const GroupOut &o, uint32_t *hdr,
                             bool ids_in_smem = false) {
+    constexpr int kW = kGroupThreads / 32;
     __shared__ int cnt[kMaxExperts];
-    __shared__ int cursor[kMaxExperts];
+    __shared__ int wbase[kW][kGroupParExperts];       // per-warp counts, then per-warp cursors
+    __shared__ int wsum[kW][6];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = T * kps;
+    const bool par = n_tot <= kGroupParExperts;
+    const int seg = (n + kW - 1) / kW;                 // entries of a warp's segment
 
     for (int e = tid; e < n_tot; e += blockDim.x)
         cnt[e] = 0;
+    if (par)
+        for (int i = tid; i < kW * n_tot; i += blockDim.x)
+            wbase[i / n_tot][i % n_tot] = 0;
     for (int i = tid; i < o.n_counters; i += blockDim.x)
         o.counters[i] = 0;
     __syncthreads();
     int bad = 0;
     auto id_at = [&](int i) { return ids_in_smem ? ids[i] : __ldcg(ids + i); };
-    for (int i = tid; i < n; i += blockDim.x) {
+    for (int i = warp * seg + lane; i < min(n, (warp + 1) * seg); i += 32) {
         const int e = id_at(i);
-        if (e < 0 || e >= n_tot)
+        if (e < 0 || e >= n_tot) {
             bad = 1;
-        else
+        } else {
             atomicAdd(&cnt[e], 1);
+            if (par)
+                atomicAdd(&wbase[warp][e], 1);
+        }
     }
     bad = __syncthreads_or(bad);
     if (bad) {
@@ -151,70 +174,101 @@ __device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const
         return;
     }
 
-    if (warp == 0) {
-        // pass lists: caps kPassTokens (gate/up), kPassEntries (down) and the
-        // wide caps of the tiled kernels
-        constexpr int NL = 4;
-        const int caps[NL] = {kPassTokens, kPassEntries, kWidePassTokens, kWidePassEntries};
-        Pass *const lists[NL] = {o.passes, o.passes4, o.passesw, o.passesw4};
-        int run = 0, na = 0;
-        int np[NL] = {0, 0, 0, 0};
-        for (int base = 0; base < n_tot; base += 32) {
-            const int e = base + lane;
-            const int v = e < n_tot ? cnt[e] : 0;
-            int incl = v;
+    // block-wide exclusive scan of (count, active, passes of the four caps):
+    // thread tid owns experts [per tid, per tid + per)
+    const int caps[4] = {kPassTokens, kPassEntries, kWidePassTokens, kWidePassEntries};
+    Pass *const lists[4] = {o.passes, o.passes4, o.passesw, o.passesw4};
+    const int per = (n_tot + kGroupThreads - 1) / kGroupThreads;
+    const int e0 = tid * per, e1 = min(n_tot, e0 + per);
+    int loc[6] = {0, 0, 0, 0, 0, 0};
+    for (int e = e0; e < e1; ++e) {
+        const int v = cnt[e];
+        loc[0] += v;
+        loc[1] += v > 0;
 #pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, d);
-                if (lane >= d)
-                    incl += y;
-            }
-            const int excl = run + incl - v;
-            const unsigned act = __ballot_sync(0xffffffffu, v > 0);
-            const int rank = __popc(act & ((1u << lane) - 1u));
-            if (e < n_tot) {
-                cursor[e] = excl;
-                o.offsets[e] = excl;
-                if (v > 0)
-                    o.active[na + rank] = e;
-            }
+        for (int l = 0; l < 4; ++l)
+            loc[2 + l] += (v + caps[l] - 1) / caps[l];
+    }
+    int inc[6];
 #pragma unroll
-            for (int li = 0; li < NL; ++li) {
-                const int npass = (v + caps[li] - 1) / caps[li];
-                int pincl = npass;
+    for (int q = 0; q < 6; ++q) {
+        inc[q] = loc[q];
 #pragma unroll
-                for (int d = 1; d < 32; d <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, pincl, d);
-                    if (lane >= d)
-                        pincl += y;
-                }
-                const int pexcl = np[li] + pincl - npass;
-                if (o.passes && e < n_tot)
-                    for (int p = 0; p < npass; ++p)
-                        lists[li][pexcl + p] = Pass{e, excl + p * caps[li], min(caps[li], v - p * caps[li]), 0};
-                np[li] += __shfl_sync(0xffffffffu, pincl, 31);
-            }
-            run += __shfl_sync(0xffffffffu, incl, 31);
-            na += __popc(act);
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, inc[q], d);
+            if (lane >= d)
+                inc[q] += y;
         }
-        if (lane == 0) {
-            o.offsets[n_tot] = run;
-            hdr[kHdrNumActive] = na;
-            hdr[kHdrNumPasses] = np[0];
-            hdr[kHdrNumPasses4] = np[1];
-            hdr[kHdrNumPassesW] = np[2];
-            hdr[kHdrNumPassesW4] = np[3];
-            if (o.num_active)
-                *o.num_active = na;
+    }
+    if (lane == 31)
+#pragma unroll
+        for (int q = 0; q < 6; ++q)
+            wsum[warp][q] = inc[q];
+    __syncthreads();
+    int ex[6];
+#pragma unroll
+    for (int q = 0; q < 6; ++q) {
+        int before = 0;
+        for (int w2 = 0; w2 < warp; ++w2)
+            before += wsum[w2][q];
+        ex[q] = before + inc[q] - loc[q];
+    }
+    for (int e = e0; e < e1; ++e) {
+        const int v = cnt[e];
+        o.offsets[e] = ex[0];
+        if (v > 0)
+            o.active[ex[1]++] = e;
+#pragma unroll
+        for (int l = 0; l < 4; ++l) {
+            const int np = (v + caps[l] - 1) / caps[l];
+            if (o.passes)
+                for (int p = 0; p < np; ++p)
+                    lists[l][ex[2 + l] + p] = Pass{e, ex[0] + p * caps[l], min(caps[l], v - p * caps[l]), 0};
+            ex[2 + l] += np;
         }
+        ex[0] += v;
+    }
+    if (tid == kGroupThreads - 1) {                    // the totals
+        o.offsets[n_tot] = ex[0];
+        hdr[kHdrNumActive] = ex[1];
+        hdr[kHdrNumPasses] = ex[2];
+        hdr[kHdrNumPasses4] = ex[3];
+        hdr[kHdrNumPassesW] = ex[4];
+        hdr[kHdrNumPassesW4] = ex[5];
+        if (o.num_active)
+            *o.num_active = ex[1];
+    }
+    __syncthreads();                                   // offsets written (read back below through global memory)
+
+    // cursors: per warp, the offset of the expert plus its counts in the
+    // earlier segments
+    if (par) {
+        for (int e = tid; e < n_tot; e += blockDim.x) {
+            int run = __ldcg(o.offsets + e);
+#pragma unroll
+            for (int w2 = 0; w2 < kW; ++w2) {
+                const int h = wbase[w2][e];
+                wbase[w2][e] = run;
+                run += h;
+            }
+        }
+        __syncthreads();
+    } else if (warp == 0) {
+        for (int e = lane; e < n_tot; e += 32)
+            cnt[e] = __ldcg(o.offsets + e);            // cursors of the single-warp scatter
         __syncwarp();
-        // stable scatter in entry order, 32 entries at a time
-        for (int base = 0; base < n; base += 32) {
+    }
+    // stable scatter, 32 entries at a time: every warp its own segment, or
+    // warp 0 all entries
+    if (par || warp == 0) {
+        int *cur = par ? wbase[warp] : cnt;
+        const int i0 = par ? warp * seg : 0, i1 = par ? min(n, (warp + 1) * seg) : n;
+        for (int base = i0; base < i1; base += 32) {
             const int i = base + lane;
-            const int e = i < n ? id_at(i) : -1;
+            const int e = i < i1 ? id_at(i) : -1;
             const unsigned same = __match_any_sync(0xffffffffu, e);
-            if (i < n) {
-                const int pos = cursor[e] + __popc(same & ((1u << lane) - 1u));
+            if (i < i1) {
+                const int pos = cur[e] + __popc(same & ((1u << lane) - 1u));
                 if (MOE_DBG_IN_RANGE(pos, n, hdr)) {
                     o.sorted_tok[pos] = i / kps;
                     o.sorted_slot[pos] = i % kps;
@@ -223,8 +277,8 @@ __device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const
                 }
             }
             __syncwarp();
-            if (i < n && lane == 31 - __clz(same))
-                cursor[e] += __popc(same);
+            if (i < i1 && lane == 31 - __clz(same))
+                cur[e] += __popc(same);
             __syncwarp();
         }
     }
@@ -239,9 +293,11 @@ group_kernel(const int32_t *ids, int T, int kps, int n_tot, GroupOut o, uint32_t
 
 // ------------------------------------------------------- top-k + shared slot
 
-// Entries the grouping CTA copies into shared memory (32 KB: with the static
+// Entries the grouping CTA copies into shared memory (16 KB: with the static
 // arrays this stays under the 48 KB that need no opt-in).
-constexpr int kGroupSmemIds = 8 * 1024;
+constexpr int kGroupSmemIds = 4 * 1024;
+
+constexpr int kRankWarps = 8;          // warps of route_finish_kernel (256 threads)
 
 // One CTA per token.  All threads sum the partial pairs of the experts in a
 // fixed order (the loads of one expert issued together) and add the bias;
@@ -254,7 +310,7 @@ route_finish_kernel(const float2 *__restrict__ part, int nh, const float *__rest
                     int has_shared, float shared_weight, int32_t *__restrict__ ids_out, float *__restrict__ w_out,
                     uint32_t *__restrict__ hdr, int do_group, GroupOut go, const uint16_t *__restrict__ x, int H,
                     __half *x16, float *xundo) {
-    extern __shared__ float2 L[];   // [E] normalised (hi, lo) logits
+    extern __shared__ float2 L[];   // [E] (hi, lo) logits, then the partial ranks; later the grouping's ids
     __shared__ int last_cta;
     __shared__ int sids[kMaxSlots];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -286,55 +342,56 @@ route_finish_kernel(const float2 *__restrict__ part, int nh, const float *__rest
     }
     __syncthreads();
 
-    if (warp == 0) {
-        const int per_lane = (E + 31) / 32;   // <= 32 (E <= 1024)
-        unsigned taken = 0;
-        float sel_num = 0.0f, top_hi = 0.0f, top_lo = 0.0f, denom = 0.0f;
-        int sel_id = 0;
-        for (int r = 0; r < k; ++r) {
-            float bh = -INFINITY, bl = -INFINITY;
-            int bi = 0x7fffffff;
-            for (int j = 0; j < per_lane; ++j) {
-                const int e = lane + 32 * j;
-                if (e >= E || ((taken >> j) & 1u))
-                    continue;
-                const float2 v = L[e];
-                if (v.x > bh || (v.x == bh && (v.y > bl || (v.y == bl && e < bi)))) {
-                    bh = v.x;
-                    bl = v.y;
-                    bi = e;
-                }
+    // rank of every expert in the order (logit pair descending, equal pairs:
+    // the lower index first; a NaN logit counts as -inf): the experts of
+    // rank < k are the selection and their rank is their slot
+    __shared__ int sel[kMaxSlots];
+    __shared__ float sel_ex[kMaxSlots];
+    unsigned short *prank = reinterpret_cast<unsigned short *>(L + E);   // [kRankWarps][E] after the logits
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        if (L[e].x != L[e].x)
+            L[e] = make_float2(-INFINITY, -INFINITY);
+    __syncthreads();
+    {
+        // warp w counts, for every expert, the experts of its slice
+        // [f0, f1) that come before it; the partial counts are then added
+        const int f0 = (int)((long long)E * warp / kRankWarps), f1 = (int)((long long)E * (warp + 1) / kRankWarps);
+        for (int e = lane; e < E; e += 32) {
+            const float2 v = L[e];
+            int c = 0;
+#pragma unroll 4
+            for (int f = f0; f < f1; ++f) {
+                const float2 u = L[f];
+                c += (u.x > v.x || (u.x == v.x && (u.y > v.y || (u.y == v.y && f < e)))) ? 1 : 0;
             }
-#pragma unroll
-            for (int d = 16; d > 0; d >>= 1) {
-                const float oh = __shfl_xor_sync(0xffffffffu, bh, d);
-                const float ol = __shfl_xor_sync(0xffffffffu, bl, d);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
-                if (oh > bh || (oh == bh && (ol > bl || (ol == bl && oi < bi)))) {
-                    bh = oh;
-                    bl = ol;
-                    bi = oi;
-                }
-            }
-            if (bi < E && (bi & 31) == lane)
-                taken |= 1u << (bi >> 5);
-            if (r == 0) {
-                top_hi = bh;
-                top_lo = bl;
-            }
-            // softmax numerator relative to the largest logit
-            const float dlt = __fadd_rn(__fsub_rn(bh, top_hi), __fsub_rn(bl, top_lo));
-            const float ex = expf(dlt);
-            denom += ex;
-            if (lane == r) {
-                sel_num = ex;
-                sel_id = bi;
-            }
+            prank[warp * E + e] = (unsigned short)c;
         }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int rank = 0;
+#pragma unroll
+        for (int w2 = 0; w2 < kRankWarps; ++w2)
+            rank += prank[w2 * E + e];
+        if (rank < k)
+            sel[rank] = e;
+    }
+    __syncthreads();
+    // softmax over the kept logits relative to the largest, the denominator
+    // summed in slot order
+    if (threadIdx.x < k) {
+        const float2 top = L[sel[0]], v = L[sel[threadIdx.x]];
+        sel_ex[threadIdx.x] = expf(__fadd_rn(__fsub_rn(v.x, top.x), __fsub_rn(v.y, top.y)));
+    }
+    __syncthreads();
+    if (warp == 0) {
+        float denom = 0.0f;
+        for (int r = 0; r < k; ++r)
+            denom += sel_ex[r];
         if (lane < k) {
-            ids_out[(size_t)t * kps + lane] = sel_id;
-            w_out[(size_t)t * kps + lane] = sel_num / denom;
-            sids[lane] = sel_id;
+            ids_out[(size_t)t * kps + lane] = sel[lane];
+            w_out[(size_t)t * kps + lane] = sel_ex[lane] / denom;
+            sids[lane] = sel[lane];
         }
         if (has_shared && lane == k) {
             ids_out[(size_t)t * kps + k] = E;
@@ -370,6 +427,7 @@ route_finish_kernel(const float2 *__restrict__ part, int nh, const float *__rest
             sm_ids[i] = __ldcg(ids_out + i);
         __syncthreads();
         group_block(sm_ids, T, kps, E + has_shared, go, hdr, true);
+        __syncthreads();
     } else {
         group_block(ids_out, T, kps, E + has_shared, go, hdr);
     }
@@ -386,15 +444,20 @@ cudaError_t launch_route(const uint16_t *x, const float *wr, const float *bias, 
     uint32_t *hdr = ws_at<uint32_t>(ws, 0);
     float2 *part = ws_at<float2>(ws, L.route_part);
     const int nh = (H + kRouteRows - 1) / kRouteRows;
-    dim3 g1((E + kRouteCols - 1) / kRouteCols, nh, (T + 7) / 8);   // one CTA per 8 tokens of a tile
-    cudaError_t err = launch_pdl(route_partial_kernel, g1, dim3(kRouteThreads), 0, stream, x, wr, T, H, E, part, hdr);
+    // tokens per CTA: fewer at small T, so that the grid covers the SMs
+    const int tok = 8;
+    dim3 g1((E + kRouteCols - 1) / kRouteCols, nh, (T + tok - 1) / tok);
+    cudaError_t err =
+        tok == 8   ? launch_pdl(route_partial_kernel<8>, g1, dim3(kRouteThreads), 0, stream, x, wr, T, H, E, part, hdr)
+        : tok == 4 ? launch_pdl(route_partial_kernel<4>, g1, dim3(kRouteThreads), 0, stream, x, wr, T, H, E, part, hdr)
+                   : launch_pdl(route_partial_kernel<2>, g1, dim3(kRouteThreads), 0, stream, x, wr, T, H, E, part, hdr);
     if (err != cudaSuccess)
         return err;
     if (ev_after_partial &&
         (err = cudaEventRecord(ev_after_partial, stream)) != cudaSuccess)
         return err;
     const size_t n_ids = (size_t)T * (k + has_shared);
-    size_t smem = (size_t)E * sizeof(float2);
+    size_t smem = (size_t)E * (sizeof(float2) + kRankWarps * sizeof(unsigned short));
     if (do_group && T > 1 && n_ids <= (size_t)kGroupSmemIds && n_ids * sizeof(int) > smem)
         smem = n_ids * sizeof(int);
     __half *x16 = do_group ? ws_at<__half>(ws, L.x16) : nullptr;
