@@ -1,6 +1,8 @@
 // kernels.h -- launch functions of the MoE kernels (internal to the library).
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace moe {
@@ -74,7 +76,7 @@ cudaError_t launch_combine(const float *yent, int entries, const int32_t *inv_po
 struct Mx8Problem {
     const uint16_t *x;       // [T, H] bf16
     const moe_mxfp4_bank_t *bank;
-    const uint8_t *packed_mx;   // stage-ordered bank (launch_mx8_pack)
+    const uint8_t *packed_mx;   // the variant's bank (launch_mx8_pack)
     const float *topk_w;     // [T, kps]
     uint16_t *y;             // [T, H] bf16
     int T, kps;
@@ -138,6 +140,11 @@ cudaError_t launch_selftest_decode(const uint8_t *codes, uint16_t *out, int n, c
 
 // Shape rules shared by validation and the kernels' staging choices.
 bool ffn_shape_supported(int H, int I);
+
+// A tiled tensor map (tc.cu): dims / strides / box innermost first, strides
+// in bytes (rank - 1 of them); the driver's encoder is looked up at run time.
+cudaError_t encode_tiled(CUtensorMap *m, CUtensorMapDataType type, int rank, const void *base, const uint64_t *dims,
+                         const uint64_t *strides, const uint32_t *box, CUtensorMapSwizzle swizzle);
 
 // Tensor-memory expert FFN for T > 8 (tc.cu): H and I multiples of 512.
 bool tc_shape_supported(int H, int I);

@@ -8,8 +8,8 @@
 // conversion -- and both projections run as block-scaled tensor-core MMAs,
 // `tcgen05.mma.kind::mxf8f6f4.block_scale`: A = MXFP4 weights read as E2M1 by
 // the tensor core, B = the MXFP8 activations, both block scales applied by the
-// hardware, fp32 accumulators in TMEM.  The weights are read from a
-// stage-ordered copy of the bank (below); no decode instruction runs.
+// hardware, fp32 accumulators in TMEM.  The weight codes reach shared memory
+// by tensor copies straight from row-major arrays; no decode instruction runs.
 //
 // Launches: routing + grouping and the x quantisation (for T <= 8 the
 // routing phases of the single-launch kernel, which quantise x while they
@@ -19,32 +19,31 @@
 // (ffn.cu's combine_kernel).
 //
 // GEMM CTA: 128 weight rows x one pass of <= N entries (MMA M = 128, N = 16,
-// or 32 for T > 128), K in stages of 128 (four MMAs of K = 32), warp-specialised: four
-// producer warps load every operand of a stage into registers kMxRegStages
-// stages ahead, store it into a 3-buffer shared-memory ring, write its scale
-// factors into TMEM and arrive on the buffer's "full" mbarrier; a fifth warp
-// waits on it, issues the four MMAs and commits them to the buffer's "empty"
-// mbarrier, which the producers wait on before refilling the buffer.  The
-// shared operands use the
-// K-major no-swizzle layout: core matrices of 8 rows x 16 bytes, adjacent in
-// K 128 bytes apart, 8-row groups 1,024 bytes apart.  An E2M1 operand of
-// kind::mxf8f6f4 occupies a 16-byte slot per 16 elements with the 8 bytes of
-// codes in the low half.  Scale factors go into TMEM with tcgen05.st: row r
-// of A at lane r % 32 (in every 32-lane quarter), column base + r / 32;
-// column n of B at lane n; byte j of a 32-bit cell is the scale of the
-// stage's K block j, selected by the MMA's scale-factor id.
+// or 32 for T > 128), K in stages of 128 (four MMAs of K = 32), over a
+// 3-buffer shared-memory ring.  Thread 0 issues a stage's weight tile as two
+// tensor copies of 64 rows x 128 codes (gate/up: the 64 gate rows, then the
+// 64 up rows of the same indices) with the data type that gives every 16
+// E2M1 codes a 16-byte slot (8 bytes of codes, the other 8 not written) and
+// the 128-byte swizzle; the copies' 8,192 bytes complete the buffer's "full"
+// mbarrier together with the four producer warps, which load the other
+// operands into registers kMxRegStages stages ahead -- the activation codes
+// (stored in the K-major no-swizzle layout: core matrices of 8 rows x 16
+// bytes, adjacent in K 128 bytes apart, 8-row groups 1,024 bytes apart), the
+// weight rows' and the activation rows' scale words (written into TMEM with
+// tcgen05.st: row r of A at lane r % 32 of every 32-lane quarter, column base
+// + r / 32; column n of B at lane n; byte j of a 32-bit cell is the scale of
+// the stage's K block j, selected by the MMA's scale-factor id).  A fifth
+// warp waits on the full barrier, issues the four MMAs (the weight operand
+// through a 128-byte-swizzle descriptor: rows of 128 bytes, 8-row atoms 1,024
+// bytes apart, a K step of 32 moving the start by 32 bytes) and commits them
+// to the buffer's "empty" mbarrier, which the producers wait on before
+// refilling the buffer; thread 0 then issues that buffer's next weight tile.
+// Scale-factor regions start on 32-column (A) and 16-column (B) boundaries of
+// the CTA's 128-column allocation (three CTAs per SM).
 //
-// The GEMMs read a stage-ordered copy of the bank (moe_pack_bank_mx): per
-// (expert, 128-row tile, K stage) one contiguous block of 8,704 bytes: the
-// codes in the order of the shared-memory image ([8-row group][16-byte slot]
-// [row], 8 bytes each, at half the image's stride) except that within a
-// group pieces w and w + 32 sit side by side, then the 128 rows' four scale
-// bytes.  A stage is one linear 8.5 KB read (instead of 64 bytes from each
-// of 128 rows), streamed through registers kMxRegStages stages ahead; a
-// 16-byte chunk then holds two pieces whose slots are 32 apart, so the
-// 8-byte shared stores of a warp cover 32 consecutive slots.  Scale-factor
-// regions start on 32-column (A) and 16-column (B) boundaries of the CTA's
-// 128-column allocation (three CTAs per SM).
+// The bank (moe_pack_bank_mx) is K-chunk major (below), so that a stage's
+// 64-row tensor copy reads 4 KB of consecutive bytes.
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include <atomic>
@@ -62,12 +61,12 @@ constexpr int kMxStages = 3;                   // shared-memory ring buffers
 constexpr int kMxRegStages = 3;                // stages of operands in flight in registers
 constexpr int kMxLbo = 128;                    // bytes between core matrices adjacent in K
 constexpr int kMxSbo = 8 * 128;                // bytes between 8-row groups (8 K slots of 16 B)
-constexpr int kMxABytes = 128 * kMxStageK;     // 128 rows x 8 slots x 16 B
+constexpr int kMxABytes = 128 * kMxStageK;     // 128 rows x 8 slots x 16 B (the padded E2M1 image)
+constexpr int kMxATx = 128 * kMxStageK / 2;    // bytes the tensor copies of a stage write (the codes)
 constexpr int kMxTmemCols = 128;               // D: columns 0..N-1; scale factors on aligned columns
 constexpr int kMxColSfa = 32;                  // SFA of buffer b: 4 columns at 32 + 32 b
 constexpr int kMxColSfb = 48;                  // SFB of buffer b: 1 column at 48 + 32 b
 constexpr int kMxCtasPerSm = 3;                // 3 x 128 TMEM columns, 3 x 55 (N = 16) or 61 KB shared memory
-constexpr int kMxBlockBytes = 8192 + 512;      // one stage of a 128-row tile in the stage-ordered bank
 constexpr unsigned long long kMxWaitLimitNs = 200ull * 1000 * 1000;
 // Per MMA width N (entries of one pass: 16, or 32 for the wide passes of
 // the multi-launch grouping): the B tile, a ring stage and the shared memory.
@@ -128,7 +127,8 @@ __device__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 }
 
 struct MxGemmArgs {
-    const uint8_t *blocks;      // section of the stage-ordered bank: [n_tot][tiles][K/128] blocks
+    const uint8_t *wscale;      // E8M0 scales of the weight rows [n_tot * rows][K/32]
+    int rows;                   // weight rows per expert: 2I (gate/up) or H (down)
     const uint8_t *aq;          // E4M3 activations [act_rows][K]
     const uint8_t *asc;         // E8M0 scales [act_rows][K/32]
     const Pass *passes;         // passes of <= N entries
@@ -150,8 +150,22 @@ struct MxGemmArgs {
 
 // ------------------------------------------------------------------ GEMM
 
+// 128-byte-swizzle K-major shared-memory descriptor (the weight tiles the
+// tensor copies write): rows of 128 bytes, 8-row atoms 1,024 bytes apart,
+// layout type 2 in bits 61-63; a K step of 32 elements moves the start by
+// 32 bytes inside the atom.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    uint64_t d = (uint64_t)((addr & 0x3FFFF) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
 template <bool GATEUP, int NN>
-__global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(const __grid_constant__ MxGemmArgs a) {
+__global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm)
+    mx8_gemm_kernel(const __grid_constant__ MxGemmArgs a, const __grid_constant__ CUtensorMap wmap) {
     using Tile = MxTile<NN>;
     extern __shared__ __align__(1024) uint8_t mx_smem[];
     __shared__ uint32_t s_taddr;
@@ -181,17 +195,20 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
     const int nst = a.K / kMxStageK / a.kc;          // stages of this chunk
     const int s_first = chunk * nst;
     const uint32_t sbase = smem_addr(mx_smem);
-    // ---- producers.  Every operand of a stage is loaded into registers
-    // kMxRegStages stages ahead: weight codes as 16-byte chunks c = tid +
-    // 128 i (i < 4) of the block, holding the pieces q0 = 64 (c / 32) +
-    // c % 32 and q0 + 32 of the shared-memory image (each 8-byte store of
-    // a warp then covers 32 consecutive slots); the scale words of rows
+    // ---- weights: the tensor copies of a stage bring its 128 rows x 128
+    // codes (gate/up: 64 gate rows, then the 64 up rows of the same
+    // indices; down: 128 rows) into the stage's 128-byte-swizzled tile,
+    // expanded by the copy to a 16-byte slot per 16 codes.
+    // ---- producers: every other operand of a stage is loaded into
+    // registers kMxRegStages stages ahead: the scale words of weight rows
     // lane + 32 q (q < 4); 16 bytes of activation rows tid / 8 + 16 j
     // (j < N / 16), slot tid % 8; the scale word of activation row
     // lane % N.  Each warp writes the scale factors into its own 32-lane
     // quarter of TMEM.
-    const uint8_t *wblk =
-        a.blocks + (((size_t)ps.expert * a.tiles + tile) * a.kc * nst + s_first) * kMxBlockBytes;
+    auto wrow = [&](int r) {                      // weight row (within the expert) of MMA row r
+        return GATEUP ? (r < 64 ? 64 * tile + r : a.half + 64 * tile + r - 64) : 128 * tile + r;
+    };
+    const int nch = a.K / kMxStageK;
     auto arow = [&](int n) {
         const int e = ps.begin + min(n, ps.count - 1);
         return GATEUP ? a.sorted_tok[e] : e;
@@ -203,24 +220,37 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
     for (int j = 0; j < NB; ++j)
         asrc[j] = a.aq + (size_t)arow(r0 + 16 * j) * a.K + (size_t)s_first * kMxStageK + slot * 16;
     const uint8_t *sfb_src = a.asc + (size_t)arow(lane % NN) * K32 + s_first * 4;
+    const uint8_t *sfa_src[4];                   // scale words: [expert][chunk][row][4]
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        sfa_src[i] = a.wscale + (((size_t)ps.expert * nch + s_first) * a.rows + wrow(lane + 32 * i)) * 4;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const uint64_t pol = l2_evict_first_policy();
-    uint4 rq[kMxRegStages][4];
     uint32_t rsa[kMxRegStages][4];
     uint4 rb[kMxRegStages][NB];
     uint32_t rsb[kMxRegStages];
-    auto load_stage = [&](int s, uint4(&q)[4], uint32_t(&sa)[4], uint4(&bq)[NB], uint32_t &sb) {
-        const uint8_t *blk = wblk + (size_t)s * kMxBlockBytes;
+    auto load_stage = [&](int s, uint32_t(&sa)[4], uint4(&bq)[NB], uint32_t &sb) {
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            q[i] = ld_stream16(blk + 16 * (tid + kMxProducers * i), pol);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            sa[i] = __ldg(reinterpret_cast<const uint32_t *>(blk + 8192 + 4 * (lane + 32 * i)));
+            sa[i] = __ldg(reinterpret_cast<const uint32_t *>(sfa_src[i] + (size_t)s * a.rows * 4));
 #pragma unroll
         for (int j = 0; j < NB; ++j)
             bq[j] = __ldg(reinterpret_cast<const uint4 *>(asrc[j] + (size_t)s * kMxStageK));
         sb = __ldg(reinterpret_cast<const uint32_t *>(sfb_src + s * 4));
+    };
+    // weight rows of the tile for the tensor copies (row coordinate of each 64-row box)
+    const int wr0 = wrow(0), wr1 = wrow(64);
+    auto issue_weights = [&](int s, int b, uint32_t fb) {
+        const uint32_t dst = sbase + (uint32_t)(b * kMxABytes);
+        const int ck = ps.expert * nch + s_first + s;    // the expert's chunk
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(fb), "r"(kMxATx) : "memory");
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {0, %2, %3}], "
+            "[%4];" ::"r"(dst), "l"(reinterpret_cast<uint64_t>(&wmap)), "r"(wr0), "r"(ck), "r"(fb)
+            : "memory");
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {0, %2, %3}], "
+            "[%4];" ::"r"(dst + kMxABytes / 2), "l"(reinterpret_cast<uint64_t>(&wmap)), "r"(wr1), "r"(ck), "r"(fb)
+            : "memory");
     };
     // the first stages' loads go out before the TMEM allocation and barrier
     // set-up, whose latency they hide (they need only the pass)
@@ -228,24 +258,29 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
 #pragma unroll
         for (int k = 0; k < kMxRegStages; ++k)
             if (k < nst)
-                load_stage(k, rq[k], rsa[k], rb[k], rsb[k]);
+                load_stage(k, rsa[k], rb[k], rsb[k]);
     }
     // buffer b: full[b] completes when the 128 producers have staged a stage
     // in it (shared operands, scale factors in TMEM); empty[b] when the MMAs
     // reading it are done (tcgen05.commit)
     uint64_t *full = reinterpret_cast<uint64_t *>(mx_smem + (size_t)kMxStages * Tile::kStage);
     uint64_t *empty = full + kMxStages;
+    uint8_t *bring = mx_smem + (size_t)kMxStages * kMxABytes;      // activation tiles after the weight tiles
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&s_taddr)),
                      "n"(kMxTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
+    // full[b]: the 128 producers' arrivals after their stores, plus the
+    // weight copies' arrival with their byte count
     if (tid == 0) {
         for (int b = 0; b < kMxStages; ++b) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(full + b)), "r"(kMxProducers));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(full + b)), "r"(kMxProducers + 1));
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(empty + b)));
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int s = 0; s < kMxStages && s < nst; ++s)
+            issue_weights(s, s, smem_addr(full + s));
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -262,24 +297,20 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
                     break;
                 const int b = s % kMxStages;
                 // buffer b and its TMEM columns were read by the MMAs of stage s - kMxStages
-                if (s >= kMxStages &&
-                    !__all_sync(0xffffffffu, mbar_wait(smem_addr(empty + b), ((s - kMxStages) / kMxStages) & 1))) {
-                    ok = false;           // warp-uniform: the tcgen05 stores below are .sync.aligned
-                    break;
+                if (s >= kMxStages) {
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(smem_addr(empty + b), ((s - kMxStages) / kMxStages) & 1))) {
+                        ok = false;       // warp-uniform: the tcgen05 stores below are .sync.aligned
+                        break;
+                    }
+                    if (tid == 0)         // the buffer is free: its next weight tile
+                        issue_weights(s, b, smem_addr(full + b));
                 }
-                uint8_t *st = mx_smem + (size_t)b * Tile::kStage;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int c = tid + kMxProducers * i;
-                    const int q0 = 64 * (c >> 5) + (c & 31);
-                    *reinterpret_cast<uint2 *>(st + 16 * q0) = make_uint2(rq[k][i].x, rq[k][i].y);
-                    *reinterpret_cast<uint2 *>(st + 16 * (q0 + 32)) = make_uint2(rq[k][i].z, rq[k][i].w);
-                }
+                uint8_t *st = bring + (size_t)b * Tile::kB;
 #pragma unroll
                 for (int j = 0; j < NB; ++j) {
                     const int r = r0 + 16 * j;
-                    *reinterpret_cast<uint4 *>(st + kMxABytes + (r >> 3) * kMxSbo + slot * kMxLbo + (r & 7) * 16) =
-                        rb[k][j];
+                    *reinterpret_cast<uint4 *>(st + (r >> 3) * kMxSbo + slot * kMxLbo + (r & 7) * 16) = rb[k][j];
                 }
                 const uint32_t colA = (uint32_t)(kMxColSfa + 32 * b), colB = (uint32_t)(kMxColSfb + 32 * b);
                 asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
@@ -290,7 +321,7 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
                              "r"(rsb[k])
                              : "memory");
                 if (s + kMxRegStages < nst)
-                    load_stage(s + kMxRegStages, rq[k], rsa[k], rb[k], rsb[k]);
+                    load_stage(s + kMxRegStages, rsa[k], rb[k], rsb[k]);
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -312,10 +343,11 @@ __global__ void __launch_bounds__(kMxThreads, kMxCtasPerSm) mx8_gemm_kernel(cons
             }
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const uint32_t colA = (uint32_t)(kMxColSfa + 32 * b), colB = (uint32_t)(kMxColSfb + 32 * b);
-            const uint32_t sa = sbase + (uint32_t)(b * Tile::kStage), sb = sa + kMxABytes;
+            const uint32_t sa = sbase + (uint32_t)(b * kMxABytes);
+            const uint32_t sb = smem_addr(bring) + (uint32_t)(b * Tile::kB);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const uint64_t ad = smem_desc(sa + j * 2 * kMxLbo), bd = smem_desc(sb + j * 2 * kMxLbo);
+                const uint64_t ad = smem_desc_sw128(sa + 32 * j), bd = smem_desc(sb + j * 2 * kMxLbo);
                 const uint32_t acc = (s > 0 || j > 0) ? 1u : 0u;
                 asm volatile(
                     "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
@@ -411,52 +443,71 @@ __global__ void __launch_bounds__(256) mx8_hfin_kernel(const float *__restrict__
 // piece (q < 1024) or 4-byte scale word (q >= 1024) of a block.  Tile rows:
 // gate/up (half = I) rows 0..63 are gate rows 64t.., rows 64..127 the up rows
 // I + 64t..; down (half = 0) rows 128t...
-__global__ void __launch_bounds__(256) mx8_pack_kernel(const uint8_t *__restrict__ w, const uint8_t *__restrict__ sc,
-                                                       int n_tot, int rows, int K, int tiles, int half,
-                                                       uint8_t *__restrict__ out) {
-    const int nst = K / kMxStageK, K2 = K / 2, K32 = K / 32;
-    const long long items = (long long)n_tot * tiles * nst * 1152;
-    for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < items;
-         it += (long long)gridDim.x * blockDim.x) {
-        const long long blk = it / 1152;
-        const int q = (int)(it - blk * 1152);
-        const int s = (int)(blk % nst);
-        const long long et = blk / nst;
-        const int t = (int)(et % tiles), e = (int)(et / tiles);
-        const int r = q < 1024 ? 8 * (q >> 6) + (q & 7) : q - 1024;
-        const int row = half ? (r < 64 ? 64 * t + r : half + 64 * t + r - 64) : 128 * t + r;
-        uint8_t *dst = out + blk * kMxBlockBytes;
-        if (q < 1024) {
-            const int j = (q >> 3) & 7, piece = q & 63;
-            const int pos = (q & ~63) + 2 * (piece & 31) + (piece >> 5);   // pieces l and l + 32 side by side
-            *reinterpret_cast<uint2 *>(dst + 8 * pos) =
-                *reinterpret_cast<const uint2 *>(w + ((size_t)e * rows + row) * K2 + s * 64 + j * 8);
-        } else {
-            *reinterpret_cast<uint32_t *>(dst + 8192 + 4 * r) =
-                *reinterpret_cast<const uint32_t *>(sc + ((size_t)e * rows + row) * K32 + s * 4);
-        }
-    }
-}
 
 }  // namespace
 
 // ------------------------------------------------------------------ host
 
-size_t mx8_packed_size(int H, int I, int n_tot) {
-    return (size_t)n_tot * ((size_t)(I / 64) * (H / 128) + (size_t)(H / 128) * (I / 128)) * kMxBlockBytes;
+// The MXFP8 variant's bank, K-chunk major: per section (gate/up, then down),
+// per expert, per chunk of 128 K elements, every weight row's 64 bytes of
+// codes, then (separate sections) every row's 4 scale bytes of the chunk --
+// codes [n_tot][K/128][rows][64], scales [n_tot][K/128][rows][4], each
+// section at a 256-byte aligned offset.  A stage's 64-row tensor copy is then
+// one contiguous 4 KB read and its scale words 512 contiguous bytes.
+struct MxLayout {
+    size_t w13, w2, s13, s2, total;
+};
+static MxLayout mx8_layout(int H, int I, int n_tot) {
+    MxLayout m{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) { o = align_up(o, 256); const size_t r = o; o += bytes; return r; };
+    m.w13 = take((size_t)n_tot * 2 * I * (H / 2));
+    m.w2 = take((size_t)n_tot * H * (I / 2));
+    m.s13 = take((size_t)n_tot * 2 * I * (H / 32));
+    m.s2 = take((size_t)n_tot * H * (I / 32));
+    m.total = align_up(o, 256);
+    return m;
 }
 
-static size_t mx8_dn_offset(int H, int I, int n_tot) {
-    return (size_t)n_tot * (I / 64) * (H / 128) * kMxBlockBytes;
+size_t mx8_packed_size(int H, int I, int n_tot) { return mx8_layout(H, I, n_tot).total; }
+
+// One 16-byte piece (codes) or 4-byte word (scales) per item: row r's bytes of
+// chunk c go to [e][c][r].
+__global__ void __launch_bounds__(256) mx8_pack_kernel(const uint8_t *__restrict__ w, const uint8_t *__restrict__ sc,
+                                                       int n_tot, int rows, int K, uint8_t *__restrict__ wout,
+                                                       uint8_t *__restrict__ sout) {
+    const int nch = K / kMxStageK, K2 = K / 2, K32 = K / 32;
+    const long long code_items = (long long)n_tot * rows * nch * 4;   // 4 pieces of 16 bytes per row and chunk
+    const long long items = code_items + (long long)n_tot * rows * nch;
+    for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < items;
+         it += (long long)gridDim.x * blockDim.x) {
+        if (it < code_items) {
+            const int q = (int)(it & 3);
+            const long long rc = it >> 2;                       // (e, c, r) in output order
+            const int r = (int)(rc % rows);
+            const long long ec = rc / rows;
+            const int c = (int)(ec % nch), e = (int)(ec / nch);
+            *reinterpret_cast<uint4 *>(wout + rc * 64 + 16 * q) =
+                *reinterpret_cast<const uint4 *>(w + ((size_t)e * rows + r) * K2 + (size_t)c * 64 + 16 * q);
+        } else {
+            const long long rc = it - code_items;
+            const int r = (int)(rc % rows);
+            const long long ec = rc / rows;
+            const int c = (int)(ec % nch), e = (int)(ec / nch);
+            *reinterpret_cast<uint32_t *>(sout + rc * 4) =
+                *reinterpret_cast<const uint32_t *>(sc + ((size_t)e * rows + r) * K32 + (size_t)c * 4);
+        }
+    }
 }
 
 cudaError_t launch_mx8_pack(const moe_mxfp4_bank_t &b, uint8_t *out, cudaStream_t stream) {
     const int H = b.hidden, I = b.inter, n = b.num_experts + b.has_shared;
-    mx8_pack_kernel<<<4096, 256, 0, stream>>>(b.w13, b.s13, n, 2 * I, H, I / 64, I, out);
+    const MxLayout m = mx8_layout(H, I, n);
+    mx8_pack_kernel<<<4096, 256, 0, stream>>>(b.w13, b.s13, n, 2 * I, H, out + m.w13, out + m.s13);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess)
         return err;
-    mx8_pack_kernel<<<4096, 256, 0, stream>>>(b.w2, b.s2, n, H, I, H / 128, 0, out + mx8_dn_offset(H, I, n));
+    mx8_pack_kernel<<<4096, 256, 0, stream>>>(b.w2, b.s2, n, H, I, out + m.w2, out + m.s2);
     return cudaGetLastError();
 }
 
@@ -484,8 +535,25 @@ static cudaError_t launch_gemms(const Mx8Problem &p, void *ws, const WsLayout &L
     uint32_t *hdr = ws_at<uint32_t>(ws, 0);
     uint8_t *hq = ws_at<uint8_t>(ws, L.mx_hq), *hs = ws_at<uint8_t>(ws, L.mx_hs);
     float *h32 = ws_at<float>(ws, L.mx_h32), *yent = ws_at<float>(ws, L.mx_y), *gu = ws_at<float>(ws, L.mx_gu);
+    // weight codes as 16 x E2M1 per 16-byte slot, 128-byte swizzle, boxes of
+    // 128 codes x 64 rows
+    const MxLayout ml = mx8_layout(H, I, n_tot);
+    CUtensorMap gmap, dmap;
+    {
+        const uint64_t gdims[3] = {kMxStageK, (uint64_t)2 * I, (uint64_t)n_tot * (H / kMxStageK)};
+        const uint64_t gstr[2] = {64, (uint64_t)2 * I * 64};
+        const uint64_t ddims[3] = {kMxStageK, (uint64_t)H, (uint64_t)n_tot * (I / kMxStageK)};
+        const uint64_t dstr[2] = {64, (uint64_t)H * 64};
+        const uint32_t box[3] = {kMxStageK, 64, 1};
+        if ((err = encode_tiled(&gmap, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, p.packed_mx + ml.w13, gdims, gstr,
+                                box, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess ||
+            (err = encode_tiled(&dmap, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, p.packed_mx + ml.w2, ddims, dstr,
+                                box, CU_TENSOR_MAP_SWIZZLE_128B)) != cudaSuccess)
+            return err;
+    }
     MxGemmArgs g{};
-    g.blocks = p.packed_mx;
+    g.wscale = p.packed_mx + ml.s13;
+    g.rows = 2 * I;
     g.aq = ws_at<uint8_t>(ws, L.mx_xq);
     g.asc = ws_at<uint8_t>(ws, L.mx_xs);
     g.passes = passes;
@@ -503,7 +571,7 @@ static cudaError_t launch_gemms(const Mx8Problem &p, void *ws, const WsLayout &L
     g.act_rows = T;
     g.entries = entries;
     if ((err = launch_pdl(mx8_gemm_kernel<true, NN>, dim3(I / 64 * g.kc, max_pass), dim3(kMxThreads), smem, stream,
-                          g)) != cudaSuccess)
+                          g, gmap)) != cudaSuccess)
         return err;
     if (ev && (err = cudaEventRecord(ev[1], stream)) != cudaSuccess)
         return err;
@@ -512,7 +580,8 @@ static cudaError_t launch_gemms(const Mx8Problem &p, void *ws, const WsLayout &L
                           g.kstride, entries, I, h32, hq, hs)) != cudaSuccess)
         return err;
     MxGemmArgs d = g;
-    d.blocks = p.packed_mx + mx8_dn_offset(H, I, n_tot);
+    d.wscale = p.packed_mx + ml.s2;
+    d.rows = H;
     d.aq = hq;
     d.asc = hs;
     d.sorted_tok = nullptr;
@@ -524,8 +593,8 @@ static cudaError_t launch_gemms(const Mx8Problem &p, void *ws, const WsLayout &L
     d.kstride = 0;
     d.out_ld = H;
     d.act_rows = entries;
-    if ((err = launch_pdl(mx8_gemm_kernel<false, NN>, dim3(H / 128, max_pass), dim3(kMxThreads), smem, stream, d)) !=
-        cudaSuccess)
+    if ((err = launch_pdl(mx8_gemm_kernel<false, NN>, dim3(H / 128, max_pass), dim3(kMxThreads), smem, stream, d,
+                          dmap)) != cudaSuccess)
         return err;
     return launch_combine(yent, entries, ws_at<int32_t>(ws, L.inv_pos), p.topk_w, T, kps, H, p.y, hdr, stream);
 }

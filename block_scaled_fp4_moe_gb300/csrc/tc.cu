@@ -656,6 +656,30 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+}  // namespace
+
+cudaError_t encode_tiled(CUtensorMap *m, CUtensorMapDataType type, int rank, const void *base, const uint64_t *dims,
+                         const uint64_t *strides, const uint32_t *box, CUtensorMapSwizzle swizzle) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return cudaErrorNotSupported;
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        es[i] = 1;
+        if (i < rank - 1)
+            st[i] = strides[i];
+    }
+    const CUresult r = fn(m, type, (cuuint32_t)rank, const_cast<void *>(base), d, st, b, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+namespace {
+
 // A 3-D view of rows x K f16 (rows in the tensor-memory K order) whose box of
 // 8 elements x box_rows rows x 64 chunks is one raw stage of B in the
 // core-matrix layout [chunk][row][16 bytes].

@@ -162,7 +162,7 @@ class MXFP4Bank:
     s13: torch.Tensor | None = None
     w2: torch.Tensor | None = None
     s2: torch.Tensor | None = None
-    packed_mx: torch.Tensor | None = None     # stage-ordered copy for moe_layer_forward_mxfp8
+    packed_mx: torch.Tensor | None = None     # the MXFP8 variant's bank (canonical arrays, aligned sections)
 
     def c_struct(self) -> _Bank:
         ptrs = []

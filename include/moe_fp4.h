@@ -253,7 +253,7 @@ moe_status_t moe_layer_forward_next(const uint16_t *x, const float *router_w, co
  * shapes tested), and it is compared against its own oracle mode.
  *
  * bank gives the dimensions only (its arrays are not read); the weights are
- * read from packed_mx, the stage-ordered copy moe_pack_bank_mx writes
+ * read from packed_mx, the copy moe_pack_bank_mx writes
  * (256-byte aligned).  H and I must be multiples of 128
  * (MOE_ERR_UNSUPPORTED_SHAPE).  Workspace:
  * moe_workspace_size(T, ...) bytes, as for moe_layer_forward.  Five
@@ -268,17 +268,15 @@ moe_status_t moe_layer_forward_mxfp8(const uint16_t *x, const float *router_w, c
                                      float *topk_w_out, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
- * Bytes of the stage-ordered bank of the MXFP8 variant (0 when H or I is not
- * a multiple of 128): the same codes and scales as the canonical arrays,
- * reordered so that the block-scaled GEMMs read each pipeline stage of a
- * 128-row tile as one contiguous block.  Per section (gate/up, then down),
- * per expert, per 128-row tile (gate/up tile t: gate rows 64t..64t+63 then
- * up rows I+64t..; down tile t: rows 128t..128t+127), per K stage of 128: an
- * 8,704-byte block = the codes, then the scales [row][4 bytes].  The codes
- * are 16 groups of 8 rows, each 64 eight-byte pieces (16 elements of one
- * row): piece w = 8 * slot + row-in-group holds K elements 16 slot .. +15;
- * a group stores pieces w and w + 32 side by side (piece w at position
- * 2 (w mod 32) + w / 32).
+ * Bytes of the bank of the MXFP8 variant (0 when H or I is not a multiple of
+ * 128): the same codes and scales as the canonical arrays, K-chunk major.
+ * Four sections, each at a 256-byte aligned offset: gate/up codes
+ * [E+S][H/128][2I][64 bytes], down codes [E+S][I/128][H][64 bytes], gate/up
+ * scales [E+S][H/128][2I][4 bytes], down scales [E+S][I/128][H][4 bytes] --
+ * for each expert and each chunk of 128 K elements, every weight row's bytes
+ * of that chunk in row order.  The GEMMs read the codes with tensor copies
+ * (16 E2M1 codes per 16-byte shared-memory slot, 128-byte swizzle), a
+ * 64-row copy being 4 KB of consecutive bytes.
  */
 /*
  * Diagnostics: moe_layer_forward_mxfp8 with CUDA events recorded on `stream`
@@ -298,8 +296,9 @@ size_t moe_packed_mx_bank_size(int H, int I, int E, int has_shared);
 /*
  * Fill packed_mx (moe_packed_mx_bank_size bytes, 256-byte aligned) from the
  * bank's canonical arrays (w13, s13, w2, s2: non-NULL, w13 / w2 16-byte and
- * s13 / s2 4-byte aligned).  One-time, load-time work; asynchronous on
- * `stream`; the canonical arrays may be freed once it has completed.
+ * s13 / s2 4-byte aligned) in the order above.  One-time, load-time work;
+ * asynchronous on `stream`; the canonical arrays may be freed once it has
+ * completed.
  */
 moe_status_t moe_pack_bank_mx(const moe_mxfp4_bank_t *bank, void *packed_mx, size_t packed_mx_bytes,
                               cudaStream_t stream);

@@ -105,7 +105,7 @@ def forward_mx(L, b, T=1, k=8, pmx=FAKE, x=FAKE, y=FAKE, ws=FAKE, ws_bytes=1 << 
 
 
 def test_mxfp8_argument_checks(L):
-    # stage-ordered bank: the same bytes as the canonical arrays
+    # the canonical arrays, 256-byte aligned sections (no padding at these sizes)
     n = moe.lib().moe_packed_mx_bank_size(5120, 1536, 160, 1)
     assert n == 161 * 3 * 1536 * 5120 * 17 // 32
     assert moe.lib().moe_packed_mx_bank_size(5120 + 64, 1536, 160, 1) == 0      # H % 128
