@@ -61,6 +61,9 @@ constexpr size_t kCtaStampOffset = kHdrWords * sizeof(uint32_t);
 constexpr int kFusedMaxCtaStamps = 256;
 constexpr size_t kHeaderBytes = kCtaStampOffset + kFusedMaxCtaStamps * 4 * sizeof(unsigned long long);
 
+// Most K pieces the tensor-memory FFN kernels split their last items into.
+constexpr int kTcMaxPieces = 256;
+
 // A pass: up to kPassTokens consecutive entries of one expert's group.
 struct Pass {
     int32_t expert;
@@ -125,7 +128,7 @@ inline void fused_router_tiling(int H, int E, int *groups, int *chunks, int *row
 // Offsets (bytes) of the workspace regions for one problem size.
 struct WsLayout {
     size_t route_part, topk_ids, topk_w, offsets, sorted_tok, sorted_slot, inv_pos, active, passes, passes4, passesw,
-        passesw4, x16, xundo, xs16,
+        passesw4, x16, xundo, xs16, tc_tail, tc_tickets,
         gpart, h16, hundo, ypart, counters, xstage, ystage, fz_rpart, fz_h32, fz_yent, mx_xq, mx_xs, mx_gu, mx_h32,
         mx_hq, mx_hs, mx_y, total;
     int n_kc_gu, n_kc_dn;
@@ -157,6 +160,10 @@ struct WsLayout {
         L.x16 = take((size_t)T * H * 2);
         L.xundo = take((size_t)T * sizeof(float));
         L.xs16 = T > kFusedMaxTokens ? take(entries * H * 2) : 0;   // x per sorted entry (tensor-memory kernels)
+        // tensor-memory kernels: K pieces of the last items (128 rows x 32
+        // columns of partial sums each) and their arrival counters
+        L.tc_tail = T > kFusedMaxTokens ? take((size_t)kTcMaxPieces * 128 * 32 * sizeof(float)) : 0;
+        L.tc_tickets = T > kFusedMaxTokens ? take(2 * (size_t)kTcMaxPieces * sizeof(uint32_t)) : 0;
         L.gpart = take((size_t)L.n_kc_gu * entries * 2 * I * sizeof(float));
         L.h16 = take(entries * 2 * (size_t)I * 2);
         L.hundo = take(entries * sizeof(float));
@@ -280,6 +287,22 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
 // Programmatic dependent launch: wait until the preceding grid on the stream
 // has completed and its writes are visible (a no-op without a prerequisite
 // grid), and allow the next grid to be scheduled.
+// Order key of a logit held as an unevaluated pair (hi, lo) with |lo| at most
+// half an ulp of hi: the two floats mapped to unsigned integers that sort as
+// the floats do, hi in the high word, so that keys compare as the pairs'
+// values.  logit_from_key inverts the mapping of one word.
+__device__ __forceinline__ unsigned long long logit_order_key(float hi, float lo) {
+    auto mono = [](float v) -> uint32_t {
+        const uint32_t b = __float_as_uint(v);
+        return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+    };
+    return ((unsigned long long)mono(hi) << 32) | mono(lo);
+}
+
+__device__ __forceinline__ float logit_from_key(uint32_t m) {
+    return __uint_as_float((m & 0x80000000u) ? (m & 0x7FFFFFFFu) : ~m);
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -496,13 +496,6 @@ __device__ void x_window_local(const FusedArgs &a, RouteState &rs, __half *xwin)
 
 // Order key of a normalised logit pair (hi, lo): larger value -> larger key.
 // lo is below half an ulp of hi, so (hi, lo) order is the order of the sums.
-__device__ __forceinline__ unsigned long long logit_key(float hi, float lo) {
-    auto mono = [](float v) -> uint32_t {
-        const uint32_t b = __float_as_uint(v);
-        return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-    };
-    return ((unsigned long long)mono(hi) << 32) | mono(lo);
-}
 
 // The next layer's router weights and shared expert into L2: this CTA's
 // slice of each region, issued once its own weight streams are done.
@@ -524,9 +517,6 @@ __device__ void prefetch_next_layer(const FusedArgs &a) {
     }
 }
 
-__device__ __forceinline__ float unkey_half(uint32_t m) {
-    return __uint_as_float((m & 0x80000000u) ? (m & 0x7FFFFFFFu) : ~m);
-}
 
 // Order key of logit + bias from its (P, Q) pair.
 __device__ __forceinline__ void put_key(const FusedArgs &a, RouteState &rs, unsigned long long *key, int t, int e,
@@ -536,7 +526,7 @@ __device__ __forceinline__ void put_key(const FusedArgs &a, RouteState &rs, unsi
     two_sum(P, Q, hi, lo);
     if (!isfinite(hi))
         rs.bad = 1;                                  // non-finite router logits
-    key[t * ((a.E + 31) & ~31) + e] = logit_key(hi, lo);
+    key[t * ((a.E + 31) & ~31) + e] = logit_order_key(hi, lo);
 }
 
 // Logit keys.  With r_final the router phase left each logit's pair in chunk
@@ -667,8 +657,8 @@ __device__ bool phase_route(const FusedArgs &a, RouteState &rs, uint8_t *smA, ui
         const unsigned long long k0 = __shfl_sync(full, myk, 0);
         float ex = 0.0f;
         if (lane < k) {
-            const float h0 = unkey_half((uint32_t)(k0 >> 32)), l0 = unkey_half((uint32_t)k0);
-            const float hr = unkey_half((uint32_t)(myk >> 32)), lr = unkey_half((uint32_t)myk);
+            const float h0 = logit_from_key((uint32_t)(k0 >> 32)), l0 = logit_from_key((uint32_t)k0);
+            const float hr = logit_from_key((uint32_t)(myk >> 32)), lr = logit_from_key((uint32_t)myk);
             ex = expf(__fadd_rn(__fsub_rn(hr, h0), __fsub_rn(lr, l0)));
         }
         float denom = 0.0f;

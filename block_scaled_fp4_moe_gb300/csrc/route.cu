@@ -133,7 +133,8 @@ __device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const
     constexpr int kW = kGroupThreads / 32;
     __shared__ int cnt[kMaxExperts];
     __shared__ int wbase[kW][kGroupParExperts];       // per-warp counts, then per-warp cursors
-    __shared__ int wsum[kW][6];
+    constexpr int kScanPerLane = kGroupThreads / 32;
+    __shared__ int sscan[6][kGroupThreads];          // per-thread values, then their exclusive scans
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n = T * kps;
     const bool par = n_tot <= kGroupParExperts;
@@ -149,14 +150,26 @@ __device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const
     __syncthreads();
     int bad = 0;
     auto id_at = [&](int i) { return ids_in_smem ? ids[i] : __ldcg(ids + i); };
-    for (int i = warp * seg + lane; i < min(n, (warp + 1) * seg); i += 32) {
-        const int e = id_at(i);
-        if (e < 0 || e >= n_tot) {
-            bad = 1;
-        } else {
-            atomicAdd(&cnt[e], 1);
-            if (par)
-                atomicAdd(&wbase[warp][e], 1);
+    // counts, 32 entries at a time, one update per distinct expert (its
+    // lowest lane adds the group's size): into the warp's own row (no other
+    // warp writes it; the rows are added per expert below), or with one
+    // shared-memory atomic per group when the experts are too many for rows
+    {
+        const int i1 = min(n, (warp + 1) * seg);
+        for (int base = warp * seg; base < i1; base += 32) {
+            const int i = base + lane;
+            int e = i < i1 ? id_at(i) : -1;
+            if (i < i1 && (e < 0 || e >= n_tot)) {
+                bad = 1;
+                e = -1;
+            }
+            const unsigned same = __match_any_sync(0xffffffffu, e);
+            if (e >= 0 && lane == __ffs(same) - 1) {
+                if (par)
+                    wbase[warp][e] += __popc(same);
+                else
+                    atomicAdd(&cnt[e], __popc(same));
+            }
         }
     }
     bad = __syncthreads_or(bad);
@@ -182,40 +195,56 @@ __device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const
     const int e0 = tid * per, e1 = min(n_tot, e0 + per);
     int loc[6] = {0, 0, 0, 0, 0, 0};
     for (int e = e0; e < e1; ++e) {
-        const int v = cnt[e];
+        int v = cnt[e];
+        if (par) {
+#pragma unroll
+            for (int w2 = 0; w2 < kW; ++w2)
+                v += wbase[w2][e];
+            cnt[e] = v;                                // only this thread reads it again
+        }
         loc[0] += v;
         loc[1] += v > 0;
 #pragma unroll
         for (int l = 0; l < 4; ++l)
             loc[2 + l] += (v + caps[l] - 1) / caps[l];
     }
-    int inc[6];
+    // the six exclusive scans, one warp each over the threads' values (8
+    // per lane, in loops: this runs once per call on one CTA, where compact
+    // code matters more than unrolling)
 #pragma unroll
-    for (int q = 0; q < 6; ++q) {
-        inc[q] = loc[q];
-#pragma unroll
+    for (int q = 0; q < 6; ++q)
+        sscan[q][tid] = loc[q];
+    __syncthreads();
+    if (warp < 6) {
+        int *row = sscan[warp] + kScanPerLane * lane;
+        int run = 0;
+#pragma unroll 1
+        for (int j = 0; j < kScanPerLane; ++j)
+            run += row[j];
+        int inc = run;
+#pragma unroll 1
         for (int d = 1; d < 32; d <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, inc[q], d);
+            const int y = __shfl_up_sync(0xffffffffu, inc, d);
             if (lane >= d)
-                inc[q] += y;
+                inc += y;
+        }
+        int ex = inc - run;
+#pragma unroll 1
+        for (int j = 0; j < kScanPerLane; ++j) {
+            const int v = row[j];
+            row[j] = ex;
+            ex += v;
         }
     }
-    if (lane == 31)
-#pragma unroll
-        for (int q = 0; q < 6; ++q)
-            wsum[warp][q] = inc[q];
     __syncthreads();
     int ex[6];
 #pragma unroll
-    for (int q = 0; q < 6; ++q) {
-        int before = 0;
-        for (int w2 = 0; w2 < warp; ++w2)
-            before += wsum[w2][q];
-        ex[q] = before + inc[q] - loc[q];
-    }
+    for (int q = 0; q < 6; ++q)
+        ex[q] = sscan[q][tid];
     for (int e = e0; e < e1; ++e) {
         const int v = cnt[e];
         o.offsets[e] = ex[0];
+        cnt[e] = ex[0];                                // the offset, for the cursors below
         if (v > 0)
             o.active[ex[1]++] = e;
 #pragma unroll
@@ -238,13 +267,13 @@ __device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const
         if (o.num_active)
             *o.num_active = ex[1];
     }
-    __syncthreads();                                   // offsets written (read back below through global memory)
+    __syncthreads();                                   // offsets in cnt
 
     // cursors: per warp, the offset of the expert plus its counts in the
     // earlier segments
     if (par) {
         for (int e = tid; e < n_tot; e += blockDim.x) {
-            int run = __ldcg(o.offsets + e);
+            int run = cnt[e];
 #pragma unroll
             for (int w2 = 0; w2 < kW; ++w2) {
                 const int h = wbase[w2][e];
@@ -253,10 +282,6 @@ __device__ void group_block(const int32_t *ids, int T, int kps, int n_tot, const
             }
         }
         __syncthreads();
-    } else if (warp == 0) {
-        for (int e = lane; e < n_tot; e += 32)
-            cnt[e] = __ldcg(o.offsets + e);            // cursors of the single-warp scatter
-        __syncwarp();
     }
     // stable scatter, 32 entries at a time: every warp its own segment, or
     // warp 0 all entries
@@ -297,7 +322,6 @@ group_kernel(const int32_t *ids, int T, int kps, int n_tot, GroupOut o, uint32_t
 // arrays this stays under the 48 KB that need no opt-in).
 constexpr int kGroupSmemIds = 4 * 1024;
 
-constexpr int kRankWarps = 8;          // warps of route_finish_kernel (256 threads)
 
 // One CTA per token.  All threads sum the partial pairs of the experts in a
 // fixed order (the loads of one expert issued together) and add the bias;
@@ -310,16 +334,25 @@ route_finish_kernel(const float2 *__restrict__ part, int nh, const float *__rest
                     int has_shared, float shared_weight, int32_t *__restrict__ ids_out, float *__restrict__ w_out,
                     uint32_t *__restrict__ hdr, int do_group, GroupOut go, const uint16_t *__restrict__ x, int H,
                     __half *x16, float *xundo) {
-    extern __shared__ float2 L[];   // [E] (hi, lo) logits, then the partial ranks; later the grouping's ids
+    // [Ep] order keys of the logits, then the groups' candidate lists (keys,
+    // then expert ids); later the grouping's ids
+    extern __shared__ unsigned long long rkey[];
     __shared__ int last_cta;
     __shared__ int sids[kMaxSlots];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int t = blockIdx.x;
     const int kps = k + has_shared;
+    const int Ep = (E + 31) & ~31, G = Ep >> 5;        // experts padded to whole groups of 32
+    unsigned long long *ckey = rkey + Ep;               // [G][k]
+    int *cand = reinterpret_cast<int *>(ckey + (size_t)G * k);
     pdl_wait();
     pdl_trigger();
 
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    for (int e = threadIdx.x; e < Ep; e += blockDim.x) {
+        if (e >= E) {
+            rkey[e] = 0ull;                               // padding: below every real key
+            continue;
+        }
         float p = 0.0f, s = 0.0f;
         float2 v[16];
 #pragma unroll
@@ -338,60 +371,83 @@ route_finish_kernel(const float2 *__restrict__ part, int nh, const float *__rest
         pair_add(p, s, b, 0.0f);
         float hi, lo;
         two_sum(p, s, hi, lo);
-        L[e] = make_float2(hi, lo);
+        if (hi != hi)                            // a NaN logit counts as -inf
+            hi = lo = -INFINITY;
+        rkey[e] = logit_order_key(hi, lo);
     }
     __syncthreads();
 
-    // rank of every expert in the order (logit pair descending, equal pairs:
-    // the lower index first; a NaN logit counts as -inf): the experts of
-    // rank < k are the selection and their rank is their slot
-    __shared__ int sel[kMaxSlots];
-    __shared__ float sel_ex[kMaxSlots];
-    unsigned short *prank = reinterpret_cast<unsigned short *>(L + E);   // [kRankWarps][E] after the logits
-    for (int e = threadIdx.x; e < E; e += blockDim.x)
-        if (L[e].x != L[e].x)
-            L[e] = make_float2(-INFINITY, -INFINITY);
-    __syncthreads();
-    {
-        // warp w counts, for every expert, the experts of its slice
-        // [f0, f1) that come before it; the partial counts are then added
-        const int f0 = (int)((long long)E * warp / kRankWarps), f1 = (int)((long long)E * (warp + 1) / kRankWarps);
-        for (int e = lane; e < E; e += 32) {
-            const float2 v = L[e];
-            int c = 0;
-#pragma unroll 4
-            for (int f = f0; f < f1; ++f) {
-                const float2 u = L[f];
-                c += (u.x > v.x || (u.x == v.x && (u.y > v.y || (u.y == v.y && f < e)))) ? 1 : 0;
+    // Top k in the order (logit pair descending, equal pairs: the lower index
+    // first).  Stage 1: an expert ranked k or lower inside its group of 32
+    // cannot be in the top k, so each group's first k ranks form its sorted
+    // candidate list.  Ranks come from the keys' high words (two keys per
+    // 16-byte load); a key whose high word another key shares is ranked by
+    // the full keys and the index rule.
+    for (int e = threadIdx.x; e < Ep; e += blockDim.x) {
+        const unsigned long long *g = rkey + (e & ~31);
+        const unsigned long long my = g[e & 31];
+        const uint4 *g4 = reinterpret_cast<const uint4 *>(g);
+        const uint32_t myhi = (uint32_t)(my >> 32);
+        int r = 0, eq = 0;
+#pragma unroll 8
+        for (int j2 = 0; j2 < 16; ++j2) {
+            const uint4 w = g4[j2];              // key 2 j2: (x lo, y hi), key 2 j2 + 1: (z lo, w hi)
+            r += (w.y > myhi) + (w.w > myhi);
+            eq += (w.y == myhi) + (w.w == myhi);
+        }
+        if (eq > 1) {
+            r = 0;
+            for (int j = 0; j < 32; ++j) {
+                const unsigned long long o = g[j];
+                r += (o > my) | ((o == my) & (j < (e & 31)));
             }
-            prank[warp * E + e] = (unsigned short)c;
+        }
+        if (r < k) {
+            ckey[(e >> 5) * k + r] = my;
+            cand[(e >> 5) * k + r] = e < E ? e : 0x7fffffff;
         }
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int rank = 0;
-#pragma unroll
-        for (int w2 = 0; w2 < kRankWarps; ++w2)
-            rank += prank[w2 * E + e];
-        if (rank < k)
-            sel[rank] = e;
-    }
-    __syncthreads();
-    // softmax over the kept logits relative to the largest, the denominator
-    // summed in slot order
-    if (threadIdx.x < k) {
-        const float2 top = L[sel[0]], v = L[sel[threadIdx.x]];
-        sel_ex[threadIdx.x] = expf(__fadd_rn(__fsub_rn(v.x, top.x), __fsub_rn(v.y, top.y)));
-    }
-    __syncthreads();
+    // Stage 2, warp 0: lane g holds the head of group g's list; each round
+    // takes the largest head (key, then the lower index) and that lane moves
+    // to its next entry, so slot r gets the r-th largest logit.  The softmax
+    // over the kept logits is taken relative to the largest, its denominator
+    // summed in slot order.
     if (warp == 0) {
+        const unsigned full = 0xffffffffu;
+        int pos = 0;
+        unsigned long long hk = lane < G ? ckey[lane * k] : 0ull;
+        unsigned he = lane < G ? (unsigned)cand[lane * k] : 0xffffffffu;
+        unsigned long long myk = 0ull;
+        int myid = -1;
+        for (int r = 0; r < k; ++r) {
+            const uint32_t hh = (uint32_t)(hk >> 32), mh = __reduce_max_sync(full, hh);
+            const uint32_t ml = __reduce_max_sync(full, hh == mh ? (uint32_t)hk : 0u);
+            const unsigned we = __reduce_min_sync(full, (hh == mh && (uint32_t)hk == ml) ? he : 0xffffffffu);
+            if (lane == r) {
+                myk = ((unsigned long long)mh << 32) | ml;
+                myid = (int)we;
+            }
+            if (lane < G && he == we && we < (unsigned)E) {
+                ++pos;
+                hk = pos < k ? ckey[lane * k + pos] : 0ull;
+                he = pos < k ? (unsigned)cand[lane * k + pos] : 0xffffffffu;
+            }
+        }
+        const unsigned long long k0 = __shfl_sync(full, myk, 0);
+        float ex = 0.0f;
+        if (lane < k) {
+            const float h0 = logit_from_key((uint32_t)(k0 >> 32)), l0 = logit_from_key((uint32_t)k0);
+            const float hr = logit_from_key((uint32_t)(myk >> 32)), lr = logit_from_key((uint32_t)myk);
+            ex = expf(__fadd_rn(__fsub_rn(hr, h0), __fsub_rn(lr, l0)));
+        }
         float denom = 0.0f;
         for (int r = 0; r < k; ++r)
-            denom += sel_ex[r];
+            denom += __shfl_sync(full, ex, r);
         if (lane < k) {
-            ids_out[(size_t)t * kps + lane] = sel[lane];
-            w_out[(size_t)t * kps + lane] = sel_ex[lane] / denom;
-            sids[lane] = sel[lane];
+            ids_out[(size_t)t * kps + lane] = myid;
+            w_out[(size_t)t * kps + lane] = ex / denom;
+            sids[lane] = myid;
         }
         if (has_shared && lane == k) {
             ids_out[(size_t)t * kps + k] = E;
@@ -422,7 +478,7 @@ route_finish_kernel(const float2 *__restrict__ part, int nh, const float *__rest
     if (n <= kGroupSmemIds) {
         // every token's ids into shared memory first: the grouping then reads
         // them without a global round trip per step
-        int *sm_ids = reinterpret_cast<int *>(L);
+        int *sm_ids = reinterpret_cast<int *>(rkey);
         for (int i = threadIdx.x; i < n; i += blockDim.x)
             sm_ids[i] = __ldcg(ids_out + i);
         __syncthreads();
@@ -457,7 +513,8 @@ cudaError_t launch_route(const uint16_t *x, const float *wr, const float *bias, 
         (err = cudaEventRecord(ev_after_partial, stream)) != cudaSuccess)
         return err;
     const size_t n_ids = (size_t)T * (k + has_shared);
-    size_t smem = (size_t)E * (sizeof(float2) + kRankWarps * sizeof(unsigned short));
+    const int Ep = (E + 31) & ~31;
+    size_t smem = (size_t)Ep * sizeof(unsigned long long) + (size_t)(Ep / 32) * k * (sizeof(unsigned long long) + sizeof(int));
     if (do_group && T > 1 && n_ids <= (size_t)kGroupSmemIds && n_ids * sizeof(int) > smem)
         smem = n_ids * sizeof(int);
     __half *x16 = do_group ? ws_at<__half>(ws, L.x16) : nullptr;

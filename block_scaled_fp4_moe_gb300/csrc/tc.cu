@@ -132,7 +132,46 @@ struct TcArgs {
     float *part;                // gate/up: [entries][2][I] g, u sums; down: [entries][H] outputs
     int out_len;                // I (gate/up) or H (down)
     const float *bundo;         // down: per-entry factor undoing the h scaling
+    float *tail;                // [kTcMaxPieces][128][32] partial sums of the K pieces of the last items
+    uint32_t *tickets;          // [kTcMaxPieces] pieces done per split item (zero at kernel start)
 };
+
+constexpr int kTcMinSplitSaving = 4;        // raw stages a split must save on the busiest CTA
+
+// Work of one CTA (index b of G): items b, b + G, ... whole while every CTA
+// has one, then the r = n_items mod G items that are left, each cut along K
+// into P pieces of S raw stages (P = 1: whole, round robin), so that the
+// CTAs end together.  Pieces of item q G + k go to CTAs k P .. k P + P - 1;
+// each writes its raw sums to the tail slot of its CTA index, and the CTA
+// whose piece arrives last adds the P slots in piece order and writes the
+// item's outputs -- the same order on every call.
+struct TcSchedule {
+    long long q;      // whole items per CTA
+    int r, P, S;      // items left, pieces per such item, raw stages per piece
+    int my_items;     // work items of this CTA
+};
+
+__device__ __forceinline__ TcSchedule tc_schedule(long long n_items, int G, int b, int nraw) {
+    TcSchedule w;
+    w.q = n_items / G;
+    w.r = (int)(n_items % G);
+    w.P = 1;
+    w.S = nraw;
+    if (w.r > 0) {
+        int p0 = min(nraw, min(G, kTcMaxPieces) / w.r);
+        p0 = max(p0, 1);
+        w.S = (nraw + p0 - 1) / p0;
+        w.P = (nraw + w.S - 1) / w.S;
+        // a split costs the last piece's CTA an arrival and the sum (about
+        // as long as three raw stages): only worth it for a larger saving
+        if (nraw - w.S < kTcMinSplitSaving) {
+            w.S = nraw;
+            w.P = 1;
+        }
+    }
+    w.my_items = (int)w.q + ((w.P > 1 ? b < w.r * w.P : b < w.r) ? 1 : 0);
+    return w;
+}
 
 __device__ __forceinline__ bool tc_mbar_try(uint32_t bar, uint32_t parity) {
     uint32_t done;
@@ -176,6 +215,28 @@ __device__ bool tc_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag)
 
 __device__ __forceinline__ void tc_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Named barrier 1 of the four epilogue warps; with a vote: true when every
+// thread's v is true.
+__device__ __forceinline__ void tc_epi_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kTcEpiWarps * 32) : "memory"); }
+
+__device__ __forceinline__ bool tc_epi_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, 1, %2, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(kTcEpiWarps * 32)
+        : "memory");
+    return r != 0;
+}
+
+// Arrival counter of a split item: add one with acquire-release semantics at
+// GPU scope, return the old count.
+__device__ __forceinline__ uint32_t tc_ticket(uint32_t *t) {
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(t) : "memory");
+    return old;
 }
 
 // Shared-memory descriptor, K-major, no swizzle.
@@ -242,27 +303,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ uint32_t s_taddr;
     __shared__ int s_abort;
     __shared__ int s_bad;
+    __shared__ int s_last;
     // the warp index and every value a warp's control flow depends on are
     // broadcast from lane 0, so that the compiler treats them as warp-uniform
     const int tid = threadIdx.x, lane = tid & 31;
     const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
-    pdl_wait();
+    // The pass lists and the weights are final when this grid starts (the
+    // grouping finished before the preceding kernel let it launch), so the
+    // weight stream and the decode start at once; the warps that read what
+    // the preceding kernel writes (activations, the h scale factors, the
+    // arrival counters it clears) wait for it first.
     pdl_trigger();
     const int n_passes =
         __shfl_sync(0xffffffffu, (int)*reinterpret_cast<const volatile uint32_t *>(a.hdr + a.passes_word), 0);
     const int tiles = (a.upe + kTcUnits - 1) / kTcUnits;
+    const int nraw = a.steps / kTcRawSteps;           // raw stages per item
     const long long n_items = (long long)n_passes * tiles;
-    const int my_items = n_items > blockIdx.x ? (int)((n_items - 1 - blockIdx.x) / gridDim.x + 1) : 0;
+    const TcSchedule sch = tc_schedule(n_items, (int)gridDim.x, (int)blockIdx.x, nraw);
+    const int my_items = sch.my_items;
     if (my_items == 0)
         return;
+    // work item j of this CTA: the item index, its raw stages [r0, r1) and
+    // the tail slot it writes (-1: a whole item, written directly)
+    auto item_of = [&](int j) -> long long {
+        if (j < sch.q)
+            return blockIdx.x + (long long)j * gridDim.x;
+        return sch.q * gridDim.x + (sch.P > 1 ? (int)blockIdx.x / sch.P : (int)blockIdx.x);
+    };
+    auto stage_r0 = [&](int j) { return j < sch.q || sch.P == 1 ? 0 : ((int)blockIdx.x % sch.P) * sch.S; };
+    auto stage_r1 = [&](int j) { return j < sch.q || sch.P == 1 ? nraw : min(nraw, stage_r0(j) + sch.S); };
     // every pass of this CTA's items lies inside the buffers, or the CTA does nothing
     if (tid == 0) {
         s_abort = 0;
         s_bad = 0;
+        s_last = 0;
     }
     __syncthreads();
     for (int j = tid; j < my_items; j += blockDim.x) {
-        const Pass ps = a.passes[(blockIdx.x + (long long)j * gridDim.x) / tiles];
+        const Pass ps = a.passes[item_of(j) / tiles];
         if (ps.expert < 0 || ps.expert >= a.n_tot || ps.count < 1 || ps.count * a.rows_per_entry > kTcNMax ||
             ps.begin < 0 || ps.begin + ps.count > a.n_entries)
             s_bad = 1;
@@ -273,7 +351,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             record_status(a.hdr, MOE_ERR_DEVICE_ASSERT);
         return;
     }
-    const int nraw = a.steps / kTcRawSteps;           // raw stages per item
     uint64_t *bars = reinterpret_cast<uint64_t *>(tc_smem + (size_t)kTcBOff + (size_t)kTcBStages * kTcBBytes);
     uint64_t *r_full = bars, *r_empty = bars + kTcRawStages;
     uint64_t *b_full = bars + 2 * kTcRawStages, *b_empty = b_full + kTcBStages;
@@ -308,8 +385,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = s_taddr;
     volatile int *abort_flag = &s_abort;
-    auto item_pass = [&](int j) { return a.passes[(blockIdx.x + (long long)j * gridDim.x) / tiles]; };
-    auto item_tile = [&](int j) { return (int)((blockIdx.x + (long long)j * gridDim.x) % tiles); };
+    auto item_pass = [&](int j) { return a.passes[item_of(j) / tiles]; };
+    auto item_tile = [&](int j) { return (int)(item_of(j) % tiles); };
     auto tile_units = [&](int tile) { return min(kTcUnits, a.upe - tile * kTcUnits); };
     const uint32_t raw_base = smem_u32(tc_smem);
 
@@ -331,7 +408,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t b0 = __ldg(re + g), b8 = __ldg(re + g + 8);
                 b4 = b0 | (b0 << 8) | (b8 << 16) | (b8 << 24);
             }
-            for (int r = 0; r < nraw; ++r, ++rs) {
+            const int r1 = stage_r1(j);
+            for (int r = stage_r0(j); r < r1; ++r, ++rs) {
                 const int rb = rs % kTcRawStages;
                 if (!__all_sync(0xffffffffu, tc_wait(smem_u32(r_full + rb), (rs / kTcRawStages) & 1, abort_flag))) {
                     ok = false;
@@ -395,6 +473,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // tile = the pass's rows over the same 512 K elements (one tensor
         // copy).  Both rings advance once per raw stage.
         const bool weights = warp == kTcProdWarp;
+        if (!weights)
+            pdl_wait();
         const int nst = weights ? kTcRawStages : kTcBStages;
         uint64_t *full = weights ? r_full : b_full, *empty = weights ? r_empty : b_empty;
         if (lane == 0) {
@@ -410,7 +490,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t bytes = weights ? (uint32_t)(nu * kTcUnitStage) : (narrow ? 16u : 32u) * (uint32_t)kTcRawK * 2u;
                 const int row0 = ps.begin * a.rows_per_entry;
                 const uint8_t *ubase = a.packed + ((size_t)ps.expert * a.upe + tile * kTcUnits) * a.unit_bytes;
-                for (int r = 0; r < nraw; ++r, ++rs) {
+                const int r1 = stage_r1(j);
+                for (int r = stage_r0(j); r < r1; ++r, ++rs) {
                     const int rb = rs % nst;
                     if (rs >= nst && !tc_wait(smem_u32(empty + rb), ((rs / nst) + 1) & 1, abort_flag)) {
                         ok = false;
@@ -462,7 +543,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 break;
             }
             const uint32_t dcol = tmem + (uint32_t)(kTcDCol + kTcNMax * db);
-            for (int st = 0; st < 2 * nraw; ++st, ++gs) {
+            const int nst2 = 2 * (stage_r1(j) - stage_r0(j));
+            for (int st = 0; st < nst2; ++st, ++gs) {
                 const int ab = gs % kTcAStages, rs = gs >> 1, rb = rs % kTcBStages, h = gs & 1;
                 if (!__all_sync(0xffffffffu, tc_wait(smem_u32(a_full + ab), (gs / kTcAStages) & 1, abort_flag)) ||
                     (h == 0 &&
@@ -509,6 +591,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else if (warp >= kTcEpiWarp0 && warp < kTcEpiWarp0 + kTcEpiWarps) {
         // ---- epilogue: lane quarter q of the accumulator = MMA rows 32 q ..
+        pdl_wait();
         const int qd = warp & 3;
         const int m = 32 * qd + lane;                 // MMA row of this lane
         bool ok = true;
@@ -517,35 +600,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int tile = item_tile(j);
             const int rows = ps.count * a.rows_per_entry;
             const int db = j & 1;
+            const bool piece = j >= sch.q && sch.P > 1;
             const bool present = (m >> 4) < tile_units(tile);
             const uint32_t rb = present ? __ldg(a.rowexp + ((size_t)ps.expert * a.upe + tile * kTcUnits) * 16 + m) : 0u;
             const float fac = tc_row_factor(rb);
-            if (!__all_sync(0xffffffffu, tc_wait(smem_u32(d_full + db), (j / 2) & 1, abort_flag))) {
-                ok = false;
-                break;
-            }
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            // the accumulator, 16 columns at a time, and that chunk's outputs
-            const uint32_t taddr = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(kTcDCol + kTcNMax * db);
             const int u = tile * kTcUnits + (m >> 4), r = m & 15;
             const int col = MODE == kFfnGateUp ? (r < 8 ? 8 * u + r : a.out_len + 8 * u + r - 8) : 16 * u + r;
-#pragma unroll
-            for (int c0 = 0; c0 < kTcNMax; c0 += 16) {
-                if (c0 >= rows)
-                    break;
-                uint32_t w[16];
-                asm volatile(
-                    "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
-                    "[%16];"
-                    : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]),
-                      "=r"(w[8]), "=r"(w[9]), "=r"(w[10]), "=r"(w[11]), "=r"(w[12]), "=r"(w[13]), "=r"(w[14]),
-                      "=r"(w[15])
-                    : "r"(taddr + (uint32_t)c0));
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                float v[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    v[i] = __uint_as_float(w[i]);
+            // the outputs of the 16 columns of sums from column c0 on
+            auto emit = [&](int c0, const float *v) {
                 if (MODE == kFfnGateUp) {
                     // MMA row m = unit row r of unit u: gate row 8 u + r (r < 8), up row 8 u + r - 8
 #pragma unroll
@@ -567,17 +629,127 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         }
                     }
                 }
+            };
+            ok = __all_sync(0xffffffffu, tc_wait(smem_u32(d_full + db), (j / 2) & 1, abort_flag));
+            // the four epilogue warps take every decision together (they meet
+            // at a named barrier below)
+            ok = tc_epi_and(ok);
+            if (!ok)
+                break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            // the accumulator, 16 columns at a time: a whole item's outputs,
+            // or a piece's raw sums into the tail slot of this CTA
+            const uint32_t taddr = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(kTcDCol + kTcNMax * db);
+            float4 *slot = reinterpret_cast<float4 *>(a.tail + ((size_t)blockIdx.x * 128 + m) * kTcNMax);
+#pragma unroll
+            for (int c0 = 0; c0 < kTcNMax; c0 += 16) {
+                if (c0 >= rows)
+                    break;
+                uint32_t w[16];
+                asm volatile(
+                    "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+                    "[%16];"
+                    : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]),
+                      "=r"(w[8]), "=r"(w[9]), "=r"(w[10]), "=r"(w[11]), "=r"(w[12]), "=r"(w[13]), "=r"(w[14]),
+                      "=r"(w[15])
+                    : "r"(taddr + (uint32_t)c0));
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+                float v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    v[i] = __uint_as_float(w[i]);
+                if (piece) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        slot[c0 / 4 + i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+                } else {
+                    emit(c0, v);
+                }
             }
             // the accumulators are read: the MMAs of item j + 2 may overwrite them
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
             if (lane == 0)
                 tc_arrive(smem_u32(d_empty + db));
+            if (piece) {
+                // count the piece in (the acquire-release add publishes the
+                // slot stores ordered before it by the barrier); the CTA of the
+                // item's last piece adds the slots after the final barrier below
+                tc_epi_sync();
+                if (qd == 0 && lane == 0)
+                    s_last = tc_ticket(a.tickets + (int)blockIdx.x / sch.P) == (uint32_t)(sch.P - 1);
+            }
         }
+    }
+    pdl_wait();
+    // a split item's pass, tile and row exponent, loaded before the barrier
+    // for the case that this CTA adds its pieces
+    Pass piece_ps{};
+    int piece_tile = 0;
+    uint32_t piece_rb = 0;
+    if (sch.P > 1 && my_items > sch.q) {
+        piece_ps = item_pass(my_items - 1);
+        piece_tile = item_tile(my_items - 1);
+        const int m = tid >> 2;
+        if ((m >> 4) < tile_units(piece_tile))
+            piece_rb = __ldg(a.rowexp + ((size_t)piece_ps.expert * a.upe + piece_tile * kTcUnits) * 16 + m);
     }
     __syncthreads();
     if (s_abort && tid == 0)
         record_status(a.hdr, MOE_ERR_DEVICE_TIMEOUT);
+    if (s_last && !s_abort) {
+        // the split item's outputs: thread t takes row t / 4 of the tile and,
+        // per 16 columns, columns 4 (t % 4) .. + 3, adding the P slots in
+        // piece order (all slot loads issued at once)
+        const int rows = piece_ps.count * a.rows_per_entry;
+        const int m = tid >> 2, c4 = 4 * (tid & 3);
+        const int k = (int)blockIdx.x / sch.P;
+        const int u = piece_tile * kTcUnits + (m >> 4), r = m & 15;
+        const float fac = tc_row_factor(piece_rb);
+        const bool present = (m >> 4) < tile_units(piece_tile);
+        constexpr int kBatch = 16;
+        for (int c0 = 0; c0 < kTcNMax && c0 < rows && present; c0 += 16) {
+            float v[4];
+            for (int p0 = 0; p0 < sch.P; p0 += kBatch) {
+                float4 t[kBatch];
+#pragma unroll
+                for (int i = 0; i < kBatch; ++i)
+                    if (p0 + i < sch.P)
+                        t[i] = __ldcg(reinterpret_cast<const float4 *>(
+                            a.tail + ((size_t)(k * sch.P + p0 + i) * 128 + m) * kTcNMax + c0 + c4));
+#pragma unroll
+                for (int i = 0; i < kBatch; ++i)
+                    if (p0 + i < sch.P) {
+                        if (p0 + i == 0) {
+                            v[0] = t[i].x, v[1] = t[i].y, v[2] = t[i].z, v[3] = t[i].w;
+                        } else {
+                            v[0] += t[i].x, v[1] += t[i].y, v[2] += t[i].z, v[3] += t[i].w;
+                        }
+                    }
+            }
+            if (MODE == kFfnGateUp) {
+                const int col = r < 8 ? 8 * u + r : a.out_len + 8 * u + r - 8;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int n = c0 + c4 + c;
+                    if (n < piece_ps.count && MOE_DBG_IN_RANGE(piece_ps.begin + n, a.n_entries, a.hdr) &&
+                        MOE_DBG_IN_RANGE(col, 2 * a.out_len, a.hdr))
+                        a.part[(size_t)(piece_ps.begin + n) * 2 * a.out_len + col] = v[c] * fac;
+                }
+            } else {
+                const int col = 16 * u + r;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int jj = (c0 + c4) / 2 + c;
+                    if (jj < piece_ps.count && MOE_DBG_IN_RANGE(piece_ps.begin + jj, a.n_entries, a.hdr) &&
+                        MOE_DBG_IN_RANGE(col, a.out_len, a.hdr)) {
+                        const int e = piece_ps.begin + jj;
+                        a.part[(size_t)e * a.out_len + col] = (v[2 * c] + v[2 * c + 1]) * fac * a.bundo[e];
+                    }
+                }
+            }
+        }
+    }
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTcTmemCols));
@@ -590,9 +762,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // + 16 (m % 2) + 4 ((m / 2) % 2).
 __global__ void __launch_bounds__(256) xsort_kernel(const __half *__restrict__ x16, int H,
                                                    const int32_t *__restrict__ sorted_tok, int T, int entries,
-                                                   __half *__restrict__ xs16, uint32_t *__restrict__ hdr) {
+                                                   __half *__restrict__ xs16, uint32_t *__restrict__ tickets,
+                                                   uint32_t *__restrict__ hdr) {
     pdl_wait();
     pdl_trigger();
+    // the arrival counters of the two tensor-memory kernels that follow
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < 2 * kTcMaxPieces; i += blockDim.x)
+            tickets[i] = 0;
     const int e = blockIdx.x;
     if (e >= entries)
         return;
@@ -738,6 +915,8 @@ cudaError_t launch_ffn_tc(const FfnProblem &pr, void *ws, const WsLayout &L, int
     cudaError_t err;
     __half *xs16 = ws_at<__half>(ws, L.xs16);
     __half *h16 = ws_at<__half>(ws, L.h16);
+    uint32_t *tickets = ws_at<uint32_t>(ws, L.tc_tickets);
+    float *tail = ws_at<float>(ws, L.tc_tail);
     CUtensorMap gm16, gm32, dm16, dm32;
     if ((err = encode_b_map(&gm16, xs16, entries, H, 16)) != cudaSuccess ||
         (err = encode_b_map(&gm32, xs16, entries, H, 32)) != cudaSuccess ||
@@ -745,7 +924,7 @@ cudaError_t launch_ffn_tc(const FfnProblem &pr, void *ws, const WsLayout &L, int
         (err = encode_b_map(&dm32, h16, 2LL * entries, I, 32)) != cudaSuccess)
         return err;
     err = launch_pdl(xsort_kernel, dim3(entries), dim3(256), 0, stream, (const __half *)ws_at<__half>(ws, L.x16), H,
-                     (const int32_t *)ws_at<int32_t>(ws, L.sorted_tok), T, entries, xs16, hdr);
+                     (const int32_t *)ws_at<int32_t>(ws, L.sorted_tok), T, entries, xs16, tickets, hdr);
     if (err != cudaSuccess)
         return err;
     TcArgs g{};
@@ -762,6 +941,8 @@ cudaError_t launch_ffn_tc(const FfnProblem &pr, void *ws, const WsLayout &L, int
     g.hdr = hdr;
     g.part = ws_at<float>(ws, L.gpart);
     g.out_len = I;
+    g.tail = tail;
+    g.tickets = tickets;
     if ((err = launch_tc<kFfnGateUp>(g, gm16, gm32, num_sms, stream)) != cudaSuccess)
         return err;
     if ((err = launch_hfin(ws, L, entries, I, true, stream)) != cudaSuccess)
@@ -783,6 +964,8 @@ cudaError_t launch_ffn_tc(const FfnProblem &pr, void *ws, const WsLayout &L, int
     d.part = ws_at<float>(ws, L.ypart);
     d.out_len = H;
     d.bundo = ws_at<float>(ws, L.hundo);
+    d.tail = tail;
+    d.tickets = tickets + kTcMaxPieces;
     if ((err = launch_tc<kFfnDown>(d, dm16, dm32, num_sms, stream)) != cudaSuccess)
         return err;
     return launch_combine(ws_at<float>(ws, L.ypart), entries, ws_at<int32_t>(ws, L.inv_pos), pr.topk_w, T, kps, H,

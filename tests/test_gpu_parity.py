@@ -162,6 +162,27 @@ def test_route_topk_matches_oracle(name):
     np.testing.assert_allclose(w.cpu().numpy(), r["w"], rtol=2e-6, atol=1e-7)
 
 
+@pytest.mark.parametrize("T,E,k", [(12, 1024, 31), (9, 5, 5), (10, 70, 20), (11, 33, 8)])
+def test_route_topk_group_lists_match_the_oracle(T, E, k):
+    """Top k at the extremes of the group-list selection (candidates: each
+    group of 32 experts' first k ranks, merged by one warp): 32 groups with
+    k + 1 = 32 slots, one group holding fewer experts than 32 with k = E, a
+    partial last group, and more k than one group's real experts."""
+    rng = np.random.default_rng(100 + E)
+    H = 512
+    x = inputs.f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    wr = (0.02 * rng.standard_normal((H, E))).astype(np.float32)
+    bias = (0.05 * rng.standard_normal(E)).astype(np.float32)
+    ids = torch.empty((T, k + 1), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k + 1), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(moe.moe_workspace_size(T, H, 64, E, k, 1), dtype=torch.uint8, device="cuda")
+    moe.moe_route_topk(dev_bf16(x), torch.from_numpy(wr).cuda(), torch.from_numpy(bias).cuda(), k, 1, 1.0, ids, w, ws)
+    assert moe.moe_check_device_status(ws) == 0
+    r = oracle.route(x, wr, bias, k)
+    np.testing.assert_array_equal(ids.cpu().numpy(), r["ids"])
+    np.testing.assert_allclose(w.cpu().numpy(), r["w"], rtol=2e-6, atol=1e-7)
+
+
 # ------------------------------------------------------------- whole layer, small
 
 SMALL = [

@@ -97,3 +97,35 @@ def test_pass_widths_select_16_and_32_column_mmas(T, E, k):
     p = problem(T, 1024, E, k, 512, seed=50 + T + E, s13=narrow, s2=narrow)
     got, ref = layer_and_oracle(p)
     check_output(got["y"], ref, f"pass widths T={T} E={E} k={k}")
+
+
+def k_split(n_items, G, nraw, max_pieces=256, min_saving=4):
+    """Pieces P and raw stages per piece S of the items left after every CTA
+    of the G has taken the same number of whole ones (P = 1: not split)."""
+    q, r = divmod(n_items, G)
+    if r == 0:
+        return 1, nraw
+    p0 = max(min(nraw, min(G, max_pieces) // r), 1)
+    S = -(-nraw // p0)
+    P = -(-nraw // S)
+    return (1, nraw) if nraw - S < min_saving else (P, S)
+
+
+@pytest.mark.parametrize("H", [4096, 2560])
+def test_last_items_split_along_k_match_the_oracle(H):
+    """The gate/up items left over after every CTA has taken the same number
+    of whole ones are cut along K into pieces whose sums the CTA of the last
+    piece adds in piece order.  The shape is chosen from the GPU's SM count
+    so that a few items are left over: 16 tiles per pass (I = 1024) and one
+    more pass than fill the SMs, with H / 512 = 8 or 5 raw stages per item."""
+    G = torch.cuda.get_device_properties(0).multi_processor_count
+    I, tiles = 1024, 2 * 1024 // 128
+    passes = G // tiles + 1                          # one pass per expert at T = 16
+    E = passes - 1
+    p = problem(16, H, E, min(4, E), I, seed=H, s13=narrow, s2=narrow)
+    r = p.oracle_route()
+    n_items = len(np.unique(r["ids"])) * tiles       # every expert active: one pass each
+    P, S = k_split(n_items, G, H // 512)
+    assert P > 1, (n_items, G, P, S)                  # the shape exercises the split
+    out, ref = layer_and_oracle(p)
+    check_output(out["y"], ref, f"split H={H} P={P} S={S}")
