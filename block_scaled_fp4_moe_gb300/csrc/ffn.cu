@@ -385,50 +385,81 @@ constexpr int kTiledMinTokens = 9;
 // entry.  Loads of four columns x all K-chunks are issued together.
 __global__ void __launch_bounds__(512)
 hfin_kernel(const float *__restrict__ part, int n_kc, int n_entries, int I, const int32_t *__restrict__ sorted_tok,
-            const float *__restrict__ xundo, __half *__restrict__ h16, float *__restrict__ hundo,
+            const float *__restrict__ xundo, int T, __half *__restrict__ h16, float *__restrict__ hundo,
             const uint32_t *__restrict__ hdr, int tc_order) {
-    extern __shared__ float hbuf[];   // [I]
+    extern __shared__ float hbuf[];   // [2I]: the g and u sums, then h in the first I
     __shared__ float wmax[16];
     const int r = blockIdx.x;
     pdl_wait();
     pdl_trigger();
-    if (*reinterpret_cast<const volatile int *>(hdr + kHdrNumPasses) == 0)
-        return;                       // grouping rejected the routing
-    const float xu = xundo[sorted_tok[r]];
+    // every load that does not depend on another goes out first: the
+    // entry's token and its x factor, the routing status and the sums
+    const int tok = sorted_tok[r];
+    const bool routed = *reinterpret_cast<const volatile int *>(hdr + kHdrNumPasses) != 0;
+    const float xu = (unsigned)tok < (unsigned)T ? __ldg(xundo + tok) : 0.0f;
     const float *base = part + (size_t)r * 2 * I;
     const size_t kstride = (size_t)n_entries * 2 * I;
-    float mx = 0.0f;
-    for (int j0 = threadIdx.x; j0 < I; j0 += 2 * blockDim.x) {
-        float gv[2][kMaxKChunks], uv[2][kMaxKChunks];
+    if (n_kc == 1) {
+        constexpr int kBatch = 8;
+        for (int j0 = threadIdx.x; j0 < I; j0 += kBatch * blockDim.x) {
+            float gv[kBatch], uv[kBatch];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int j = j0 + q * blockDim.x;
+            for (int q = 0; q < kBatch; ++q) {
+                const int j = j0 + q * blockDim.x;
+                if (j < I) {
+                    gv[q] = base[j];
+                    uv[q] = base[I + j];
+                }
+            }
 #pragma unroll
-            for (int kc = 0; kc < kMaxKChunks; ++kc) {
-                if (j < I && kc < n_kc) {
-                    gv[q][kc] = base[kc * kstride + j];
-                    uv[q][kc] = base[kc * kstride + I + j];
+            for (int q = 0; q < kBatch; ++q) {
+                const int j = j0 + q * blockDim.x;
+                if (j < I) {
+                    hbuf[j] = gv[q];
+                    hbuf[I + j] = uv[q];
                 }
             }
         }
+    } else {
+        for (int j0 = threadIdx.x; j0 < I; j0 += 2 * blockDim.x) {
+            float gv[2][kMaxKChunks], uv[2][kMaxKChunks];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int j = j0 + q * blockDim.x;
-            if (j < I) {
-                float G = 0.0f, U = 0.0f;
+            for (int q = 0; q < 2; ++q) {
+                const int j = j0 + q * blockDim.x;
 #pragma unroll
-                for (int kc = 0; kc < kMaxKChunks; ++kc)
-                    if (kc < n_kc) {
-                        G += gv[q][kc];
-                        U += uv[q][kc];
+                for (int kc = 0; kc < kMaxKChunks; ++kc) {
+                    if (j < I && kc < n_kc) {
+                        gv[q][kc] = base[kc * kstride + j];
+                        uv[q][kc] = base[kc * kstride + I + j];
                     }
-                G *= xu;
-                U *= xu;
-                const float h = G / (1.0f + expf(-G)) * U;
-                hbuf[j] = h;
-                mx = fmaxf(mx, fabsf(h));
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int j = j0 + q * blockDim.x;
+                if (j < I) {
+                    float G = 0.0f, U = 0.0f;
+#pragma unroll
+                    for (int kc = 0; kc < kMaxKChunks; ++kc)
+                        if (kc < n_kc) {
+                            G += gv[q][kc];
+                            U += uv[q][kc];
+                        }
+                    hbuf[j] = G;
+                    hbuf[I + j] = U;
+                }
             }
         }
+    }
+    if (!routed)
+        return;                       // grouping rejected the routing
+    // h from this thread's own sums (the same j as above: no barrier)
+    float mx = 0.0f;
+    for (int j = threadIdx.x; j < I; j += blockDim.x) {
+        const float G = hbuf[j] * xu, U = hbuf[I + j] * xu;
+        const float h = G / (1.0f + expf(-G)) * U;
+        hbuf[j] = h;
+        mx = fmaxf(mx, fabsf(h));
     }
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1)
@@ -619,14 +650,14 @@ cudaError_t launch_ffn(const FfnProblem &pr, void *ws, const WsLayout &L, int nu
     if ((err = launch_mode<kFfnGateUp>(g, num_sms, cache_passes, T, stream)) != cudaSuccess)
         return err;
 
-    const size_t hsmem = (size_t)I * sizeof(float);
+    const size_t hsmem = 2 * (size_t)I * sizeof(float);
     if (hsmem > 48 * 1024 &&
         (err = cudaFuncSetAttribute(hfin_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsmem)) !=
             cudaSuccess)
         return err;
     err = launch_pdl(hfin_kernel, dim3(entries), dim3(512), hsmem, stream, (const float *)ws_at<float>(ws, L.gpart),
                      L.n_kc_gu, entries, I, (const int32_t *)ws_at<int32_t>(ws, L.sorted_tok),
-                     (const float *)ws_at<float>(ws, L.xundo), ws_at<__half>(ws, L.h16), ws_at<float>(ws, L.hundo),
+                     (const float *)ws_at<float>(ws, L.xundo), T, ws_at<__half>(ws, L.h16), ws_at<float>(ws, L.hundo),
                      (const uint32_t *)hdr, 0);
     if (err != cudaSuccess)
         return err;
@@ -668,8 +699,8 @@ cudaError_t launch_combine(const float *yent, int entries, const int32_t *inv_po
                       topk_w, T, kps, H, y, hdr);
 }
 
-cudaError_t launch_hfin(void *ws, const WsLayout &L, int entries, int I, bool tc_order, cudaStream_t stream) {
-    const size_t hsmem = (size_t)I * sizeof(float);
+cudaError_t launch_hfin(void *ws, const WsLayout &L, int T, int entries, int I, bool tc_order, cudaStream_t stream) {
+    const size_t hsmem = 2 * (size_t)I * sizeof(float);
     cudaError_t err;
     if (hsmem > 48 * 1024 &&
         (err = cudaFuncSetAttribute(hfin_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsmem)) !=
@@ -677,7 +708,7 @@ cudaError_t launch_hfin(void *ws, const WsLayout &L, int entries, int I, bool tc
         return err;
     return launch_pdl(hfin_kernel, dim3(entries), dim3(512), hsmem, stream, (const float *)ws_at<float>(ws, L.gpart),
                       1, entries, I, (const int32_t *)ws_at<int32_t>(ws, L.sorted_tok),
-                      (const float *)ws_at<float>(ws, L.xundo), ws_at<__half>(ws, L.h16), ws_at<float>(ws, L.hundo),
+                      (const float *)ws_at<float>(ws, L.xundo), T, ws_at<__half>(ws, L.h16), ws_at<float>(ws, L.hundo),
                       (const uint32_t *)ws_at<uint32_t>(ws, 0), tc_order ? 1 : 0);
 }
 

@@ -157,6 +157,6 @@ cudaError_t launch_ffn_tc(const FfnProblem &p, void *ws, const WsLayout &L, int 
                           cudaEvent_t ev_after_gateup);
 // h = silu(g) u from the gate/up sums (one K chunk) into h16 (hi, lo) and
 // hundo; tc_order: each 64-element step of h16 in the tensor-memory K order.
-cudaError_t launch_hfin(void *ws, const WsLayout &L, int entries, int I, bool tc_order, cudaStream_t stream);
+cudaError_t launch_hfin(void *ws, const WsLayout &L, int T, int entries, int I, bool tc_order, cudaStream_t stream);
 
 }  // namespace moe

@@ -945,7 +945,7 @@ cudaError_t launch_ffn_tc(const FfnProblem &pr, void *ws, const WsLayout &L, int
     g.tickets = tickets;
     if ((err = launch_tc<kFfnGateUp>(g, gm16, gm32, num_sms, stream)) != cudaSuccess)
         return err;
-    if ((err = launch_hfin(ws, L, entries, I, true, stream)) != cudaSuccess)
+    if ((err = launch_hfin(ws, L, T, entries, I, true, stream)) != cudaSuccess)
         return err;
     if (ev_after_gateup && (err = cudaEventRecord(ev_after_gateup, stream)) != cudaSuccess)
         return err;
