@@ -532,7 +532,7 @@ def run_mine(args, cfg):
         roof_bytes = b["total"]
         roof_us = per_call * 1e6
     else:
-        roof_kernel, traffic_key = "ffn_kernel<gate/up> (+ h finalize)", "ffn_gateup"
+        roof_kernel, traffic_key = "ffn_tc_kernel<gate/up> (+ h finalisation)", "ffn_tc_gateup"
         roof_bytes = b["gateup"]
         roof_us = kern_us["gateup_hfin"]
     achieved = roof_bytes / (roof_us * 1e-6) / 1e9
