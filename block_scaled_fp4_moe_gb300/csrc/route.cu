@@ -13,7 +13,9 @@
 // first), ordered by descending logit; softmax over the k kept logits; the
 // shared expert, always selected, appended as slot k ("Optimizing GLM4-MoE for
 // production", section 1 "Shared experts fusion": top-9 of 161, the shared
-// expert always in the 9th position).
+// expert always in the 9th position).  For T > 8 the selection is the one the
+// single-launch kernel uses: each group of 32 experts keeps its first k ranks
+// as a sorted candidate list, and one warp merges the lists.
 #include <cuda_bf16.h>
 
 #include "common.cuh"

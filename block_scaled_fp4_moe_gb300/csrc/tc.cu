@@ -67,6 +67,14 @@
 // Every wait is bounded (200 ms, then MOE_ERR_DEVICE_TIMEOUT) and stops the
 // whole CTA.
 //
+// Items per CTA: the items are equal in cost, so every CTA first takes the
+// same number of whole ones; the few left over are cut along K into pieces
+// that go to the first CTAs, each writing its raw sums to a tail slot, and
+// the CTA whose piece arrives last adds the slots in piece order (see
+// TcSchedule).  The weight warp and the decoders start before the wait on
+// the preceding grid: the pass lists and the weights are final when this
+// grid launches; the activation warp and the epilogue wait first.
+//
 // Issue costs measured on the GPU (clock64 around back-to-back MMAs of one
 // warp): a kind::f16 MMA with A in TMEM issues every ~17 cycles at N <= 32
 // when its warp runs alone on its scheduler (A from shared memory: ~42, the
@@ -304,6 +312,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ int s_abort;
     __shared__ int s_bad;
     __shared__ int s_last;
+    __shared__ Pass s_pps;                    // the split item's pass and tile, and its rows'
+    __shared__ int s_ptile;                   // exponent bases, left by the epilogue for the
+    __shared__ uint32_t s_prb[128];           // sum after the final barrier
     // the warp index and every value a warp's control flow depends on are
     // broadcast from lane 0, so that the compiler treats them as warp-uniform
     const int tid = threadIdx.x, lane = tid & 31;
@@ -604,6 +615,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const bool present = (m >> 4) < tile_units(tile);
             const uint32_t rb = present ? __ldg(a.rowexp + ((size_t)ps.expert * a.upe + tile * kTcUnits) * 16 + m) : 0u;
             const float fac = tc_row_factor(rb);
+            if (piece) {
+                s_prb[m] = rb;
+                if (m == 0) {
+                    s_pps = ps;
+                    s_ptile = tile;
+                }
+            }
             const int u = tile * kTcUnits + (m >> 4), r = m & 15;
             const int col = MODE == kFfnGateUp ? (r < 8 ? 8 * u + r : a.out_len + 8 * u + r - 8) : 16 * u + r;
             // the outputs of the 16 columns of sums from column c0 on
@@ -682,18 +700,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
     }
     pdl_wait();
-    // a split item's pass, tile and row exponent, loaded before the barrier
-    // for the case that this CTA adds its pieces
-    Pass piece_ps{};
-    int piece_tile = 0;
-    uint32_t piece_rb = 0;
-    if (sch.P > 1 && my_items > sch.q) {
-        piece_ps = item_pass(my_items - 1);
-        piece_tile = item_tile(my_items - 1);
-        const int m = tid >> 2;
-        if ((m >> 4) < tile_units(piece_tile))
-            piece_rb = __ldg(a.rowexp + ((size_t)piece_ps.expert * a.upe + piece_tile * kTcUnits) * 16 + m);
-    }
     __syncthreads();
     if (s_abort && tid == 0)
         record_status(a.hdr, MOE_ERR_DEVICE_TIMEOUT);
@@ -701,11 +707,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // the split item's outputs: thread t takes row t / 4 of the tile and,
         // per 16 columns, columns 4 (t % 4) .. + 3, adding the P slots in
         // piece order (all slot loads issued at once)
+        const Pass piece_ps = s_pps;
+        const int piece_tile = s_ptile;
         const int rows = piece_ps.count * a.rows_per_entry;
         const int m = tid >> 2, c4 = 4 * (tid & 3);
         const int k = (int)blockIdx.x / sch.P;
         const int u = piece_tile * kTcUnits + (m >> 4), r = m & 15;
-        const float fac = tc_row_factor(piece_rb);
+        const float fac = tc_row_factor(s_prb[m]);
         const bool present = (m >> 4) < tile_units(piece_tile);
         constexpr int kBatch = 16;
         for (int c0 = 0; c0 < kTcNMax && c0 < rows && present; c0 += 16) {
