@@ -82,3 +82,19 @@ def test_debug_build_mxfp8_variant(T):
     np.testing.assert_array_equal(ids1, ids0)
     d = np.abs(inputs.bf16_bits_to_f32(y1).astype(np.float64) - inputs.bf16_bits_to_f32(y0))
     assert d.max() <= 1e-2 * np.abs(inputs.bf16_bits_to_f32(y0)).max()
+
+
+def test_debug_build_split_items():
+    """The tensor-memory kernels' leftover items cut along K (tail slots,
+    arrival counters, the sum by the last piece's CTA) under the range
+    checks: a T = 16 shape with one pass more than fill the SMs at 16 tiles
+    per pass and 8 raw stages per item."""
+    G = torch.cuda.get_device_properties(0).multi_processor_count
+    E = G // 16                              # passes = E + 1 (shared): n_items = 16 (G // 16 + 1) > G
+    p = random_problem(T=16, H=4096, E=E, k=min(4, E), I=1024, seed=140)
+    with moe.debug_bounds():
+        st, y, ids, w = run_layer(p)
+    assert st == 0, moe.moe_status_string(st)
+    r = p.oracle_route()
+    np.testing.assert_array_equal(ids, r["ids"])
+    check_output(y, p.oracle_tokens(r, np.arange(p.T))["y"], "debug build split items")
