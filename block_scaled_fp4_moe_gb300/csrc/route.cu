@@ -466,16 +466,21 @@ route_finish_kernel(const float2 *__restrict__ part, int nh, const float *__rest
         group_block(sids, T, kps, E + has_shared, go, hdr, true);
         return;
     }
-    __threadfence();
+    // the CTA barrier orders this CTA's ids before thread 0's acquire-release
+    // add (cumulative); the add that finds every other CTA counted acquires
+    // their ids for the whole CTA through the barrier after it
     __syncthreads();
     if (threadIdx.x == 0) {
-        const unsigned ticket = atomicAdd(hdr + kHdrRouteTicket, 1u);
+        unsigned ticket;
+        asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+                     : "=r"(ticket)
+                     : "l"(hdr + kHdrRouteTicket)
+                     : "memory");
         last_cta = ticket == gridDim.x - 1;
     }
     __syncthreads();
     if (!last_cta)
         return;
-    __threadfence();
     const int n = T * kps;
     if (n <= kGroupSmemIds) {
         // every token's ids into shared memory first: the grouping then reads
